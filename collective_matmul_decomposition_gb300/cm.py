@@ -1,0 +1,190 @@
+"""Python binding of the C ABI in include/cm.h (argument marshalling only).
+
+Every step of the decomposed collective matmul runs in the CUDA library
+(_build/libcm.so); this module only turns torch tensors into device pointers
+and the current CUDA stream into a cudaStream_t.  It raises if the library is
+missing -- there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "_build", "libcm.so")
+
+CM_OK, CM_ERR_INVALID_ARG, CM_ERR_SHAPE, CM_ERR_ALIGNMENT = 0, 1, 2, 3
+CM_ERR_UNSUPPORTED, CM_ERR_CUDA, CM_ERR_TIMEOUT, CM_ERR_WORKSPACE = 4, 5, 6, 7
+CM_RING_UNI, CM_RING_BIDI, CM_RING_NONE = 0, 1, 2
+CM_BF16, CM_F32 = 0, 1
+CM_W_KN, CM_W_NK = 0, 1
+CM_OP_AG_GEMM, CM_OP_GEMM_RS = 0, 1
+CM_OPT_TIMEOUT_NS, CM_OPT_SERIAL_STEPS, CM_OPT_GRID, CM_OPT_SKIP_SIGNAL = 0, 1, 2, 3
+CM_MAX_RANKS, CM_MAX_CHUNKS = 16, 8
+
+DIRECTIONS = {"uni": CM_RING_UNI, "bidi": CM_RING_BIDI, "none": CM_RING_NONE}
+LAYOUTS = {"kn": CM_W_KN, "nk": CM_W_NK}
+
+# Every symbol include/cm.h declares.
+EXPORTS = ["cm_plan", "cm_plan_destroy", "cm_plan_steps", "cm_plan_step", "cm_plan_tasks",
+           "cm_ag_gemm_workspace_size", "cm_gemm_rs_workspace_size", "cm_ag_gemm", "cm_gemm_rs",
+           "cm_check_status", "cm_status_string", "cm_plan_set_option", "cm_version"]
+
+
+class cm_task(ctypes.Structure):
+    _fields_ = [("rank", ctypes.c_int16), ("a_slab", ctypes.c_int16), ("a_src", ctypes.c_int16),
+                ("out_idx", ctypes.c_int16), ("out_buf", ctypes.c_int16),
+                ("in_buf", ctypes.c_int16 * 2), ("fwd_slot", ctypes.c_int16 * 2),
+                ("wait_in", ctypes.c_int16 * 2), ("wait_free", ctypes.c_int16 * 2),
+                ("sig_fwd", ctypes.c_int16 * 2), ("sig_done", ctypes.c_int16),
+                ("step", ctypes.c_int16), ("stream", ctypes.c_int16), ("reserved", ctypes.c_int16)]
+
+
+class CMError(RuntimeError):
+    def __init__(self, status, what=""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+_lib = None
+
+
+def load():
+    """Load the in-tree library (built by __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing "
+                           "(run __graft_entry__.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    i32, i64, p, sz = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    lib.cm_plan.argtypes = [i32, i32, i32, ctypes.POINTER(p)]
+    lib.cm_plan.restype = i32
+    lib.cm_plan_destroy.argtypes = [p]
+    lib.cm_plan_destroy.restype = i32
+    lib.cm_plan_steps.argtypes = [p, i32]
+    lib.cm_plan_steps.restype = i32
+    lib.cm_plan_step.argtypes = [p, i32, i32, i32, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                 ctypes.POINTER(i32)]
+    lib.cm_plan_step.restype = i32
+    lib.cm_plan_tasks.argtypes = [p, i32, p, i32]
+    lib.cm_plan_tasks.restype = i32
+    lib.cm_ag_gemm_workspace_size.argtypes = [p, i64, i64]
+    lib.cm_ag_gemm_workspace_size.restype = sz
+    lib.cm_gemm_rs_workspace_size.argtypes = [p, i64, i64]
+    lib.cm_gemm_rs_workspace_size.restype = sz
+    lib.cm_ag_gemm.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p, sz, p]
+    lib.cm_ag_gemm.restype = i32
+    lib.cm_gemm_rs.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p, sz, p]
+    lib.cm_gemm_rs.restype = i32
+    lib.cm_check_status.argtypes = [p, p, ctypes.POINTER(i32)]
+    lib.cm_check_status.restype = i32
+    lib.cm_status_string.argtypes = [i32]
+    lib.cm_status_string.restype = ctypes.c_char_p
+    lib.cm_plan_set_option.argtypes = [p, i32, i64]
+    lib.cm_plan_set_option.restype = i32
+    lib.cm_version.argtypes = []
+    lib.cm_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().cm_status_string(int(status)).decode()
+
+
+def _check(status, what):
+    if status != CM_OK:
+        raise CMError(status, what)
+
+
+class Plan:
+    """Owns a cm_plan_t (cm_plan / cm_plan_destroy)."""
+
+    def __init__(self, n_ranks: int, chunks: int = 1, direction: str = "uni"):
+        lib = load()
+        h = ctypes.c_void_p()
+        _check(lib.cm_plan(int(n_ranks), int(chunks), DIRECTIONS[direction], ctypes.byref(h)), "cm_plan")
+        self.handle = h
+        self.N, self.chunks, self.direction = int(n_ranks), int(chunks), direction
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and h.value and _lib is not None:
+            _lib.cm_plan_destroy(h)
+            self.handle = None
+
+    def steps(self, op: int) -> int:
+        return load().cm_plan_steps(self.handle, int(op))
+
+    def step(self, op: int, rank: int, step: int, stream: int = 0):
+        o, s, d = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        _check(load().cm_plan_step(self.handle, int(op), rank, step, stream,
+                                   ctypes.byref(o), ctypes.byref(s), ctypes.byref(d)), "cm_plan_step")
+        return o.value, s.value, d.value
+
+    def tasks(self, op: int):
+        lib = load()
+        n = lib.cm_plan_tasks(self.handle, int(op), None, 0)
+        arr = (cm_task * max(n, 1))()
+        lib.cm_plan_tasks(self.handle, int(op), ctypes.cast(arr, ctypes.c_void_p), n)
+        return [arr[i] for i in range(n)]
+
+    def set_option(self, option: int, value: int):
+        _check(load().cm_plan_set_option(self.handle, int(option), int(value)), "cm_plan_set_option")
+
+    def ag_workspace_size(self, m: int, K: int) -> int:
+        return int(load().cm_ag_gemm_workspace_size(self.handle, int(m), int(K)))
+
+    def rs_workspace_size(self, M: int, n: int) -> int:
+        return int(load().cm_gemm_rs_workspace_size(self.handle, int(M), int(n)))
+
+
+def _stream_ptr(stream):
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _ydtype(y):
+    import torch
+    if y.dtype == torch.bfloat16:
+        return CM_BF16
+    if y.dtype == torch.float32:
+        return CM_F32
+    raise TypeError("y must be bf16 or fp32")
+
+
+def cm_ag_gemm(plan: Plan, x, w, y, ws, w_layout: str = "nk", stream=None):
+    """Decomposed AllGather->GEMM: x [N][m][K], w per rank, y [N][N*m][n]."""
+    N, m, K = x.shape
+    n = w.shape[1] if w_layout == "nk" else w.shape[2]
+    st = load().cm_ag_gemm(plan.handle, _ptr(x), _ptr(w), LAYOUTS[w_layout], _ptr(y), _ydtype(y),
+                           m, K, n, _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream))
+    _check(st, "cm_ag_gemm")
+
+
+def cm_gemm_rs(plan: Plan, x, w, y, ws, w_layout: str = "nk", stream=None):
+    """Decomposed GEMM->ReduceScatter: x [N][M][k], w per rank, y [N][M/N][n]."""
+    N, M, k = x.shape
+    n = w.shape[1] if w_layout == "nk" else w.shape[2]
+    st = load().cm_gemm_rs(plan.handle, _ptr(x), _ptr(w), LAYOUTS[w_layout], _ptr(y), _ydtype(y),
+                           M, k, n, _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream))
+    _check(st, "cm_gemm_rs")
+
+
+def cm_check_status(ws, stream=None):
+    """Synchronise and return (status, info[4]) of the last call that used ws."""
+    info = (ctypes.c_int * 4)()
+    st = load().cm_check_status(_ptr(ws), _stream_ptr(stream), info)
+    return st, list(info)
+
+
+def version() -> str:
+    return load().cm_version().decode()

@@ -1,0 +1,271 @@
+// cm_api.cu -- the C ABI: argument checks, workspace layout, TMA tensor maps
+// and the launch of the persistent kernel.
+#include <cudaTypedefs.h>
+
+#include <cstring>
+#include <mutex>
+
+#include "cm_internal.h"
+#include "cm_kernel.cuh"
+
+namespace cm {
+namespace {
+
+constexpr size_t kStatusBytes = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct WsLayout {
+    size_t flags_off = kStatusBytes, flags_bytes = 0, buf_off = 0, buf_bytes = 0, total = 0;
+};
+
+int streams_of(const PlanImpl &p) { return p.dir == CM_RING_BIDI ? 2 : 1; }
+
+WsLayout ag_layout(const PlanImpl &p, int64_t m, int64_t K) {
+    WsLayout l;
+    l.flags_bytes = size_t(p.flag_ids[CM_OP_AG_GEMM]) * size_t(p.chunks) * sizeof(uint32_t);
+    l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
+    const bool ring = p.dir != CM_RING_NONE && p.N > 1;
+    const size_t slots = ring ? size_t(2 * p.N * streams_of(p)) : 0;
+    l.buf_bytes = slots * size_t(m) * size_t(K) * 2;
+    l.total = l.buf_off + l.buf_bytes;
+    return l;
+}
+
+WsLayout rs_layout(const PlanImpl &p, int64_t M, int64_t n) {
+    WsLayout l;
+    l.flags_bytes = size_t(p.flag_ids[CM_OP_GEMM_RS]) * size_t(p.chunks) * sizeof(uint32_t);
+    l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
+    const bool ring = p.dir != CM_RING_NONE && p.N > 1;
+    const size_t bufs = ring ? size_t(2 * p.N * streams_of(p)) : 0;
+    l.buf_bytes = bufs * size_t(M / p.N) * size_t(n) * sizeof(float);
+    l.total = l.buf_off + l.buf_bytes;
+    return l;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// bf16 3-D tensor [d2][d1][d0] (d0 contiguous), 128-byte swizzled boxes of b0 x b1.
+bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {d0, d1, d2};
+    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint32_t box[3] = {b0, b1, 1};
+    cuuint32_t es[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+cm_status run(const PlanImpl &pl, int op, KParams &kp, const WsLayout &l, void *ws, bool b_mn,
+              cudaStream_t stream) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return CM_ERR_CUDA;
+    int sms = 0;
+    if (prepare_device(dev, &sms) != cudaSuccess) return CM_ERR_CUDA;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    kp.status = reinterpret_cast<uint32_t *>(w8);
+    kp.flags = reinterpret_cast<uint32_t *>(w8 + l.flags_off);
+    kp.timeout_ns = uint64_t(pl.timeout_ns);
+    const auto &tasks = pl.tasks[op];
+    const int ntasks = int(tasks.size());
+    if (ntasks > kMaxTasks) return CM_ERR_UNSUPPORTED;
+    std::memcpy(kp.tasks, tasks.data(), sizeof(cm_task) * size_t(ntasks));
+    // status word and flags start at zero for every call
+    if (cudaMemsetAsync(ws, 0, l.buf_off, stream) != cudaSuccess) return CM_ERR_CUDA;
+    const auto &sb = pl.step_begin[op];
+    const int nsteps = int(sb.size()) - 1;
+    const int launches = pl.serial_steps ? nsteps : 1;
+    for (int i = 0; i < launches; ++i) {
+        kp.task_begin = pl.serial_steps ? sb[size_t(i)] : 0;
+        kp.task_end = pl.serial_steps ? sb[size_t(i) + 1] : ntasks;
+        if (kp.task_end <= kp.task_begin) continue;
+        const int64_t tiles = int64_t(kp.task_end - kp.task_begin) * kp.tiles_per_task;
+        int grid = pl.grid > 0 ? std::min(pl.grid, sms) : sms;
+        if (tiles < grid) grid = int(tiles);
+        if (launch_persistent(kp, b_mn, grid, stream) != cudaSuccess) return CM_ERR_CUDA;
+    }
+    return CM_OK;
+}
+
+cm_status check_common(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl, void *y, cm_dtype yd,
+                       int64_t rows, int64_t K, int64_t n) {
+    if (!plan || !x || !w || !y) return CM_ERR_INVALID_ARG;
+    if (wl != CM_W_KN && wl != CM_W_NK) return CM_ERR_INVALID_ARG;
+    if (yd != CM_BF16 && yd != CM_F32) return CM_ERR_INVALID_ARG;
+    if (rows <= 0 || K <= 0 || n <= 0) return CM_ERR_SHAPE;
+    if (K % 8 != 0 || n % 8 != 0) return CM_ERR_ALIGNMENT;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(y)) return CM_ERR_ALIGNMENT;
+    if (K > (int64_t(1) << 30) || n > (int64_t(1) << 30) || rows > (int64_t(1) << 30)) return CM_ERR_SHAPE;
+    return CM_OK;
+}
+
+}  // namespace
+}  // namespace cm
+
+using namespace cm;
+
+extern "C" {
+
+size_t cm_ag_gemm_workspace_size(cm_plan_t plan, int64_t m, int64_t K) {
+    if (!plan || m <= 0 || K <= 0) return 0;
+    return ag_layout(plan->impl, m, K).total;
+}
+
+size_t cm_gemm_rs_workspace_size(cm_plan_t plan, int64_t M, int64_t n) {
+    if (!plan || M <= 0 || n <= 0) return 0;
+    return rs_layout(plan->impl, M, n).total;
+}
+
+cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y, cm_dtype y_dtype,
+                     int64_t m, int64_t K, int64_t n, void *ws, size_t ws_bytes, cm_stream_t stream) {
+    cm_status st = check_common(plan, x, w, wlayout, y, y_dtype, m, K, n);
+    if (st != CM_OK) return st;
+    const PlanImpl &pl = plan->impl;
+    const int N = pl.N;
+    if (m % pl.chunks != 0) return CM_ERR_SHAPE;
+    const WsLayout l = ag_layout(pl, m, K);
+    if (!ws || ws_bytes < l.total) return CM_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return CM_ERR_ALIGNMENT;
+
+    const bool none = pl.dir == CM_RING_NONE;
+    const int c = none ? 1 : pl.chunks;
+    const int64_t rows_c = none ? int64_t(N) * m : m / c;
+    const int64_t slabs = none ? 1 : int64_t(N) * c;
+    static KParams kp;   // ~9 KB; calls are serialised by the mutex below
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    std::memset(static_cast<void *>(&kp), 0, sizeof kp);
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
+    if (!make_map(&kp.tmA0, x, uint64_t(K), uint64_t(rows_c), uint64_t(slabs), kBK, box_rows)) return CM_ERR_CUDA;
+    uint8_t *bufs = static_cast<uint8_t *>(ws) + l.buf_off;
+    if (l.buf_bytes > 0) {
+        const int64_t nslots = int64_t(2) * N * streams_of(pl);
+        if (!make_map(&kp.tmA1, bufs, uint64_t(K), uint64_t(rows_c), uint64_t(nslots * c), kBK, box_rows))
+            return CM_ERR_CUDA;
+    } else {
+        kp.tmA1 = kp.tmA0;
+    }
+    const bool b_mn = wlayout == CM_W_KN;
+    if (b_mn) {
+        if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(K), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+    } else {
+        if (!make_map(&kp.tmB, w, uint64_t(K), uint64_t(n), uint64_t(N), kBK, kBN)) return CM_ERR_CUDA;
+    }
+    kp.y = y;
+    kp.acc = nullptr;
+    kp.y_rank_stride = int64_t(N) * m * n;
+    kp.out_rows_per_idx = none ? int64_t(N) * m : m;
+    kp.acc_buf_stride = 0;
+    kp.op = 0;
+    kp.N = N;
+    kp.chunks = c;
+    kp.rows_c = int(rows_c);
+    kp.mtiles_c = int((rows_c + kBM - 1) / kBM);
+    kp.ntiles = int((n + kBN - 1) / kBN);
+    kp.kblocks = int((K + kBK - 1) / kBK);
+    kp.n = int(n);
+    kp.y_f32 = y_dtype == CM_F32;
+    kp.a_box_rows = int(box_rows);
+    kp.tiles_per_task = c * kp.mtiles_c * kp.ntiles;
+    kp.tgt_in = uint32_t(kp.mtiles_c);                    // forwarded row tiles per chunk
+    kp.tgt_free = uint32_t(kp.mtiles_c * kp.ntiles);      // tiles that read a slot chunk
+    return run(pl, CM_OP_AG_GEMM, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y, cm_dtype y_dtype,
+                     int64_t M, int64_t k, int64_t n, void *ws, size_t ws_bytes, cm_stream_t stream) {
+    cm_status st = check_common(plan, x, w, wlayout, y, y_dtype, M, k, n);
+    if (st != CM_OK) return st;
+    const PlanImpl &pl = plan->impl;
+    const int N = pl.N;
+    if (M % N != 0) return CM_ERR_SHAPE;
+    const int64_t Mb = M / N;
+    if (Mb % pl.chunks != 0) return CM_ERR_SHAPE;
+    const WsLayout l = rs_layout(pl, M, n);
+    if (!ws || ws_bytes < l.total) return CM_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return CM_ERR_ALIGNMENT;
+
+    const bool none = pl.dir == CM_RING_NONE;
+    const int c = none ? 1 : pl.chunks;
+    const int64_t rows_c = Mb / c;
+    static KParams kp;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    std::memset(static_cast<void *>(&kp), 0, sizeof kp);
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
+    // x [N][M][k] viewed as [N*N*c][rows_c][k]: slab (r*N + bucket)*c + chunk
+    if (!make_map(&kp.tmA0, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
+    kp.tmA1 = kp.tmA0;
+    const bool b_mn = wlayout == CM_W_KN;
+    if (b_mn) {
+        if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(k), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+    } else {
+        if (!make_map(&kp.tmB, w, uint64_t(k), uint64_t(n), uint64_t(N), kBK, kBN)) return CM_ERR_CUDA;
+    }
+    kp.y = y;
+    kp.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
+    kp.y_rank_stride = 0;
+    kp.out_rows_per_idx = Mb;
+    kp.acc_buf_stride = Mb * n;
+    kp.op = 1;
+    kp.N = N;
+    kp.chunks = c;
+    kp.rows_c = int(rows_c);
+    kp.mtiles_c = int((rows_c + kBM - 1) / kBM);
+    kp.ntiles = int((n + kBN - 1) / kBN);
+    kp.kblocks = int((k + kBK - 1) / kBK);
+    kp.n = int(n);
+    kp.y_f32 = y_dtype == CM_F32;
+    kp.a_box_rows = int(box_rows);
+    kp.tiles_per_task = c * kp.mtiles_c * kp.ntiles;
+    kp.tgt_in = uint32_t(kp.mtiles_c * kp.ntiles);        // finished tiles per chunk
+    kp.tgt_free = uint32_t(kp.mtiles_c * kp.ntiles);
+    return run(pl, CM_OP_GEMM_RS, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
+}
+
+cm_status cm_check_status(const void *ws, cm_stream_t stream, int32_t info[4]) {
+    if (!ws) return CM_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return CM_ERR_CUDA;
+    uint32_t h[4] = {0, 0, 0, 0};
+    if (cudaMemcpy(h, ws, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return CM_ERR_CUDA;
+    if (info)
+        for (int i = 0; i < 4; ++i) info[i] = int32_t(h[i]);
+    if (h[0] == 0) return CM_OK;
+    return h[0] == uint32_t(CM_ERR_TIMEOUT) ? CM_ERR_TIMEOUT : CM_ERR_CUDA;
+}
+
+const char *cm_status_string(cm_status s) {
+    switch (s) {
+        case CM_OK: return "ok";
+        case CM_ERR_INVALID_ARG: return "invalid argument";
+        case CM_ERR_SHAPE: return "shape not supported (divisibility)";
+        case CM_ERR_ALIGNMENT: return "pointer or extent not aligned for TMA";
+        case CM_ERR_UNSUPPORTED: return "unsupported configuration";
+        case CM_ERR_CUDA: return "CUDA error";
+        case CM_ERR_TIMEOUT: return "device-side wait timed out";
+        case CM_ERR_WORKSPACE: return "workspace missing or too small";
+    }
+    return "unknown status";
+}
+
+const char *cm_version(void) { return "cm 0.1 (sm_103a tcgen05/TMA persistent kernel)"; }
+
+}  // extern "C"

@@ -1,0 +1,50 @@
+// cm_internal.h -- types shared by the planner, the C ABI and the kernel.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "cm.h"
+
+namespace cm {
+
+constexpr int kMaxTasks = CM_MAX_RANKS * CM_MAX_RANKS;   // N tasks per rank at most
+
+// Ring schedule entry of one (rank, step, stream); see cm_plan_step.
+struct StepEntry {
+    int obj = -1, src = -1, dst = -1;
+};
+
+struct Schedule {
+    int steps = 0;
+    int streams = 1;
+    std::vector<StepEntry> e;   // [rank][step][stream]
+    StepEntry &at(int N, int r, int i, int s) { return e[(size_t(r) * steps + i) * streams + s]; }
+    const StepEntry &at(int N, int r, int i, int s) const {
+        return e[(size_t(r) * steps + i) * streams + s];
+    }
+};
+
+// Flag id families (word = id * chunks + chunk).  Each family spans
+// N * steps * 2 ids so ids never collide.
+enum FlagKind { kFlagReady = 0, kFlagReadDone = 1, kFlagDone = 0 };
+
+struct PlanImpl {
+    int N = 1;
+    int chunks = 1;
+    cm_direction dir = CM_RING_UNI;
+    int64_t timeout_ns = 1000000000LL;
+    int serial_steps = 0;
+    int grid = 0;
+    int64_t skip_signal = -1;
+    Schedule sched[2];                    // per cm_op
+    std::vector<cm_task> tasks[2];        // per cm_op, execution order
+    int flag_ids[2] = {0, 0};             // ids used per op (before * chunks)
+    std::vector<int> step_begin[2];       // first task index of each step (+ end sentinel)
+};
+
+}  // namespace cm
+
+struct cm_plan_s {
+    cm::PlanImpl impl;
+};

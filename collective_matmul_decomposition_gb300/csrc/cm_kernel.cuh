@@ -1,0 +1,67 @@
+// cm_kernel.cuh -- parameters and launch entry of the persistent tile kernel.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "cm_internal.h"
+
+namespace cm {
+
+// Tile geometry: one CTA per SM computes 128 x 256 output tiles with K
+// slices of 64 (one 128-byte swizzle row of bf16), 4-stage smem ring.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 256;
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBN * kBK * 2;
+constexpr uint32_t kTmemCols = 512;   // two 128 x 256 fp32 accumulators
+constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 /*barriers*/ + 1024 /*align slack*/;
+
+// Status word sites (which wait gave up), reported by cm_check_status.
+enum Site : uint32_t {
+    kSiteProducerFlag = 1,
+    kSiteForwardFlag = 2,
+    kSiteEpilogueFlag = 3,
+    kSiteEmpty = 4,
+    kSiteFull = 5,
+    kSiteTmemEmpty = 6,
+    kSiteTmemFull = 7,
+    kSiteForwardFull = 8,
+};
+
+struct KParams {
+    CUtensorMap tmA0;   // x: AG shards / RS per-rank row slabs, as [slabs*chunks][rows_c][K]
+    CUtensorMap tmA1;   // AG workspace receive slots, same view (loads and forward stores)
+    CUtensorMap tmB;    // weights: [N][n][K] (K-major) or [N][K][n] (n-major)
+    void *y;
+    float *acc;                // RS circulating accumulators
+    uint32_t *flags;
+    uint32_t *status;
+    int64_t y_rank_stride;     // AG: elements between Y_r and Y_{r+1}
+    int64_t out_rows_per_idx;  // AG: rows per shard id (m, or N*m undecomposed); RS: rows per bucket
+    int64_t acc_buf_stride;    // RS: elements per accumulator buffer
+    uint64_t timeout_ns;
+    int op;                    // 0 AllGather->GEMM, 1 GEMM->ReduceScatter
+    int N, chunks;
+    int rows_c;                // rows per chunk
+    int mtiles_c, ntiles, kblocks;
+    int n;
+    int y_f32;
+    int a_box_rows;
+    int tiles_per_task, task_begin, task_end;
+    uint32_t tgt_in, tgt_free;
+    cm_task tasks[kMaxTasks];
+};
+
+// Launch the persistent kernel for tasks [p.task_begin, p.task_end).
+cudaError_t launch_persistent(const KParams &p, bool b_mn_major, int grid, cudaStream_t stream);
+
+// One-time per-device kernel attributes; returns the SM count.
+cudaError_t prepare_device(int device, int *num_sms);
+
+}  // namespace cm

@@ -1,0 +1,354 @@
+// cm_plan.cpp -- ring schedules and the task table the persistent kernel runs.
+//
+// Schedules ("Overlap Communication with Dependent Computation via
+// Decomposition in Large Deep Learning Models", section "The idea";
+// "Hiding Tensor-Parallel Collectives: AG/RS Overlap in Megatron", sections
+// 3 and 5):
+//   AG, one ring: rank r multiplies shard (r - i) mod N at step i; it received
+//     it from r-1 and forwards it to r+1 until every rank has used it.
+//   RS, one ring: rank r adds its product for bucket (r - i - 1) mod N at step
+//     i to the partial bucket received from r-1 and forwards it to r+1; at
+//     step N-1 that bucket is r's own and is written out.
+//   Bidirectional: a = ceil((N-1)/2) clockwise hops, b = floor((N-1)/2)
+//     counter-clockwise hops.  AG: the own shard leaves both ways at step 0;
+//     rank r uses (r - i) and (r + i) at step i.  RS: the bucket of owner o
+//     collects ranks o-a .. o-1 clockwise and o+b .. o+1 counter-clockwise;
+//     the owner adds both partials and its own product (the realigning add).
+//
+// Task table: one task per (rank, step, stream) that multiplies, ordered
+// step-major and, inside a step, by the shard / bucket it serves, so that the
+// task consuming what another task forwarded sits at the same position one
+// step later.  Every flag a task waits on is signalled only by tasks of an
+// earlier step, which makes the static round-robin tile order of the kernel
+// free of deadlock (the earliest unfinished tile never waits).
+#include <algorithm>
+#include <cstring>
+#include <new>
+
+#include "cm_internal.h"
+
+namespace cm {
+namespace {
+
+inline int md(int a, int N) { return ((a % N) + N) % N; }
+
+void hop_split(int N, int *a, int *b) {
+    *a = N / 2;          // ceil((N-1)/2)
+    *b = (N - 1) / 2;    // floor((N-1)/2)
+}
+
+void build_ag_schedule(PlanImpl &p) {
+    const int N = p.N;
+    Schedule &s = p.sched[CM_OP_AG_GEMM];
+    if (p.dir == CM_RING_NONE) {
+        s.steps = 1; s.streams = 1;
+        s.e.assign(size_t(N), StepEntry{});
+        return;
+    }
+    if (p.dir == CM_RING_UNI) {
+        s.steps = N; s.streams = 1;
+        s.e.assign(size_t(N) * N, StepEntry{});
+        for (int r = 0; r < N; ++r)
+            for (int i = 0; i < N; ++i) {
+                StepEntry &e = s.at(N, r, i, 0);
+                e.obj = md(r - i, N);
+                e.src = i == 0 ? r : md(r - 1, N);
+                e.dst = i < N - 1 ? md(r + 1, N) : -1;
+            }
+        return;
+    }
+    int a, b;
+    hop_split(N, &a, &b);
+    s.steps = a + 1; s.streams = 2;
+    s.e.assign(size_t(N) * s.steps * 2, StepEntry{});
+    for (int r = 0; r < N; ++r) {
+        s.at(N, r, 0, 0) = StepEntry{r, r, a >= 1 ? md(r + 1, N) : -1};
+        s.at(N, r, 0, 1) = StepEntry{r, r, b >= 1 ? md(r - 1, N) : -1};
+        for (int i = 1; i <= a; ++i)
+            s.at(N, r, i, 0) = StepEntry{md(r - i, N), md(r - 1, N), i < a ? md(r + 1, N) : -1};
+        for (int i = 1; i <= b; ++i)
+            s.at(N, r, i, 1) = StepEntry{md(r + i, N), md(r + 1, N), i < b ? md(r - 1, N) : -1};
+    }
+}
+
+void build_rs_schedule(PlanImpl &p) {
+    const int N = p.N;
+    Schedule &s = p.sched[CM_OP_GEMM_RS];
+    if (p.dir == CM_RING_NONE) {
+        s.steps = 1; s.streams = 1;
+        s.e.assign(size_t(N), StepEntry{});
+        return;
+    }
+    if (p.dir == CM_RING_UNI) {
+        s.steps = N; s.streams = 1;
+        s.e.assign(size_t(N) * N, StepEntry{});
+        for (int r = 0; r < N; ++r)
+            for (int i = 0; i < N; ++i) {
+                StepEntry &e = s.at(N, r, i, 0);
+                e.obj = md(r - i - 1, N);
+                e.src = i == 0 ? -1 : md(r - 1, N);
+                e.dst = i < N - 1 ? md(r + 1, N) : -1;
+            }
+        return;
+    }
+    int a, b;
+    hop_split(N, &a, &b);
+    s.steps = a + 1; s.streams = 2;
+    s.e.assign(size_t(N) * s.steps * 2, StepEntry{});
+    for (int r = 0; r < N; ++r) {
+        for (int i = 0; i < a; ++i)
+            s.at(N, r, i, 0) = StepEntry{md(r + a - i, N), i == 0 ? -1 : md(r - 1, N), md(r + 1, N)};
+        s.at(N, r, a, 0) = StepEntry{r, a >= 1 ? md(r - 1, N) : -1, -1};   // owner
+        for (int i = 0; i < b; ++i)
+            s.at(N, r, i, 1) = StepEntry{md(r - b + i, N), i == 0 ? -1 : md(r + 1, N), md(r - 1, N)};
+    }
+}
+
+cm_task blank_task(int rank, int step, int stream) {
+    cm_task t;
+    std::memset(&t, 0, sizeof t);
+    t.rank = int16_t(rank);
+    t.out_buf = -1;
+    t.in_buf[0] = t.in_buf[1] = -1;
+    t.fwd_slot[0] = t.fwd_slot[1] = -1;
+    t.wait_in[0] = t.wait_in[1] = -1;
+    t.wait_free[0] = t.wait_free[1] = -1;
+    t.sig_fwd[0] = t.sig_fwd[1] = -1;
+    t.sig_done = -1;
+    t.step = int16_t(step);
+    t.stream = int16_t(stream);
+    return t;
+}
+
+struct Ids {
+    int N, S;
+    // flag id of family `kind` for (rank, step, stream)
+    int fid(int kind, int r, int i, int d) const { return ((kind * N + r) * S + i) * 2 + d; }
+};
+
+void order_and_index(PlanImpl &p, int op, std::vector<cm_task> &tasks) {
+    std::stable_sort(tasks.begin(), tasks.end(), [](const cm_task &x, const cm_task &y) {
+        if (x.step != y.step) return x.step < y.step;
+        if (x.out_idx != y.out_idx) return x.out_idx < y.out_idx;
+        return x.stream < y.stream;
+    });
+    auto &sb = p.step_begin[op];
+    sb.assign(size_t(p.sched[op].steps) + 1, int(tasks.size()));
+    for (int t = int(tasks.size()) - 1; t >= 0; --t) sb[tasks[size_t(t)].step] = t;
+    for (int i = int(sb.size()) - 2; i >= 0; --i) sb[size_t(i)] = std::min(sb[size_t(i)], sb[size_t(i) + 1]);
+}
+
+void build_ag_tasks(PlanImpl &p) {
+    const int N = p.N;
+    const Schedule &s = p.sched[CM_OP_AG_GEMM];
+    const int S = s.steps, D = s.streams;
+    Ids ids{N, S};
+    p.flag_ids[CM_OP_AG_GEMM] = 2 * N * S * 2;
+    std::vector<cm_task> tasks;
+    auto slot = [&](int r, int d, int parity) { return (r * D + d) * 2 + parity; };
+    if (p.dir == CM_RING_NONE) {
+        for (int r = 0; r < N; ++r) {
+            cm_task t = blank_task(r, 0, 0);
+            t.a_src = 0; t.a_slab = 0; t.out_idx = 0;   // all N shards as one row block
+            tasks.push_back(t);
+        }
+    } else {
+        for (int r = 0; r < N; ++r) {
+            // step 0: the own shard, read in place, forwarded on every stream that has hops
+            cm_task t = blank_task(r, 0, 0);
+            t.a_src = 0; t.a_slab = int16_t(r); t.out_idx = int16_t(r);
+            for (int d = 0; d < D; ++d) {
+                const StepEntry &e = s.at(N, r, 0, d);
+                if (e.dst < 0) continue;
+                t.fwd_slot[d] = int16_t(slot(e.dst, d, 1));
+                t.sig_fwd[d] = int16_t(ids.fid(kFlagReady, e.dst, 1, d));
+            }
+            tasks.push_back(t);
+            for (int i = 1; i < S; ++i)
+                for (int d = 0; d < D; ++d) {
+                    const StepEntry &e = s.at(N, r, i, d);
+                    if (e.obj < 0) continue;
+                    cm_task u = blank_task(r, i, d);
+                    u.a_src = 1; u.a_slab = int16_t(slot(r, d, i % 2)); u.out_idx = int16_t(e.obj);
+                    u.wait_in[0] = int16_t(ids.fid(kFlagReady, r, i, d));
+                    u.sig_done = int16_t(ids.fid(kFlagReadDone, r, i, d));
+                    if (e.dst >= 0) {
+                        u.fwd_slot[0] = int16_t(slot(e.dst, d, (i + 1) % 2));
+                        u.sig_fwd[0] = int16_t(ids.fid(kFlagReady, e.dst, i + 1, d));
+                        // the slot last held what e.dst used at step i-1 (slots exist from step 1)
+                        if (i - 1 >= 1) u.wait_free[0] = int16_t(ids.fid(kFlagReadDone, e.dst, i - 1, d));
+                    }
+                    tasks.push_back(u);
+                }
+        }
+    }
+    order_and_index(p, CM_OP_AG_GEMM, tasks);
+    p.tasks[CM_OP_AG_GEMM] = tasks;
+}
+
+void build_rs_tasks(PlanImpl &p) {
+    const int N = p.N;
+    const Schedule &s = p.sched[CM_OP_GEMM_RS];
+    const int S = s.steps, D = s.streams;
+    Ids ids{N, S};
+    p.flag_ids[CM_OP_GEMM_RS] = N * S * 2;
+    std::vector<cm_task> tasks;
+    auto acc = [&](int r, int d, int parity) { return (r * D + d) * 2 + parity; };
+    if (p.dir == CM_RING_NONE) {
+        for (int o = 0; o < N; ++o) {
+            cm_task t = blank_task(o, 0, 0);
+            t.a_src = 2; t.a_slab = 0; t.out_idx = int16_t(o);   // sum over every rank in TMEM
+            tasks.push_back(t);
+        }
+    } else {
+        int a = N - 1, b = 0;
+        if (p.dir == CM_RING_BIDI) hop_split(N, &a, &b);
+        for (int r = 0; r < N; ++r)
+            for (int i = 0; i < S; ++i)
+                for (int d = 0; d < D; ++d) {
+                    const StepEntry &e = s.at(N, r, i, d);
+                    if (e.obj < 0) continue;
+                    cm_task t = blank_task(r, i, d);
+                    t.a_src = 0; t.a_slab = int16_t(r * N + e.obj); t.out_idx = int16_t(e.obj);
+                    t.sig_done = int16_t(ids.fid(kFlagDone, r, i, d));
+                    const bool owner = e.dst < 0;
+                    if (!owner) {
+                        // partial bucket goes to the next rank of this stream
+                        t.out_buf = int16_t(acc(e.dst, d, (i + 1) % 2));
+                        if (i >= 2) t.wait_free[0] = int16_t(ids.fid(kFlagDone, e.dst, i - 1, d));
+                        if (i > 0) {
+                            t.in_buf[0] = int16_t(acc(r, d, i % 2));
+                            t.wait_in[0] = int16_t(ids.fid(kFlagDone, e.src, i - 1, d));
+                        }
+                    } else if (p.dir == CM_RING_UNI) {
+                        if (i > 0) {
+                            t.in_buf[0] = int16_t(acc(r, 0, i % 2));
+                            t.wait_in[0] = int16_t(ids.fid(kFlagDone, e.src, i - 1, 0));
+                        }
+                    } else {
+                        // realigning addition: clockwise partial arrived at step a,
+                        // counter-clockwise partial at step b
+                        if (a >= 1) {
+                            t.in_buf[0] = int16_t(acc(r, 0, a % 2));
+                            t.wait_in[0] = int16_t(ids.fid(kFlagDone, md(r - 1, N), a - 1, 0));
+                        }
+                        if (b >= 1) {
+                            t.in_buf[1] = int16_t(acc(r, 1, b % 2));
+                            t.wait_in[1] = int16_t(ids.fid(kFlagDone, md(r + 1, N), b - 1, 1));
+                        }
+                    }
+                    tasks.push_back(t);
+                }
+    }
+    order_and_index(p, CM_OP_GEMM_RS, tasks);
+    p.tasks[CM_OP_GEMM_RS] = tasks;
+}
+
+void apply_skip(PlanImpl &p) {
+    if (p.skip_signal < 0) return;
+    const int op = int((p.skip_signal >> 16) & 0xff);
+    const int rank = int((p.skip_signal >> 8) & 0xff);
+    const int step = int(p.skip_signal & 0xff);
+    if (op > 1) return;
+    for (cm_task &t : p.tasks[op])
+        if (t.rank == rank && t.step == step) {
+            t.sig_fwd[0] = t.sig_fwd[1] = -1;
+            t.sig_done = -1;
+        }
+}
+
+}  // namespace
+
+void rebuild(PlanImpl &p) {
+    build_ag_schedule(p);
+    build_rs_schedule(p);
+    build_ag_tasks(p);
+    build_rs_tasks(p);
+    apply_skip(p);
+}
+
+}  // namespace cm
+
+extern "C" {
+
+cm_status cm_plan(int n_ranks, int chunks, cm_direction dir, cm_plan_t *out) {
+    if (!out) return CM_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (n_ranks < 1 || n_ranks > CM_MAX_RANKS || chunks < 1 || chunks > CM_MAX_CHUNKS)
+        return CM_ERR_INVALID_ARG;
+    if (dir != CM_RING_UNI && dir != CM_RING_BIDI && dir != CM_RING_NONE) return CM_ERR_INVALID_ARG;
+    cm_plan_s *p = new (std::nothrow) cm_plan_s();
+    if (!p) return CM_ERR_INVALID_ARG;
+    p->impl.N = n_ranks;
+    p->impl.chunks = dir == CM_RING_NONE ? 1 : chunks;
+    p->impl.dir = dir;
+    try {
+        cm::rebuild(p->impl);
+    } catch (...) {
+        delete p;
+        return CM_ERR_INVALID_ARG;
+    }
+    *out = p;
+    return CM_OK;
+}
+
+cm_status cm_plan_destroy(cm_plan_t plan) {
+    delete plan;
+    return CM_OK;
+}
+
+int cm_plan_steps(cm_plan_t plan, cm_op op) {
+    if (!plan || (op != CM_OP_AG_GEMM && op != CM_OP_GEMM_RS)) return -1;
+    return plan->impl.sched[op].steps;
+}
+
+cm_status cm_plan_step(cm_plan_t plan, cm_op op, int rank, int step, int stream,
+                       int *obj, int *src, int *dst) {
+    if (!plan || (op != CM_OP_AG_GEMM && op != CM_OP_GEMM_RS)) return CM_ERR_INVALID_ARG;
+    const cm::PlanImpl &p = plan->impl;
+    const cm::Schedule &s = p.sched[op];
+    if (rank < 0 || rank >= p.N || step < 0 || step >= s.steps || stream < 0 || stream > 1)
+        return CM_ERR_INVALID_ARG;
+    cm::StepEntry e;
+    if (stream < s.streams) e = s.at(p.N, rank, step, stream);
+    if (obj) *obj = e.obj;
+    if (src) *src = e.src;
+    if (dst) *dst = e.dst;
+    return CM_OK;
+}
+
+int cm_plan_tasks(cm_plan_t plan, cm_op op, cm_task *out, int capacity) {
+    if (!plan || (op != CM_OP_AG_GEMM && op != CM_OP_GEMM_RS)) return -1;
+    const auto &t = plan->impl.tasks[op];
+    for (int i = 0; i < capacity && i < int(t.size()); ++i) out[i] = t[size_t(i)];
+    return int(t.size());
+}
+
+cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
+    if (!plan) return CM_ERR_INVALID_ARG;
+    cm::PlanImpl &p = plan->impl;
+    switch (option) {
+        case CM_OPT_TIMEOUT_NS:
+            if (value <= 0) return CM_ERR_INVALID_ARG;
+            p.timeout_ns = value;
+            return CM_OK;
+        case CM_OPT_SERIAL_STEPS:
+            p.serial_steps = value != 0;
+            return CM_OK;
+        case CM_OPT_GRID:
+            if (value < 0) return CM_ERR_INVALID_ARG;
+            p.grid = int(value);
+            return CM_OK;
+        case CM_OPT_SKIP_SIGNAL:
+            p.skip_signal = value < 0 ? -1 : value;
+            try {
+                cm::rebuild(p);
+            } catch (...) {
+                return CM_ERR_INVALID_ARG;
+            }
+            return CM_OK;
+    }
+    return CM_ERR_INVALID_ARG;
+}
+
+}  // extern "C"

@@ -1,0 +1,226 @@
+/*
+ * cm.h -- C ABI of the decomposed collective matmul on one GB300 (sm_103a).
+ *
+ * Two operations, each over N logical ranks whose buffers all live in one
+ * GPU's HBM:
+ *
+ *  AllGather -> GEMM (cm_ag_gemm).  Rank r holds the row shard X_r [m, K] of
+ *  an activation that is gathered along rows, and its weight shard W_r
+ *  [K, n]; it needs Y_r = concat_j(X_j) @ W_r [N*m, n].  The decomposition
+ *  ("Overlap Communication with Dependent Computation via Decomposition in
+ *  Large Deep Learning Models", section "The idea", AllGather -> Einsum;
+ *  "Hiding Tensor-Parallel Collectives: AG/RS Overlap in Megatron",
+ *  section 3) runs N steps: at step i rank r multiplies the shard it holds
+ *  and writes the product into that shard's rows of Y_r (a
+ *  DynamicUpdateSlice), while forwarding the shard to its ring neighbour.
+ *
+ *  GEMM -> ReduceScatter (cm_gemm_rs).  Rank r holds X_r [M, k] and W_r
+ *  [k, n]; bucket o (rows o*M/N .. (o+1)*M/N - 1) of sum_r X_r @ W_r belongs
+ *  to rank o.  The decomposition (same page, Einsum -> ReduceScatter; "Hiding
+ *  Tensor-Parallel Collectives", section 5) circulates fp32 accumulating
+ *  buckets: a rank adds its partial product to the bucket it received and
+ *  forwards it; after N hops the bucket is home and is written out.
+ *
+ * Ring schedules (cm_plan):
+ *  - CM_RING_UNI: one ring, rank r sends to r+1 (mod N), receives from r-1.
+ *  - CM_RING_BIDI: the N-1 foreign shards / contributions are split between
+ *    a clockwise stream of a = ceil((N-1)/2) hops and a counter-clockwise
+ *    stream of b = floor((N-1)/2) hops (same page, bidirectional rings; the
+ *    owner's "realigning addition" of section "What it costs" adds the two
+ *    partial buckets and its own product).
+ *  - CM_RING_NONE: the undecomposed operation ("Hiding Tensor-Parallel
+ *    Collectives", sections 2 and 4): every shard is read in place and each
+ *    output is one GEMM (for ReduceScatter, all ranks' products summed in
+ *    one fp32 accumulator).  The monolithic comparator.
+ *  - chunks: each shard (AG) or bucket (RS) moves and is signalled as
+ *    `chunks` contiguous row blocks ("Hiding Tensor-Parallel Collectives",
+ *    section 3, the chunk-size trade-off).  Results do not depend on it.
+ *
+ * Conventions shared by every call:
+ *  - Ownership: the caller owns every device buffer (inputs, outputs,
+ *    workspace).  The library owns only the host-side plan.  No call
+ *    allocates device memory.
+ *  - Asynchrony: compute calls enqueue work on `stream` and return; argument
+ *    errors are returned synchronously; device-side errors (a bounded wait
+ *    that timed out) are reported by cm_check_status.
+ *  - Pointers are device pointers unless stated, 16-byte aligned.
+ *  - bf16 inputs, fp32 accumulation (tensor memory), output bf16 (RNE) or fp32.
+ *  - No C++ exception crosses this boundary.
+ */
+#ifndef CM_H_
+#define CM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum cm_status {
+    CM_OK = 0,
+    CM_ERR_INVALID_ARG = 1,   /* null / out-of-range argument */
+    CM_ERR_SHAPE = 2,         /* shape not divisible as required */
+    CM_ERR_ALIGNMENT = 3,     /* pointer or inner extent misaligned for TMA */
+    CM_ERR_UNSUPPORTED = 4,   /* legal request this build does not run */
+    CM_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
+    CM_ERR_TIMEOUT = 6,       /* a device-side bounded wait expired */
+    CM_ERR_WORKSPACE = 7      /* workspace null or smaller than required */
+} cm_status;
+
+typedef enum cm_direction {
+    CM_RING_UNI = 0,
+    CM_RING_BIDI = 1,
+    CM_RING_NONE = 2
+} cm_direction;
+
+typedef enum cm_dtype { CM_BF16 = 0, CM_F32 = 1 } cm_dtype;
+
+/* Weight layout per rank: CM_W_KN = W_r stored [K][n] row-major;
+ * CM_W_NK = W_r stored [n][K] (nn.Linear order, K contiguous). */
+typedef enum cm_wlayout { CM_W_KN = 0, CM_W_NK = 1 } cm_wlayout;
+
+typedef enum cm_op { CM_OP_AG_GEMM = 0, CM_OP_GEMM_RS = 1 } cm_op;
+
+typedef struct cm_plan_s *cm_plan_t;
+typedef struct CUstream_st *cm_stream_t;   /* identical to cudaStream_t */
+
+/* Largest N a plan accepts, and largest chunk count. */
+#define CM_MAX_RANKS 16
+#define CM_MAX_CHUNKS 8
+
+/*
+ * cm_plan -- build the ring schedule for N logical ranks.  Host only; no
+ * device work.  n_ranks in [1, CM_MAX_RANKS], chunks in [1, CM_MAX_CHUNKS].
+ * On success *out owns a plan to be released with cm_plan_destroy.
+ * Errors: CM_ERR_INVALID_ARG.
+ */
+cm_status cm_plan(int n_ranks, int chunks, cm_direction dir, cm_plan_t *out);
+
+/* Release a plan (NULL is accepted). */
+cm_status cm_plan_destroy(cm_plan_t plan);
+
+/* Number of ring steps of `op` under this plan (N for the unidirectional
+ * ring, ceil((N-1)/2)+1 for the bidirectional one, 1 for CM_RING_NONE). */
+int cm_plan_steps(cm_plan_t plan, cm_op op);
+
+/*
+ * cm_plan_step -- the schedule entry of `rank` at `step` on ring stream
+ * `stream` (0 = clockwise, r -> r+1; 1 = counter-clockwise, r -> r-1).
+ *  *obj: shard (AG) or bucket (RS) id the rank multiplies for, -1 if idle.
+ *  *src: rank the shard / partial bucket came from (AG: the rank itself at
+ *        step 0; RS: -1 when the rank starts the bucket).
+ *  *dst: rank it is forwarded to after this step, -1 if it goes no further
+ *        (RS: -1 means the bucket is home and written to the output).
+ * At step 0 of a bidirectional AG plan the own shard is listed on both
+ * streams (it is sent both ways) and multiplied once.  In a bidirectional RS
+ * plan the owner's entry at the last step lists the clockwise source; the
+ * owner also adds the partial bucket that came counter-clockwise.  A
+ * CM_RING_NONE plan has no ring: its single step lists obj = src = dst = -1.
+ * Host only.
+ * Errors: CM_ERR_INVALID_ARG for an out-of-range rank/step/stream.
+ */
+cm_status cm_plan_step(cm_plan_t plan, cm_op op, int rank, int step, int stream,
+                       int *obj, int *src, int *dst);
+
+/*
+ * One entry of the task table the persistent kernel executes, in execution
+ * order (step-major).  A task is one partial GEMM of one rank at one step;
+ * flag ids name per-chunk device counters (word = id * chunks + chunk).
+ * Exposed so tests can check the table's dependency structure on the host.
+ */
+typedef struct cm_task {
+    int16_t rank;          /* r: selects W_r (and Y_r for AG) */
+    int16_t a_slab;        /* AG: shard slab in x / slot slab in workspace; RS: r*N + bucket */
+    int16_t a_src;         /* 0 = one slab of x read in place, 1 = a workspace slot,
+                              2 = every rank's slab summed in one accumulator (RS, no ring) */
+    int16_t out_idx;       /* AG: shard id s (rows s*m of Y_r); RS: bucket id o */
+    int16_t out_buf;       /* RS: accumulator buffer written, -1 = final output y[o] */
+    int16_t in_buf[2];     /* RS: accumulator buffers read (-1 none) */
+    int16_t fwd_slot[2];   /* AG: workspace slots the shard is forwarded into (-1 none) */
+    int16_t wait_in[2];    /* flags that must reach their target before reading inputs */
+    int16_t wait_free[2];  /* flags that must reach their target before overwriting a slot/buffer */
+    int16_t sig_fwd[2];    /* AG: flags bumped once per forwarded row tile */
+    int16_t sig_done;      /* AG: bumped per tile once its slot reads landed; RS: per finished tile */
+    int16_t step;          /* ring step of this task */
+    int16_t stream;        /* 0 clockwise (or own / owner), 1 counter-clockwise */
+    int16_t reserved;      /* 0 */
+} cm_task;
+
+/* Copy the task table of `op` into out[0..capacity); returns the number of
+ * tasks (which may exceed capacity), or -1 for a bad plan/op.  Host only. */
+int cm_plan_tasks(cm_plan_t plan, cm_op op, cm_task *out, int capacity);
+
+/*
+ * Workspace bytes for one call; 0 for a bad plan.  Holds a status word, the
+ * per-chunk flags and, for AG, the receive slots (2 per rank and stream, each
+ * [m][K] bf16); for RS, the circulating fp32 accumulators (2 per rank and
+ * stream, each [M/N][n]).  The caller allocates it (256-byte aligned); its
+ * contents need no initialisation.
+ */
+size_t cm_ag_gemm_workspace_size(cm_plan_t plan, int64_t m, int64_t K);
+size_t cm_gemm_rs_workspace_size(cm_plan_t plan, int64_t M, int64_t n);
+
+/*
+ * cm_ag_gemm -- decomposed AllGather -> GEMM.
+ *  x  [N][m][K] bf16: shard X_j at x + j*m*K (the gathered X is x itself).
+ *  w  N weight shards, bf16: W_r at w + r*K*n, laid out per `wlayout`.
+ *  y  [N][N*m][n] (y_dtype): Y_r at y + r*N*m*n; rows j*m..j*m+m-1 hold X_j @ W_r.
+ *  m % chunks == 0; K and n multiples of 8.  Outputs must not alias inputs
+ *  or the workspace.  Enqueued on `stream`.
+ */
+cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout,
+                     void *y, cm_dtype y_dtype, int64_t m, int64_t K, int64_t n,
+                     void *ws, size_t ws_bytes, cm_stream_t stream);
+
+/*
+ * cm_gemm_rs -- decomposed GEMM -> ReduceScatter.
+ *  x  [N][M][k] bf16: X_r at x + r*M*k.
+ *  w  N weight shards, bf16: W_r at w + r*k*n, laid out per `wlayout`.
+ *  y  [N][M/N][n] (y_dtype): bucket o = rows o*M/N.. of sum_r X_r @ W_r.
+ *  M % N == 0, (M/N) % chunks == 0; k and n multiples of 8.  Accumulation
+ *  across ranks is fp32; the home rank rounds once to y_dtype.
+ */
+cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout,
+                     void *y, cm_dtype y_dtype, int64_t M, int64_t k, int64_t n,
+                     void *ws, size_t ws_bytes, cm_stream_t stream);
+
+/*
+ * cm_check_status -- synchronise `stream` and read the device status word of
+ * the last call that used `ws`.  Returns CM_OK, CM_ERR_TIMEOUT (a bounded
+ * wait expired; the outputs of that call are undefined) or CM_ERR_CUDA.
+ * If info is non-NULL it receives {code, task, chunk, site} of the first
+ * failure.
+ */
+cm_status cm_check_status(const void *ws, cm_stream_t stream, int32_t info[4]);
+
+/* Static English text for a status code. */
+const char *cm_status_string(cm_status status);
+
+/*
+ * Plan options (host only):
+ *  CM_OPT_TIMEOUT_NS     bound of every device-side wait, in ns (default 1e9).
+ *  CM_OPT_SERIAL_STEPS   1: launch one kernel per ring step (step barriers
+ *                        instead of flags between steps); a debugging mode.
+ *  CM_OPT_GRID           persistent grid size, 0 = one CTA per SM.
+ *  CM_OPT_SKIP_SIGNAL    fault injection: value = (op << 16) | (rank << 8) | step;
+ *                        that task never signals its forward/done flags, so
+ *                        its consumers time out.  -1 clears it.
+ */
+typedef enum cm_option {
+    CM_OPT_TIMEOUT_NS = 0,
+    CM_OPT_SERIAL_STEPS = 1,
+    CM_OPT_GRID = 2,
+    CM_OPT_SKIP_SIGNAL = 3
+} cm_option;
+
+cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);
+
+/* Library version string. */
+const char *cm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CM_H_ */

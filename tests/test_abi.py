@@ -1,0 +1,112 @@
+"""The C ABI library loads on a machine without a GPU, exports every symbol
+include/cm.h declares, and rejects bad arguments before any device work."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from collective_matmul_decomposition_gb300 import cm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return cm.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "cm.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(cm_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 12
+    for name in names:
+        assert hasattr(lib, name), name
+    assert sorted(cm.EXPORTS) == names
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in cm.version()
+    for s in range(8):
+        assert cm.status_string(s)
+
+
+def test_plan_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.cm_plan(0, 1, 0, ctypes.byref(h)) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_plan(17, 1, 0, ctypes.byref(h)) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_plan(4, 0, 0, ctypes.byref(h)) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_plan(4, 9, 0, ctypes.byref(h)) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_plan(4, 1, 7, ctypes.byref(h)) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_plan(4, 1, 0, None) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_plan_destroy(None) == cm.CM_OK
+    p = cm.Plan(4, 2, "bidi")
+    with pytest.raises(cm.CMError):
+        p.step(cm.CM_OP_AG_GEMM, 4, 0, 0)
+    with pytest.raises(cm.CMError):
+        p.set_option(cm.CM_OPT_TIMEOUT_NS, 0)
+
+
+def test_steps_counts(lib):
+    for N in range(1, 17):
+        assert cm.Plan(N, 1, "uni").steps(cm.CM_OP_AG_GEMM) == N
+        assert cm.Plan(N, 1, "uni").steps(cm.CM_OP_GEMM_RS) == N
+        assert cm.Plan(N, 1, "bidi").steps(cm.CM_OP_AG_GEMM) == (N - 1 + 1) // 2 + 1
+        assert cm.Plan(N, 1, "none").steps(cm.CM_OP_GEMM_RS) == 1
+
+
+def test_workspace_sizes(lib):
+    p = cm.Plan(8, 1, "uni")
+    m, K = 1024, 8192
+    assert p.ag_workspace_size(m, K) >= 2 * 8 * m * K * 2
+    assert p.rs_workspace_size(8192, 8192) >= 2 * 8 * 1024 * 8192 * 4
+    b = cm.Plan(8, 1, "bidi")
+    assert b.ag_workspace_size(m, K) >= 4 * 8 * m * K * 2
+    assert cm.Plan(8, 1, "none").ag_workspace_size(m, K) < 1 << 20
+    assert cm.Plan(1, 1, "uni").ag_workspace_size(m, K) < 1 << 20
+    assert lib.cm_ag_gemm_workspace_size(None, 1, 1) == 0
+
+
+def test_compute_calls_reject_bad_arguments_without_device_work(lib):
+    p = cm.Plan(2, 2, "uni")
+    fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every check fails first
+    ws = p.ag_workspace_size(64, 256)
+    # null pointers
+    assert lib.cm_ag_gemm(p.handle, None, fake, 1, fake, 0, 64, 256, 512, fake, ws, None) == cm.CM_ERR_INVALID_ARG
+    # K not a multiple of 8
+    assert lib.cm_ag_gemm(p.handle, fake, fake, 1, fake, 0, 64, 250, 512, fake, ws, None) == cm.CM_ERR_ALIGNMENT
+    # m not divisible by chunks
+    assert lib.cm_ag_gemm(p.handle, fake, fake, 1, fake, 0, 63, 256, 512, fake, ws, None) == cm.CM_ERR_SHAPE
+    # workspace too small
+    assert lib.cm_ag_gemm(p.handle, fake, fake, 1, fake, 0, 64, 256, 512, fake, 16, None) == cm.CM_ERR_WORKSPACE
+    # misaligned pointer
+    odd = ctypes.c_void_p((1 << 20) + 8)
+    assert lib.cm_ag_gemm(p.handle, odd, fake, 1, fake, 0, 64, 256, 512, fake, ws, None) == cm.CM_ERR_ALIGNMENT
+    # RS: M not divisible by N
+    wsr = p.rs_workspace_size(128, 512)
+    assert lib.cm_gemm_rs(p.handle, fake, fake, 1, fake, 0, 127, 128, 512, fake, wsr, None) == cm.CM_ERR_SHAPE
+    # RS: bucket rows not divisible by chunks
+    assert lib.cm_gemm_rs(p.handle, fake, fake, 1, fake, 0, 6, 128, 512, fake, wsr, None) == cm.CM_ERR_SHAPE
+    # bad enums
+    assert lib.cm_gemm_rs(p.handle, fake, fake, 5, fake, 0, 128, 128, 512, fake, wsr, None) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_gemm_rs(p.handle, fake, fake, 1, fake, 9, 128, 128, 512, fake, wsr, None) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_check_status(None, None, None) == cm.CM_ERR_INVALID_ARG
+
+
+def test_no_oracle_in_product_path():
+    """The product package never imports the oracle."""
+    pkg = os.path.join(ROOT, "collective_matmul_decomposition_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".cpp", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "cm_oracle" not in text, f

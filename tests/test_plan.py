@@ -1,0 +1,236 @@
+"""Host-side checks of the ring schedules and of the kernel's task table.
+
+* cm_plan_step matches the schedule of the oracle's rank-by-rank ring
+  simulation, which derives its own schedule from the pages.
+* every flag a task waits on is signalled only by tasks of earlier steps, by
+  exactly one task, so the kernel's static tile order cannot deadlock.
+* an event-level simulation runs the task table the way the kernel does --
+  G co-resident CTAs, each walking its tiles in order, flags as counters,
+  slots / accumulator buffers as tagged contents -- under random interleaving
+  and checks that every tile reads the shard or partial bucket it should and
+  that every output ends with each rank's contribution exactly once.
+"""
+
+import random
+
+import pytest
+
+import __graft_entry__
+from collective_matmul_decomposition_gb300 import cm
+from collective_matmul_decomposition_gb300 import inputs as gen
+from oracle import ring
+
+AG, RS = cm.CM_OP_AG_GEMM, cm.CM_OP_GEMM_RS
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    __graft_entry__.build()
+
+
+def _plan_sends(p, op):
+    out = set()
+    streams = 2 if p.direction == "bidi" else 1
+    for r in range(p.N):
+        for i in range(p.steps(op)):
+            for d in range(streams):
+                obj, src, dst = p.step(op, r, i, d)
+                if obj >= 0 and dst >= 0:
+                    out.add((i, "cw" if d == 0 else "ccw", r, dst, obj))
+    return out
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 13, 16])
+@pytest.mark.parametrize("direction", ["uni", "bidi"])
+def test_schedule_matches_oracle_ring(N, direction):
+    p = cm.Plan(N, 1, direction)
+    x, w = gen.ag_inputs(N, 2, 8, 2, gen.NORMAL1, gen.NORMAL002, seed=1, w_layout="nk")
+    _, log = ring.ag_gemm_ring(gen.bf16_bits(x), gen.bf16_bits(w), "nk", direction=direction,
+                               return_log=True)
+    assert _plan_sends(p, AG) == {(s, st, a, b, o) for (s, st, a, b, o, q) in log}
+    xr, wr = gen.rs_inputs(N, 2 * N, 8, 2, gen.NORMAL1, gen.NORMAL002, seed=1, w_layout="nk")
+    _, log = ring.gemm_rs_ring(gen.bf16_bits(xr), gen.bf16_bits(wr), "nk", direction=direction,
+                               return_log=True)
+    assert _plan_sends(p, RS) == {(s, st, a, b, o) for (s, st, a, b, o, q) in log}
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 7, 8, 16])
+@pytest.mark.parametrize("direction", ["uni", "bidi"])
+def test_each_rank_uses_each_shard_once(N, direction):
+    p = cm.Plan(N, 1, direction)
+    for op in (AG, RS):
+        tasks = p.tasks(op)
+        assert len(tasks) == N * N
+        pairs = sorted((t.rank, t.out_idx) for t in tasks)
+        assert pairs == sorted((r, s) for r in range(N) for s in range(N))
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("direction", ["uni", "bidi", "none"])
+def test_waits_point_to_earlier_steps(N, direction):
+    p = cm.Plan(N, 2, direction)
+    for op in (AG, RS):
+        tasks = p.tasks(op)
+        steps = [t.step for t in tasks]
+        assert steps == sorted(steps)
+        signallers = {}
+        for t in tasks:
+            sigs = [t.sig_done] + ([t.sig_fwd[0], t.sig_fwd[1]] if op == AG else [])
+            for s in sigs:
+                if s >= 0:
+                    assert s not in signallers, "a flag has one signaller"
+                    signallers[s] = t.step
+        for t in tasks:
+            for f in list(t.wait_in) + list(t.wait_free):
+                if f >= 0:
+                    assert f in signallers, (op, f)
+                    assert signallers[f] < t.step
+
+
+def _simulate(p, op, mtiles, ntiles, grid, seed):
+    """Run the task table like the kernel: returns final outputs (see module doc)."""
+    rnd = random.Random(seed)
+    N, c = p.N, p.chunks
+    tasks = p.tasks(op)
+    tiles = [(ti, q, mt, nt) for ti in range(len(tasks)) for q in range(c)
+             for mt in range(mtiles) for nt in range(ntiles)]
+    flags = {}
+    tgt_ag_in, tgt_ag_free = mtiles, mtiles * ntiles
+    tgt_rs = mtiles * ntiles
+
+    def f(i, q):
+        return flags.get((i, q), 0)
+
+    def bump(i, q):
+        flags[(i, q)] = f(i, q) + 1
+
+    slots = {}     # AG: (slot, q, mt) -> shard id
+    bufs = {}      # RS: (buf, q, mt, nt) -> (bucket, frozenset(contributors))
+    outputs = {}   # AG: (rank, shard, q, mt, nt) -> True ; RS: (bucket, q, mt, nt) -> contributors
+    # per CTA: list of tile indices; cursor; phase within a tile
+    queues = [[t for t in range(len(tiles)) if t % grid == b] for b in range(grid)]
+    cur = [0] * grid
+    phase = [0] * grid
+
+    def try_step(b):
+        if cur[b] >= len(queues[b]):
+            return False
+        ti, q, mt, nt = tiles[queues[b][cur[b]]]
+        t = tasks[ti]
+        if op == AG:
+            if phase[b] == 0:       # load A (needs the slot chunk forwarded)
+                if t.wait_in[0] >= 0 and f(t.wait_in[0], q) < tgt_ag_in:
+                    return False
+                shard = t.a_slab if t.a_src == 0 else slots.get((t.a_slab, q, mt))
+                if p.direction != "none":
+                    assert shard == t.out_idx, f"task {ti} read shard {shard}, wants {t.out_idx}"
+                outputs[(t.rank, t.out_idx, q, mt, nt)] = True
+                if t.sig_done >= 0:
+                    bump(t.sig_done, q)
+                phase[b] = 1
+                return True
+            fwd = nt == 0 and (t.fwd_slot[0] >= 0 or t.fwd_slot[1] >= 0)
+            if fwd:
+                for j in range(2):
+                    if t.fwd_slot[j] >= 0 and t.wait_free[j] >= 0 and f(t.wait_free[j], q) < tgt_ag_free:
+                        return False
+                for j in range(2):
+                    if t.fwd_slot[j] >= 0:
+                        slots[(t.fwd_slot[j], q, mt)] = t.out_idx
+                        if t.sig_fwd[j] >= 0:
+                            bump(t.sig_fwd[j], q)
+        else:
+            if phase[b] == 0:       # main loop: no cross-CTA dependency
+                phase[b] = 1
+                return True
+            for fl in list(t.wait_in) + [t.wait_free[0]]:
+                if fl >= 0 and f(fl, q) < tgt_rs:
+                    return False
+            if t.a_src == 2:
+                contrib = frozenset(range(N))
+            else:
+                contrib = {t.rank}
+                for j in range(2):
+                    if t.in_buf[j] >= 0:
+                        key = (t.in_buf[j], q, mt, nt)
+                        assert key in bufs, f"task {ti} read buffer {key} before any write"
+                        bk, cs = bufs[key]
+                        assert bk == t.out_idx, f"task {ti} read bucket {bk}, wants {t.out_idx}"
+                        assert not (cs & contrib)
+                        contrib |= cs
+                contrib = frozenset(contrib)
+            if t.out_buf >= 0:
+                bufs[(t.out_buf, q, mt, nt)] = (t.out_idx, contrib)
+            else:
+                assert (t.out_idx, q, mt, nt) not in outputs
+                outputs[(t.out_idx, q, mt, nt)] = contrib
+            if t.sig_done >= 0:
+                bump(t.sig_done, q)
+        phase[b] = 0
+        cur[b] += 1
+        return True
+
+    live = list(range(grid))
+    while live:
+        order = live[:]
+        rnd.shuffle(order)
+        progressed = False
+        for b in order:
+            if try_step(b):
+                progressed = True
+                break
+        if not progressed:
+            raise AssertionError(f"deadlock: cursors {cur}")
+        live = [b for b in range(grid) if cur[b] < len(queues[b])]
+    return outputs
+
+
+@pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8])
+@pytest.mark.parametrize("direction", ["uni", "bidi", "none"])
+@pytest.mark.parametrize("chunks", [1, 2, 4])
+@pytest.mark.parametrize("grid", [1, 3, 16])
+def test_protocol_simulation(N, direction, chunks, grid):
+    p = cm.Plan(N, chunks, direction)
+    c = p.chunks
+    mtiles, ntiles = 2, 2
+    for seed in range(3):
+        out = _simulate(p, AG, mtiles, ntiles, grid, seed)
+        if direction != "none":
+            assert len(out) == N * N * c * mtiles * ntiles
+        out = _simulate(p, RS, mtiles, ntiles, grid, seed)
+        assert len(out) == N * c * mtiles * ntiles
+        assert all(v == frozenset(range(N)) for v in out.values())
+
+
+def test_skip_signal_starves_consumer():
+    """Fault injection drops a task's signals: its consumer can never run."""
+    p = cm.Plan(4, 1, "uni")
+    p.set_option(cm.CM_OPT_SKIP_SIGNAL, (AG << 16) | (1 << 8) | 0)
+    with pytest.raises(AssertionError, match="deadlock"):
+        _simulate(p, AG, 1, 1, 4, 0)
+    p.set_option(cm.CM_OPT_SKIP_SIGNAL, -1)
+    _simulate(p, AG, 1, 1, 4, 0)
+
+
+@pytest.mark.parametrize("op", [AG, RS])
+@pytest.mark.parametrize("which", ["wait_in", "wait_free"])
+def test_simulation_catches_a_missing_wait(op, which):
+    """Planted mistake: a task table without one kind of wait must fail the
+    simulation for some interleaving."""
+    p = cm.Plan(5, 1, "uni")
+    real = p.tasks
+
+    def broken(o):
+        ts = real(o)
+        for t in ts:
+            getattr(t, which)[0] = -1
+        return ts
+
+    p.tasks = broken
+    caught = 0
+    for seed in range(12):
+        try:
+            _simulate(p, op, 2, 2, 7, seed)
+        except AssertionError:
+            caught += 1
+    assert caught > 0
