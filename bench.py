@@ -1,0 +1,574 @@
+#!/usr/bin/env python3
+"""Benchmark of the decomposed collective matmul on one GB300.
+
+One step = the whole hot path over one batch: the fc1 AllGather->GEMM
+(cm_ag_gemm) and the fc2 GEMM->ReduceScatter (cm_gemm_rs) of a Megatron-SP
+MLP with h=8192, ffn=28672, s=8192, N=8 logical ranks on the GPU, one chunk
+per shard, unidirectional ring (synthetic bf16 data, inputs resident in HBM).
+
+Prints one JSON line (rank 0).  Metric: TFLOP/s (sum over ranks of 2*M*K*n
+per op), with the roofline of the persistent kernel against the measured
+dense bf16 peak, the same metric end to end through the C ABI with host
+buffers, the oracle timed on the host cores, and SM clocks sampled during the
+timed region.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--sweep]   # the N x chunks x ring sweep, one JSON line per point
+
+For --gpus N > 1 (launched by torch.distributed.run), every rank runs an
+independent replica of the step on its own GPU (the path does not shard
+across GPUs); value = all ranks' FLOPs / max-over-ranks time.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "AG-GEMM / GEMM-RS bf16 TFLOP/s and % of dense tensor peak on 1 GB300"
+UNIT = "TFLOP/s"
+WORKLOAD = "mlp_h8192_ffn28672_s8192"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["cm_kernel.cu", "cm_kernel_pair.cu", "cm_device.cuh", "cm_kernel.cuh", "cm_kernel_common.cuh"]
+
+
+# ---- distributed host logic (also exercised by the gloo tests on CPU) ---------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, world
+
+
+def dist_barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def dist_max(value: float, device=None) -> float:
+    """Max of a float over ranks (the job's time is its slowest rank's)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(flops_per_step_per_rank: float, steps: int, world: int, seconds_max: float) -> float:
+    """Whole-job TFLOP/s: every rank's work over the slowest rank's time."""
+    return flops_per_step_per_rank * steps * world / seconds_max / 1e12
+
+
+# ---- helpers ------------------------------------------------------------------------
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "collective_matmul_decomposition_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic():
+    """Per-launch DRAM bytes from the committed ncu summary, if it matches this kernel."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return d
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.gpu_id is not None:
+            cmd += ["-i", str(self.gpu_id)]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+            os.unlink(self.path)
+        except OSError:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        # samples under load: power well above idle
+        load = [s for s, p in zip(sm, pw) if p is not None and pw and p > 0.5 * max(pw)] or sm
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(pw) if pw else None}
+
+
+def physical_gpu_id(local_rank):
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        if local_rank < len(ids):
+            return ids[local_rank]
+    return local_rank
+
+
+# ---- the workload ---------------------------------------------------------------------
+
+def make_step_inputs(N: int, device):
+    """fc1 AG-GEMM and fc2 GEMM-RS operands (CPU copies kept for the oracle)."""
+    from collective_matmul_decomposition_gb300 import inputs as gen
+    s = gen.mlp_shapes(N)
+    a, r = s["ag"], s["rs"]
+    wl = gen.WORKLOADS[WORKLOAD]
+    x1, w1 = gen.ag_inputs(N, a["m"], a["K"], a["n"], wl["ag"]["x"], wl["ag"]["w"], wl["ag"]["seed"], "nk")
+    x2, w2 = gen.rs_inputs(N, r["M"], r["k"], r["n"], wl["rs"]["x"], wl["rs"]["w"], wl["rs"]["seed"], "nk")
+    return dict(shapes=s, cpu=(x1, w1, x2, w2))
+
+
+def flops(s, N):
+    a, r = s["ag"], s["rs"]
+    ag = 2.0 * N * (N * a["m"]) * a["K"] * a["n"]        # sum over ranks of 2*M*K*n
+    rs = 2.0 * r["M"] * r["k"] * r["n"] * N
+    return ag, rs
+
+
+class Step:
+    """Device buffers and plans of one step; run() enqueues both ops."""
+
+    def __init__(self, N, chunks, direction, data, device):
+        import torch
+        from collective_matmul_decomposition_gb300 import cm
+        self.cm = cm
+        self.N = N
+        s = data["shapes"]
+        a, r = s["ag"], s["rs"]
+        x1, w1, x2, w2 = data["cpu"]
+        self.x1, self.w1 = x1.to(device), w1.to(device)
+        self.x2, self.w2 = x2.to(device), w2.to(device)
+        self.y1 = torch.empty(N, N * a["m"], a["n"], dtype=torch.bfloat16, device=device)
+        self.y2 = torch.empty(N, r["M"] // N, r["n"], dtype=torch.bfloat16, device=device)
+        self.plan = cm.Plan(N, chunks, direction)
+        self.ws1 = torch.empty(self.plan.ag_workspace_size(a["m"], a["K"]), dtype=torch.uint8, device=device)
+        self.ws2 = torch.empty(self.plan.rs_workspace_size(r["M"], r["n"]), dtype=torch.uint8, device=device)
+
+    def ag(self):
+        self.cm.cm_ag_gemm(self.plan, self.x1, self.w1, self.y1, self.ws1, "nk")
+
+    def rs(self):
+        self.cm.cm_gemm_rs(self.plan, self.x2, self.w2, self.y2, self.ws2, "nk")
+
+    def check(self):
+        for ws in (self.ws1, self.ws2):
+            st, info = self.cm.cm_check_status(ws)
+            if st != 0:
+                raise RuntimeError(f"device status {st} {info}")
+
+
+def time_loop(fn, iters, torch, warmup=3):
+    """Mean ms per call of fn() over iters calls after `warmup` untimed calls
+    (CUDA events, synchronised)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(iters):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / iters
+
+
+def oracle_sample(cpu, shapes, N, seconds: float, seed=0):
+    """Time the fp64 oracle on sampled output rows for about `seconds`.
+    Returns (flops done, seconds taken, threads, description)."""
+    import numpy as np
+    import oracle
+    from collective_matmul_decomposition_gb300 import inputs as gen
+    x1, w1, x2, w2 = cpu
+    xb1, wb1, xb2, wb2 = (gen.bf16_bits(t) for t in cpu)
+    a, r = shapes["ag"], shapes["rs"]
+    rng = np.random.default_rng(seed)
+    f_ag_row = 2.0 * a["K"] * a["n"]
+    f_rs_row = 2.0 * r["k"] * r["n"] * N
+
+    def run(n_ag, n_rs):
+        ranks = rng.integers(0, N, n_ag)
+        rows = rng.integers(0, N * a["m"], n_ag)
+        owners = rng.integers(0, N, n_rs)
+        rrows = rng.integers(0, r["M"] // N, n_rs)
+        t0 = time.perf_counter()
+        oracle.ag_gemm_rows(xb1, wb1, ranks, rows, "nk")
+        oracle.gemm_rs_rows(xb2, wb2, owners, rrows, "nk")
+        return time.perf_counter() - t0, n_ag * f_ag_row + n_rs * f_rs_row
+
+    nthr = oracle.threads()
+    dt, fl = run(nthr, max(1, nthr // 4))               # calibration
+    rate = fl / max(dt, 1e-6)
+    target = max(seconds * rate, fl)
+    # same mix as the step: equal flops for the two ops
+    n_ag = max(1, int(target / 2 / f_ag_row))
+    n_rs = max(1, int(target / 2 / f_rs_row))
+    dt, fl = run(n_ag, n_rs)
+    desc = (f"{n_ag} AG-GEMM output rows + {n_rs} GEMM-RS output rows of the {WORKLOAD} step at "
+            f"N={N} (fp64 oracle, OpenMP {nthr} threads)")
+    return fl, dt, nthr, desc
+
+
+# ---- arms -----------------------------------------------------------------------------
+
+def run_reference(args):
+    """The oracle, as it stands, timed on the host cores over bounded samples."""
+    rank, world, _ = dist_env()
+    if world > 1:
+        dist_init("gloo")
+        if rank != 0:
+            return 0
+    import oracle
+    oracle.build()
+    N = 8
+    data = make_step_inputs(N, "cpu")
+    shapes = data["shapes"]
+    budget = args.ref_seconds  # seconds of oracle work for the whole run
+    per_step = budget / max(1, args.steps + args.warmup)
+    for _ in range(args.warmup):
+        oracle_sample(data["cpu"], shapes, N, per_step)
+    tot_f, tot_t, thr, desc = 0.0, 0.0, 1, ""
+    for i in range(args.steps):
+        f, t, thr, desc = oracle_sample(data["cpu"], shapes, N, per_step, seed=i + 1)
+        tot_f += f
+        tot_t += t
+    value = tot_f / tot_t / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tot_t / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": step_config(N, 1, "uni", shapes),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle",
+                             "sample": "each step: " + desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def step_config(N, chunks, direction, shapes):
+    a, r = shapes["ag"], shapes["rs"]
+    return {"workload": WORKLOAD, "logical_ranks": N, "chunks": chunks, "ring": direction,
+            "ops": ["fc1 AG-GEMM", "fc2 GEMM-RS"],
+            "ag": {"x": [N, a["m"], a["K"]], "w": [N, a["n"], a["K"]], "y": [N, N * a["m"], a["n"]]},
+            "rs": {"x": [N, r["M"], r["k"]], "w": [N, r["n"], r["k"]], "y": [N, r["M"] // N, r["n"]]},
+            "w_layout": "nk", "accumulate": "fp32", "out": "bf16",
+            "l2": "inputs larger than L2 (fc1 598 MB, fc2 940 MB of operands per op), no flush",
+            "parallelism": "logical ranks on one GPU; replicas across GPUs"}
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist_init("nccl")
+    device = torch.device("cuda", torch.cuda.current_device())
+    import __graft_entry__
+    __graft_entry__.build()
+    N, chunks, direction = 8, 1, "uni"
+    data = make_step_inputs(N, device)
+    shapes = data["shapes"]
+    f_ag, f_rs = flops(shapes, N)
+    st = Step(N, chunks, direction, data, device)
+
+    def step():
+        st.ag()
+        st.rs()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st.check()
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(physical_gpu_id(local)) as clk:
+        t_start.record()
+        for i in range(K):
+            evs[i][0].record()
+            st.ag()
+            evs[i][1].record()
+            st.rs()
+            evs[i][2].record()
+        t_end.record()
+        torch.cuda.synchronize()
+    dist_barrier()
+    st.check()
+    elapsed = t_start.elapsed_time(t_end) / 1e3
+    elapsed_max = dist_max(elapsed, device)
+    ag_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    rs_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    value = aggregate(f_ag + f_rs, K, world, elapsed_max)
+    clocks = clk.summary()
+
+    peaks, peak_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    launch_ms = statistics.mean(ag_ms + rs_ms)
+    achieved = (f_ag + f_rs) / 2 / (launch_ms / 1e3) / 1e12
+    traffic = ncu_traffic()
+
+    # comparators on the same data: the undecomposed op in this kernel, and cuBLAS
+    iters = max(5, min(20, K))
+    mono = Step(N, 1, "none", {"shapes": shapes, "cpu": data["cpu"]}, device) if rank == 0 else None
+    detail = {}
+    if rank == 0:
+        detail["ag_ms"] = statistics.mean(ag_ms)
+        detail["rs_ms"] = statistics.mean(rs_ms)
+        detail["ag_tflops"] = f_ag / (detail["ag_ms"] / 1e3) / 1e12
+        detail["rs_tflops"] = f_rs / (detail["rs_ms"] / 1e3) / 1e12
+        detail["none_ag_ms"] = time_loop(mono.ag, iters, torch)
+        detail["none_rs_ms"] = time_loop(mono.rs, iters, torch)
+        mono.check()
+        a, r = shapes["ag"], shapes["rs"]
+        X1 = st.x1.reshape(N * a["m"], a["K"])
+        W1 = st.w1.reshape(N * a["n"], a["K"])
+        X2 = st.x2.permute(1, 0, 2).reshape(r["M"], N * r["k"]).contiguous()
+        W2 = st.w2.permute(1, 0, 2).reshape(r["n"], N * r["k"]).contiguous()
+        detail["torch_ag_ms"] = time_loop(lambda: torch.matmul(X1, W1.t()), iters, torch)
+        detail["torch_rs_ms"] = time_loop(lambda: torch.matmul(X2, W2.t()), iters, torch)
+        for op in ("ag", "rs"):
+            detail[f"{op}_vs_torch_time"] = detail[f"{op}_ms"] / detail[f"torch_{op}_ms"]
+            detail[f"{op}_vs_none_time"] = detail[f"{op}_ms"] / detail[f"none_{op}_ms"]
+        del X2, W2
+    del mono
+
+    # end to end through the C ABI with host buffers: pinned H2D of every input,
+    # both calls, D2H of both outputs, host reads the result
+    e2e = None
+    if rank == 0 or world > 1:
+        host_in = [t.pin_memory() for t in data["cpu"]]
+        host_out = [torch.empty(st.y1.shape, dtype=st.y1.dtype).pin_memory(),
+                    torch.empty(st.y2.shape, dtype=st.y2.dtype).pin_memory()]
+        dev_in = [st.x1, st.w1, st.x2, st.w2]
+        h2d = sum(t.numel() * t.element_size() for t in host_in)
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        n_e2e = max(3, min(10, K))
+
+        def e2e_step():
+            for d, h in zip(dev_in, host_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            host_out[0].copy_(st.y1, non_blocking=True)
+            host_out[1].copy_(st.y2, non_blocking=True)
+            torch.cuda.synchronize()
+            return float(host_out[1][0, 0, 0])
+
+        e2e_step()
+        dist_barrier()
+        t0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        dt = time.perf_counter() - t0
+        dt_max = dist_max(dt, device)
+        e2e = {"value": aggregate(f_ag + f_rs, n_e2e, world, dt_max), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": dt / n_e2e * 1e3, "steps": n_e2e}
+        st.check()
+
+    cpu_baseline = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        f, t, thr, desc = oracle_sample(data["cpu"], shapes, N, args.cpu_seconds)
+        cpu_baseline = {"value": f / t / 1e12, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": desc,
+                        "seconds": t}
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": elapsed_max / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded N(0,1) activations, N(0,0.02) weights)",
+        "config": step_config(N, chunks, direction, shapes),
+        "pct_of_peak": value / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic["bytes_per_launch"] if traffic else None,
+                     "kernel": "cm_persistent_kernel (AG and RS launches)",
+                     "peak_source": f"bf16_tflops (burst) of {peak_kind}"},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": 2 * K,
+        "gpu_launch_note": "one persistent kernel per op per step (plus one flag memset each)",
+        "cpu_baseline": cpu_baseline,
+        "detail": detail,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sweep(args):
+    """All points of the MLP sweep: N in {4,8,16} x chunks {1,2,4} x {uni,bidi} x {AG, RS}."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    peaks, kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    for N in (4, 8, 16):
+        data = make_step_inputs(N, device)
+        shapes = data["shapes"]
+        f_ag, f_rs = flops(shapes, N)
+        mono = Step(N, 1, "none", data, device)
+        t_none = {"ag": time_loop(mono.ag, args.steps, torch), "rs": time_loop(mono.rs, args.steps, torch)}
+        mono.check()
+        for direction in ("uni", "bidi"):
+            for chunks in (1, 2, 4):
+                st = Step(N, chunks, direction, data, device)
+                for op, fn, fl in (("ag", st.ag, f_ag), ("rs", st.rs, f_rs)):
+                    for _ in range(args.warmup):
+                        fn()
+                    ms = time_loop(fn, args.steps, torch)
+                    st.check()
+                    tf = fl / (ms / 1e3) / 1e12
+                    print(json.dumps({"sweep": WORKLOAD, "op": op, "N": N, "chunks": chunks, "ring": direction,
+                                      "ms": ms, "tflops": tf, "frac_of_peak": tf / peak,
+                                      "vs_undecomposed_time": ms / t_none[op], "peak_source": kind}), flush=True)
+                del st
+        del mono, data
+        torch.cuda.empty_cache()
+    return 0
+
+
+def run_profile_case(args):
+    """A few calls of one op of one workload, nothing else: the command ncu captures."""
+    import torch
+    import __graft_entry__
+    from collective_matmul_decomposition_gb300 import inputs as gen
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    N = args.ranks
+    if args.workload == WORKLOAD:
+        data = make_step_inputs(N, device)
+    else:
+        wl = gen.WORKLOADS[args.workload]
+        N = wl["N"]
+        a = wl.get("ag") or {"m": 128, "K": 128, "n": 256, "x": gen.NORMAL1, "w": gen.NORMAL002, "seed": 1}
+        r = wl.get("rs") or {"M": 128 * N, "k": 128, "n": 256, "x": gen.NORMAL1, "w": gen.NORMAL002, "seed": 2}
+        x1, w1 = gen.ag_inputs(N, a["m"], a["K"], a["n"], a["x"], a["w"], a["seed"], "nk")
+        x2, w2 = gen.rs_inputs(N, r["M"], r["k"], r["n"], r["x"], r["w"], r["seed"], "nk")
+        data = {"shapes": {"ag": dict(m=a["m"], K=a["K"], n=a["n"]), "rs": dict(M=r["M"], k=r["k"], n=r["n"])},
+                "cpu": (x1, w1, x2, w2)}
+    st = Step(N, args.chunks, args.ring, data, device)
+    fn = st.ag if args.profile == "ag" else st.rs
+    f_ag, f_rs = flops(data["shapes"], N)
+    for _ in range(args.warmup):
+        fn()
+    ms = time_loop(fn, args.steps, torch)
+    st.check()
+    fl = f_ag if args.profile == "ag" else f_rs
+    print(json.dumps({"profile_case": args.workload, "op": args.profile, "N": N, "chunks": args.chunks,
+                      "ring": args.ring, "ms": ms, "tflops": fl / (ms / 1e3) / 1e12}), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--profile", choices=["ag", "rs"], default=None,
+                    help="run only --steps calls of one op (for ncu captures)")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--ranks", type=int, default=8)
+    ap.add_argument("--chunks", type=int, default=1)
+    ap.add_argument("--ring", choices=["uni", "bidi", "none"], default="uni")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="oracle seconds for the cpu_baseline of the default arm")
+    ap.add_argument("--ref-seconds", type=float, default=120.0,
+                    help="oracle seconds for a whole --impl reference run")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)        # at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return run_reference(args)
+    if args.sweep:
+        return run_sweep(args)
+    if args.profile:
+        return run_profile_case(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -20,7 +20,7 @@ CM_RING_UNI, CM_RING_BIDI, CM_RING_NONE = 0, 1, 2
 CM_BF16, CM_F32 = 0, 1
 CM_W_KN, CM_W_NK = 0, 1
 CM_OP_AG_GEMM, CM_OP_GEMM_RS = 0, 1
-CM_OPT_TIMEOUT_NS, CM_OPT_SERIAL_STEPS, CM_OPT_GRID, CM_OPT_SKIP_SIGNAL = 0, 1, 2, 3
+CM_OPT_TIMEOUT_NS, CM_OPT_SERIAL_STEPS, CM_OPT_GRID, CM_OPT_SKIP_SIGNAL, CM_OPT_KERNEL = 0, 1, 2, 3, 4
 CM_MAX_RANKS, CM_MAX_CHUNKS = 16, 8
 
 DIRECTIONS = {"uni": CM_RING_UNI, "bidi": CM_RING_BIDI, "none": CM_RING_NONE}

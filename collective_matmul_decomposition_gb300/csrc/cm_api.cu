@@ -2,6 +2,7 @@
 // and the launch of the persistent kernel.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 
@@ -11,7 +12,9 @@
 namespace cm {
 namespace {
 
-constexpr size_t kStatusBytes = 256;
+constexpr size_t kStatusBytes = 256;   // status word at 0, tile counters at kCounterOff
+constexpr size_t kCounterOff = 64;
+static_assert(kCounterOff + 4 * (CM_MAX_RANKS + 1) <= kStatusBytes, "tile counters fit the status block");
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -57,15 +60,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// bf16 3-D tensor [d2][d1][d0] (d0 contiguous), 128-byte swizzled boxes of b0 x b1.
-bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1) {
+// 3-D tensor [d2][d1][d0] (d0 contiguous) of bf16 (or fp32), 128-byte swizzled boxes of b0 x b1.
+bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
+              bool f32 = false) {
     auto enc = encode_fn();
     if (!enc) return false;
+    const uint64_t es_bytes = f32 ? 4 : 2;
     cuuint64_t dims[3] = {d0, d1, d2};
-    cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    cuuint64_t strides[2] = {d0 * es_bytes, d0 * d1 * es_bytes};
     cuuint32_t box[3] = {b0, b1, 1};
     cuuint32_t es[3] = {1, 1, 1};
-    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, es,
+    CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                     const_cast<void *>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
@@ -73,12 +79,35 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Tile rows of the kernel the plan selects.
+int tile_rows(const PlanImpl &pl) { return pl.kernel == 0 ? pair_rows() : kBM; }
+
+// Row tiles, column tiles and flag targets for the selected kernel.
+void set_tiling(const PlanImpl &pl, int op, KParams &kp, int64_t rows_c, int64_t n) {
+    const int tm = tile_rows(pl);
+    const int per_tile = pl.kernel == 0 ? 2 : 1;   // signals per tile (one per CTA of a pair)
+    kp.mtiles_c = int((rows_c + tm - 1) / tm);
+    kp.ntiles = int((n + kBN - 1) / kBN);
+    kp.tiles_per_task = kp.chunks * kp.mtiles_c * kp.ntiles;
+    if (op == CM_OP_AG_GEMM) {
+        kp.tgt_in = uint32_t(per_tile * kp.mtiles_c);           // forwarded row-tile halves per chunk
+        // reads of a slot chunk: every tile's A loads, plus (CTA pairs) each
+        // forwarder's own copy of its half of every row tile
+        kp.tgt_free = uint32_t(kp.mtiles_c * kp.ntiles + (pl.kernel == 0 ? 2 * kp.mtiles_c : 0));
+    } else {
+        kp.tgt_in = uint32_t(per_tile * kp.mtiles_c * kp.ntiles);   // finished tile halves per chunk
+        kp.tgt_free = kp.tgt_in;
+    }
+}
+
 cm_status run(const PlanImpl &pl, int op, KParams &kp, const WsLayout &l, void *ws, bool b_mn,
               cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CM_ERR_CUDA;
     int sms = 0;
     if (prepare_device(dev, &sms) != cudaSuccess) return CM_ERR_CUDA;
+    int max_clusters = 0;
+    if (pl.kernel == 0 && prepare_pair(dev, &max_clusters) != cudaSuccess) return CM_ERR_CUDA;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     kp.status = reinterpret_cast<uint32_t *>(w8);
     kp.flags = reinterpret_cast<uint32_t *>(w8 + l.flags_off);
@@ -93,13 +122,22 @@ cm_status run(const PlanImpl &pl, int op, KParams &kp, const WsLayout &l, void *
     const int nsteps = int(sb.size()) - 1;
     const int launches = pl.serial_steps ? nsteps : 1;
     for (int i = 0; i < launches; ++i) {
+        // each launch has its own tile counter (zeroed with the flags)
+        kp.tile_counter = reinterpret_cast<uint32_t *>(w8 + kCounterOff) + i;
         kp.task_begin = pl.serial_steps ? sb[size_t(i)] : 0;
         kp.task_end = pl.serial_steps ? sb[size_t(i) + 1] : ntasks;
         if (kp.task_end <= kp.task_begin) continue;
         const int64_t tiles = int64_t(kp.task_end - kp.task_begin) * kp.tiles_per_task;
-        int grid = pl.grid > 0 ? std::min(pl.grid, sms) : sms;
-        if (tiles < grid) grid = int(tiles);
-        if (launch_persistent(kp, b_mn, grid, stream) != cudaSuccess) return CM_ERR_CUDA;
+        if (pl.kernel == 0) {
+            int clusters = pl.grid > 0 ? std::min(pl.grid / 2, max_clusters) : max_clusters;
+            clusters = std::max(1, clusters);
+            if (tiles < clusters) clusters = int(tiles);
+            if (launch_pair(kp, b_mn, clusters, stream) != cudaSuccess) return CM_ERR_CUDA;
+        } else {
+            int grid = pl.grid > 0 ? std::min(pl.grid, sms) : sms;
+            if (tiles < grid) grid = int(tiles);
+            if (launch_persistent(kp, b_mn, grid, stream) != cudaSuccess) return CM_ERR_CUDA;
+        }
     }
     return CM_OK;
 }
@@ -163,13 +201,17 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
         kp.tmA1 = kp.tmA0;
     }
     const bool b_mn = wlayout == CM_W_KN;
+    const uint32_t b_rows = pl.kernel == 0 ? kBN / 2 : kBN;   // a pair CTA stages half the columns
     if (b_mn) {
         if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(K), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     } else {
-        if (!make_map(&kp.tmB, w, uint64_t(K), uint64_t(n), uint64_t(N), kBK, kBN)) return CM_ERR_CUDA;
+        if (!make_map(&kp.tmB, w, uint64_t(K), uint64_t(n), uint64_t(N), kBK, b_rows)) return CM_ERR_CUDA;
     }
     kp.y = y;
     kp.acc = nullptr;
+    kp.x_bytes = static_cast<const uint8_t *>(x);
+    kp.slot_bytes = bufs;
+    kp.row_bytes = K * 2;
     kp.y_rank_stride = int64_t(N) * m * n;
     kp.out_rows_per_idx = none ? int64_t(N) * m : m;
     kp.acc_buf_stride = 0;
@@ -177,15 +219,11 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.N = N;
     kp.chunks = c;
     kp.rows_c = int(rows_c);
-    kp.mtiles_c = int((rows_c + kBM - 1) / kBM);
-    kp.ntiles = int((n + kBN - 1) / kBN);
     kp.kblocks = int((K + kBK - 1) / kBK);
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    kp.tiles_per_task = c * kp.mtiles_c * kp.ntiles;
-    kp.tgt_in = uint32_t(kp.mtiles_c);                    // forwarded row tiles per chunk
-    kp.tgt_free = uint32_t(kp.mtiles_c * kp.ntiles);      // tiles that read a slot chunk
+    set_tiling(pl, CM_OP_AG_GEMM, kp, rows_c, n);
     return run(pl, CM_OP_AG_GEMM, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -214,13 +252,19 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     if (!make_map(&kp.tmA0, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
     kp.tmA1 = kp.tmA0;
     const bool b_mn = wlayout == CM_W_KN;
+    const uint32_t b_rows = pl.kernel == 0 ? kBN / 2 : kBN;
     if (b_mn) {
         if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(k), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     } else {
-        if (!make_map(&kp.tmB, w, uint64_t(k), uint64_t(n), uint64_t(N), kBK, kBN)) return CM_ERR_CUDA;
+        if (!make_map(&kp.tmB, w, uint64_t(k), uint64_t(n), uint64_t(N), kBK, b_rows)) return CM_ERR_CUDA;
     }
     kp.y = y;
     kp.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
+    if (l.buf_bytes > 0) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
+        const int64_t nbufs = int64_t(2) * N * streams_of(pl);
+        if (!make_map(&kp.tmAcc, kp.acc, uint64_t(n), uint64_t(rows_c), uint64_t(nbufs * c), 32, 32, true))
+            return CM_ERR_CUDA;
+    }
     kp.y_rank_stride = 0;
     kp.out_rows_per_idx = Mb;
     kp.acc_buf_stride = Mb * n;
@@ -228,15 +272,11 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.N = N;
     kp.chunks = c;
     kp.rows_c = int(rows_c);
-    kp.mtiles_c = int((rows_c + kBM - 1) / kBM);
-    kp.ntiles = int((n + kBN - 1) / kBN);
     kp.kblocks = int((k + kBK - 1) / kBK);
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    kp.tiles_per_task = c * kp.mtiles_c * kp.ntiles;
-    kp.tgt_in = uint32_t(kp.mtiles_c * kp.ntiles);        // finished tiles per chunk
-    kp.tgt_free = uint32_t(kp.mtiles_c * kp.ntiles);
+    set_tiling(pl, CM_OP_GEMM_RS, kp, rows_c, n);
     return run(pl, CM_OP_GEMM_RS, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
 }
 

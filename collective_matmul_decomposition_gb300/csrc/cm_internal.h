@@ -36,6 +36,7 @@ struct PlanImpl {
     int64_t timeout_ns = 1000000000LL;
     int serial_steps = 0;
     int grid = 0;
+    int kernel = 0;   // 0 CTA-pair tiles, 1 single-CTA tiles
     int64_t skip_signal = -1;
     Schedule sched[2];                    // per cm_op
     std::vector<cm_task> tasks[2];        // per cm_op, execution order

@@ -31,13 +31,13 @@
 // flight, releases TMEM and exits.
 #include <cuda_bf16.h>
 
-#include "cm_device.cuh"
-#include "cm_kernel.cuh"
+#include "cm_kernel_common.cuh"
 
 namespace cm {
 namespace {
 
 using namespace dev;
+using namespace kc;
 
 struct Smem {
     uint8_t *a[kStages];
@@ -46,89 +46,6 @@ struct Smem {
     uint32_t *tmem_slot;
     volatile int *abort;
 };
-
-struct TileCoord {
-    int task, q, mt, nt;
-};
-
-__device__ __forceinline__ TileCoord decode(const KParams &p, int t) {
-    TileCoord c;
-    const int tl = t / p.tiles_per_task;
-    int rem = t - tl * p.tiles_per_task;
-    c.task = p.task_begin + tl;
-    const int per_q = p.mtiles_c * p.ntiles;
-    c.q = rem / per_q;
-    rem -= c.q * per_q;
-    c.mt = rem / p.ntiles;
-    c.nt = rem - c.mt * p.ntiles;
-    return c;
-}
-
-__device__ __forceinline__ uint32_t *flag_ptr(const KParams &p, int id, int q) {
-    return p.flags + size_t(id) * size_t(p.chunks) + size_t(q);
-}
-
-__device__ void report(const KParams &p, uint32_t site, const TileCoord &c) {
-    if (atomicCAS(p.status, 0u, uint32_t(CM_ERR_TIMEOUT)) == 0u) {
-        p.status[1] = uint32_t(c.task);
-        p.status[2] = uint32_t(c.q);
-        p.status[3] = site;
-        __threadfence();
-    }
-}
-
-// Bounded wait on an mbarrier phase.  Returns false (and marks the CTA as
-// aborting) if the bound expires or another thread of the CTA has aborted.
-__device__ bool wait_mbar(const KParams &p, const Smem &s, uint64_t *bar, uint32_t parity, uint32_t site,
-                          const TileCoord &c) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 63u) == 0u) {
-            if (*s.abort) return false;
-            if (globaltimer() - t0 > p.timeout_ns) {
-                report(p, site, c);
-                *s.abort = 1;
-                return false;
-            }
-        }
-    }
-}
-
-// Bounded wait for a cross-CTA counter to reach `target` (acquire).
-__device__ bool wait_flag(const KParams &p, const Smem &s, const uint32_t *f, uint32_t target, uint32_t site,
-                          const TileCoord &c) {
-    if (ld_acquire(f) >= target) return true;
-    const uint64_t t0 = globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (ld_acquire(f) >= target) return true;
-        if ((it & 15u) == 0u) {
-            if (*s.abort) return false;
-            if (ld_relaxed(p.status) != 0u) {   // some CTA gave up: stop waiting
-                *s.abort = 1;
-                return false;
-            }
-            if (globaltimer() - t0 > p.timeout_ns) {
-                report(p, site, c);
-                *s.abort = 1;
-                return false;
-            }
-        }
-        __nanosleep(64);
-    }
-}
-
-// Wait that ignores the abort flag (used only to drain work already issued).
-__device__ void drain_mbar(const KParams &p, uint64_t *bar, uint32_t parity) {
-    const uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer() - t0 > p.timeout_ns) break;
-}
-
-__device__ __forceinline__ int kslices(const KParams &p, const cm_task &tk) {
-    return tk.a_src == 2 ? p.kblocks * p.N : p.kblocks;
-}
 
 template <bool B_MN>
 __device__ void producer(const KParams &p, const Smem &s, int total) {
@@ -142,7 +59,7 @@ __device__ void producer(const KParams &p, const Smem &s, int total) {
         const TileCoord c = decode(p, t);
         const cm_task &tk = p.tasks[c.task];
         if (p.op == 0 && tk.wait_in[0] >= 0) {
-            if (!wait_flag(p, s, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c)) break;
+            if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q)) break;
             fence_proxy_async_global();
         }
         const void *tmA = tk.a_src == 1 ? static_cast<const void *>(&p.tmA1) : static_cast<const void *>(&p.tmA0);
@@ -156,7 +73,7 @@ __device__ void producer(const KParams &p, const Smem &s, int total) {
                 kb = kk - rr * p.kblocks;
                 slab = (rr * p.N + tk.out_idx) * p.chunks + c.q;
             }
-            if (!wait_mbar(p, s, &s.empty[stage], phase ^ 1u, kSiteEmpty, c)) {
+            if (!wait_mbar<false>(p, s.abort, &s.empty[stage], phase ^ 1u, kSiteEmpty, c.task, c.q)) {
                 ok = false;
                 break;
             }
@@ -178,7 +95,7 @@ __device__ void producer(const KParams &p, const Smem &s, int total) {
     }
     // no CTA may exit with a TMA load still writing its shared memory
     for (int i = 0; i < kStages; ++i)
-        if (last_parity[i] >= 0) drain_mbar(p, &s.full[i], uint32_t(last_parity[i]));
+        if (last_parity[i] >= 0) drain_mbar<false>(p, &s.full[i], uint32_t(last_parity[i]));
 }
 
 template <bool B_MN>
@@ -198,13 +115,13 @@ __device__ void mma_issuer(const KParams &p, const Smem &s, int total, uint32_t 
         if (*s.abort) break;
         const TileCoord c = decode(p, t);
         const cm_task &tk = p.tasks[c.task];
-        if (!wait_mbar(p, s, &s.tempty[accb], acc_phase ^ 1u, kSiteTmemEmpty, c)) break;
+        if (!wait_mbar<false>(p, s.abort, &s.tempty[accb], acc_phase ^ 1u, kSiteTmemEmpty, c.task, c.q)) break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(accb * kBN);
         const int nk = kslices(p, tk);
         bool ok = true;
         for (int kk = 0; kk < nk; ++kk) {
-            if (!wait_mbar(p, s, &s.full[stage], phase, kSiteFull, c)) {
+            if (!wait_mbar<false>(p, s.abort, &s.full[stage], phase, kSiteFull, c.task, c.q)) {
                 ok = false;
                 break;
             }
@@ -232,7 +149,7 @@ __device__ void mma_issuer(const KParams &p, const Smem &s, int total, uint32_t 
     }
     // every MMA this thread issued must finish before TMEM is released
     mma_commit(s.drain);
-    drain_mbar(p, s.drain, 0);
+    drain_mbar<false>(p, s.drain, 0);
 }
 
 __device__ void forwarder(const KParams &p, const Smem &s, int total) {
@@ -247,14 +164,14 @@ __device__ void forwarder(const KParams &p, const Smem &s, int total) {
         if (fwd) {
             for (int j = 0; j < 2 && ok; ++j)
                 if (tk.fwd_slot[j] >= 0 && tk.wait_free[j] >= 0)
-                    ok = wait_flag(p, s, flag_ptr(p, tk.wait_free[j], c.q), p.tgt_free, kSiteForwardFlag, c);
+                    ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[j], c.q), p.tgt_free, kSiteForwardFlag, c.task, c.q);
             if (!ok) break;
             fence_proxy_async_global();
         }
         const int nk = kslices(p, tk);
         int pending = -1;
         for (int kk = 0; kk < nk; ++kk) {
-            if (!wait_mbar(p, s, &s.full[stage], phase, kSiteForwardFull, c)) {
+            if (!wait_mbar<false>(p, s.abort, &s.full[stage], phase, kSiteForwardFull, c.task, c.q)) {
                 ok = false;
                 break;
             }
@@ -289,13 +206,6 @@ __device__ void forwarder(const KParams &p, const Smem &s, int total) {
     bulk_wait<0>();
 }
 
-__device__ __forceinline__ void add4(float *v, const float4 &a) {
-    v[0] += a.x;
-    v[1] += a.y;
-    v[2] += a.z;
-    v[3] += a.w;
-}
-
 __device__ void epilogue(const KParams &p, const Smem &s, int total, uint32_t tmem_base) {
     const int et = int(threadIdx.x) - 128;   // 0..127 = row of the tile
     const int ew = et >> 5;                   // warp 4..7 reads TMEM lanes 32*(warp%4)..
@@ -304,13 +214,13 @@ __device__ void epilogue(const KParams &p, const Smem &s, int total, uint32_t tm
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
         const TileCoord c = decode(p, t);
         const cm_task &tk = p.tasks[c.task];
-        bool bad = !wait_mbar(p, s, &s.tfull[accb], acc_phase, kSiteTmemFull, c);
+        bool bad = !wait_mbar<false>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
         if (p.op == 1 && et == 0 && !bad) {
             for (int j = 0; j < 2 && !bad; ++j)
                 if (tk.wait_in[j] >= 0)
-                    bad = !wait_flag(p, s, flag_ptr(p, tk.wait_in[j], c.q), p.tgt_in, kSiteEpilogueFlag, c);
+                    bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q), p.tgt_in, kSiteEpilogueFlag, c.task, c.q);
             if (!bad && tk.wait_free[0] >= 0)
-                bad = !wait_flag(p, s, flag_ptr(p, tk.wait_free[0], c.q), p.tgt_free, kSiteEpilogueFlag, c);
+                bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[0], c.q), p.tgt_free, kSiteEpilogueFlag, c.task, c.q);
         }
         bad = bar_or(1, 128, bad || *s.abort != 0);
         if (bad) break;

@@ -38,10 +38,15 @@ struct KParams {
     CUtensorMap tmA0;   // x: AG shards / RS per-rank row slabs, as [slabs*chunks][rows_c][K]
     CUtensorMap tmA1;   // AG workspace receive slots, same view (loads and forward stores)
     CUtensorMap tmB;    // weights: [N][n][K] (K-major) or [N][K][n] (n-major)
+    CUtensorMap tmAcc;  // RS fp32 accumulators as [bufs*chunks][rows_c][n], 32 x 32 boxes (CTA pairs)
     void *y;
     float *acc;                // RS circulating accumulators
     uint32_t *flags;
     uint32_t *status;
+    uint32_t *tile_counter;    // dynamic tile scheduler (CTA-pair kernel), zero at launch
+    const uint8_t *x_bytes;    // AG: x and the receive slots as bytes (pair forwarder)
+    uint8_t *slot_bytes;
+    int64_t row_bytes;         // bytes per A row (K * 2)
     int64_t y_rank_stride;     // AG: elements between Y_r and Y_{r+1}
     int64_t out_rows_per_idx;  // AG: rows per shard id (m, or N*m undecomposed); RS: rows per bucket
     int64_t acc_buf_stride;    // RS: elements per accumulator buffer
@@ -58,10 +63,15 @@ struct KParams {
     cm_task tasks[kMaxTasks];
 };
 
-// Launch the persistent kernel for tasks [p.task_begin, p.task_end).
+// Single-CTA kernel (128 x 256 tiles): launch for tasks [p.task_begin, p.task_end).
 cudaError_t launch_persistent(const KParams &p, bool b_mn_major, int grid, cudaStream_t stream);
 
 // One-time per-device kernel attributes; returns the SM count.
 cudaError_t prepare_device(int device, int *num_sms);
+
+// CTA-pair kernel (256 x 256 tiles on clusters of two CTAs).
+int pair_rows();
+cudaError_t prepare_pair(int device, int *max_clusters);
+cudaError_t launch_pair(const KParams &p, bool b_mn_major, int clusters, cudaStream_t stream);
 
 }  // namespace cm

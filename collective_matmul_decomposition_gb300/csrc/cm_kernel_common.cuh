@@ -1,0 +1,118 @@
+// cm_kernel_common.cuh -- tile decoding, flags and bounded waits shared by
+// the single-CTA and the CTA-pair persistent kernels.
+#pragma once
+
+#include "cm_device.cuh"
+#include "cm_kernel.cuh"
+
+namespace cm {
+namespace kc {
+namespace {   // internal linkage: each kernel translation unit has its own copy
+
+using namespace dev;
+
+struct TileCoord {
+    int task, q, mt, nt;
+};
+
+// Linear tile index -> (task, chunk, column tile, row tile); row tile fastest,
+// so tiles running together share a weight column block (each W_r column
+// block streams through L2 once per task) and the row tiles that forward
+// (column tile 0) come first in every chunk.
+__device__ __forceinline__ TileCoord decode(const KParams &p, int t) {
+    TileCoord c;
+    const int tl = t / p.tiles_per_task;
+    int rem = t - tl * p.tiles_per_task;
+    c.task = p.task_begin + tl;
+    const int per_q = p.mtiles_c * p.ntiles;
+    c.q = rem / per_q;
+    rem -= c.q * per_q;
+    c.nt = rem / p.mtiles_c;
+    c.mt = rem - c.nt * p.mtiles_c;
+    return c;
+}
+
+__device__ __forceinline__ uint32_t *flag_ptr(const KParams &p, int id, int q) {
+    return p.flags + size_t(id) * size_t(p.chunks) + size_t(q);
+}
+
+__device__ __forceinline__ int kslices(const KParams &p, const cm_task &tk) {
+    return tk.a_src == 2 ? p.kblocks * p.N : p.kblocks;
+}
+
+__device__ __noinline__ void report(const KParams &p, uint32_t site, int task, int q) {
+    if (atomicCAS(p.status, 0u, uint32_t(CM_ERR_TIMEOUT)) == 0u) {
+        p.status[1] = uint32_t(task);
+        p.status[2] = uint32_t(q);
+        p.status[3] = site;
+        __threadfence();
+    }
+}
+
+// Bounded wait on an mbarrier phase (cluster-scope acquire when `cluster`).
+// Returns false -- and marks the CTA as aborting -- if the bound expires, the
+// CTA is already aborting, or another CTA has reported a failure.
+template <bool kCluster>
+__device__ bool wait_mbar(const KParams &p, volatile int *abort, uint64_t *bar, uint32_t parity, uint32_t site,
+                          int task, int q) {
+    auto try_once = [&]() { return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (try_once()) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (try_once()) return true;
+        if ((it & 63u) == 0u) {
+            if (*abort) return false;
+            if ((it & 1023u) == 0u && ld_relaxed(p.status) != 0u) {
+                *abort = 1;
+                return false;
+            }
+            if (globaltimer() - t0 > p.timeout_ns) {
+                report(p, site, task, q);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Bounded wait for a cross-CTA counter to reach `target` (gpu-scope acquire).
+__device__ bool wait_flag(const KParams &p, volatile int *abort, const uint32_t *f, uint32_t target, uint32_t site,
+                          int task, int q) {
+    if (ld_acquire(f) >= target) return true;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (ld_acquire(f) >= target) return true;
+        if ((it & 15u) == 0u) {
+            if (*abort) return false;
+            if (ld_relaxed(p.status) != 0u) {
+                *abort = 1;
+                return false;
+            }
+            if (globaltimer() - t0 > p.timeout_ns) {
+                report(p, site, task, q);
+                *abort = 1;
+                return false;
+            }
+        }
+        __nanosleep(64);
+    }
+}
+
+// Wait that ignores the abort flag (only to drain work already issued).
+template <bool kCluster>
+__device__ void drain_mbar(const KParams &p, uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = globaltimer();
+    while (!(kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)))
+        if (globaltimer() - t0 > p.timeout_ns) break;
+}
+
+__device__ __forceinline__ void add4(float *v, const float4 &a) {
+    v[0] += a.x;
+    v[1] += a.y;
+    v[2] += a.z;
+    v[3] += a.w;
+}
+
+}  // namespace
+}  // namespace kc
+}  // namespace cm

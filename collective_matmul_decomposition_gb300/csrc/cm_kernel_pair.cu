@@ -1,0 +1,685 @@
+// cm_kernel_pair.cu -- the persistent kernel on CTA pairs (tcgen05 .cta_group::2).
+//
+// Same task table and the same per-tile work as the single-CTA kernel, but
+// every output tile is 256 x 256 and belongs to a cluster of two CTAs on two
+// SMs: CTA c of the pair stages rows 128c..128c+127 of the A tile and columns
+// 128c..128c+127 of the B tile, and one tcgen05.mma.cta_group::2 issued by the
+// leader CTA multiplies the whole 256-row tile into both CTAs' tensor memory
+// (each CTA holds its 128 rows x 256 fp32 columns).  Each CTA fetches half the
+// operand bytes per MMA of the single-CTA tile, so a 6-stage ring of 32 KB
+// stages fits in shared memory.
+//
+// Tiles are handed out dynamically: the leader's producer takes the next
+// tile index from a global counter and publishes it to both CTAs through a
+// small shared-memory queue, so clusters that finish early take the next
+// tile in order (the tiles running at any time stay close together, which
+// keeps their operands in L2) and a tile's dependencies are always on tiles
+// handed out earlier.
+//
+// Roles (384 threads per CTA):
+//   warp 0    producer: leader = scheduler + TMA loads of its halves;
+//             peer = TMA loads of its halves.  All loads complete on the
+//             leader's ring barrier; the leader posts the byte count.
+//   warp 1    MMA issuer (leader only): pair MMAs; commits each stage and,
+//             per tile, the accumulator to the barriers of both CTAs.
+//   warp 2    AG forwarder (both CTAs): for the first column tile of each row
+//             tile it copies its CTA's 128 shard rows to the ring neighbour's
+//             receive slot with 1-D TMA bulk copies through two 16 KB buffers,
+//             then releases the slot's ready flag -- the rotation copy in flight
+//             while the partial GEMMs read the shard.
+//   warps 4-11  epilogue (both CTAs): 8 warps, TMEM lane quarter = warp % 4,
+//             column half = (warp - 4) / 4.  AG writes shard rows of Y_r; RS
+//             moves the fp32 bucket through a 4 KB swizzled buffer per warp
+//             with TMA loads and stores.
+// All waits are bounded; see cm_kernel.cu for the failure protocol.
+#include <cuda_bf16.h>
+
+#include "cm_kernel_common.cuh"
+
+namespace cm {
+namespace {
+
+using namespace dev;
+using namespace kc;
+
+constexpr int kPairRows = 256;          // output rows per pair tile
+constexpr int kCtaRows = 128;           // rows staged per CTA
+constexpr int kPStages = 6;
+constexpr int kPThreads = 384;
+constexpr int kPEpiWarps = 8;
+constexpr int kHalfA = kCtaRows * kBK * 2;   // 16 KB
+constexpr int kHalfB = (kBN / 2) * kBK * 2;  // 16 KB
+constexpr int kFwdPiece = 16384;             // forwarder copy granule
+constexpr int kQueue = 6;                    // tile-index queue depth
+constexpr int kPSmemBytes = kPStages * (kHalfA + kHalfB) + 2 * kFwdPiece + 1024 + 1024;
+
+struct PSmem {
+    uint8_t *a[kPStages];
+    uint8_t *b[kPStages];
+    uint8_t *fbuf[2];   // AG: forwarder copy buffers; RS: the same 32 KB as 8 epilogue-warp buffers
+    uint64_t *full, *empty, *tfull, *tempty, *drain, *fbar, *qfull, *qempty, *ebar;
+    volatile int32_t *qtile;
+    uint32_t *tmem_slot;
+    volatile int *abort;
+};
+
+// Consumer side of the tile queue: returns the next tile index (-1 = no more
+// work or failure) and releases the slot on the leader.
+struct QueueReader {
+    int slot = 0;
+    uint32_t phase = 0;
+    uint32_t qempty_leader[kQueue];
+
+    __device__ void init(const PSmem &s) {
+        for (int i = 0; i < kQueue; ++i) qempty_leader[i] = mapa_shared(smem_u32(&s.qempty[i]), 0);
+    }
+    __device__ int next(const KParams &p, const PSmem &s) {
+        int t = -1;
+        if (wait_mbar<true>(p, s.abort, &s.qfull[slot], phase, kSiteEmpty, -1, -1)) t = s.qtile[slot];
+        mbar_arrive_cluster(qempty_leader[slot]);
+        if (++slot == kQueue) {
+            slot = 0;
+            phase ^= 1u;
+        }
+        return t;
+    }
+};
+
+template <bool B_MN>
+__device__ void producer(const KParams &p, const PSmem &s, int total, uint32_t crank) {
+    int stage = 0;
+    uint32_t phase = 0;
+    int last_parity[kPStages];
+    for (int i = 0; i < kPStages; ++i) last_parity[i] = -1;
+    uint32_t full_leader[kPStages];
+    for (int i = 0; i < kPStages; ++i) full_leader[i] = mapa_shared(smem_u32(&s.full[i]), 0);
+    const uint32_t tx_pair = 2u * (uint32_t(p.a_box_rows) * kBK * 2 + kHalfB);
+    QueueReader qr;
+    qr.init(s);
+    int qslot = 0;
+    uint32_t qphase = 0;
+    uint32_t q_peer[kQueue], qfull_peer[kQueue];
+    for (int i = 0; i < kQueue; ++i) {
+        q_peer[i] = mapa_shared(smem_u32(const_cast<int32_t *>(&s.qtile[i])), 1);
+        qfull_peer[i] = mapa_shared(smem_u32(&s.qfull[i]), 1);
+    }
+    for (;;) {
+        int t;
+        if (crank == 0) {   // scheduler: next tile in order, published to both CTAs
+            if (!wait_mbar<true>(p, s.abort, &s.qempty[qslot], qphase ^ 1u, kSiteEmpty, -1, -1)) break;
+            t = int(atomic_add_relaxed(p.tile_counter, 1u));
+            if (t >= total) t = -1;
+            s.qtile[qslot] = t;
+            st_shared_cluster(q_peer[qslot], uint32_t(t));
+            mbar_arrive(&s.qfull[qslot]);
+            mbar_arrive_cluster(qfull_peer[qslot]);
+            if (++qslot == kQueue) {
+                qslot = 0;
+                qphase ^= 1u;
+            }
+        } else {
+            t = qr.next(p, s);
+        }
+        if (t < 0 || *s.abort) break;
+        const TileCoord c = decode(p, t);
+        const cm_task &tk = p.tasks[c.task];
+        if (p.op == 0 && tk.wait_in[0] >= 0) {
+            if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q))
+                break;
+            fence_proxy_async_global();
+        }
+        const void *tmA = tk.a_src == 1 ? static_cast<const void *>(&p.tmA1) : static_cast<const void *>(&p.tmA0);
+        const int row0 = c.mt * kPairRows + int(crank) * kCtaRows;
+        const int n0 = c.nt * kBN + int(crank) * (kBN / 2);
+        const int nk = kslices(p, tk);
+        bool ok = true;
+        for (int kk = 0; kk < nk; ++kk) {
+            int rr = tk.rank, kb = kk, slab = tk.a_slab * p.chunks + c.q;
+            if (tk.a_src == 2) {
+                rr = kk / p.kblocks;
+                kb = kk - rr * p.kblocks;
+                slab = (rr * p.N + tk.out_idx) * p.chunks + c.q;
+            }
+            if (!wait_mbar<true>(p, s.abort, &s.empty[stage], phase ^ 1u, kSiteEmpty, c.task, c.q)) {
+                ok = false;
+                break;
+            }
+            if (crank == 0) mbar_expect_tx(&s.full[stage], tx_pair);
+            tma_load_3d_pair(s.a[stage], tmA, full_leader[stage], kb * kBK, row0, slab);
+            if (B_MN) {
+                for (int j = 0; j < kBN / 2 / 64; ++j)
+                    tma_load_3d_pair(s.b[stage] + j * (64 * kBK * 2), &p.tmB, full_leader[stage], n0 + 64 * j,
+                                     kb * kBK, rr);
+            } else {
+                tma_load_3d_pair(s.b[stage], &p.tmB, full_leader[stage], kb * kBK, n0, rr);
+            }
+            last_parity[stage] = int(phase);
+            if (++stage == kPStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+    }
+    // the leader's ring barriers count both CTAs' loads: once they complete,
+    // no load of this pair is still writing shared memory
+    if (crank == 0)
+        for (int i = 0; i < kPStages; ++i)
+            if (last_parity[i] >= 0) drain_mbar<true>(p, &s.full[i], uint32_t(last_parity[i]));
+}
+
+template <bool B_MN>
+__device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base) {
+    constexpr uint32_t kIdesc = idesc_bf16(kPairRows, kBN, B_MN);
+    constexpr uint32_t kBLbo = B_MN ? 64 * kBK * 2 : 16;
+    constexpr uint32_t kBStep = B_MN ? (16 * 128) >> 4 : 32 >> 4;
+    QueueReader qr;
+    qr.init(s);
+    int stage = 0;
+    uint32_t phase = 0;
+    int accb = 0;
+    uint32_t acc_phase = 0;
+    for (;;) {
+        const int t = qr.next(p, s);
+        if (t < 0 || *s.abort) break;
+        const TileCoord c = decode(p, t);
+        const cm_task &tk = p.tasks[c.task];
+        if (!wait_mbar<true>(p, s.abort, &s.tempty[accb], acc_phase ^ 1u, kSiteTmemEmpty, c.task, c.q)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + uint32_t(accb * kBN);
+        const int nk = kslices(p, tk);
+        bool ok = true;
+        for (int kk = 0; kk < nk; ++kk) {
+            if (!wait_mbar<true>(p, s.abort, &s.full[stage], phase, kSiteFull, c.task, c.q)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t ad = desc_sw128(smem_u32(s.a[stage]), 16, 1024);
+            const uint64_t bd = desc_sw128(smem_u32(s.b[stage]), kBLbo, 1024);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)
+                mma_bf16_pair(d, ad + uint64_t(2 * k), bd + uint64_t(kBStep * k), kIdesc, (kk | k) != 0 ? 1u : 0u);
+            mma_commit_pair_mc(&s.empty[stage], 0x3);
+            if (++stage == kPStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        mma_commit_pair_mc(&s.tfull[accb], 0x3);
+        // AG: both CTAs' A slices of this tile have landed; the slot rows may be reused
+        if (p.op == 0 && tk.sig_done >= 0) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
+        if (++accb == 2) {
+            accb = 0;
+            acc_phase ^= 1u;
+        }
+    }
+    mma_commit_pair(s.drain);
+    drain_mbar<true>(p, s.drain, 0);
+}
+
+__device__ void forwarder(const KParams &p, const PSmem &s, uint32_t crank) {
+    QueueReader qr;
+    qr.init(s);
+    uint32_t fph[2] = {0u, 0u};
+    for (;;) {
+        const int t = qr.next(p, s);
+        if (t < 0 || *s.abort) break;
+        const TileCoord c = decode(p, t);
+        const cm_task &tk = p.tasks[c.task];
+        if (!(c.nt == 0 && (tk.fwd_slot[0] >= 0 || tk.fwd_slot[1] >= 0))) continue;
+        bool ok = true;
+        if (tk.a_src == 1 && tk.wait_in[0] >= 0)   // the shard chunk has arrived here
+            ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteForwardFlag, c.task, c.q);
+        for (int j = 0; j < 2 && ok; ++j)          // the neighbour's slot is no longer read
+            if (tk.fwd_slot[j] >= 0 && tk.wait_free[j] >= 0)
+                ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[j], c.q), p.tgt_free, kSiteForwardFlag, c.task,
+                               c.q);
+        if (!ok) break;
+        fence_proxy_async_global();
+        const int row0 = c.mt * kPairRows + int(crank) * kCtaRows;
+        const int nrows = min(kCtaRows, p.rows_c - row0);
+        if (nrows > 0) {
+            const int64_t rb = p.row_bytes;
+            const uint8_t *src = (tk.a_src == 1 ? p.slot_bytes : p.x_bytes) +
+                                 (int64_t(tk.a_slab * p.chunks + c.q) * p.rows_c + row0) * rb;
+            uint8_t *dst[2] = {nullptr, nullptr};
+            for (int j = 0; j < 2; ++j)
+                if (tk.fwd_slot[j] >= 0)
+                    dst[j] = p.slot_bytes + (int64_t(tk.fwd_slot[j] * p.chunks + c.q) * p.rows_c + row0) * rb;
+            const int64_t bytes = int64_t(nrows) * rb;
+            const int np = int((bytes + kFwdPiece - 1) / kFwdPiece);
+            auto piece = [&](int i) { return uint32_t(min(int64_t(kFwdPiece), bytes - int64_t(i) * kFwdPiece)); };
+            mbar_expect_tx(&s.fbar[0], piece(0));
+            bulk_load(s.fbuf[0], src, piece(0), &s.fbar[0]);
+            for (int i = 0; i < np && ok; ++i) {
+                const int b = i & 1;
+                if (i + 1 < np) {
+                    if (i >= 1) bulk_wait_read<0>();   // the store of piece i-1 has left buffer b^1
+                    mbar_expect_tx(&s.fbar[b ^ 1], piece(i + 1));
+                    bulk_load(s.fbuf[b ^ 1], src + int64_t(i + 1) * kFwdPiece, piece(i + 1), &s.fbar[b ^ 1]);
+                }
+                ok = wait_mbar<false>(p, s.abort, &s.fbar[b], fph[b], kSiteForwardFull, c.task, c.q);
+                fph[b] ^= 1u;
+                if (!ok) break;
+                for (int j = 0; j < 2; ++j)
+                    if (dst[j]) bulk_store(dst[j] + int64_t(i) * kFwdPiece, s.fbuf[b], piece(i));
+                bulk_commit();
+            }
+            bulk_wait<0>();   // the copies are complete in global memory
+            if (!ok) break;
+        }
+        fence_proxy_async_global();
+        for (int j = 0; j < 2; ++j)
+            if (tk.fwd_slot[j] >= 0 && tk.sig_fwd[j] >= 0) red_release_add(flag_ptr(p, tk.sig_fwd[j], c.q), 1u);
+        if (tk.a_src == 1 && tk.sig_done >= 0)   // this forwarder's reads of the slot are done
+            red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
+    }
+    bulk_wait<0>();
+}
+
+// One 32-column slice of one row: add received partial buckets (RS), then
+// store to the next accumulator or to the output (bf16 RNE or fp32).
+__device__ __forceinline__ void epi_slice(const KParams &p, const cm_task &tk, int64_t crow, int col0,
+                                          const uint32_t (&v)[32], const float4 (&in)[2][8]) {
+    float f[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+    int64_t orow;
+    bool to_acc = false;
+    if (p.op == 0) {
+        orow = int64_t(tk.rank) * p.y_rank_stride + (int64_t(tk.out_idx) * p.out_rows_per_idx + crow) * p.n;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            if (tk.in_buf[j] >= 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) add4(f + 4 * i, in[j][i]);
+            }
+        if (tk.out_buf >= 0) {
+            to_acc = true;
+            orow = int64_t(tk.out_buf) * p.acc_buf_stride + crow * p.n;
+        } else {
+            orow = (int64_t(tk.out_idx) * p.out_rows_per_idx + crow) * p.n;
+        }
+    }
+    if (to_acc || p.y_f32) {
+        float4 *dst = reinterpret_cast<float4 *>((to_acc ? p.acc : static_cast<float *>(p.y)) + orow + col0);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (col0 + 4 * i < p.n) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+    } else {
+        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.y) + orow + col0);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (col0 + 8 * i >= p.n) break;
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * i + 2 * h], f[8 * i + 2 * h + 1]);
+                w[h] = *reinterpret_cast<uint32_t *>(&b2);
+            }
+            dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+__device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base, uint32_t crank) {
+    const int e = int(threadIdx.x) / 32 - 4;   // 0..7
+    const int lane = int(threadIdx.x) & 31;
+    const int quad = e & 3;                      // TMEM lanes 32*quad.. (warp % 4)
+    const int half = e >> 2;                     // columns 128*half..
+    const bool leader_thread = e == 0 && lane == 0;
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&s.tempty[0]), 0), mapa_shared(smem_u32(&s.tempty[1]), 0)};
+    QueueReader qr;
+    if (lane == 0) qr.init(s);
+    int accb = 0;
+    uint32_t acc_phase = 0;
+    for (;;) {
+        int t = -1;
+        if (lane == 0) t = qr.next(p, s);
+        t = __shfl_sync(0xffffffffu, t, 0);
+        bool bad = t < 0;
+        TileCoord c = {0, 0, 0, 0};
+        if (!bad) c = decode(p, t);
+        const cm_task &tk = p.tasks[c.task];
+        if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
+        if (p.op == 1 && leader_thread && !bad) {
+            for (int j = 0; j < 2 && !bad; ++j)
+                if (tk.wait_in[j] >= 0)
+                    bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q), p.tgt_in, kSiteEpilogueFlag, c.task,
+                                     c.q);
+            if (!bad && tk.wait_free[0] >= 0)
+                bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[0], c.q), p.tgt_free, kSiteEpilogueFlag, c.task,
+                                 c.q);
+        }
+        bad = bar_or(1, kPEpiWarps * 32, bad || *s.abort != 0);
+        if (bad) break;
+        tc_fence_after();
+
+        const int row = c.mt * kPairRows + int(crank) * kCtaRows + quad * 32 + lane;   // row inside the chunk
+        const bool row_ok = row < p.rows_c;
+        const int64_t crow = int64_t(c.q) * p.rows_c + row;
+        const bool rs_in = p.op == 1 && (tk.in_buf[0] >= 0 || tk.in_buf[1] >= 0);
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+            const int col_local = half * 128 + cb * 32;
+            const int col0 = c.nt * kBN + col_local;
+            float4 in[2][8];
+            const bool live = row_ok && col0 < p.n;
+            if (rs_in && live) {   // issue the partial-bucket loads before the TMEM read
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    if (tk.in_buf[j] >= 0) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            p.acc + int64_t(tk.in_buf[j]) * p.acc_buf_stride + crow * p.n + col0);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            in[j][i] = col0 + 4 * i < p.n ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+            }
+            uint32_t v[32];
+            tmem_ld32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN + col_local), v);
+            tmem_wait_ld();
+            if (live) epi_slice(p, tk, crow, col0, v, in);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader[accb]);
+        if (p.op == 1 && tk.sig_done >= 0) {
+            __threadfence();
+            bar_sync(1, kPEpiWarps * 32);
+            if (leader_thread) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
+        }
+        if (++accb == 2) {
+            accb = 0;
+            acc_phase ^= 1u;
+        }
+    }
+}
+
+
+// Row `row` of a 32 x 32 fp32 box staged by TMA with the 128-byte swizzle:
+// 16-byte chunk j of row r sits at chunk position j ^ (r & 7).
+__device__ __forceinline__ float4 *swz_row(uint8_t *buf, int row) { return reinterpret_cast<float4 *>(buf + row * 128); }
+
+// GEMM -> ReduceScatter epilogue.  The circulating fp32 bucket moves through
+// shared memory by TMA: per 32-column slice each warp loads the received
+// partial bucket(s) for its 32 rows (one 4 KB box), adds the TMEM slice, and
+// TMA-stores the sum to the next rank's receive buffer -- or, at the owner,
+// rounds it into the output.
+__device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base, uint32_t crank) {
+    const int e = int(threadIdx.x) / 32 - 4;   // 0..7
+    const int lane = int(threadIdx.x) & 31;
+    const int quad = e & 3;
+    const int half = e >> 2;
+    const bool leader_thread = e == 0 && lane == 0;
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&s.tempty[0]), 0), mapa_shared(smem_u32(&s.tempty[1]), 0)};
+    uint8_t *buf = s.fbuf[0] + e * 4096;
+    uint64_t *eb = &s.ebar[e];
+    uint32_t eph = 0;
+    bool store_pending = false;   // lane 0: a TMA store may still be reading buf
+    QueueReader qr;
+    if (lane == 0) qr.init(s);
+    int accb = 0;
+    uint32_t acc_phase = 0;
+    for (;;) {
+        int t = -1;
+        if (lane == 0) t = qr.next(p, s);
+        t = __shfl_sync(0xffffffffu, t, 0);
+        bool bad = t < 0;
+        TileCoord c = {0, 0, 0, 0};
+        if (!bad) c = decode(p, t);
+        const cm_task &tk = p.tasks[c.task];
+        if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
+        if (leader_thread && !bad) {
+            for (int j = 0; j < 2 && !bad; ++j)
+                if (tk.wait_in[j] >= 0)
+                    bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q), p.tgt_in, kSiteEpilogueFlag, c.task,
+                                     c.q);
+            if (!bad && tk.wait_free[0] >= 0)
+                bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[0], c.q), p.tgt_free, kSiteEpilogueFlag, c.task,
+                                 c.q);
+        }
+        bad = bar_or(1, kPEpiWarps * 32, bad || *s.abort != 0);
+        if (bad) break;
+        if (lane == 0) fence_proxy_async_global();   // the received buckets were released by other CTAs
+        tc_fence_after();
+
+        const int row_w = c.mt * kPairRows + int(crank) * kCtaRows + quad * 32;   // warp's first row in the chunk
+        const int row = row_w + lane;
+        const bool row_ok = row < p.rows_c;
+        const int64_t crow = int64_t(c.q) * p.rows_c + row;
+#pragma unroll 1
+        for (int cb = 0; cb < 4; ++cb) {
+            const int col_local = half * 128 + cb * 32;
+            const int col0 = c.nt * kBN + col_local;
+            uint32_t v[32];
+            tmem_ld32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN + col_local), v);
+            tmem_wait_ld();
+            if (col0 >= p.n) continue;   // the whole slice lies past the last column
+            float f[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
+            for (int j = 0; j < 2; ++j) {
+                if (tk.in_buf[j] < 0) continue;
+                if (lane == 0) {
+                    if (store_pending) {
+                        bulk_wait_read<0>();
+                        store_pending = false;
+                    }
+                    mbar_expect_tx(eb, 32 * 32 * 4);
+                    tma_load_3d(buf, &p.tmAcc, eb, col0, row_w, tk.in_buf[j] * p.chunks + c.q);
+                }
+                wait_mbar<false>(p, s.abort, eb, eph, kSiteEpilogueFlag, c.task, c.q);
+                eph ^= 1u;
+                float4 *r = swz_row(buf, lane);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) add4(f + 4 * i, r[i ^ (lane & 7)]);
+                __syncwarp();
+            }
+            if (tk.out_buf >= 0) {
+                if (lane == 0 && store_pending) {
+                    bulk_wait_read<0>();
+                    store_pending = false;
+                }
+                __syncwarp();
+                float4 *r = swz_row(buf, lane);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) r[i ^ (lane & 7)] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_3d(&p.tmAcc, buf, col0, row_w, tk.out_buf * p.chunks + c.q);
+                    bulk_commit();
+                    store_pending = true;
+                }
+            } else if (row_ok) {   // owner: the bucket is home
+                const int64_t orow = (int64_t(tk.out_idx) * p.out_rows_per_idx + crow) * p.n;
+                if (p.y_f32) {
+                    float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + orow + col0);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (col0 + 4 * i < p.n) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+                } else {
+                    uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.y) + orow + col0);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (col0 + 8 * i >= p.n) break;
+                        uint32_t w[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * i + 2 * h], f[8 * i + 2 * h + 1]);
+                            w[h] = *reinterpret_cast<uint32_t *>(&b2);
+                        }
+                        dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                }
+            }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader[accb]);
+        if (tk.sig_done >= 0) {
+            if (lane == 0) {
+                bulk_wait<0>();            // this warp's bucket slices are in global memory
+                store_pending = false;
+                fence_proxy_async_global();
+            }
+            __threadfence();
+            bar_sync(1, kPEpiWarps * 32);
+            if (leader_thread) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
+        }
+        if (++accb == 2) {
+            accb = 0;
+            acc_phase ^= 1u;
+        }
+    }
+    if (lane == 0) bulk_wait<0>();
+}
+
+template <bool B_MN>
+__global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_constant__ KParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PSmem s;
+    for (int i = 0; i < kPStages; ++i) {
+        s.a[i] = base + i * kHalfA;
+        s.b[i] = base + kPStages * kHalfA + i * kHalfB;
+    }
+    s.fbuf[0] = base + kPStages * (kHalfA + kHalfB);
+    s.fbuf[1] = s.fbuf[0] + kFwdPiece;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s.fbuf[1] + kFwdPiece);
+    s.full = bars;
+    s.empty = s.full + kPStages;
+    s.tfull = s.empty + kPStages;
+    s.tempty = s.tfull + 2;
+    s.drain = s.tempty + 2;
+    s.fbar = s.drain + 1;
+    s.qfull = s.fbar + 2;
+    s.qempty = s.qfull + kQueue;
+    s.ebar = s.qempty + kQueue;
+    s.qtile = reinterpret_cast<volatile int32_t *>(s.ebar + kPEpiWarps);
+    s.tmem_slot = reinterpret_cast<uint32_t *>(const_cast<int32_t *>(s.qtile) + kQueue);
+    s.abort = reinterpret_cast<volatile int *>(s.tmem_slot + 1);
+
+    const int warp = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
+    const uint32_t crank = cluster_ctarank();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kPStages; ++i) {
+            mbar_init(&s.full[i], 1);
+            mbar_init(&s.empty[i], 1);   // the pair MMA's commit
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s.tfull[i], 1);
+            mbar_init(&s.tempty[i], 2 * kPEpiWarps);   // epilogue warps of both CTAs
+            mbar_init(&s.fbar[i], 1);
+        }
+        mbar_init(s.drain, 1);
+        // queue readers: leader MMA + peer producer + 8 epilogue warps per CTA (+ 2 forwarders)
+        const uint32_t readers = 2 + 2 * kPEpiWarps + (p.op == 0 ? 2 : 0);
+        for (int i = 0; i < kQueue; ++i) {
+            mbar_init(&s.qfull[i], 1);
+            mbar_init(&s.qempty[i], readers);
+        }
+        for (int i = 0; i < kPEpiWarps; ++i) mbar_init(&s.ebar[i], 1);
+        *s.abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&p.tmA0);
+        prefetch_tmap(&p.tmA1);
+        prefetch_tmap(&p.tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(s.tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // both CTAs' barriers exist before any cross-CTA arrive or load
+    tc_fence_after();
+    const uint32_t tmem_base = *s.tmem_slot;
+    const int total = (p.task_end - p.task_begin) * p.tiles_per_task;
+
+    if (warp == 0) {
+        if (lane == 0) producer<B_MN>(p, s, total, crank);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && crank == 0) mma_issuer<B_MN>(p, s, tmem_base);
+        __syncwarp();
+    } else if (warp == 2) {
+        if (lane == 0 && p.op == 0) forwarder(p, s, crank);
+        __syncwarp();
+    } else if (warp >= 4) {
+        if (p.op == 0)
+            epilogue_ag(p, s, tmem_base, crank);
+        else
+            epilogue_rs(p, s, tmem_base, crank);
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();   // no cross-CTA traffic is left when either CTA releases TMEM
+    tc_fence_after();
+    if (warp == 1) {
+        __syncwarp();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+}  // namespace
+
+int pair_rows() { return kPairRows; }
+
+cudaError_t prepare_pair(int device, int *max_clusters) {
+    static int cached[64] = {0};
+    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
+    if (cached[device] == 0) {
+        for (int v = 0; v < 2; ++v) {
+            auto fn = v ? cm_pair_kernel<true> : cm_pair_kernel<false>;
+            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
+            if (e != cudaSuccess) return e;
+        }
+        cudaLaunchConfig_t cfg = {};
+        int sms = 0;
+        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+        if (e != cudaSuccess) return e;
+        cfg.gridDim = dim3(unsigned(sms & ~1), 1, 1);
+        cfg.blockDim = dim3(kPThreads, 1, 1);
+        cfg.dynamicSmemBytes = kPSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        e = cudaOccupancyMaxActiveClusters(&n, cm_pair_kernel<false>, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n <= 0) return cudaErrorInvalidConfiguration;
+        cached[device] = n;
+    }
+    *max_clusters = cached[device];
+    return cudaSuccess;
+}
+
+cudaError_t launch_pair(const KParams &p, bool b_mn_major, int clusters, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned(2 * clusters), 1, 1);
+    cfg.blockDim = dim3(kPThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (b_mn_major) return cudaLaunchKernelEx(&cfg, cm_pair_kernel<true>, p);
+    return cudaLaunchKernelEx(&cfg, cm_pair_kernel<false>, p);
+}
+
+}  // namespace cm

@@ -339,6 +339,10 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
             if (value < 0) return CM_ERR_INVALID_ARG;
             p.grid = int(value);
             return CM_OK;
+        case CM_OPT_KERNEL:
+            if (value != 0 && value != 1) return CM_ERR_INVALID_ARG;
+            p.kernel = int(value);
+            return CM_OK;
         case CM_OPT_SKIP_SIGNAL:
             p.skip_signal = value < 0 ? -1 : value;
             try {

@@ -206,12 +206,16 @@ const char *cm_status_string(cm_status status);
  *  CM_OPT_SKIP_SIGNAL    fault injection: value = (op << 16) | (rank << 8) | step;
  *                        that task never signals its forward/done flags, so
  *                        its consumers time out.  -1 clears it.
+ *  CM_OPT_KERNEL         0 (default): 256 x 256 tiles on CTA pairs
+ *                        (tcgen05 cta_group::2, clusters of 2);
+ *                        1: 128 x 256 tiles on single CTAs.
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
     CM_OPT_SERIAL_STEPS = 1,
     CM_OPT_GRID = 2,
-    CM_OPT_SKIP_SIGNAL = 3
+    CM_OPT_SKIP_SIGNAL = 3,
+    CM_OPT_KERNEL = 4
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);

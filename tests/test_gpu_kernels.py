@@ -1,0 +1,77 @@
+"""Both tile kernels (CTA pairs with tcgen05 cta_group::2, and single CTAs)
+against the oracle and against each other."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from collective_matmul_decomposition_gb300 import cm
+from collective_matmul_decomposition_gb300 import inputs as gen
+from test_gpu_parity import TOL_F32, _np, run_ag, run_rs
+
+pytestmark = pytest.mark.gpu
+
+PAIR, SINGLE = 0, 1
+
+
+def _plan(N, chunks, direction, kernel):
+    p = cm.Plan(N, chunks, direction)
+    p.set_option(cm.CM_OPT_KERNEL, kernel)
+    return p
+
+
+@pytest.mark.parametrize("kernel", [PAIR, SINGLE])
+@pytest.mark.parametrize("N,m,K,n,chunks,direction", [
+    (2, 64, 256, 512, 1, "uni"),        # rows per chunk below one CTA's 128
+    (3, 200, 200, 296, 2, "bidi"),      # ragged rows / columns / K
+    (4, 384, 320, 768, 1, "uni"),       # row tiles straddling the pair split
+    (5, 136, 72, 520, 1, "none"),
+])
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+def test_kernel_vs_oracle(kernel, N, m, K, n, chunks, direction, layout):
+    x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=m + K, w_layout=layout)
+    ref = oracle.ag_gemm(gen.bf16_bits(x), gen.bf16_bits(w), layout)
+    y, _, _ = run_ag(_plan(N, chunks, direction, kernel), x, w, layout)
+    assert oracle.normwise_max_rel_err(_np(y), ref) <= TOL_F32
+    xr, wr = gen.rs_inputs(N, N * m, K, n, gen.NORMAL1, gen.NORMAL002, seed=m + K + 1, w_layout=layout)
+    refr = oracle.gemm_rs(gen.bf16_bits(xr), gen.bf16_bits(wr), layout)
+    yr, _, _ = run_rs(_plan(N, chunks, direction, kernel), xr, wr, layout)
+    assert oracle.normwise_max_rel_err(_np(yr), refr) <= TOL_F32
+
+
+def test_pair_and_single_agree_bitwise_on_ag():
+    N, m, K, n = 4, 512, 1024, 1024
+    x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=99, w_layout="nk")
+    a, _, _ = run_ag(_plan(N, 1, "uni", PAIR), x, w, "nk")
+    b, _, _ = run_ag(_plan(N, 1, "uni", SINGLE), x, w, "nk")
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("kernel", [PAIR, SINGLE])
+def test_tagged_placement_each_kernel(kernel):
+    N, m, K, n = 8, 384, 64, 512
+    x, w = gen.tagged_ag_inputs(N, m, K, n, "nk")
+    ref = oracle.ag_gemm(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
+    for direction, chunks in (("uni", 1), ("bidi", 2), ("uni", 4)):
+        y, _, _ = run_ag(_plan(N, chunks, direction, kernel), x, w, "nk", torch.bfloat16)
+        assert np.array_equal(_np(y), ref)
+
+
+@pytest.mark.parametrize("kernel", [PAIR, SINGLE])
+def test_timeout_each_kernel(kernel):
+    N = 4
+    x, w = gen.ag_inputs(N, 256, 128, 256, gen.NORMAL1, gen.NORMAL002, seed=3, w_layout="nk")
+    p = _plan(N, 1, "uni", kernel)
+    p.set_option(cm.CM_OPT_TIMEOUT_NS, 50_000_000)
+    p.set_option(cm.CM_OPT_SKIP_SIGNAL, (cm.CM_OP_AG_GEMM << 16) | (1 << 8) | 0)
+    _, st, info = run_ag(p, x, w, "nk", check=False)
+    assert st == cm.CM_ERR_TIMEOUT, (st, info)
+    xr, wr = gen.rs_inputs(N, 1024, 128, 256, gen.NORMAL1, gen.NORMAL002, seed=4, w_layout="nk")
+    p.set_option(cm.CM_OPT_SKIP_SIGNAL, (cm.CM_OP_GEMM_RS << 16) | (2 << 8) | 1)
+    _, st, info = run_rs(p, xr, wr, "nk", check=False)
+    assert st == cm.CM_ERR_TIMEOUT, (st, info)
+    p.set_option(cm.CM_OPT_SKIP_SIGNAL, -1)
+    ref = oracle.ag_gemm(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
+    y, _, _ = run_ag(p, x, w, "nk")
+    assert oracle.normwise_max_rel_err(_np(y), ref) <= TOL_F32

@@ -92,8 +92,9 @@ def _simulate(p, op, mtiles, ntiles, grid, seed):
     rnd = random.Random(seed)
     N, c = p.N, p.chunks
     tasks = p.tasks(op)
+    # the kernel's order: task, chunk, column tile, row tile (row tile fastest)
     tiles = [(ti, q, mt, nt) for ti in range(len(tasks)) for q in range(c)
-             for mt in range(mtiles) for nt in range(ntiles)]
+             for nt in range(ntiles) for mt in range(mtiles)]
     flags = {}
     tgt_ag_in, tgt_ag_free = mtiles, mtiles * ntiles
     tgt_rs = mtiles * ntiles
