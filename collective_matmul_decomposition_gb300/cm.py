@@ -29,7 +29,9 @@ LAYOUTS = {"kn": CM_W_KN, "nk": CM_W_NK}
 # Every symbol include/cm.h declares.
 EXPORTS = ["cm_plan", "cm_plan_destroy", "cm_plan_steps", "cm_plan_step", "cm_plan_tasks",
            "cm_ag_gemm_workspace_size", "cm_gemm_rs_workspace_size", "cm_ag_gemm", "cm_gemm_rs",
-           "cm_check_status", "cm_status_string", "cm_plan_set_option", "cm_version"]
+           "cm_check_status", "cm_status_string", "cm_plan_set_option", "cm_version",
+           "cm_ag_gemm_noalloc"]
+CM_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class cm_task(ctypes.Structure):
@@ -87,6 +89,8 @@ def load():
     lib.cm_plan_set_option.restype = i32
     lib.cm_version.argtypes = []
     lib.cm_version.restype = ctypes.c_char_p
+    lib.cm_ag_gemm_noalloc.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p]
+    lib.cm_ag_gemm_noalloc.restype = i32
     _lib = lib
     return lib
 
@@ -168,6 +172,17 @@ def cm_ag_gemm(plan: Plan, x, w, y, ws, w_layout: str = "nk", stream=None):
     st = load().cm_ag_gemm(plan.handle, _ptr(x), _ptr(w), LAYOUTS[w_layout], _ptr(y), _ydtype(y),
                            m, K, n, _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream))
     _check(st, "cm_ag_gemm")
+
+
+def cm_ag_gemm_noalloc(plan: Plan, x, w, y, w_layout: str = "nk", stream=None):
+    """cm_ag_gemm without a workspace: for callers that cannot allocate device
+    memory; the library's fixed scratch array (CM_NOALLOC_SCRATCH_BYTES) is
+    used instead, shared by every call (calls must not overlap on the GPU)."""
+    N, m, K = x.shape
+    n = w.shape[1] if w_layout == "nk" else w.shape[2]
+    st = load().cm_ag_gemm_noalloc(plan.handle, _ptr(x), _ptr(w), LAYOUTS[w_layout], _ptr(y), _ydtype(y),
+                                   m, K, n, _stream_ptr(stream))
+    _check(st, "cm_ag_gemm_noalloc")
 
 
 def cm_gemm_rs(plan: Plan, x, w, y, ws, w_layout: str = "nk", stream=None):

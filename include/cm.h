@@ -223,6 +223,29 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);
 /* Library version string. */
 const char *cm_version(void);
 
+/*
+ * cm_ag_gemm_noalloc -- cm_ag_gemm without a workspace argument, for callers
+ * that cannot allocate device memory (for example a plugin that is handed
+ * only its input and output buffers by a framework owning all device memory,
+ * or a loop that must not call cudaMalloc).  The pages have no counterpart:
+ * this is a packaging of the same operation.
+ *  Scratch: one device array of CM_NOALLOC_SCRATCH_BYTES defined in the
+ *  library and held by every GPU that loads it until the process exits.
+ *  Arguments, layouts and results are those of cm_ag_gemm.
+ *  Errors: CM_ERR_WORKSPACE if the call needs more scratch than the array
+ *  holds (checked before any device work); otherwise as cm_ag_gemm.
+ *  The first call on a device looks up the array's address with that device
+ *  current; make it outside any stream capture.  Every call shares the array:
+ *  its status word, flags and counters are cleared on `stream` at the start
+ *  of each call, and calls that may overlap on the GPU race on it.  Only
+ *  argument and launch errors are returned; the array's device status word
+ *  is not exposed, so a device-side wait that expires (which leaves the
+ *  outputs undefined) is not reported to this caller.  Never allocates.
+ */
+#define CM_NOALLOC_SCRATCH_BYTES (64u << 20)
+cm_status cm_ag_gemm_noalloc(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y,
+                             cm_dtype y_dtype, int64_t m, int64_t K, int64_t n, cm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
