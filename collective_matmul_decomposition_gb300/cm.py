@@ -21,6 +21,7 @@ CM_BF16, CM_F32 = 0, 1
 CM_W_KN, CM_W_NK = 0, 1
 CM_OP_AG_GEMM, CM_OP_GEMM_RS = 0, 1
 CM_OPT_TIMEOUT_NS, CM_OPT_SERIAL_STEPS, CM_OPT_GRID, CM_OPT_SKIP_SIGNAL, CM_OPT_KERNEL = 0, 1, 2, 3, 4
+CM_OPT_STATIC_TILES, CM_OPT_TILE_GROUP = 5, 6
 CM_MAX_RANKS, CM_MAX_CHUNKS = 16, 8
 
 DIRECTIONS = {"uni": CM_RING_UNI, "bidi": CM_RING_BIDI, "none": CM_RING_NONE}
@@ -40,7 +41,7 @@ class cm_task(ctypes.Structure):
                 ("in_buf", ctypes.c_int16 * 2), ("fwd_slot", ctypes.c_int16 * 2),
                 ("wait_in", ctypes.c_int16 * 2), ("wait_free", ctypes.c_int16 * 2),
                 ("sig_fwd", ctypes.c_int16 * 2), ("sig_done", ctypes.c_int16),
-                ("step", ctypes.c_int16), ("stream", ctypes.c_int16), ("reserved", ctypes.c_int16)]
+                ("step", ctypes.c_int16), ("stream", ctypes.c_int16), ("tile_group", ctypes.c_int16)]
 
 
 class CMError(RuntimeError):

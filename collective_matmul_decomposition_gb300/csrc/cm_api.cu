@@ -29,7 +29,7 @@ WsLayout ag_layout(const PlanImpl &p, int64_t m, int64_t K) {
     l.flags_bytes = size_t(p.flag_ids[CM_OP_AG_GEMM]) * size_t(p.chunks) * sizeof(uint32_t);
     l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
     const bool ring = p.dir != CM_RING_NONE && p.N > 1;
-    const size_t slots = ring ? size_t(2 * p.N * streams_of(p)) : 0;
+    const size_t slots = ring ? size_t(p.N * streams_of(p) * p.sched[CM_OP_AG_GEMM].steps) : 0;   // one per (rank, stream, step)
     l.buf_bytes = slots * size_t(m) * size_t(K) * 2;
     l.total = l.buf_off + l.buf_bytes;
     return l;
@@ -40,7 +40,7 @@ WsLayout rs_layout(const PlanImpl &p, int64_t M, int64_t n) {
     l.flags_bytes = size_t(p.flag_ids[CM_OP_GEMM_RS]) * size_t(p.chunks) * sizeof(uint32_t);
     l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
     const bool ring = p.dir != CM_RING_NONE && p.N > 1;
-    const size_t bufs = ring ? size_t(2 * p.N * streams_of(p)) : 0;
+    const size_t bufs = ring ? size_t(p.N * streams_of(p) * p.sched[CM_OP_GEMM_RS].steps) : 0;
     l.buf_bytes = bufs * size_t(M / p.N) * size_t(n) * sizeof(float);
     l.total = l.buf_off + l.buf_bytes;
     return l;
@@ -79,39 +79,54 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Tile rows of the kernel the plan selects.
-int tile_rows(const PlanImpl &pl) { return pl.kernel == 0 ? pair_rows() : kBM; }
+// The kernel a call runs: single CTAs, or CTA pairs in clusters of 2 or 4.
+struct KernelChoice {
+    bool pair;
+    int cluster_ctas;   // 2 or 4 for the pair kernel
+};
+
+KernelChoice choose_kernel(const PlanImpl &pl, int64_t n) {
+    (void)n;
+    switch (pl.kernel) {
+        case 1: return {false, 1};
+        case 2: return {true, 2};
+        case 3: return {true, 4};
+        default: return {true, 2};   // measured fastest: one pair per cluster
+    }
+}
 
 // Row tiles, column tiles and flag targets for the selected kernel.
-void set_tiling(const PlanImpl &pl, int op, KParams &kp, int64_t rows_c, int64_t n) {
-    const int tm = tile_rows(pl);
-    const int per_tile = pl.kernel == 0 ? 2 : 1;   // signals per tile (one per CTA of a pair)
+void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int64_t n) {
+    const int tm = kc.pair ? pair_rows() : kBM;
+    const int per_tile = kc.pair ? 2 : 1;   // signals per tile (one per CTA of a pair)
     kp.mtiles_c = int((rows_c + tm - 1) / tm);
     kp.ntiles = int((n + kBN - 1) / kBN);
-    kp.tiles_per_task = kp.chunks * kp.mtiles_c * kp.ntiles;
+    const int pairs = kc.pair ? kc.cluster_ctas / 2 : 1;
+    kp.ntile_groups = (kp.ntiles + pairs - 1) / pairs;   // single CTAs: one column tile per group
+    kp.tiles_per_task = kp.chunks * kp.mtiles_c * kp.ntile_groups;
     if (op == CM_OP_AG_GEMM) {
         kp.tgt_in = uint32_t(per_tile * kp.mtiles_c);           // forwarded row-tile halves per chunk
-        // reads of a slot chunk: every tile's A loads, plus (CTA pairs) each
-        // forwarder's own copy of its half of every row tile
-        kp.tgt_free = uint32_t(kp.mtiles_c * kp.ntiles + (pl.kernel == 0 ? 2 * kp.mtiles_c : 0));
+        kp.tgt_free = 0;   // receive slots are written once: nothing waits for a slot to be free
     } else {
         kp.tgt_in = uint32_t(per_tile * kp.mtiles_c * kp.ntiles);   // finished tile halves per chunk
         kp.tgt_free = kp.tgt_in;
     }
 }
 
-cm_status run(const PlanImpl &pl, int op, KParams &kp, const WsLayout &l, void *ws, bool b_mn,
-              cudaStream_t stream) {
+cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, const WsLayout &l, void *ws,
+              bool b_mn, cudaStream_t stream) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CM_ERR_CUDA;
     int sms = 0;
     if (prepare_device(dev, &sms) != cudaSuccess) return CM_ERR_CUDA;
     int max_clusters = 0;
-    if (pl.kernel == 0 && prepare_pair(dev, &max_clusters) != cudaSuccess) return CM_ERR_CUDA;
+    if (kc.pair && prepare_pair(dev, kc.cluster_ctas, &max_clusters) != cudaSuccess) return CM_ERR_CUDA;
+    if (kc.pair && max_clusters <= 0) return CM_ERR_UNSUPPORTED;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     kp.status = reinterpret_cast<uint32_t *>(w8);
     kp.flags = reinterpret_cast<uint32_t *>(w8 + l.flags_off);
     kp.timeout_ns = uint64_t(pl.timeout_ns);
+    kp.static_tiles = pl.static_tiles;
     const auto &tasks = pl.tasks[op];
     const int ntasks = int(tasks.size());
     if (ntasks > kMaxTasks) return CM_ERR_UNSUPPORTED;
@@ -128,11 +143,11 @@ cm_status run(const PlanImpl &pl, int op, KParams &kp, const WsLayout &l, void *
         kp.task_end = pl.serial_steps ? sb[size_t(i) + 1] : ntasks;
         if (kp.task_end <= kp.task_begin) continue;
         const int64_t tiles = int64_t(kp.task_end - kp.task_begin) * kp.tiles_per_task;
-        if (pl.kernel == 0) {
-            int clusters = pl.grid > 0 ? std::min(pl.grid / 2, max_clusters) : max_clusters;
+        if (kc.pair) {
+            int clusters = pl.grid > 0 ? std::min(pl.grid / kc.cluster_ctas, max_clusters) : max_clusters;
             clusters = std::max(1, clusters);
             if (tiles < clusters) clusters = int(tiles);
-            if (launch_pair(kp, b_mn, clusters, stream) != cudaSuccess) return CM_ERR_CUDA;
+            if (launch_pair(kp, b_mn, kc.cluster_ctas, clusters, stream) != cudaSuccess) return CM_ERR_CUDA;
         } else {
             int grid = pl.grid > 0 ? std::min(pl.grid, sms) : sms;
             if (tiles < grid) grid = int(tiles);
@@ -190,18 +205,21 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
-    const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
+    const KernelChoice kc = choose_kernel(pl, n);
+    // A box: a CTA's 128 rows, or a 64-row quarter when two pairs multicast it
+    const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(a_rows, rows_c));
     if (!make_map(&kp.tmA0, x, uint64_t(K), uint64_t(rows_c), uint64_t(slabs), kBK, box_rows)) return CM_ERR_CUDA;
     uint8_t *bufs = static_cast<uint8_t *>(ws) + l.buf_off;
     if (l.buf_bytes > 0) {
-        const int64_t nslots = int64_t(2) * N * streams_of(pl);
+        const int64_t nslots = int64_t(N) * streams_of(pl) * pl.sched[CM_OP_AG_GEMM].steps;
         if (!make_map(&kp.tmA1, bufs, uint64_t(K), uint64_t(rows_c), uint64_t(nslots * c), kBK, box_rows))
             return CM_ERR_CUDA;
     } else {
         kp.tmA1 = kp.tmA0;
     }
     const bool b_mn = wlayout == CM_W_KN;
-    const uint32_t b_rows = pl.kernel == 0 ? kBN / 2 : kBN;   // a pair CTA stages half the columns
+    const uint32_t b_rows = kc.pair ? kBN / 2 : kBN;   // a pair CTA stages half the columns
     if (b_mn) {
         if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(K), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     } else {
@@ -223,8 +241,8 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    set_tiling(pl, CM_OP_AG_GEMM, kp, rows_c, n);
-    return run(pl, CM_OP_AG_GEMM, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
+    set_tiling(kc, CM_OP_AG_GEMM, kp, rows_c, n);
+    return run(pl, kc, CM_OP_AG_GEMM, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
 }
 
 cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y, cm_dtype y_dtype,
@@ -247,12 +265,14 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
-    const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
+    const KernelChoice kc = choose_kernel(pl, n);
+    const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(a_rows, rows_c));
     // x [N][M][k] viewed as [N*N*c][rows_c][k]: slab (r*N + bucket)*c + chunk
     if (!make_map(&kp.tmA0, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
     kp.tmA1 = kp.tmA0;
     const bool b_mn = wlayout == CM_W_KN;
-    const uint32_t b_rows = pl.kernel == 0 ? kBN / 2 : kBN;
+    const uint32_t b_rows = kc.pair ? kBN / 2 : kBN;
     if (b_mn) {
         if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(k), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     } else {
@@ -261,7 +281,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.y = y;
     kp.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
     if (l.buf_bytes > 0) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
-        const int64_t nbufs = int64_t(2) * N * streams_of(pl);
+        const int64_t nbufs = int64_t(N) * streams_of(pl) * pl.sched[CM_OP_GEMM_RS].steps;
         if (!make_map(&kp.tmAcc, kp.acc, uint64_t(n), uint64_t(rows_c), uint64_t(nbufs * c), 32, 32, true))
             return CM_ERR_CUDA;
     }
@@ -276,8 +296,8 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    set_tiling(pl, CM_OP_GEMM_RS, kp, rows_c, n);
-    return run(pl, CM_OP_GEMM_RS, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
+    set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n);
+    return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
 }
 
 cm_status cm_check_status(const void *ws, cm_stream_t stream, int32_t info[4]) {

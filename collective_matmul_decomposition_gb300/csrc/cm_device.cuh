@@ -232,6 +232,17 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const void *tmap, ui
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr)
         : "memory");
 }
+// Same, multicast: the box lands at the same shared-memory offset in every CTA
+// of `cta_mask`, and each landing counts on the ring barrier of that CTA's
+// pair leader.
+__device__ __forceinline__ void tma_load_3d_pair_mc(void *dst, const void *tmap, uint32_t bar_cluster_addr, int c0,
+                                                    int c1, int c2, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr), "h"(cta_mask)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
                  "r"(ncols)

@@ -25,9 +25,9 @@ struct Schedule {
     }
 };
 
-// Flag id families (word = id * chunks + chunk).  Each family spans
-// N * steps * 2 ids so ids never collide.
-enum FlagKind { kFlagReady = 0, kFlagReadDone = 1, kFlagDone = 0 };
+// Flag ids (word = id * chunks + chunk): AG "chunk forwarded into this
+// slot" or RS "partial bucket chunk written", one per (rank, step, stream).
+enum FlagKind { kFlagReady = 0, kFlagDone = 0 };
 
 struct PlanImpl {
     int N = 1;
@@ -36,7 +36,9 @@ struct PlanImpl {
     int64_t timeout_ns = 1000000000LL;
     int serial_steps = 0;
     int grid = 0;
-    int kernel = 0;   // 0 CTA-pair tiles, 1 single-CTA tiles
+    int kernel = 0;         // see CM_OPT_KERNEL
+    int static_tiles = 0;   // see CM_OPT_STATIC_TILES
+    int tile_group = 4;     // see CM_OPT_TILE_GROUP
     int64_t skip_signal = -1;
     Schedule sched[2];                    // per cm_op
     std::vector<cm_task> tasks[2];        // per cm_op, execution order

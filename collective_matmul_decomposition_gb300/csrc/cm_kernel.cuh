@@ -44,6 +44,7 @@ struct KParams {
     uint32_t *flags;
     uint32_t *status;
     uint32_t *tile_counter;    // dynamic tile scheduler (CTA-pair kernel), zero at launch
+    int static_tiles;          // CTA-pair kernel: 1 = cluster c takes tiles c, c + clusters, ... instead
     const uint8_t *x_bytes;    // AG: x and the receive slots as bytes (pair forwarder)
     uint8_t *slot_bytes;
     int64_t row_bytes;         // bytes per A row (K * 2)
@@ -55,6 +56,7 @@ struct KParams {
     int N, chunks;
     int rows_c;                // rows per chunk
     int mtiles_c, ntiles, kblocks;
+    int ntile_groups;          // CTA-pair kernel: column-tile groups (one column tile per pair of a cluster)
     int n;
     int y_f32;
     int a_box_rows;
@@ -69,9 +71,10 @@ cudaError_t launch_persistent(const KParams &p, bool b_mn_major, int grid, cudaS
 // One-time per-device kernel attributes; returns the SM count.
 cudaError_t prepare_device(int device, int *num_sms);
 
-// CTA-pair kernel (256 x 256 tiles on clusters of two CTAs).
+// CTA-pair kernel (256 x 256 tiles; clusters of one pair, or of two pairs
+// that share the A tile by TMA multicast).
 int pair_rows();
-cudaError_t prepare_pair(int device, int *max_clusters);
-cudaError_t launch_pair(const KParams &p, bool b_mn_major, int clusters, cudaStream_t stream);
+cudaError_t prepare_pair(int device, int cluster_ctas, int *max_clusters);
+cudaError_t launch_pair(const KParams &p, bool b_mn_major, int cluster_ctas, int clusters, cudaStream_t stream);
 
 }  // namespace cm

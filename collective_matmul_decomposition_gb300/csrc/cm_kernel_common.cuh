@@ -15,22 +15,34 @@ struct TileCoord {
     int task, q, mt, nt;
 };
 
-// Linear tile index -> (task, chunk, column tile, row tile); row tile fastest,
-// so tiles running together share a weight column block (each W_r column
-// block streams through L2 once per task) and the row tiles that forward
-// (column tile 0) come first in every chunk.
-__device__ __forceinline__ TileCoord decode(const KParams &p, int t) {
+// Linear tile index -> (task, chunk, row tile, column tile) of one CTA (or
+// one CTA pair).  Tiles run task group by task group (see cm_task.tile_group);
+// inside a group the order is chunk, column-tile group, task, row tile, so
+// the tiles running together share one block of weight columns (W_r of the
+// group's rank) and the row tiles that forward (column tile 0) come first in
+// every chunk.  A column-tile group is `pairs` adjacent column tiles, one per
+// CTA pair of a cluster; `pair` selects this pair's.
+__device__ __forceinline__ TileCoord decode_cl(const KParams &p, int t, uint32_t pair, int pairs) {
     TileCoord c;
-    const int tl = t / p.tiles_per_task;
-    int rem = t - tl * p.tiles_per_task;
-    c.task = p.task_begin + tl;
-    const int per_q = p.mtiles_c * p.ntiles;
-    c.q = rem / per_q;
-    rem -= c.q * per_q;
-    c.nt = rem / p.mtiles_c;
-    c.mt = rem - c.nt * p.mtiles_c;
+    const int task = p.task_begin + t / p.tiles_per_task;
+    const int16_t grp = p.tasks[task].tile_group;
+    const int gsize = grp >> 8, gpos = grp & 0xff;
+    const int gfirst = task - gpos;
+    int u = t - (gfirst - p.task_begin) * p.tiles_per_task;   // tile index inside the group
+    const int per_q = gsize * p.mtiles_c * p.ntile_groups;
+    c.q = u / per_q;
+    u -= c.q * per_q;
+    const int per_g = gsize * p.mtiles_c;
+    const int g = u / per_g;
+    u -= g * per_g;
+    const int off = u / p.mtiles_c;
+    c.mt = u - off * p.mtiles_c;
+    c.task = gfirst + off;
+    c.nt = g * pairs + int(pair);
     return c;
 }
+
+__device__ __forceinline__ TileCoord decode(const KParams &p, int t) { return decode_cl(p, t, 0, 1); }
 
 __device__ __forceinline__ uint32_t *flag_ptr(const KParams &p, int id, int q) {
     return p.flags + size_t(id) * size_t(p.chunks) + size_t(q);

@@ -1,13 +1,20 @@
 // cm_kernel_pair.cu -- the persistent kernel on CTA pairs (tcgen05 .cta_group::2).
 //
 // Same task table and the same per-tile work as the single-CTA kernel, but
-// every output tile is 256 x 256 and belongs to a cluster of two CTAs on two
-// SMs: CTA c of the pair stages rows 128c..128c+127 of the A tile and columns
+// every output tile is 256 x 256 and belongs to a pair of CTAs on two SMs:
+// CTA c of the pair stages rows 128c..128c+127 of the A tile and columns
 // 128c..128c+127 of the B tile, and one tcgen05.mma.cta_group::2 issued by the
-// leader CTA multiplies the whole 256-row tile into both CTAs' tensor memory
+// pair leader multiplies the whole 256-row tile into both CTAs' tensor memory
 // (each CTA holds its 128 rows x 256 fp32 columns).  Each CTA fetches half the
 // operand bytes per MMA of the single-CTA tile, so a 6-stage ring of 32 KB
 // stages fits in shared memory.
+//
+// A cluster holds one pair (CL = 2) or two pairs (CL = 4).  With two pairs
+// they compute adjacent column tiles of the same rows, so their A tiles are
+// the same: each CTA loads a 64-row quarter of its A half and multicasts it
+// to its counterpart in the other pair, cutting L2 requests by a quarter.
+// Both pairs' MMA commits release every CTA's ring stage, so a multicast
+// never lands in a stage still being read.
 //
 // Tiles are handed out dynamically: the leader's producer takes the next
 // tile index from a global counter and publishes it to both CTAs through a
@@ -19,7 +26,8 @@
 // Roles (384 threads per CTA):
 //   warp 0    producer: leader = scheduler + TMA loads of its halves;
 //             peer = TMA loads of its halves.  All loads complete on the
-//             leader's ring barrier; the leader posts the byte count.
+//             leader's ring barrier; the leader posts the byte count.  The
+//             producer takes the next tile index one tile early.
 //   warp 1    MMA issuer (leader only): pair MMAs; commits each stage and,
 //             per tile, the accumulator to the barriers of both CTAs.
 //   warp 2    AG forwarder (both CTAs): for the first column tile of each row
@@ -53,6 +61,14 @@ constexpr int kFwdPiece = 16384;             // forwarder copy granule
 constexpr int kQueue = 6;                    // tile-index queue depth
 constexpr int kPSmemBytes = kPStages * (kHalfA + kHalfB) + 2 * kFwdPiece + 1024 + 1024;
 
+// Position of this CTA in its cluster.
+struct Cl {
+    uint32_t rank;     // %cluster_ctarank
+    uint32_t pair;     // which CTA pair of the cluster
+    uint32_t pos;      // 0 = pair leader (issues the MMAs), 1 = its peer
+    uint32_t leader;   // cluster rank of this pair's leader
+};
+
 struct PSmem {
     uint8_t *a[kPStages];
     uint8_t *b[kPStages];
@@ -85,73 +101,111 @@ struct QueueReader {
     }
 };
 
-template <bool B_MN>
-__device__ void producer(const KParams &p, const PSmem &s, int total, uint32_t crank) {
+// Operand coordinates of K slice `kk` of tile `c` for this CTA's halves.
+struct SliceCoord {
+    const void *tmA;
+    int a0, a1, a2;   // A: K offset, row, slab
+    int b0, b1, b2;   // B: K offset (or column), column (or K offset), rank
+};
+
+template <bool B_MN, int CL>
+__device__ __forceinline__ SliceCoord slice_coord(const KParams &p, const TileCoord &c, const cm_task &tk, int kk,
+                                                  const Cl &cl) {
+    SliceCoord sc;
+    int rr = tk.rank, kb = kk, slab = tk.a_slab * p.chunks + c.q;
+    if (tk.a_src == 2) {
+        rr = kk / p.kblocks;
+        kb = kk - rr * p.kblocks;
+        slab = (rr * p.N + tk.out_idx) * p.chunks + c.q;
+    }
+    sc.tmA = tk.a_src == 1 ? static_cast<const void *>(&p.tmA1) : static_cast<const void *>(&p.tmA0);
+    sc.a0 = kb * kBK;
+    // two-pair clusters: this CTA loads quarter `pair` of its A half (multicast)
+    sc.a1 = c.mt * kPairRows + int(cl.pos) * kCtaRows + (CL == 4 ? int(cl.pair) * (kCtaRows / 2) : 0);
+    sc.a2 = slab;
+    const int n0 = c.nt * kBN + int(cl.pos) * (kBN / 2);
+    sc.b0 = B_MN ? n0 : kb * kBK;
+    sc.b1 = B_MN ? kb * kBK : n0;
+    sc.b2 = rr;
+    return sc;
+}
+
+template <bool B_MN, int CL>
+__device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &cl) {
     int stage = 0;
     uint32_t phase = 0;
     int last_parity[kPStages];
     for (int i = 0; i < kPStages; ++i) last_parity[i] = -1;
     uint32_t full_leader[kPStages];
-    for (int i = 0; i < kPStages; ++i) full_leader[i] = mapa_shared(smem_u32(&s.full[i]), 0);
-    const uint32_t tx_pair = 2u * (uint32_t(p.a_box_rows) * kBK * 2 + kHalfB);
+    for (int i = 0; i < kPStages; ++i) full_leader[i] = mapa_shared(smem_u32(&s.full[i]), cl.leader);
+    // bytes per stage for the pair: each CTA's A half (one box, or two
+    // multicast quarters) and B half
+    const uint32_t a_half = uint32_t(p.a_box_rows) * kBK * 2 * (CL == 4 ? 2u : 1u);
+    const uint32_t tx_pair = 2u * (a_half + kHalfB);
+    const uint16_t mc_mask = uint16_t((1u << cl.rank) | (1u << (cl.rank ^ 2u)));
     QueueReader qr;
     qr.init(s);
     int qslot = 0;
     uint32_t qphase = 0;
-    uint32_t q_peer[kQueue], qfull_peer[kQueue];
-    for (int i = 0; i < kQueue; ++i) {
-        q_peer[i] = mapa_shared(smem_u32(const_cast<int32_t *>(&s.qtile[i])), 1);
-        qfull_peer[i] = mapa_shared(smem_u32(&s.qfull[i]), 1);
-    }
-    for (;;) {
+    // next tile index: the cluster leader takes it from the counter (or, with
+    // static tiles, the next of its round-robin share) and publishes it to
+    // every CTA of the cluster; the others read the queue
+    const int cid = int(blockIdx.x) / CL, ncl = int(gridDim.x) / CL;
+    int static_next = cid;
+    auto fetch = [&]() -> int {
+        if (cl.rank != 0) return qr.next(p, s);
+        if (!wait_mbar<true>(p, s.abort, &s.qempty[qslot], qphase ^ 1u, kSiteEmpty, -1, -1)) return -1;
         int t;
-        if (crank == 0) {   // scheduler: next tile in order, published to both CTAs
-            if (!wait_mbar<true>(p, s.abort, &s.qempty[qslot], qphase ^ 1u, kSiteEmpty, -1, -1)) break;
-            t = int(atomic_add_relaxed(p.tile_counter, 1u));
-            if (t >= total) t = -1;
-            s.qtile[qslot] = t;
-            st_shared_cluster(q_peer[qslot], uint32_t(t));
-            mbar_arrive(&s.qfull[qslot]);
-            mbar_arrive_cluster(qfull_peer[qslot]);
-            if (++qslot == kQueue) {
-                qslot = 0;
-                qphase ^= 1u;
-            }
+        if (p.static_tiles) {
+            t = static_next;
+            static_next += ncl;
         } else {
-            t = qr.next(p, s);
+            t = int(atomic_add_relaxed(p.tile_counter, 1u));
         }
-        if (t < 0 || *s.abort) break;
-        const TileCoord c = decode(p, t);
+        if (t >= total) t = -1;
+        s.qtile[qslot] = t;
+        for (uint32_t r = 1; r < uint32_t(CL); ++r)
+            st_shared_cluster(mapa_shared(smem_u32(const_cast<int32_t *>(&s.qtile[qslot])), r), uint32_t(t));
+        mbar_arrive(&s.qfull[qslot]);
+        for (uint32_t r = 1; r < uint32_t(CL); ++r) mbar_arrive_cluster(mapa_shared(smem_u32(&s.qfull[qslot]), r));
+        if (++qslot == kQueue) {
+            qslot = 0;
+            qphase ^= 1u;
+        }
+        return t;
+    };
+    // the next tile is taken while the current one streams, so no tile
+    // boundary waits on the global counter
+    int cur = fetch();
+    int nxt = cur >= 0 ? fetch() : -1;
+    while (cur >= 0 && !*s.abort) {
+        const TileCoord c = decode_cl(p, cur, cl.pair, CL / 2);
         const cm_task &tk = p.tasks[c.task];
         if (p.op == 0 && tk.wait_in[0] >= 0) {
             if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q))
                 break;
             fence_proxy_async_global();
         }
-        const void *tmA = tk.a_src == 1 ? static_cast<const void *>(&p.tmA1) : static_cast<const void *>(&p.tmA0);
-        const int row0 = c.mt * kPairRows + int(crank) * kCtaRows;
-        const int n0 = c.nt * kBN + int(crank) * (kBN / 2);
         const int nk = kslices(p, tk);
         bool ok = true;
         for (int kk = 0; kk < nk; ++kk) {
-            int rr = tk.rank, kb = kk, slab = tk.a_slab * p.chunks + c.q;
-            if (tk.a_src == 2) {
-                rr = kk / p.kblocks;
-                kb = kk - rr * p.kblocks;
-                slab = (rr * p.N + tk.out_idx) * p.chunks + c.q;
-            }
+            const SliceCoord sc = slice_coord<B_MN, CL>(p, c, tk, kk, cl);
             if (!wait_mbar<true>(p, s.abort, &s.empty[stage], phase ^ 1u, kSiteEmpty, c.task, c.q)) {
                 ok = false;
                 break;
             }
-            if (crank == 0) mbar_expect_tx(&s.full[stage], tx_pair);
-            tma_load_3d_pair(s.a[stage], tmA, full_leader[stage], kb * kBK, row0, slab);
+            if (cl.pos == 0) mbar_expect_tx(&s.full[stage], tx_pair);
+            if (CL == 4)
+                tma_load_3d_pair_mc(s.a[stage] + cl.pair * (kHalfA / 2), sc.tmA, full_leader[stage], sc.a0, sc.a1,
+                                    sc.a2, mc_mask);
+            else
+                tma_load_3d_pair(s.a[stage], sc.tmA, full_leader[stage], sc.a0, sc.a1, sc.a2);
             if (B_MN) {
                 for (int j = 0; j < kBN / 2 / 64; ++j)
-                    tma_load_3d_pair(s.b[stage] + j * (64 * kBK * 2), &p.tmB, full_leader[stage], n0 + 64 * j,
-                                     kb * kBK, rr);
+                    tma_load_3d_pair(s.b[stage] + j * (64 * kBK * 2), &p.tmB, full_leader[stage], sc.b0 + 64 * j,
+                                     sc.b1, sc.b2);
             } else {
-                tma_load_3d_pair(s.b[stage], &p.tmB, full_leader[stage], kb * kBK, n0, rr);
+                tma_load_3d_pair(s.b[stage], &p.tmB, full_leader[stage], sc.b0, sc.b1, sc.b2);
             }
             last_parity[stage] = int(phase);
             if (++stage == kPStages) {
@@ -160,16 +214,18 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, uint32_t c
             }
         }
         if (!ok) break;
+        cur = nxt;
+        nxt = cur >= 0 ? fetch() : -1;
     }
-    // the leader's ring barriers count both CTAs' loads: once they complete,
-    // no load of this pair is still writing shared memory
-    if (crank == 0)
+    // a pair leader's ring barriers count every load into its pair: once they
+    // complete, no load is still writing this pair's shared memory
+    if (cl.pos == 0)
         for (int i = 0; i < kPStages; ++i)
             if (last_parity[i] >= 0) drain_mbar<true>(p, &s.full[i], uint32_t(last_parity[i]));
 }
 
-template <bool B_MN>
-__device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base) {
+template <bool B_MN, int CL>
+__device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     constexpr uint32_t kIdesc = idesc_bf16(kPairRows, kBN, B_MN);
     constexpr uint32_t kBLbo = B_MN ? 64 * kBK * 2 : 16;
     constexpr uint32_t kBStep = B_MN ? (16 * 128) >> 4 : 32 >> 4;
@@ -182,7 +238,7 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base)
     for (;;) {
         const int t = qr.next(p, s);
         if (t < 0 || *s.abort) break;
-        const TileCoord c = decode(p, t);
+        const TileCoord c = decode_cl(p, t, cl.pair, CL / 2);
         const cm_task &tk = p.tasks[c.task];
         if (!wait_mbar<true>(p, s.abort, &s.tempty[accb], acc_phase ^ 1u, kSiteTmemEmpty, c.task, c.q)) break;
         tc_fence_after();
@@ -200,14 +256,14 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base)
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
                 mma_bf16_pair(d, ad + uint64_t(2 * k), bd + uint64_t(kBStep * k), kIdesc, (kk | k) != 0 ? 1u : 0u);
-            mma_commit_pair_mc(&s.empty[stage], 0x3);
+            mma_commit_pair_mc(&s.empty[stage], uint16_t((1u << CL) - 1u));   // every CTA's stage s
             if (++stage == kPStages) {
                 stage = 0;
                 phase ^= 1u;
             }
         }
         if (!ok) break;
-        mma_commit_pair_mc(&s.tfull[accb], 0x3);
+        mma_commit_pair_mc(&s.tfull[accb], uint16_t(3u << (2u * cl.pair)));   // this pair's CTAs
         // AG: both CTAs' A slices of this tile have landed; the slot rows may be reused
         if (p.op == 0 && tk.sig_done >= 0) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
         if (++accb == 2) {
@@ -219,14 +275,15 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base)
     drain_mbar<true>(p, s.drain, 0);
 }
 
-__device__ void forwarder(const KParams &p, const PSmem &s, uint32_t crank) {
+template <int CL>
+__device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
     QueueReader qr;
     qr.init(s);
     uint32_t fph[2] = {0u, 0u};
     for (;;) {
         const int t = qr.next(p, s);
         if (t < 0 || *s.abort) break;
-        const TileCoord c = decode(p, t);
+        const TileCoord c = decode_cl(p, t, cl.pair, CL / 2);
         const cm_task &tk = p.tasks[c.task];
         if (!(c.nt == 0 && (tk.fwd_slot[0] >= 0 || tk.fwd_slot[1] >= 0))) continue;
         bool ok = true;
@@ -238,7 +295,7 @@ __device__ void forwarder(const KParams &p, const PSmem &s, uint32_t crank) {
                                c.q);
         if (!ok) break;
         fence_proxy_async_global();
-        const int row0 = c.mt * kPairRows + int(crank) * kCtaRows;
+        const int row0 = c.mt * kPairRows + int(cl.pos) * kCtaRows;
         const int nrows = min(kCtaRows, p.rows_c - row0);
         if (nrows > 0) {
             const int64_t rb = p.row_bytes;
@@ -325,13 +382,15 @@ __device__ __forceinline__ void epi_slice(const KParams &p, const cm_task &tk, i
     }
 }
 
-__device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base, uint32_t crank) {
+template <int CL>
+__device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     const int e = int(threadIdx.x) / 32 - 4;   // 0..7
     const int lane = int(threadIdx.x) & 31;
     const int quad = e & 3;                      // TMEM lanes 32*quad.. (warp % 4)
     const int half = e >> 2;                     // columns 128*half..
     const bool leader_thread = e == 0 && lane == 0;
-    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&s.tempty[0]), 0), mapa_shared(smem_u32(&s.tempty[1]), 0)};
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&s.tempty[0]), cl.leader),
+                                       mapa_shared(smem_u32(&s.tempty[1]), cl.leader)};
     QueueReader qr;
     if (lane == 0) qr.init(s);
     int accb = 0;
@@ -342,7 +401,7 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
         t = __shfl_sync(0xffffffffu, t, 0);
         bool bad = t < 0;
         TileCoord c = {0, 0, 0, 0};
-        if (!bad) c = decode(p, t);
+        if (!bad) c = decode_cl(p, t, cl.pair, CL / 2);
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
         if (p.op == 1 && leader_thread && !bad) {
@@ -358,7 +417,7 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
         if (bad) break;
         tc_fence_after();
 
-        const int row = c.mt * kPairRows + int(crank) * kCtaRows + quad * 32 + lane;   // row inside the chunk
+        const int row = c.mt * kPairRows + int(cl.pos) * kCtaRows + quad * 32 + lane;   // row inside the chunk
         const bool row_ok = row < p.rows_c;
         const int64_t crow = int64_t(c.q) * p.rows_c + row;
         const bool rs_in = p.op == 1 && (tk.in_buf[0] >= 0 || tk.in_buf[1] >= 0);
@@ -409,13 +468,15 @@ __device__ __forceinline__ float4 *swz_row(uint8_t *buf, int row) { return reint
 // partial bucket(s) for its 32 rows (one 4 KB box), adds the TMEM slice, and
 // TMA-stores the sum to the next rank's receive buffer -- or, at the owner,
 // rounds it into the output.
-__device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base, uint32_t crank) {
+template <int CL>
+__device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     const int e = int(threadIdx.x) / 32 - 4;   // 0..7
     const int lane = int(threadIdx.x) & 31;
     const int quad = e & 3;
     const int half = e >> 2;
     const bool leader_thread = e == 0 && lane == 0;
-    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&s.tempty[0]), 0), mapa_shared(smem_u32(&s.tempty[1]), 0)};
+    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&s.tempty[0]), cl.leader),
+                                       mapa_shared(smem_u32(&s.tempty[1]), cl.leader)};
     uint8_t *buf = s.fbuf[0] + e * 4096;
     uint64_t *eb = &s.ebar[e];
     uint32_t eph = 0;
@@ -430,10 +491,11 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         t = __shfl_sync(0xffffffffu, t, 0);
         bool bad = t < 0;
         TileCoord c = {0, 0, 0, 0};
-        if (!bad) c = decode(p, t);
+        if (!bad) c = decode_cl(p, t, cl.pair, CL / 2);
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
-        if (leader_thread && !bad) {
+        const bool real = c.nt < p.ntiles;   // a cluster's second pair may have no column tile
+        if (leader_thread && !bad && real) {
             for (int j = 0; j < 2 && !bad; ++j)
                 if (tk.wait_in[j] >= 0)
                     bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q), p.tgt_in, kSiteEpilogueFlag, c.task,
@@ -447,7 +509,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         if (lane == 0) fence_proxy_async_global();   // the received buckets were released by other CTAs
         tc_fence_after();
 
-        const int row_w = c.mt * kPairRows + int(crank) * kCtaRows + quad * 32;   // warp's first row in the chunk
+        const int row_w = c.mt * kPairRows + int(cl.pos) * kCtaRows + quad * 32;   // warp's first row in the chunk
         const int row = row_w + lane;
         const bool row_ok = row < p.rows_c;
         const int64_t crow = int64_t(c.q) * p.rows_c + row;
@@ -521,7 +583,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(tempty_leader[accb]);
-        if (tk.sig_done >= 0) {
+        if (tk.sig_done >= 0 && real) {
             if (lane == 0) {
                 bulk_wait<0>();            // this warp's bucket slices are in global memory
                 store_pending = false;
@@ -539,7 +601,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
     if (lane == 0) bulk_wait<0>();
 }
 
-template <bool B_MN>
+template <bool B_MN, int CL>
 __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_constant__ KParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -565,11 +627,15 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     s.abort = reinterpret_cast<volatile int *>(s.tmem_slot + 1);
 
     const int warp = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
-    const uint32_t crank = cluster_ctarank();
+    Cl cl;
+    cl.rank = cluster_ctarank();
+    cl.pair = cl.rank >> 1;
+    cl.pos = cl.rank & 1u;
+    cl.leader = cl.rank & ~1u;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kPStages; ++i) {
             mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], 1);   // the pair MMA's commit
+            mbar_init(&s.empty[i], CL / 2);   // the commit of every pair's MMA
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.tfull[i], 1);
@@ -577,8 +643,9 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
             mbar_init(&s.fbar[i], 1);
         }
         mbar_init(s.drain, 1);
-        // queue readers: leader MMA + peer producer + 8 epilogue warps per CTA (+ 2 forwarders)
-        const uint32_t readers = 2 + 2 * kPEpiWarps + (p.op == 0 ? 2 : 0);
+        // queue readers: the pair leaders' MMA threads, the other CTAs'
+        // producers, 8 epilogue warps per CTA and (AG) every forwarder
+        const uint32_t readers = CL / 2 + (CL - 1) + CL * kPEpiWarps + (p.op == 0 ? CL : 0);
         for (int i = 0; i < kQueue; ++i) {
             mbar_init(&s.qfull[i], 1);
             mbar_init(&s.qempty[i], readers);
@@ -604,19 +671,19 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     const int total = (p.task_end - p.task_begin) * p.tiles_per_task;
 
     if (warp == 0) {
-        if (lane == 0) producer<B_MN>(p, s, total, crank);
+        if (lane == 0) producer<B_MN, CL>(p, s, total, cl);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && crank == 0) mma_issuer<B_MN>(p, s, tmem_base);
+        if (lane == 0 && cl.pos == 0) mma_issuer<B_MN, CL>(p, s, tmem_base, cl);
         __syncwarp();
     } else if (warp == 2) {
-        if (lane == 0 && p.op == 0) forwarder(p, s, crank);
+        if (lane == 0 && p.op == 0) forwarder<CL>(p, s, cl);
         __syncwarp();
     } else if (warp >= 4) {
         if (p.op == 0)
-            epilogue_ag(p, s, tmem_base, crank);
+            epilogue_ag<CL>(p, s, tmem_base, cl);
         else
-            epilogue_rs(p, s, tmem_base, crank);
+            epilogue_rs<CL>(p, s, tmem_base, cl);
     }
     tc_fence_before();
     __syncthreads();
@@ -628,58 +695,74 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     }
 }
 
-}  // namespace
 
-int pair_rows() { return kPairRows; }
-
-cudaError_t prepare_pair(int device, int *max_clusters) {
-    static int cached[64] = {0};
-    if (device < 0 || device >= 64) return cudaErrorInvalidDevice;
-    if (cached[device] == 0) {
-        for (int v = 0; v < 2; ++v) {
-            auto fn = v ? cm_pair_kernel<true> : cm_pair_kernel<false>;
-            cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
-            if (e != cudaSuccess) return e;
-        }
-        cudaLaunchConfig_t cfg = {};
-        int sms = 0;
-        cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+template <int CL>
+cudaError_t prepare_one(int device, int *max_clusters) {
+    for (int v = 0; v < 2; ++v) {
+        auto fn = v ? cm_pair_kernel<true, CL> : cm_pair_kernel<false, CL>;
+        cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
         if (e != cudaSuccess) return e;
-        cfg.gridDim = dim3(unsigned(sms & ~1), 1, 1);
-        cfg.blockDim = dim3(kPThreads, 1, 1);
-        cfg.dynamicSmemBytes = kPSmemBytes;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int n = 0;
-        e = cudaOccupancyMaxActiveClusters(&n, cm_pair_kernel<false>, &cfg);
-        if (e != cudaSuccess) return e;
-        if (n <= 0) return cudaErrorInvalidConfiguration;
-        cached[device] = n;
     }
-    *max_clusters = cached[device];
+    cudaLaunchConfig_t cfg = {};
+    int sms = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(unsigned(sms / CL * CL), 1, 1);
+    cfg.blockDim = dim3(kPThreads, 1, 1);
+    cfg.dynamicSmemBytes = kPSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CL;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, cm_pair_kernel<false, CL>, &cfg);
+    if (e != cudaSuccess) return e;
+    *max_clusters = n;
     return cudaSuccess;
 }
 
-cudaError_t launch_pair(const KParams &p, bool b_mn_major, int clusters, cudaStream_t stream) {
+template <int CL>
+cudaError_t launch_one(const KParams &p, bool b_mn_major, int clusters, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(unsigned(2 * clusters), 1, 1);
+    cfg.gridDim = dim3(unsigned(CL * clusters), 1, 1);
     cfg.blockDim = dim3(kPThreads, 1, 1);
     cfg.dynamicSmemBytes = kPSmemBytes;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.x = CL;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (b_mn_major) return cudaLaunchKernelEx(&cfg, cm_pair_kernel<true>, p);
-    return cudaLaunchKernelEx(&cfg, cm_pair_kernel<false>, p);
+    if (b_mn_major) return cudaLaunchKernelEx(&cfg, cm_pair_kernel<true, CL>, p);
+    return cudaLaunchKernelEx(&cfg, cm_pair_kernel<false, CL>, p);
+}
+
+}  // namespace
+
+int pair_rows() { return kPairRows; }
+
+cudaError_t prepare_pair(int device, int cluster_ctas, int *max_clusters) {
+    static int cached[64][2] = {{0}};
+    if (device < 0 || device >= 64 || (cluster_ctas != 2 && cluster_ctas != 4)) return cudaErrorInvalidValue;
+    const int k = cluster_ctas == 4;
+    if (cached[device][k] == 0) {
+        int n = 0;
+        cudaError_t e = cluster_ctas == 4 ? prepare_one<4>(device, &n) : prepare_one<2>(device, &n);
+        if (e != cudaSuccess) return e;
+        cached[device][k] = n > 0 ? n : -1;
+    }
+    *max_clusters = cached[device][k] > 0 ? cached[device][k] : 0;
+    return cudaSuccess;
+}
+
+cudaError_t launch_pair(const KParams &p, bool b_mn_major, int cluster_ctas, int clusters, cudaStream_t stream) {
+    if (cluster_ctas == 4) return launch_one<4>(p, b_mn_major, clusters, stream);
+    return launch_one<2>(p, b_mn_major, clusters, stream);
 }
 
 }  // namespace cm

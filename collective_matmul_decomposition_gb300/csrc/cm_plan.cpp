@@ -15,12 +15,20 @@
 //     collects ranks o-a .. o-1 clockwise and o+b .. o+1 counter-clockwise;
 //     the owner adds both partials and its own product (the realigning add).
 //
-// Task table: one task per (rank, step, stream) that multiplies, ordered
-// step-major and, inside a step, by the shard / bucket it serves, so that the
-// task consuming what another task forwarded sits at the same position one
-// step later.  Every flag a task waits on is signalled only by tasks of an
-// earlier step, which makes the static round-robin tile order of the kernel
-// free of deadlock (the earliest unfinished tile never waits).
+// Task table: one task per (rank, step, stream) that multiplies.  Every
+// (rank, stream, step) has its own receive slot (AG) or accumulator buffer
+// (RS), written once, so the only dependency is readiness: task (r, i) needs
+// what its ring predecessor produced at step i-1.  Every flag a task waits on
+// is signalled by a task earlier in the table, which makes the in-order tile
+// hand-out of the kernels free of deadlock (the earliest unfinished tile
+// never waits).
+//
+// Order.  One ring (uni): rank-blocked --
+//   (0,0) | (1,0..1) | (2,0..2) | ... | (N-1,0..N-1) | (0,1..N-1) | (1,2..N-1) | ...
+// -- each rank's steps run in order right after its predecessor's, and a
+// rank's weight shard W_r is streamed in two runs instead of once per step.
+// Bidirectional rings (two predecessors, one each way), the undecomposed op
+// and the step-serial mode: step-major, and inside a step by shard / bucket.
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -126,12 +134,36 @@ struct Ids {
     int fid(int kind, int r, int i, int d) const { return ((kind * N + r) * S + i) * 2 + d; }
 };
 
+// Position of task (r, i) in the rank-blocked order of a one-way ring.
+int rank_blocked_key(int N, int r, int i) {
+    if (i <= r) return r * (r + 1) / 2 + i;                          // block (r, 0..r)
+    const int first = N * (N + 1) / 2;                               // after all (r, 0..r) blocks
+    return first + r * (N - 1) - r * (r - 1) / 2 + (i - r - 1);      // block (r, r+1..N-1)
+}
+
 void order_and_index(PlanImpl &p, int op, std::vector<cm_task> &tasks) {
-    std::stable_sort(tasks.begin(), tasks.end(), [](const cm_task &x, const cm_task &y) {
-        if (x.step != y.step) return x.step < y.step;
-        if (x.out_idx != y.out_idx) return x.out_idx < y.out_idx;
-        return x.stream < y.stream;
-    });
+    if (p.dir == CM_RING_UNI && !p.serial_steps) {
+        const int N = p.N;
+        std::stable_sort(tasks.begin(), tasks.end(), [N](const cm_task &x, const cm_task &y) {
+            return rank_blocked_key(N, x.rank, x.step) < rank_blocked_key(N, y.rank, y.step);
+        });
+    } else {
+        std::stable_sort(tasks.begin(), tasks.end(), [](const cm_task &x, const cm_task &y) {
+            if (x.step != y.step) return x.step < y.step;
+            if (x.out_idx != y.out_idx) return x.out_idx < y.out_idx;
+            return x.stream < y.stream;
+        });
+    }
+    // tile groups: runs of consecutive same-rank tasks, at most tile_group long
+    // (same-rank tasks never depend on each other, so their tiles may interleave)
+    // (the step-serial mode launches step by step, so there every task is its own group)
+    const int gmax = p.serial_steps ? 1 : p.tile_group;
+    for (size_t t = 0; t < tasks.size();) {
+        size_t e = t + 1;
+        while (e < tasks.size() && int(e - t) < gmax && tasks[e].rank == tasks[t].rank) ++e;
+        for (size_t j = t; j < e; ++j) tasks[j].tile_group = int16_t(((e - t) << 8) | (j - t));
+        t = e;
+    }
     auto &sb = p.step_begin[op];
     sb.assign(size_t(p.sched[op].steps) + 1, int(tasks.size()));
     for (int t = int(tasks.size()) - 1; t >= 0; --t) sb[tasks[size_t(t)].step] = t;
@@ -143,9 +175,9 @@ void build_ag_tasks(PlanImpl &p) {
     const Schedule &s = p.sched[CM_OP_AG_GEMM];
     const int S = s.steps, D = s.streams;
     Ids ids{N, S};
-    p.flag_ids[CM_OP_AG_GEMM] = 2 * N * S * 2;
+    p.flag_ids[CM_OP_AG_GEMM] = N * S * 2;
     std::vector<cm_task> tasks;
-    auto slot = [&](int r, int d, int parity) { return (r * D + d) * 2 + parity; };
+    auto slot = [&](int r, int d, int step) { return (r * D + d) * S + step; };   // written once
     if (p.dir == CM_RING_NONE) {
         for (int r = 0; r < N; ++r) {
             cm_task t = blank_task(r, 0, 0);
@@ -169,14 +201,11 @@ void build_ag_tasks(PlanImpl &p) {
                     const StepEntry &e = s.at(N, r, i, d);
                     if (e.obj < 0) continue;
                     cm_task u = blank_task(r, i, d);
-                    u.a_src = 1; u.a_slab = int16_t(slot(r, d, i % 2)); u.out_idx = int16_t(e.obj);
+                    u.a_src = 1; u.a_slab = int16_t(slot(r, d, i)); u.out_idx = int16_t(e.obj);
                     u.wait_in[0] = int16_t(ids.fid(kFlagReady, r, i, d));
-                    u.sig_done = int16_t(ids.fid(kFlagReadDone, r, i, d));
                     if (e.dst >= 0) {
-                        u.fwd_slot[0] = int16_t(slot(e.dst, d, (i + 1) % 2));
+                        u.fwd_slot[0] = int16_t(slot(e.dst, d, i + 1));
                         u.sig_fwd[0] = int16_t(ids.fid(kFlagReady, e.dst, i + 1, d));
-                        // the slot last held what e.dst used at step i-1 (slots exist from step 1)
-                        if (i - 1 >= 1) u.wait_free[0] = int16_t(ids.fid(kFlagReadDone, e.dst, i - 1, d));
                     }
                     tasks.push_back(u);
                 }
@@ -193,7 +222,7 @@ void build_rs_tasks(PlanImpl &p) {
     Ids ids{N, S};
     p.flag_ids[CM_OP_GEMM_RS] = N * S * 2;
     std::vector<cm_task> tasks;
-    auto acc = [&](int r, int d, int parity) { return (r * D + d) * 2 + parity; };
+    auto acc = [&](int r, int d, int step) { return (r * D + d) * S + step; };   // written once
     if (p.dir == CM_RING_NONE) {
         for (int o = 0; o < N; ++o) {
             cm_task t = blank_task(o, 0, 0);
@@ -214,26 +243,25 @@ void build_rs_tasks(PlanImpl &p) {
                     const bool owner = e.dst < 0;
                     if (!owner) {
                         // partial bucket goes to the next rank of this stream
-                        t.out_buf = int16_t(acc(e.dst, d, (i + 1) % 2));
-                        if (i >= 2) t.wait_free[0] = int16_t(ids.fid(kFlagDone, e.dst, i - 1, d));
+                        t.out_buf = int16_t(acc(e.dst, d, i + 1));
                         if (i > 0) {
-                            t.in_buf[0] = int16_t(acc(r, d, i % 2));
+                            t.in_buf[0] = int16_t(acc(r, d, i));
                             t.wait_in[0] = int16_t(ids.fid(kFlagDone, e.src, i - 1, d));
                         }
                     } else if (p.dir == CM_RING_UNI) {
                         if (i > 0) {
-                            t.in_buf[0] = int16_t(acc(r, 0, i % 2));
+                            t.in_buf[0] = int16_t(acc(r, 0, i));
                             t.wait_in[0] = int16_t(ids.fid(kFlagDone, e.src, i - 1, 0));
                         }
                     } else {
                         // realigning addition: clockwise partial arrived at step a,
                         // counter-clockwise partial at step b
                         if (a >= 1) {
-                            t.in_buf[0] = int16_t(acc(r, 0, a % 2));
+                            t.in_buf[0] = int16_t(acc(r, 0, a));
                             t.wait_in[0] = int16_t(ids.fid(kFlagDone, md(r - 1, N), a - 1, 0));
                         }
                         if (b >= 1) {
-                            t.in_buf[1] = int16_t(acc(r, 1, b % 2));
+                            t.in_buf[1] = int16_t(acc(r, 1, b));
                             t.wait_in[1] = int16_t(ids.fid(kFlagDone, md(r + 1, N), b - 1, 1));
                         }
                     }
@@ -334,14 +362,31 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
             return CM_OK;
         case CM_OPT_SERIAL_STEPS:
             p.serial_steps = value != 0;
+            try {
+                cm::rebuild(p);   // the step-serial mode runs the table in step-major order
+            } catch (...) {
+                return CM_ERR_INVALID_ARG;
+            }
             return CM_OK;
         case CM_OPT_GRID:
             if (value < 0) return CM_ERR_INVALID_ARG;
             p.grid = int(value);
             return CM_OK;
         case CM_OPT_KERNEL:
-            if (value != 0 && value != 1) return CM_ERR_INVALID_ARG;
+            if (value < 0 || value > 3) return CM_ERR_INVALID_ARG;
             p.kernel = int(value);
+            return CM_OK;
+        case CM_OPT_TILE_GROUP:
+            if (value < 1 || value > 8) return CM_ERR_INVALID_ARG;
+            p.tile_group = int(value);
+            try {
+                cm::rebuild(p);
+            } catch (...) {
+                return CM_ERR_INVALID_ARG;
+            }
+            return CM_OK;
+        case CM_OPT_STATIC_TILES:
+            p.static_tiles = value != 0;
             return CM_OK;
         case CM_OPT_SKIP_SIGNAL:
             p.skip_signal = value < 0 ? -1 : value;

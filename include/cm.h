@@ -144,7 +144,9 @@ typedef struct cm_task {
     int16_t sig_done;      /* AG: bumped per tile once its slot reads landed; RS: per finished tile */
     int16_t step;          /* ring step of this task */
     int16_t stream;        /* 0 clockwise (or own / owner), 1 counter-clockwise */
-    int16_t reserved;      /* 0 */
+    int16_t tile_group;    /* (size << 8) | position: the tiles of a group of
+                              consecutive same-rank tasks are interleaved
+                              (column tile outermost) so they share W_r in L2 */
 } cm_task;
 
 /* Copy the task table of `op` into out[0..capacity); returns the number of
@@ -206,16 +208,25 @@ const char *cm_status_string(cm_status status);
  *  CM_OPT_SKIP_SIGNAL    fault injection: value = (op << 16) | (rank << 8) | step;
  *                        that task never signals its forward/done flags, so
  *                        its consumers time out.  -1 clears it.
- *  CM_OPT_KERNEL         0 (default): 256 x 256 tiles on CTA pairs
- *                        (tcgen05 cta_group::2, clusters of 2);
- *                        1: 128 x 256 tiles on single CTAs.
+ *  CM_OPT_KERNEL         tile kernel.  0 (default) and 2: 256 x 256 tiles on
+ *                        CTA pairs (tcgen05 cta_group::2), one pair per
+ *                        cluster; 1: 128 x 256 tiles on single CTAs; 3: CTA
+ *                        pairs, two pairs per cluster sharing the A tile by
+ *                        TMA multicast.
+ *  CM_OPT_STATIC_TILES   CTA-pair kernel: 0 (default) hands tiles out in
+ *                        order from a global counter as clusters free up;
+ *                        1 gives cluster c the tiles c, c + clusters, ...
+ *  CM_OPT_TILE_GROUP     largest number of consecutive same-rank tasks whose
+ *                        tiles are interleaved (1..8, default 4).
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
     CM_OPT_SERIAL_STEPS = 1,
     CM_OPT_GRID = 2,
     CM_OPT_SKIP_SIGNAL = 3,
-    CM_OPT_KERNEL = 4
+    CM_OPT_KERNEL = 4,
+    CM_OPT_STATIC_TILES = 5,
+    CM_OPT_TILE_GROUP = 6
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);

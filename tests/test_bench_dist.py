@@ -1,0 +1,57 @@
+"""bench.py's multi-process host logic with two gloo ranks on CPU: process
+group set-up from the launcher's environment, barrier, max-over-ranks time
+and the whole-job aggregate (every rank's work over the slowest rank's time)."""
+
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, out):
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank),
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import bench
+    import torch.distributed as dist
+    r, w = bench.dist_init("gloo")
+    assert (r, w) == (rank, world)
+    bench.dist_barrier()
+    t = 1.0 + rank                        # rank 1 is the slow one
+    t_max = bench.dist_max(t)
+    value = bench.aggregate(1e12, 10, w, t_max)
+    out.put((rank, t_max, value))
+    bench.dist_barrier()
+    dist.destroy_process_group()
+
+
+def test_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    out = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(out.get(timeout=120) for _ in range(2))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, t_max, value in res:
+        assert t_max == pytest.approx(2.0)
+        # 2 ranks x 10 steps x 1 TFLOP over the slowest rank's 2 s
+        assert value == pytest.approx(10.0)
+
+
+def test_single_process_defaults(monkeypatch):
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    import bench
+    assert bench.dist_env() == (0, 1, 0)
+    assert bench.dist_max(3.5) == 3.5
+    assert bench.aggregate(2e12, 5, 1, 2.0) == pytest.approx(5.0)

@@ -1,4 +1,5 @@
-"""Both tile kernels (CTA pairs with tcgen05 cta_group::2, and single CTAs)
+"""Every tile kernel -- CTA pairs (tcgen05 cta_group::2) with one or two pairs
+per cluster (two pairs share the A tile by TMA multicast), and single CTAs --
 against the oracle and against each other."""
 
 import numpy as np
@@ -12,7 +13,8 @@ from test_gpu_parity import TOL_F32, _np, run_ag, run_rs
 
 pytestmark = pytest.mark.gpu
 
-PAIR, SINGLE = 0, 1
+PAIR, SINGLE, PAIR_CL2, PAIR_CL4 = 0, 1, 2, 3
+KERNELS = [PAIR, SINGLE, PAIR_CL2, PAIR_CL4]
 
 
 def _plan(N, chunks, direction, kernel):
@@ -21,12 +23,13 @@ def _plan(N, chunks, direction, kernel):
     return p
 
 
-@pytest.mark.parametrize("kernel", [PAIR, SINGLE])
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("N,m,K,n,chunks,direction", [
     (2, 64, 256, 512, 1, "uni"),        # rows per chunk below one CTA's 128
     (3, 200, 200, 296, 2, "bidi"),      # ragged rows / columns / K
-    (4, 384, 320, 768, 1, "uni"),       # row tiles straddling the pair split
-    (5, 136, 72, 520, 1, "none"),
+    (4, 384, 320, 768, 1, "uni"),       # row tiles straddling the pair split; 3 column tiles
+    (5, 136, 72, 520, 1, "none"),       # odd column-tile count: a cluster's second pair idles
+    (2, 48, 64, 256, 1, "uni"),         # rows below one multicast quarter, one column tile
 ])
 @pytest.mark.parametrize("layout", ["nk", "kn"])
 def test_kernel_vs_oracle(kernel, N, m, K, n, chunks, direction, layout):
@@ -40,15 +43,16 @@ def test_kernel_vs_oracle(kernel, N, m, K, n, chunks, direction, layout):
     assert oracle.normwise_max_rel_err(_np(yr), refr) <= TOL_F32
 
 
-def test_pair_and_single_agree_bitwise_on_ag():
-    N, m, K, n = 4, 512, 1024, 1024
+def test_kernels_agree_bitwise_on_ag():
+    N, m, K, n = 4, 512, 1024, 1280
     x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=99, w_layout="nk")
-    a, _, _ = run_ag(_plan(N, 1, "uni", PAIR), x, w, "nk")
-    b, _, _ = run_ag(_plan(N, 1, "uni", SINGLE), x, w, "nk")
-    assert torch.equal(a, b)
+    base, _, _ = run_ag(_plan(N, 1, "uni", SINGLE), x, w, "nk")
+    for k in (PAIR, PAIR_CL2, PAIR_CL4):
+        y, _, _ = run_ag(_plan(N, 1, "uni", k), x, w, "nk")
+        assert torch.equal(y, base), k
 
 
-@pytest.mark.parametrize("kernel", [PAIR, SINGLE])
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_tagged_placement_each_kernel(kernel):
     N, m, K, n = 8, 384, 64, 512
     x, w = gen.tagged_ag_inputs(N, m, K, n, "nk")
@@ -58,7 +62,7 @@ def test_tagged_placement_each_kernel(kernel):
         assert np.array_equal(_np(y), ref)
 
 
-@pytest.mark.parametrize("kernel", [PAIR, SINGLE])
+@pytest.mark.parametrize("kernel", KERNELS)
 def test_timeout_each_kernel(kernel):
     N = 4
     x, w = gen.ag_inputs(N, 256, 128, 256, gen.NORMAL1, gen.NORMAL002, seed=3, w_layout="nk")

@@ -67,24 +67,96 @@ def test_each_rank_uses_each_shard_once(N, direction):
 
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 16])
 @pytest.mark.parametrize("direction", ["uni", "bidi", "none"])
-def test_waits_point_to_earlier_steps(N, direction):
+@pytest.mark.parametrize("serial", [False, True])
+def test_waits_point_to_earlier_tasks(N, direction, serial):
+    """Every flag has exactly one signalling task, earlier in the table than
+    every task waiting on it, and of an earlier ring step."""
     p = cm.Plan(N, 2, direction)
+    if serial:
+        p.set_option(cm.CM_OPT_SERIAL_STEPS, 1)
     for op in (AG, RS):
         tasks = p.tasks(op)
-        steps = [t.step for t in tasks]
-        assert steps == sorted(steps)
+        if serial or direction != "uni":
+            assert [t.step for t in tasks] == sorted(t.step for t in tasks)
         signallers = {}
-        for t in tasks:
+        for idx, t in enumerate(tasks):
             sigs = [t.sig_done] + ([t.sig_fwd[0], t.sig_fwd[1]] if op == AG else [])
-            for s in sigs:
-                if s >= 0:
-                    assert s not in signallers, "a flag has one signaller"
-                    signallers[s] = t.step
-        for t in tasks:
+            for s_ in sigs:
+                if s_ >= 0:
+                    assert s_ not in signallers, "a flag has one signaller"
+                    signallers[s_] = (idx, t.step)
+        for idx, t in enumerate(tasks):
             for f in list(t.wait_in) + list(t.wait_free):
                 if f >= 0:
                     assert f in signallers, (op, f)
-                    assert signallers[f] < t.step
+                    assert signallers[f][0] < idx
+                    assert signallers[f][1] < t.step
+
+
+@pytest.mark.parametrize("N", [2, 3, 5, 8, 16])
+def test_uni_ring_runs_each_rank_in_two_blocks(N):
+    """One-way ring: each rank's tasks form at most two contiguous runs, in
+    step order (so its weight shard streams twice, not once per step)."""
+    p = cm.Plan(N, 1, "uni")
+    for op in (AG, RS):
+        ranks = [t.rank for t in p.tasks(op)]
+        runs = {}
+        prev = None
+        for r in ranks:
+            if r != prev:
+                runs[r] = runs.get(r, 0) + 1
+            prev = r
+        assert max(runs.values()) <= 2
+        for r in range(N):
+            steps = [t.step for t in p.tasks(op) if t.rank == r]
+            assert steps == sorted(steps) == list(range(N))
+
+
+@pytest.mark.parametrize("group", [1, 2, 4, 8])
+def test_tile_groups(group):
+    """Groups are runs of at most `group` consecutive tasks of one rank."""
+    p = cm.Plan(8, 2, "uni")
+    p.set_option(cm.CM_OPT_TILE_GROUP, group)
+    for op in (AG, RS):
+        tasks = p.tasks(op)
+        order = kernel_tile_order(tasks, 2, 3, 4)
+        assert len(order) == len(tasks) * 2 * 3 * 4
+        assert len(set(order)) == len(order)
+        assert max(t.tile_group >> 8 for t in tasks) <= group
+    for N in (2, 4):
+        for d in ("uni", "bidi", "none"):
+            q = cm.Plan(N, 1, d)
+            q.set_option(cm.CM_OPT_TILE_GROUP, group)
+            q.set_option(cm.CM_OPT_SERIAL_STEPS, 1)
+            assert all(t.tile_group >> 8 == 1 for t in q.tasks(AG) + q.tasks(RS))
+
+
+def test_slots_written_once():
+    """Every receive slot (AG) and accumulator buffer (RS) has one writer."""
+    for d in ("uni", "bidi"):
+        p = cm.Plan(8, 1, d)
+        ag = [s_ for t in p.tasks(AG) for s_ in t.fwd_slot if s_ >= 0]
+        assert len(ag) == len(set(ag))
+        rs = [t.out_buf for t in p.tasks(RS) if t.out_buf >= 0]
+        assert len(rs) == len(set(rs))
+
+
+def kernel_tile_order(tasks, c, mtiles, ntiles):
+    """The kernels' tile order: task groups (cm_task.tile_group) in table
+    order; inside a group chunk, column tile, task, row tile."""
+    out = []
+    t = 0
+    while t < len(tasks):
+        size = tasks[t].tile_group >> 8
+        assert size >= 1 and all((tasks[t + j].tile_group & 0xff) == j for j in range(size))
+        assert len({tasks[t + j].rank for j in range(size)}) == 1, "a group is one rank's tasks"
+        for q in range(c):
+            for nt in range(ntiles):
+                for j in range(size):
+                    for mt in range(mtiles):
+                        out.append((t + j, q, mt, nt))
+        t += size
+    return out
 
 
 def _simulate(p, op, mtiles, ntiles, grid, seed):
@@ -92,9 +164,7 @@ def _simulate(p, op, mtiles, ntiles, grid, seed):
     rnd = random.Random(seed)
     N, c = p.N, p.chunks
     tasks = p.tasks(op)
-    # the kernel's order: task, chunk, column tile, row tile (row tile fastest)
-    tiles = [(ti, q, mt, nt) for ti in range(len(tasks)) for q in range(c)
-             for nt in range(ntiles) for mt in range(mtiles)]
+    tiles = kernel_tile_order(tasks, c, mtiles, ntiles)
     flags = {}
     tgt_ag_in, tgt_ag_free = mtiles, mtiles * ntiles
     tgt_rs = mtiles * ntiles
@@ -190,8 +260,10 @@ def _simulate(p, op, mtiles, ntiles, grid, seed):
 @pytest.mark.parametrize("direction", ["uni", "bidi", "none"])
 @pytest.mark.parametrize("chunks", [1, 2, 4])
 @pytest.mark.parametrize("grid", [1, 3, 16])
-def test_protocol_simulation(N, direction, chunks, grid):
+@pytest.mark.parametrize("group", [1, 4])
+def test_protocol_simulation(N, direction, chunks, grid, group):
     p = cm.Plan(N, chunks, direction)
+    p.set_option(cm.CM_OPT_TILE_GROUP, group)
     c = p.chunks
     mtiles, ntiles = 2, 2
     for seed in range(3):
@@ -214,10 +286,11 @@ def test_skip_signal_starves_consumer():
 
 
 @pytest.mark.parametrize("op", [AG, RS])
-@pytest.mark.parametrize("which", ["wait_in", "wait_free"])
+@pytest.mark.parametrize("which", ["wait_in"])
 def test_simulation_catches_a_missing_wait(op, which):
-    """Planted mistake: a task table without one kind of wait must fail the
-    simulation for some interleaving."""
+    """Planted mistake: a task table without its readiness waits must fail
+    the simulation for some interleaving (slots are written once, so
+    readiness is the only dependency)."""
     p = cm.Plan(5, 1, "uni")
     real = p.tasks
 
