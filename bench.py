@@ -40,7 +40,9 @@ METRIC = "AG-GEMM / GEMM-RS bf16 TFLOP/s and % of dense tensor peak on 1 GB300"
 UNIT = "TFLOP/s"
 WORKLOAD = "mlp_h8192_ffn28672_s8192"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}  # of fallback
-KERNEL_SOURCES = ["cm_kernel.cu", "cm_kernel_pair.cu", "cm_device.cuh", "cm_kernel.cuh", "cm_kernel_common.cuh"]
+# every source that decides what the kernels do (tile order, task table, launch shape)
+KERNEL_SOURCES = ["cm_kernel.cu", "cm_kernel_pair.cu", "cm_device.cuh", "cm_kernel.cuh", "cm_kernel_common.cuh",
+                  "cm_api.cu", "cm_plan.cpp", "cm_internal.h"]
 
 
 # ---- distributed host logic (also exercised by the gloo tests on CPU) ---------------

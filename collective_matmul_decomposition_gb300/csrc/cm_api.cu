@@ -105,7 +105,9 @@ void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int
     kp.ntile_groups = (kp.ntiles + pairs - 1) / pairs;   // single CTAs: one column tile per group
     kp.tiles_per_task = kp.chunks * kp.mtiles_c * kp.ntile_groups;
     if (op == CM_OP_AG_GEMM) {
-        kp.tgt_in = uint32_t(per_tile * kp.mtiles_c);           // forwarded row-tile halves per chunk
+        // forwards per chunk: CTA pairs forward a row slice from every tile
+        // (2 CTAs each); single CTAs forward whole row tiles from column tile 0
+        kp.tgt_in = uint32_t(kc.pair ? per_tile * kp.mtiles_c * kp.ntiles : kp.mtiles_c);
         kp.tgt_free = 0;   // receive slots are written once: nothing waits for a slot to be free
     } else {
         kp.tgt_in = uint32_t(per_tile * kp.mtiles_c * kp.ntiles);   // finished tile halves per chunk

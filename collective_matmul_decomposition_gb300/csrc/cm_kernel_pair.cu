@@ -30,10 +30,10 @@
 //             producer takes the next tile index one tile early.
 //   warp 1    MMA issuer (leader only): pair MMAs; commits each stage and,
 //             per tile, the accumulator to the barriers of both CTAs.
-//   warp 2    AG forwarder (both CTAs): for the first column tile of each row
-//             tile it copies its CTA's 128 shard rows to the ring neighbour's
+//   warp 2    AG forwarder (both CTAs): every tile copies a slice of its CTA's
+//             128 shard rows (1/column-tiles of them) to the ring neighbour's
 //             receive slot with 1-D TMA bulk copies through two 16 KB buffers,
-//             then releases the slot's ready flag -- the rotation copy in flight
+//             then bumps the slot's ready flag -- the rotation copy in flight
 //             while the partial GEMMs read the shard.
 //   warps 4-11  epilogue (both CTAs): 8 warps, TMEM lane quarter = warp % 4,
 //             column half = (warp - 4) / 4.  AG writes shard rows of Y_r; RS
@@ -280,23 +280,24 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
     QueueReader qr;
     qr.init(s);
     uint32_t fph[2] = {0u, 0u};
+    // every tile of a row tile forwards a slice of the rows: column tile nt
+    // copies rows [nt*per, (nt+1)*per) of this CTA's 128, so the shard chunk
+    // moves while all its tiles run instead of one tile doing all of it
+    const int per = (kCtaRows + p.ntiles - 1) / p.ntiles;
     for (;;) {
         const int t = qr.next(p, s);
         if (t < 0 || *s.abort) break;
         const TileCoord c = decode_cl(p, t, cl.pair, CL / 2);
         const cm_task &tk = p.tasks[c.task];
-        if (!(c.nt == 0 && (tk.fwd_slot[0] >= 0 || tk.fwd_slot[1] >= 0))) continue;
+        if (!(tk.fwd_slot[0] >= 0 || tk.fwd_slot[1] >= 0) || c.nt >= p.ntiles) continue;
         bool ok = true;
         if (tk.a_src == 1 && tk.wait_in[0] >= 0)   // the shard chunk has arrived here
             ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteForwardFlag, c.task, c.q);
-        for (int j = 0; j < 2 && ok; ++j)          // the neighbour's slot is no longer read
-            if (tk.fwd_slot[j] >= 0 && tk.wait_free[j] >= 0)
-                ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[j], c.q), p.tgt_free, kSiteForwardFlag, c.task,
-                               c.q);
         if (!ok) break;
         fence_proxy_async_global();
-        const int row0 = c.mt * kPairRows + int(cl.pos) * kCtaRows;
-        const int nrows = min(kCtaRows, p.rows_c - row0);
+        const int lo = c.nt * per;
+        const int row0 = c.mt * kPairRows + int(cl.pos) * kCtaRows + lo;
+        const int nrows = min(min(per, kCtaRows - lo), p.rows_c - row0);
         if (nrows > 0) {
             const int64_t rb = p.row_bytes;
             const uint8_t *src = (tk.a_src == 1 ? p.slot_bytes : p.x_bytes) +
@@ -330,8 +331,6 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
         fence_proxy_async_global();
         for (int j = 0; j < 2; ++j)
             if (tk.fwd_slot[j] >= 0 && tk.sig_fwd[j] >= 0) red_release_add(flag_ptr(p, tk.sig_fwd[j], c.q), 1u);
-        if (tk.a_src == 1 && tk.sig_done >= 0)   // this forwarder's reads of the slot are done
-            red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
     }
     bulk_wait<0>();
 }
