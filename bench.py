@@ -558,13 +558,17 @@ def run_profile_case(args):
     st.plan.set_option(st.cm.CM_OPT_STATIC_TILES, args.static_tiles)
     if args.tile_group:
         st.plan.set_option(st.cm.CM_OPT_TILE_GROUP, args.tile_group)
+    if args.l2_hints >= 0:
+        st.plan.set_option(st.cm.CM_OPT_L2_HINTS, args.l2_hints)
+    if args.l2_promotion >= 0:
+        st.plan.set_option(st.cm.CM_OPT_L2_PROMOTION, args.l2_promotion)
     fn = st.ag if args.profile == "ag" else st.rs
     f_ag, f_rs = flops(data["shapes"], N)
     ms = time_loop(fn, args.steps, torch, warmup=args.warmup)
     st.check((args.profile,))
     fl = f_ag if args.profile == "ag" else f_rs
     print(json.dumps({"profile_case": args.workload, "op": args.profile, "N": N, "chunks": args.chunks,
-                      "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group,
+                      "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group, "l2_hints": args.l2_hints, "l2_promotion": args.l2_promotion,
                       "ms": ms, "tflops": fl / (ms / 1e3) / 1e12}), flush=True)
     return 0
 
@@ -585,6 +589,8 @@ def main(argv=None):
     ap.add_argument("--kernel", type=int, default=0, help="CM_OPT_KERNEL for --profile")
     ap.add_argument("--static-tiles", type=int, default=0, help="CM_OPT_STATIC_TILES for --profile")
     ap.add_argument("--tile-group", type=int, default=0, help="CM_OPT_TILE_GROUP for --profile (0 = default)")
+    ap.add_argument("--l2-hints", type=int, default=-1, help="CM_OPT_L2_HINTS for --profile (-1 = default)")
+    ap.add_argument("--l2-promotion", type=int, default=-1, help="CM_OPT_L2_PROMOTION for --profile (-1 = default)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="oracle seconds for the cpu_baseline of the default arm")
     ap.add_argument("--ref-seconds", type=float, default=120.0,

@@ -61,6 +61,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D tensor [d2][d1][d0] (d0 contiguous) of bf16 (or fp32), 128-byte swizzled boxes of b0 x b1.
+int g_l2_promotion = 3;   // promotion of the maps being built (set per call under the call's lock)
+
 bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
               bool f32 = false) {
     auto enc = encode_fn();
@@ -72,7 +74,8 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
     cuuint32_t es[3] = {1, 1, 1};
     CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                      const_cast<void *>(base), dims, strides, box, es,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     static_cast<CUtensorMapL2promotion>(g_l2_promotion),
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
@@ -129,6 +132,8 @@ cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, c
     kp.flags = reinterpret_cast<uint32_t *>(w8 + l.flags_off);
     kp.timeout_ns = uint64_t(pl.timeout_ns);
     kp.static_tiles = pl.static_tiles;
+    kp.l2_hint_a = pl.l2_hints & 0xf;
+    kp.l2_hint_b = (pl.l2_hints >> 4) & 0xf;
     const auto &tasks = pl.tasks[op];
     const int ntasks = int(tasks.size());
     if (ntasks > kMaxTasks) return CM_ERR_UNSUPPORTED;
@@ -207,6 +212,7 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
+    g_l2_promotion = pl.l2_promotion;
     const KernelChoice kc = choose_kernel(pl, n);
     // A box: a CTA's 128 rows, or a 64-row quarter when two pairs multicast it
     const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
@@ -267,6 +273,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
+    g_l2_promotion = pl.l2_promotion;
     const KernelChoice kc = choose_kernel(pl, n);
     const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
     const uint32_t box_rows = uint32_t(std::min<int64_t>(a_rows, rows_c));

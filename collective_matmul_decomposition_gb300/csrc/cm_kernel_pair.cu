@@ -143,6 +143,11 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
     const uint32_t a_half = uint32_t(p.a_box_rows) * kBK * 2 * (CL == 4 ? 2u : 1u);
     const uint32_t tx_pair = 2u * (a_half + kHalfB);
     const uint16_t mc_mask = uint16_t((1u << cl.rank) | (1u << (cl.rank ^ 2u)));
+    auto policy = [](int h) {
+        return h == 1 ? policy_evict_last() : h == 2 ? policy_evict_first() : policy_evict_normal();
+    };
+    const uint64_t pol_a = policy(p.l2_hint_a), pol_b = policy(p.l2_hint_b);
+    const bool hinted = p.l2_hint_a != 0 || p.l2_hint_b != 0;
     QueueReader qr;
     qr.init(s);
     int qslot = 0;
@@ -198,12 +203,16 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
             if (CL == 4)
                 tma_load_3d_pair_mc(s.a[stage] + cl.pair * (kHalfA / 2), sc.tmA, full_leader[stage], sc.a0, sc.a1,
                                     sc.a2, mc_mask);
+            else if (hinted)
+                tma_load_3d_pair_hint(s.a[stage], sc.tmA, full_leader[stage], sc.a0, sc.a1, sc.a2, pol_a);
             else
                 tma_load_3d_pair(s.a[stage], sc.tmA, full_leader[stage], sc.a0, sc.a1, sc.a2);
             if (B_MN) {
                 for (int j = 0; j < kBN / 2 / 64; ++j)
                     tma_load_3d_pair(s.b[stage] + j * (64 * kBK * 2), &p.tmB, full_leader[stage], sc.b0 + 64 * j,
                                      sc.b1, sc.b2);
+            } else if (hinted) {
+                tma_load_3d_pair_hint(s.b[stage], &p.tmB, full_leader[stage], sc.b0, sc.b1, sc.b2, pol_b);
             } else {
                 tma_load_3d_pair(s.b[stage], &p.tmB, full_leader[stage], sc.b0, sc.b1, sc.b2);
             }

@@ -385,6 +385,14 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
                 return CM_ERR_INVALID_ARG;
             }
             return CM_OK;
+        case CM_OPT_L2_HINTS:
+            if (value < 0 || value > 0xff) return CM_ERR_INVALID_ARG;
+            p.l2_hints = int(value);
+            return CM_OK;
+        case CM_OPT_L2_PROMOTION:
+            if (value < 0 || value > 3) return CM_ERR_INVALID_ARG;
+            p.l2_promotion = int(value);
+            return CM_OK;
         case CM_OPT_STATIC_TILES:
             p.static_tiles = value != 0;
             return CM_OK;

@@ -218,6 +218,11 @@ const char *cm_status_string(cm_status status);
  *                        1 gives cluster c the tiles c, c + clusters, ...
  *  CM_OPT_TILE_GROUP     largest number of consecutive same-rank tasks whose
  *                        tiles are interleaved (1..8, default 4).
+ *  CM_OPT_L2_HINTS       CTA-pair kernel, L2 eviction priority of operand
+ *                        loads: bits 0-3 for A, 4-7 for B; 0 normal,
+ *                        1 evict_last, 2 evict_first (default 0).
+ *  CM_OPT_L2_PROMOTION   TMA L2 promotion of operand loads: 0 none, 1 64 B,
+ *                        2 128 B, 3 256 B (default 3).
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
@@ -226,7 +231,9 @@ typedef enum cm_option {
     CM_OPT_SKIP_SIGNAL = 3,
     CM_OPT_KERNEL = 4,
     CM_OPT_STATIC_TILES = 5,
-    CM_OPT_TILE_GROUP = 6
+    CM_OPT_TILE_GROUP = 6,
+    CM_OPT_L2_HINTS = 7,
+    CM_OPT_L2_PROMOTION = 8
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);

@@ -53,6 +53,12 @@ def test_plan_arguments(lib):
         p.step(cm.CM_OP_AG_GEMM, 4, 0, 0)
     with pytest.raises(cm.CMError):
         p.set_option(cm.CM_OPT_TIMEOUT_NS, 0)
+    for opt, bad in ((cm.CM_OPT_L2_HINTS, -1), (cm.CM_OPT_L2_HINTS, 256),
+                     (cm.CM_OPT_L2_PROMOTION, -1), (cm.CM_OPT_L2_PROMOTION, 4)):
+        with pytest.raises(cm.CMError):
+            p.set_option(opt, bad)
+    p.set_option(cm.CM_OPT_L2_HINTS, 0x21)
+    p.set_option(cm.CM_OPT_L2_PROMOTION, 0)
 
 
 def test_steps_counts(lib):

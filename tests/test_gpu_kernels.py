@@ -52,6 +52,23 @@ def test_kernels_agree_bitwise_on_ag():
         assert torch.equal(y, base), k
 
 
+@pytest.mark.parametrize("hints,promotion", [(0x01, 3), (0x21, 0), (0x12, 2)])
+def test_l2_options_change_no_bits(hints, promotion):
+    """Cache-priority hints and L2 promotion only steer caching: same bits out."""
+    N, m, K, n = 4, 320, 512, 768
+    x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=7, w_layout="nk")
+    xr, wr = gen.rs_inputs(N, N * m, K, n, gen.NORMAL1, gen.NORMAL002, seed=8, w_layout="kn")
+    base, _, _ = run_ag(_plan(N, 1, "uni", PAIR), x, w, "nk")
+    base_r, _, _ = run_rs(_plan(N, 1, "uni", PAIR), xr, wr, "kn")
+    p = _plan(N, 1, "uni", PAIR)
+    p.set_option(cm.CM_OPT_L2_HINTS, hints)
+    p.set_option(cm.CM_OPT_L2_PROMOTION, promotion)
+    y, _, _ = run_ag(p, x, w, "nk")
+    yr, _, _ = run_rs(p, xr, wr, "kn")
+    assert torch.equal(y, base)
+    assert torch.equal(yr, base_r)
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_tagged_placement_each_kernel(kernel):
     N, m, K, n = 8, 384, 64, 512
