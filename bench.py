@@ -562,13 +562,15 @@ def run_profile_case(args):
         st.plan.set_option(st.cm.CM_OPT_L2_HINTS, args.l2_hints)
     if args.l2_promotion >= 0:
         st.plan.set_option(st.cm.CM_OPT_L2_PROMOTION, args.l2_promotion)
+    if args.row_band >= 0:
+        st.plan.set_option(st.cm.CM_OPT_ROW_BAND, args.row_band)
     fn = st.ag if args.profile == "ag" else st.rs
     f_ag, f_rs = flops(data["shapes"], N)
     ms = time_loop(fn, args.steps, torch, warmup=args.warmup)
     st.check((args.profile,))
     fl = f_ag if args.profile == "ag" else f_rs
     print(json.dumps({"profile_case": args.workload, "op": args.profile, "N": N, "chunks": args.chunks,
-                      "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group, "l2_hints": args.l2_hints, "l2_promotion": args.l2_promotion,
+                      "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group, "l2_hints": args.l2_hints, "l2_promotion": args.l2_promotion, "row_band": args.row_band,
                       "ms": ms, "tflops": fl / (ms / 1e3) / 1e12}), flush=True)
     return 0
 
@@ -591,6 +593,7 @@ def main(argv=None):
     ap.add_argument("--tile-group", type=int, default=0, help="CM_OPT_TILE_GROUP for --profile (0 = default)")
     ap.add_argument("--l2-hints", type=int, default=-1, help="CM_OPT_L2_HINTS for --profile (-1 = default)")
     ap.add_argument("--l2-promotion", type=int, default=-1, help="CM_OPT_L2_PROMOTION for --profile (-1 = default)")
+    ap.add_argument("--row-band", type=int, default=-1, help="CM_OPT_ROW_BAND for --profile (-1 = default)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="oracle seconds for the cpu_baseline of the default arm")
     ap.add_argument("--ref-seconds", type=float, default=120.0,

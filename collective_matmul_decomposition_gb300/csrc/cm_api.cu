@@ -134,6 +134,7 @@ cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, c
     kp.static_tiles = pl.static_tiles;
     kp.l2_hint_a = pl.l2_hints & 0xf;
     kp.l2_hint_b = (pl.l2_hints >> 4) & 0xf;
+    kp.row_band = pl.row_band;
     const auto &tasks = pl.tasks[op];
     const int ntasks = int(tasks.size());
     if (ntasks > kMaxTasks) return CM_ERR_UNSUPPORTED;

@@ -232,6 +232,32 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const void *tmap, ui
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr)
         : "memory");
 }
+// Same with the destination as a shared-window address and the tensor map as
+// a generic address, for loops that keep both in registers.
+__device__ __forceinline__ void tma_load_3d_pair_a(uint32_t dst, uint64_t tmap, uint32_t bar_cluster_addr, int c0,
+                                                   int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_hint_a(uint32_t dst, uint64_t tmap, uint32_t bar_cluster_addr,
+                                                        int c0, int c1, int c2, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr), "l"(policy)
+        : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_pair_mc_a(uint32_t dst, uint64_t tmap, uint32_t bar_cluster_addr, int c0,
+                                                      int c1, int c2, uint16_t cta_mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
+        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr), "h"(cta_mask)
+        : "memory");
+}
 // Same, with an L2 eviction-priority policy for the loaded lines.
 __device__ __forceinline__ void tma_load_3d_pair_hint(void *dst, const void *tmap, uint32_t bar_cluster_addr, int c0,
                                                       int c1, int c2, uint64_t policy) {

@@ -45,7 +45,8 @@ struct KParams {
     uint32_t *status;
     uint32_t *tile_counter;    // dynamic tile scheduler (CTA-pair kernel), zero at launch
     int static_tiles;          // CTA-pair kernel: 1 = cluster c takes tiles c, c + clusters, ... instead
-    int l2_hint_a, l2_hint_b;  // CTA-pair kernel: L2 priority of A / B loads (0 normal, 1 evict_last, 2 evict_first)
+    int l2_hint_a, l2_hint_b;
+    int row_band;              // row tiles per band of the tile order (0 = a whole task group)  // CTA-pair kernel: L2 priority of A / B loads (0 normal, 1 evict_last, 2 evict_first)
     const uint8_t *x_bytes;    // AG: x and the receive slots as bytes (pair forwarder)
     uint8_t *slot_bytes;
     int64_t row_bytes;         // bytes per A row (K * 2)

@@ -17,11 +17,13 @@ struct TileCoord {
 
 // Linear tile index -> (task, chunk, row tile, column tile) of one CTA (or
 // one CTA pair).  Tiles run task group by task group (see cm_task.tile_group);
-// inside a group the order is chunk, column-tile group, task, row tile, so
-// the tiles running together share one block of weight columns (W_r of the
-// group's rank) and the row tiles that forward (column tile 0) come first in
-// every chunk.  A column-tile group is `pairs` adjacent column tiles, one per
-// CTA pair of a cluster; `pair` selects this pair's.
+// inside a group the order is chunk, row band, column-tile group, row tile of
+// the band.  The group's row tiles (task by task) are cut into bands of
+// `row_band` row tiles (0: one band); each band runs through every column
+// tile before the next band starts, so the tiles running together share one
+// block of weight columns (W_r of the group's rank) and one band of A rows.
+// A column-tile group is `pairs` adjacent column tiles, one per CTA pair of a
+// cluster; `pair` selects this pair's.
 __device__ __forceinline__ TileCoord decode_cl(const KParams &p, int t, uint32_t pair, int pairs) {
     TileCoord c;
     const int task = p.task_begin + t / p.tiles_per_task;
@@ -29,14 +31,28 @@ __device__ __forceinline__ TileCoord decode_cl(const KParams &p, int t, uint32_t
     const int gsize = grp >> 8, gpos = grp & 0xff;
     const int gfirst = task - gpos;
     int u = t - (gfirst - p.task_begin) * p.tiles_per_task;   // tile index inside the group
-    const int per_q = gsize * p.mtiles_c * p.ntile_groups;
+    const int rows = gsize * p.mtiles_c;                       // row tiles of the group
+    const int per_q = rows * p.ntile_groups;
     c.q = u / per_q;
     u -= c.q * per_q;
-    const int per_g = gsize * p.mtiles_c;
-    const int g = u / per_g;
-    u -= g * per_g;
-    const int off = u / p.mtiles_c;
-    c.mt = u - off * p.mtiles_c;
+    const int band = p.row_band > 0 && p.row_band < rows ? p.row_band : rows;
+    const int full = rows / band;
+    const int in_full = full * band * p.ntile_groups;
+    int b0, bs;   // first row tile and row tiles of this tile's band
+    if (u < in_full) {
+        const int b = u / (band * p.ntile_groups);
+        b0 = b * band;
+        bs = band;
+        u -= b * band * p.ntile_groups;
+    } else {
+        b0 = full * band;
+        bs = rows - b0;
+        u -= in_full;
+    }
+    const int g = u / bs;
+    const int rho = b0 + (u - g * bs);
+    const int off = rho / p.mtiles_c;
+    c.mt = rho - off * p.mtiles_c;
     c.task = gfirst + off;
     c.nt = g * pairs + int(pair);
     return c;

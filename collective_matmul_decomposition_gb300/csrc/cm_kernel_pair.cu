@@ -27,7 +27,7 @@
 //   warp 0    producer: leader = scheduler + TMA loads of its halves;
 //             peer = TMA loads of its halves.  All loads complete on the
 //             leader's ring barrier; the leader posts the byte count.  The
-//             producer takes the next tile index one tile early.
+//             leader takes the next tile index while the current tile loads.
 //   warp 1    MMA issuer (leader only): pair MMAs; commits each stage and,
 //             per tile, the accumulator to the barriers of both CTAs.
 //   warp 2    AG forwarder (both CTAs): every tile copies a slice of its CTA's
@@ -70,8 +70,7 @@ struct Cl {
 };
 
 struct PSmem {
-    uint8_t *a[kPStages];
-    uint8_t *b[kPStages];
+    uint8_t *a0, *b0;   // ring stage 0 of A and B; stage i is kHalfA (kHalfB) bytes further
     uint8_t *fbuf[2];   // AG: forwarder copy buffers; RS: the same 32 KB as 8 epilogue-warp buffers
     uint64_t *full, *empty, *tfull, *tempty, *drain, *fbar, *qfull, *qempty, *ebar;
     volatile int32_t *qtile;
@@ -84,15 +83,13 @@ struct PSmem {
 struct QueueReader {
     int slot = 0;
     uint32_t phase = 0;
-    uint32_t qempty_leader[kQueue];
+    uint32_t qempty_leader0;   // slot i's release barrier on the leader: 8*i bytes further
 
-    __device__ void init(const PSmem &s) {
-        for (int i = 0; i < kQueue; ++i) qempty_leader[i] = mapa_shared(smem_u32(&s.qempty[i]), 0);
-    }
+    __device__ void init(const PSmem &s) { qempty_leader0 = mapa_shared(smem_u32(&s.qempty[0]), 0); }
     __device__ int next(const KParams &p, const PSmem &s) {
         int t = -1;
         if (wait_mbar<true>(p, s.abort, &s.qfull[slot], phase, kSiteEmpty, -1, -1)) t = s.qtile[slot];
-        mbar_arrive_cluster(qempty_leader[slot]);
+        mbar_arrive_cluster(qempty_leader0 + 8u * uint32_t(slot));
         if (++slot == kQueue) {
             slot = 0;
             phase ^= 1u;
@@ -101,43 +98,23 @@ struct QueueReader {
     }
 };
 
-// Operand coordinates of K slice `kk` of tile `c` for this CTA's halves.
-struct SliceCoord {
-    const void *tmA;
-    int a0, a1, a2;   // A: K offset, row, slab
-    int b0, b1, b2;   // B: K offset (or column), column (or K offset), rank
-};
-
-template <bool B_MN, int CL>
-__device__ __forceinline__ SliceCoord slice_coord(const KParams &p, const TileCoord &c, const cm_task &tk, int kk,
-                                                  const Cl &cl) {
-    SliceCoord sc;
-    int rr = tk.rank, kb = kk, slab = tk.a_slab * p.chunks + c.q;
-    if (tk.a_src == 2) {
-        rr = kk / p.kblocks;
-        kb = kk - rr * p.kblocks;
-        slab = (rr * p.N + tk.out_idx) * p.chunks + c.q;
-    }
-    sc.tmA = tk.a_src == 1 ? static_cast<const void *>(&p.tmA1) : static_cast<const void *>(&p.tmA0);
-    sc.a0 = kb * kBK;
-    // two-pair clusters: this CTA loads quarter `pair` of its A half (multicast)
-    sc.a1 = c.mt * kPairRows + int(cl.pos) * kCtaRows + (CL == 4 ? int(cl.pair) * (kCtaRows / 2) : 0);
-    sc.a2 = slab;
-    const int n0 = c.nt * kBN + int(cl.pos) * (kBN / 2);
-    sc.b0 = B_MN ? n0 : kb * kBK;
-    sc.b1 = B_MN ? kb * kBK : n0;
-    sc.b2 = rr;
-    return sc;
+// Ring-barrier wait: one inline try first (the common case -- the stage is
+// already free or full), the bounded loop only when that fails.
+__device__ __forceinline__ bool ring_wait(const KParams &p, volatile int *abort, uint64_t *bar, uint32_t parity,
+                                          uint32_t site, int task, int q) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return wait_mbar<false>(p, abort, bar, parity, site, task, q);
 }
 
 template <bool B_MN, int CL>
 __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &cl) {
     int stage = 0;
     uint32_t phase = 0;
-    int last_parity[kPStages];
-    for (int i = 0; i < kPStages; ++i) last_parity[i] = -1;
-    uint32_t full_leader[kPStages];
-    for (int i = 0; i < kPStages; ++i) full_leader[i] = mapa_shared(smem_u32(&s.full[i]), cl.leader);
+    uint32_t issued = 0;   // ring stages filled so far
+    // the leader's ring barrier of stage i sits 8*i bytes after stage 0's
+    const uint32_t full_leader0 = mapa_shared(smem_u32(&s.full[0]), cl.leader);
+    const uint32_t a_smem0 = smem_u32(s.a0) + (CL == 4 ? cl.pair * (kHalfA / 2) : 0u);
+    const uint32_t b_smem0 = smem_u32(s.b0);
     // bytes per stage for the pair: each CTA's A half (one box, or two
     // multicast quarters) and B half
     const uint32_t a_half = uint32_t(p.a_box_rows) * kBK * 2 * (CL == 4 ? 2u : 1u);
@@ -148,25 +125,30 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
     };
     const uint64_t pol_a = policy(p.l2_hint_a), pol_b = policy(p.l2_hint_b);
     const bool hinted = p.l2_hint_a != 0 || p.l2_hint_b != 0;
+    const uint64_t tm_b = reinterpret_cast<uint64_t>(&p.tmB);
     QueueReader qr;
     qr.init(s);
     int qslot = 0;
     uint32_t qphase = 0;
-    // next tile index: the cluster leader takes it from the counter (or, with
-    // static tiles, the next of its round-robin share) and publishes it to
-    // every CTA of the cluster; the others read the queue
+    // Tile indices: the cluster leader takes them from the global counter (or
+    // the next of its static round-robin share) and publishes them to every
+    // CTA of the cluster through the queue; the others read the queue.  The
+    // leader takes the index of the next tile while the first slices of the
+    // current one are already loading and publishes it a few slices later, so
+    // the counter's round trip never sits between two tiles' loads; the other
+    // CTAs read it at the tile boundary, long after it was published.
     const int cid = int(blockIdx.x) / CL, ncl = int(gridDim.x) / CL;
     int static_next = cid;
-    auto fetch = [&]() -> int {
-        if (cl.rank != 0) return qr.next(p, s);
-        if (!wait_mbar<true>(p, s.abort, &s.qempty[qslot], qphase ^ 1u, kSiteEmpty, -1, -1)) return -1;
-        int t;
+    auto take = [&]() -> int {
         if (p.static_tiles) {
-            t = static_next;
+            const int t = static_next;
             static_next += ncl;
-        } else {
-            t = int(atomic_add_relaxed(p.tile_counter, 1u));
+            return t;
         }
+        return int(atomic_add_relaxed(p.tile_counter, 1u));
+    };
+    auto publish = [&](int t) -> int {
+        if (!wait_mbar<true>(p, s.abort, &s.qempty[qslot], qphase ^ 1u, kSiteEmpty, -1, -1)) return -1;
         if (t >= total) t = -1;
         s.qtile[qslot] = t;
         for (uint32_t r = 1; r < uint32_t(CL); ++r)
@@ -179,10 +161,8 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
         }
         return t;
     };
-    // the next tile is taken while the current one streams, so no tile
-    // boundary waits on the global counter
-    int cur = fetch();
-    int nxt = cur >= 0 ? fetch() : -1;
+    const bool leads = cl.rank == 0;
+    int cur = leads ? publish(take()) : qr.next(p, s);
     while (cur >= 0 && !*s.abort) {
         const TileCoord c = decode_cl(p, cur, cl.pair, CL / 2);
         const cm_task &tk = p.tasks[c.task];
@@ -191,46 +171,69 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
                 break;
             fence_proxy_async_global();
         }
+        // Slice coordinates.  A: (K offset, row, slab); B: (K offset, column,
+        // rank), or (column, K offset, rank) when W is MN-major.  A tile that
+        // sums over ranks (a_src 2) walks rank by rank through the K slices.
+        const bool sum_ranks = tk.a_src == 2;
+        int rr = sum_ranks ? 0 : tk.rank;
+        int slab = (sum_ranks ? tk.out_idx : tk.a_slab) * p.chunks + c.q;
+        const int slab_step = p.N * p.chunks;
+        const uint64_t tm_a = reinterpret_cast<uint64_t>(tk.a_src == 1 ? &p.tmA1 : &p.tmA0);
+        // two-pair clusters: this CTA loads quarter `pair` of its A half (multicast)
+        const int a_row = c.mt * kPairRows + int(cl.pos) * kCtaRows + (CL == 4 ? int(cl.pair) * (kCtaRows / 2) : 0);
+        const int n0 = c.nt * kBN + int(cl.pos) * (kBN / 2);
         const int nk = kslices(p, tk);
+        const int publish_at = min(3, nk - 1);
+        int taken = 0, nxt = -1, kb = 0;
         bool ok = true;
         for (int kk = 0; kk < nk; ++kk) {
-            const SliceCoord sc = slice_coord<B_MN, CL>(p, c, tk, kk, cl);
-            if (!wait_mbar<true>(p, s.abort, &s.empty[stage], phase ^ 1u, kSiteEmpty, c.task, c.q)) {
+            if (!ring_wait(p, s.abort, s.empty + stage, phase ^ 1u, kSiteEmpty, c.task, c.q)) {
                 ok = false;
                 break;
             }
-            if (cl.pos == 0) mbar_expect_tx(&s.full[stage], tx_pair);
+            const uint32_t fb = full_leader0 + 8u * uint32_t(stage);
+            const uint32_t sa = a_smem0 + uint32_t(stage) * kHalfA, sb = b_smem0 + uint32_t(stage) * kHalfB;
+            const int k0 = kb * kBK;
+            if (cl.pos == 0) mbar_expect_tx(s.full + stage, tx_pair);
             if (CL == 4)
-                tma_load_3d_pair_mc(s.a[stage] + cl.pair * (kHalfA / 2), sc.tmA, full_leader[stage], sc.a0, sc.a1,
-                                    sc.a2, mc_mask);
+                tma_load_3d_pair_mc_a(sa, tm_a, fb, k0, a_row, slab, mc_mask);
             else if (hinted)
-                tma_load_3d_pair_hint(s.a[stage], sc.tmA, full_leader[stage], sc.a0, sc.a1, sc.a2, pol_a);
+                tma_load_3d_pair_hint_a(sa, tm_a, fb, k0, a_row, slab, pol_a);
             else
-                tma_load_3d_pair(s.a[stage], sc.tmA, full_leader[stage], sc.a0, sc.a1, sc.a2);
+                tma_load_3d_pair_a(sa, tm_a, fb, k0, a_row, slab);
             if (B_MN) {
                 for (int j = 0; j < kBN / 2 / 64; ++j)
-                    tma_load_3d_pair(s.b[stage] + j * (64 * kBK * 2), &p.tmB, full_leader[stage], sc.b0 + 64 * j,
-                                     sc.b1, sc.b2);
+                    tma_load_3d_pair_a(sb + uint32_t(j * (64 * kBK * 2)), tm_b, fb, n0 + 64 * j, k0, rr);
             } else if (hinted) {
-                tma_load_3d_pair_hint(s.b[stage], &p.tmB, full_leader[stage], sc.b0, sc.b1, sc.b2, pol_b);
+                tma_load_3d_pair_hint_a(sb, tm_b, fb, k0, n0, rr, pol_b);
             } else {
-                tma_load_3d_pair(s.b[stage], &p.tmB, full_leader[stage], sc.b0, sc.b1, sc.b2);
+                tma_load_3d_pair_a(sb, tm_b, fb, k0, n0, rr);
             }
-            last_parity[stage] = int(phase);
+            ++issued;
             if (++stage == kPStages) {
                 stage = 0;
                 phase ^= 1u;
             }
+            if (++kb == p.kblocks) {
+                kb = 0;
+                ++rr;
+                slab += slab_step;
+            }
+            if (leads) {
+                if (kk == 0) taken = take();   // the result is not needed until publish_at
+                if (kk == publish_at) nxt = publish(taken);
+            }
         }
         if (!ok) break;
-        cur = nxt;
-        nxt = cur >= 0 ? fetch() : -1;
+        cur = leads ? nxt : qr.next(p, s);
     }
     // a pair leader's ring barriers count every load into its pair: once they
-    // complete, no load is still writing this pair's shared memory
+    // complete, no load is still writing this pair's shared memory.  Stage i
+    // was last filled in the current round of the ring if i < stage, else in
+    // the round before (if it was filled at all).
     if (cl.pos == 0)
         for (int i = 0; i < kPStages; ++i)
-            if (last_parity[i] >= 0) drain_mbar<true>(p, &s.full[i], uint32_t(last_parity[i]));
+            if (uint32_t(i) < issued) drain_mbar<true>(p, &s.full[i], i < stage ? phase : phase ^ 1u);
 }
 
 template <bool B_MN, int CL>
@@ -238,6 +241,10 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
     constexpr uint32_t kIdesc = idesc_bf16(kPairRows, kBN, B_MN);
     constexpr uint32_t kBLbo = B_MN ? 64 * kBK * 2 : 16;
     constexpr uint32_t kBStep = B_MN ? (16 * 128) >> 4 : 32 >> 4;
+    // descriptors of ring stage 0; stage i adds its byte offset / 16 to the
+    // start-address field (shared addresses stay below 2^18, so no carry)
+    const uint64_t ad0 = desc_sw128(smem_u32(s.a0), 16, 1024);
+    const uint64_t bd0 = desc_sw128(smem_u32(s.b0), kBLbo, 1024);
     QueueReader qr;
     qr.init(s);
     int stage = 0;
@@ -255,17 +262,17 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
         const int nk = kslices(p, tk);
         bool ok = true;
         for (int kk = 0; kk < nk; ++kk) {
-            if (!wait_mbar<true>(p, s.abort, &s.full[stage], phase, kSiteFull, c.task, c.q)) {
+            if (!ring_wait(p, s.abort, s.full + stage, phase, kSiteFull, c.task, c.q)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            const uint64_t ad = desc_sw128(smem_u32(s.a[stage]), 16, 1024);
-            const uint64_t bd = desc_sw128(smem_u32(s.b[stage]), kBLbo, 1024);
+            const uint64_t ad = ad0 + uint64_t((uint32_t(stage) * kHalfA) >> 4);
+            const uint64_t bd = bd0 + uint64_t((uint32_t(stage) * kHalfB) >> 4);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
                 mma_bf16_pair(d, ad + uint64_t(2 * k), bd + uint64_t(kBStep * k), kIdesc, (kk | k) != 0 ? 1u : 0u);
-            mma_commit_pair_mc(&s.empty[stage], uint16_t((1u << CL) - 1u));   // every CTA's stage s
+            mma_commit_pair_mc(s.empty + stage, uint16_t((1u << CL) - 1u));   // every CTA's stage s
             if (++stage == kPStages) {
                 stage = 0;
                 phase ^= 1u;
@@ -397,8 +404,7 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
     const int quad = e & 3;                      // TMEM lanes 32*quad.. (warp % 4)
     const int half = e >> 2;                     // columns 128*half..
     const bool leader_thread = e == 0 && lane == 0;
-    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&s.tempty[0]), cl.leader),
-                                       mapa_shared(smem_u32(&s.tempty[1]), cl.leader)};
+    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&s.tempty[0]), cl.leader);   // buffer b: +8*b
     QueueReader qr;
     if (lane == 0) qr.init(s);
     int accb = 0;
@@ -453,7 +459,7 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty_leader[accb]);
+        if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * uint32_t(accb));
         if (p.op == 1 && tk.sig_done >= 0) {
             __threadfence();
             bar_sync(1, kPEpiWarps * 32);
@@ -483,8 +489,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
     const int quad = e & 3;
     const int half = e >> 2;
     const bool leader_thread = e == 0 && lane == 0;
-    const uint32_t tempty_leader[2] = {mapa_shared(smem_u32(&s.tempty[0]), cl.leader),
-                                       mapa_shared(smem_u32(&s.tempty[1]), cl.leader)};
+    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&s.tempty[0]), cl.leader);   // buffer b: +8*b
     uint8_t *buf = s.fbuf[0] + e * 4096;
     uint64_t *eb = &s.ebar[e];
     uint32_t eph = 0;
@@ -590,7 +595,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(tempty_leader[accb]);
+        if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * uint32_t(accb));
         if (tk.sig_done >= 0 && real) {
             if (lane == 0) {
                 bulk_wait<0>();            // this warp's bucket slices are in global memory
@@ -614,10 +619,8 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     PSmem s;
-    for (int i = 0; i < kPStages; ++i) {
-        s.a[i] = base + i * kHalfA;
-        s.b[i] = base + kPStages * kHalfA + i * kHalfB;
-    }
+    s.a0 = base;
+    s.b0 = base + kPStages * kHalfA;
     s.fbuf[0] = base + kPStages * (kHalfA + kHalfB);
     s.fbuf[1] = s.fbuf[0] + kFwdPiece;
     uint64_t *bars = reinterpret_cast<uint64_t *>(s.fbuf[1] + kFwdPiece);

@@ -223,6 +223,10 @@ const char *cm_status_string(cm_status status);
  *                        1 evict_last, 2 evict_first (default 0).
  *  CM_OPT_L2_PROMOTION   TMA L2 promotion of operand loads: 0 none, 1 64 B,
  *                        2 128 B, 3 256 B (default 3).
+ *  CM_OPT_ROW_BAND       tile order: row tiles per band (0..4096; 0 = one band
+ *                        per task group, the default).  Each band of a task
+ *                        group's row tiles runs through every column tile
+ *                        before the next band starts.
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
@@ -233,7 +237,8 @@ typedef enum cm_option {
     CM_OPT_STATIC_TILES = 5,
     CM_OPT_TILE_GROUP = 6,
     CM_OPT_L2_HINTS = 7,
-    CM_OPT_L2_PROMOTION = 8
+    CM_OPT_L2_PROMOTION = 8,
+    CM_OPT_ROW_BAND = 9
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);

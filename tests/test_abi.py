@@ -54,7 +54,8 @@ def test_plan_arguments(lib):
     with pytest.raises(cm.CMError):
         p.set_option(cm.CM_OPT_TIMEOUT_NS, 0)
     for opt, bad in ((cm.CM_OPT_L2_HINTS, -1), (cm.CM_OPT_L2_HINTS, 256),
-                     (cm.CM_OPT_L2_PROMOTION, -1), (cm.CM_OPT_L2_PROMOTION, 4)):
+                     (cm.CM_OPT_L2_PROMOTION, -1), (cm.CM_OPT_L2_PROMOTION, 4),
+                     (cm.CM_OPT_ROW_BAND, -1), (cm.CM_OPT_ROW_BAND, 4097)):
         with pytest.raises(cm.CMError):
             p.set_option(opt, bad)
     p.set_option(cm.CM_OPT_L2_HINTS, 0x21)

@@ -69,6 +69,25 @@ def test_l2_options_change_no_bits(hints, promotion):
     assert torch.equal(yr, base_r)
 
 
+@pytest.mark.parametrize("kernel", [PAIR, SINGLE, PAIR_CL4])
+@pytest.mark.parametrize("band", [1, 3])
+def test_row_bands_change_no_bits(kernel, band):
+    """The row-band tile order only reorders tiles: same bits out."""
+    N, m, K, n = 4, 320, 256, 1280
+    x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=17, w_layout="nk")
+    xr, wr = gen.rs_inputs(N, N * m, K, n, gen.NORMAL1, gen.NORMAL002, seed=18, w_layout="nk")
+    base, _, _ = run_ag(_plan(N, 2, "uni", kernel), x, w, "nk")
+    base_r, _, _ = run_rs(_plan(N, 2, "uni", kernel), xr, wr, "nk")
+    p = _plan(N, 2, "uni", kernel)
+    p.set_option(cm.CM_OPT_ROW_BAND, band)
+    y, _, _ = run_ag(p, x, w, "nk")
+    yr, _, _ = run_rs(p, xr, wr, "nk")
+    assert torch.equal(y, base)
+    assert torch.equal(yr, base_r)
+    ref = oracle.ag_gemm(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
+    assert oracle.normwise_max_rel_err(_np(y), ref) <= TOL_F32
+
+
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_tagged_placement_each_kernel(kernel):
     N, m, K, n = 8, 384, 64, 512

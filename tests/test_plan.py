@@ -141,30 +141,33 @@ def test_slots_written_once():
         assert len(rs) == len(set(rs))
 
 
-def kernel_tile_order(tasks, c, mtiles, ntiles):
+def kernel_tile_order(tasks, c, mtiles, ntiles, band=0):
     """The kernels' tile order: task groups (cm_task.tile_group) in table
-    order; inside a group chunk, column tile, task, row tile."""
+    order; inside a group chunk, row band (`band` row tiles of the group's
+    task-by-task row tiles; 0 = one band), column tile, row tile of the band."""
     out = []
     t = 0
     while t < len(tasks):
         size = tasks[t].tile_group >> 8
         assert size >= 1 and all((tasks[t + j].tile_group & 0xff) == j for j in range(size))
         assert len({tasks[t + j].rank for j in range(size)}) == 1, "a group is one rank's tasks"
+        rows = size * mtiles
+        b = band if 0 < band < rows else rows
         for q in range(c):
-            for nt in range(ntiles):
-                for j in range(size):
-                    for mt in range(mtiles):
-                        out.append((t + j, q, mt, nt))
+            for b0 in range(0, rows, b):
+                for nt in range(ntiles):
+                    for rho in range(b0, min(rows, b0 + b)):
+                        out.append((t + rho // mtiles, q, rho % mtiles, nt))
         t += size
     return out
 
 
-def _simulate(p, op, mtiles, ntiles, grid, seed):
+def _simulate(p, op, mtiles, ntiles, grid, seed, band=0):
     """Run the task table like the kernel: returns final outputs (see module doc)."""
     rnd = random.Random(seed)
     N, c = p.N, p.chunks
     tasks = p.tasks(op)
-    tiles = kernel_tile_order(tasks, c, mtiles, ntiles)
+    tiles = kernel_tile_order(tasks, c, mtiles, ntiles, band)
     flags = {}
     tgt_ag_in, tgt_ag_free = mtiles, mtiles * ntiles
     tgt_rs = mtiles * ntiles
@@ -273,6 +276,35 @@ def test_protocol_simulation(N, direction, chunks, grid, group):
         out = _simulate(p, RS, mtiles, ntiles, grid, seed)
         assert len(out) == N * c * mtiles * ntiles
         assert all(v == frozenset(range(N)) for v in out.values())
+
+
+@pytest.mark.parametrize("N", [3, 4, 8])
+@pytest.mark.parametrize("direction", ["uni", "bidi"])
+@pytest.mark.parametrize("chunks", [1, 2])
+@pytest.mark.parametrize("grid", [3, 16])
+@pytest.mark.parametrize("band", [1, 3])
+def test_protocol_simulation_row_bands(N, direction, chunks, grid, band):
+    """Row bands reorder tiles inside a task group only: no new wait cycles."""
+    p = cm.Plan(N, chunks, direction)
+    c = p.chunks
+    mtiles, ntiles = 2, 3
+    for seed in range(2):
+        out = _simulate(p, AG, mtiles, ntiles, grid, seed, band)
+        assert len(out) == N * N * c * mtiles * ntiles
+        out = _simulate(p, RS, mtiles, ntiles, grid, seed, band)
+        assert all(v == frozenset(range(N)) for v in out.values())
+
+
+@pytest.mark.parametrize("band", [0, 1, 2, 3, 5, 100])
+def test_row_band_order_is_a_permutation(band):
+    p = cm.Plan(8, 2, "uni")
+    for op in (AG, RS):
+        tasks = p.tasks(op)
+        base = kernel_tile_order(tasks, 2, 3, 4)
+        order = kernel_tile_order(tasks, 2, 3, 4, band)
+        assert sorted(order) == sorted(base)
+        if band in (0, 100):
+            assert order == base
 
 
 def test_skip_signal_starves_consumer():
