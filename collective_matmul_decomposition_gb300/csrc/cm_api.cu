@@ -98,6 +98,8 @@ KernelChoice choose_kernel(const PlanImpl &pl, int64_t n) {
     }
 }
 
+constexpr int64_t kRowBandBytes = int64_t(32) << 20;   // A bytes per row band of the tile order
+
 // Row tiles, column tiles and flag targets for the selected kernel.
 void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int64_t n) {
     const int tm = kc.pair ? pair_rows() : kBM;
@@ -134,7 +136,14 @@ cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, c
     kp.static_tiles = pl.static_tiles;
     kp.l2_hint_a = pl.l2_hints & 0xf;
     kp.l2_hint_b = (pl.l2_hints >> 4) & 0xf;
-    kp.row_band = pl.row_band;
+    // row bands: explicit, or as many row tiles as hold about 32 MB of A
+    // (a band's A rows stay in L2 while the band runs through the columns)
+    if (pl.row_band > 0) {
+        kp.row_band = pl.row_band;
+    } else {
+        const int64_t tile_bytes = int64_t(kc.pair ? pair_rows() : kBM) * kp.kblocks * kBK * 2;
+        kp.row_band = int(std::max<int64_t>(1, kRowBandBytes / tile_bytes));
+    }
     const auto &tasks = pl.tasks[op];
     const int ntasks = int(tasks.size());
     if (ntasks > kMaxTasks) return CM_ERR_UNSUPPORTED;

@@ -223,10 +223,12 @@ const char *cm_status_string(cm_status status);
  *                        1 evict_last, 2 evict_first (default 0).
  *  CM_OPT_L2_PROMOTION   TMA L2 promotion of operand loads: 0 none, 1 64 B,
  *                        2 128 B, 3 256 B (default 3).
- *  CM_OPT_ROW_BAND       tile order: row tiles per band (0..4096; 0 = one band
- *                        per task group, the default).  Each band of a task
- *                        group's row tiles runs through every column tile
- *                        before the next band starts.
+ *  CM_OPT_ROW_BAND       tile order: row tiles per band (1..4096), or 0 (the
+ *                        default) for as many row tiles as hold about 32 MB
+ *                        of the A operand.  Each band of a task group's row
+ *                        tiles runs through every column tile before the
+ *                        next band starts; 4096 puts a whole group in one
+ *                        band.
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
