@@ -98,11 +98,12 @@ struct QueueReader {
     }
 };
 
-// Ring-barrier wait: one inline try first (the common case -- the stage is
-// already free or full), the bounded loop only when that fails.
+// Ring-barrier wait.  `ready` is a non-blocking test of the same barrier
+// made right after the previous stage was handled, so its latency overlaps
+// that stage's work; only when it said "not yet" is the barrier waited on.
 __device__ __forceinline__ bool ring_wait(const KParams &p, volatile int *abort, uint64_t *bar, uint32_t parity,
-                                          uint32_t site, int task, int q) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                          bool ready, uint32_t site, int task, int q) {
+    if (ready || mbar_try_wait(bar, parity)) return true;
     return wait_mbar<false>(p, abort, bar, parity, site, task, q);
 }
 
@@ -186,8 +187,9 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
         const int publish_at = min(3, nk - 1);
         int taken = 0, nxt = -1, kb = 0;
         bool ok = true;
+        bool free_ready = mbar_test_wait(s.empty + stage, phase ^ 1u);
         for (int kk = 0; kk < nk; ++kk) {
-            if (!ring_wait(p, s.abort, s.empty + stage, phase ^ 1u, kSiteEmpty, c.task, c.q)) {
+            if (!ring_wait(p, s.abort, s.empty + stage, phase ^ 1u, free_ready, kSiteEmpty, c.task, c.q)) {
                 ok = false;
                 break;
             }
@@ -214,6 +216,7 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
                 stage = 0;
                 phase ^= 1u;
             }
+            free_ready = mbar_test_wait(s.empty + stage, phase ^ 1u);
             if (++kb == p.kblocks) {
                 kb = 0;
                 ++rr;
@@ -261,8 +264,9 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
         const uint32_t d = tmem_base + uint32_t(accb * kBN);
         const int nk = kslices(p, tk);
         bool ok = true;
+        bool full_ready = mbar_test_wait(s.full + stage, phase);
         for (int kk = 0; kk < nk; ++kk) {
-            if (!ring_wait(p, s.abort, s.full + stage, phase, kSiteFull, c.task, c.q)) {
+            if (!ring_wait(p, s.abort, s.full + stage, phase, full_ready, kSiteFull, c.task, c.q)) {
                 ok = false;
                 break;
             }
@@ -277,6 +281,7 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
                 stage = 0;
                 phase ^= 1u;
             }
+            full_ready = mbar_test_wait(s.full + stage, phase);
         }
         if (!ok) break;
         mma_commit_pair_mc(&s.tfull[accb], uint16_t(3u << (2u * cl.pair)));   // this pair's CTAs
