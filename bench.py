@@ -534,6 +534,89 @@ def run_sweep(args):
     return 0
 
 
+def named_workload_inputs(name):
+    """(N, inputs) of a named workload other than the MLP sweep; an op the
+    workload does not define gets a tiny stand-in so that Step can be built."""
+    from collective_matmul_decomposition_gb300 import inputs as gen
+    wl = gen.WORKLOADS[name]
+    N = wl["N"]
+    a = wl.get("ag") or {"m": 128, "K": 128, "n": 256, "x": gen.NORMAL1, "w": gen.NORMAL002, "seed": 1}
+    r = wl.get("rs") or {"M": 128 * N, "k": 128, "n": 256, "x": gen.NORMAL1, "w": gen.NORMAL002, "seed": 2}
+    x1, w1 = gen.ag_inputs(N, a["m"], a["K"], a["n"], a["x"], a["w"], a["seed"], "nk")
+    x2, w2 = gen.rs_inputs(N, r["M"], r["k"], r["n"], r["x"], r["w"], r["seed"], "nk")
+    return N, {"shapes": {"ag": dict(m=a["m"], K=a["K"], n=a["n"]), "rs": dict(M=r["M"], k=r["k"], n=r["n"])},
+               "cpu": (x1, w1, x2, w2)}
+
+
+# NVLink-class per-GPU rates for the gate's projection (one direction of one
+# link to a ring neighbour, and the native collective's bandwidth through the
+# same fabric); a stated assumption, not a measurement of this box.
+NVLINK_GBS, NVLINK_HOP_US = 900.0, 2.0
+
+
+def run_gate(args):
+    """The cost model against measurement.  For each workload: the decomposed
+    and the undecomposed op timed on this GPU, the model's prediction of both
+    with rates derived for one GPU (all N ranks share its GEMM rate and HBM,
+    and the native collective is free because every partial already sits in
+    one memory), its choice, and its choice for the same shapes under
+    NVLink-class rates (a projection)."""
+    import torch
+    import __graft_entry__
+    from collective_matmul_decomposition_gb300 import cm
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    peaks, kind = load_peaks()
+    hbm = float(peaks["hbm_gbs"])
+    cases = [("sp_mlp_fc1_ag_n8", ("ag",)), ("sp_mlp_fc2_rs_n8", ("rs",)), ("gpt3_h12288_s2048_n8", ("ag", "rs"))]
+    cases += [(f"{WORKLOAD}:N={N}", ("ag", "rs")) for N in (4, 8, 16)]
+    for name, ops in cases:
+        if name.startswith(WORKLOAD):
+            N = int(name.split("=")[1])
+            data, direction, chunks = make_step_inputs(N, device), "uni", 1
+        else:
+            from collective_matmul_decomposition_gb300 import inputs as gen
+            N, data = named_workload_inputs(name)
+            direction, chunks = gen.WORKLOADS[name]["direction"], gen.WORKLOADS[name]["chunks"]
+        f_ag, f_rs = flops(data["shapes"], N)
+        dec, mono = Step(N, chunks, direction, data, device), Step(N, 1, "none", data, device)
+        for op in ops:
+            fl = f_ag if op == "ag" else f_rs
+            ms_dec = time_loop(getattr(dec, op), args.steps, torch, warmup=args.warmup)
+            ms_none = time_loop(getattr(mono, op), args.steps, torch, warmup=args.warmup)
+            dec.check((op,))
+            mono.check((op,))
+            sh = data["shapes"][op]
+            rows, K, n = (sh["m"], sh["K"], sh["n"]) if op == "ag" else (sh["M"], sh["k"], sh["n"])
+            code = cm.CM_OP_AG_GEMM if op == "ag" else cm.CM_OP_GEMM_RS
+            rate = fl / (ms_none / 1e3) / 1e12   # this GPU's rate on the undecomposed op
+            # one GPU: the ranks share its GEMM rate and HBM (a rotation byte is
+            # read and written), the native collective moves nothing (every
+            # partial is already in one memory), and a message costs at least
+            # one release/acquire flag round trip (~1 us)
+            one_gpu = dict(gemm_tflops=rate / N, ring_gbs=hbm / (2 * N), coll_gbs=1e12, hop_us=1.0, mem_gbs=hbm / N)
+            pred_dec = cm.cost_estimate(N, chunks, direction, code, rows, K, n, one_gpu)
+            pred_none = cm.cost_estimate(N, 1, "none", code, rows, K, n, one_gpu)
+            pick = cm.plan_choose(N, code, rows, K, n, one_gpu)
+            nvl = dict(gemm_tflops=rate, ring_gbs=NVLINK_GBS, coll_gbs=NVLINK_GBS, hop_us=NVLINK_HOP_US, mem_gbs=hbm)
+            pick_nvl = cm.plan_choose(N, code, rows, K, n, nvl)
+            faster = "decomposed" if ms_dec < ms_none else "undecomposed"
+            # within 5 % either way is a tie, and a tie agrees with either choice
+            agrees = (ms_none <= ms_dec * 1.05) if pick[1] == "none" else (ms_dec <= ms_none * 1.05)
+            print(json.dumps({"gate": name, "op": op, "N": N, "chunks": chunks, "ring": direction,
+                              "measured_ms": {"decomposed": ms_dec, "undecomposed": ms_none, "faster": faster},
+                              "one_gpu_model": {"rates": one_gpu, "decomposed_ms": pred_dec / 1e3,
+                                                "undecomposed_ms": pred_none / 1e3,
+                                                "choice": {"chunks": pick[0], "ring": pick[1]},
+                                                "agrees_with_measurement": agrees},
+                              "nvlink_projection": {"rates": nvl, "choice": {"chunks": pick_nvl[0], "ring": pick_nvl[1]},
+                                                    "predicted_ms": pick_nvl[2] / 1e3},
+                              "peak_source": kind}), flush=True)
+        del dec, mono, data
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_profile_case(args):
     """A few calls of one op of one workload, nothing else: the command ncu captures."""
     import torch
@@ -545,14 +628,7 @@ def run_profile_case(args):
     if args.workload == WORKLOAD:
         data = make_step_inputs(N, device)
     else:
-        wl = gen.WORKLOADS[args.workload]
-        N = wl["N"]
-        a = wl.get("ag") or {"m": 128, "K": 128, "n": 256, "x": gen.NORMAL1, "w": gen.NORMAL002, "seed": 1}
-        r = wl.get("rs") or {"M": 128 * N, "k": 128, "n": 256, "x": gen.NORMAL1, "w": gen.NORMAL002, "seed": 2}
-        x1, w1 = gen.ag_inputs(N, a["m"], a["K"], a["n"], a["x"], a["w"], a["seed"], "nk")
-        x2, w2 = gen.rs_inputs(N, r["M"], r["k"], r["n"], r["x"], r["w"], r["seed"], "nk")
-        data = {"shapes": {"ag": dict(m=a["m"], K=a["K"], n=a["n"]), "rs": dict(M=r["M"], k=r["k"], n=r["n"])},
-                "cpu": (x1, w1, x2, w2)}
+        N, data = named_workload_inputs(args.workload)
     st = Step(N, args.chunks, args.ring, data, device)
     st.plan.set_option(st.cm.CM_OPT_KERNEL, args.kernel)
     st.plan.set_option(st.cm.CM_OPT_STATIC_TILES, args.static_tiles)
@@ -582,6 +658,7 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true")
+    ap.add_argument("--gate", action="store_true", help="the cost model's choices against measurement")
     ap.add_argument("--profile", choices=["ag", "rs"], default=None,
                     help="run only --steps calls of one op (for ncu captures)")
     ap.add_argument("--workload", default=WORKLOAD)
@@ -605,6 +682,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sweep:
         return run_sweep(args)
+    if args.gate:
+        return run_gate(args)
     if args.profile:
         return run_profile_case(args)
     return run_ours(args)

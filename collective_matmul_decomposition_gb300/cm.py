@@ -31,8 +31,14 @@ LAYOUTS = {"kn": CM_W_KN, "nk": CM_W_NK}
 EXPORTS = ["cm_plan", "cm_plan_destroy", "cm_plan_steps", "cm_plan_step", "cm_plan_tasks",
            "cm_ag_gemm_workspace_size", "cm_gemm_rs_workspace_size", "cm_ag_gemm", "cm_gemm_rs",
            "cm_check_status", "cm_status_string", "cm_plan_set_option", "cm_version",
-           "cm_ag_gemm_noalloc"]
+           "cm_ag_gemm_noalloc", "cm_cost_estimate", "cm_plan_choose"]
 CM_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+class cm_rates(ctypes.Structure):
+    """Per-rank peak rates for the cost model (see cm_cost_estimate)."""
+    _fields_ = [("gemm_tflops", ctypes.c_double), ("ring_gbs", ctypes.c_double), ("coll_gbs", ctypes.c_double),
+                ("hop_us", ctypes.c_double), ("mem_gbs", ctypes.c_double)]
 
 
 class cm_task(ctypes.Structure):
@@ -92,6 +98,12 @@ def load():
     lib.cm_version.restype = ctypes.c_char_p
     lib.cm_ag_gemm_noalloc.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p]
     lib.cm_ag_gemm_noalloc.restype = i32
+    rp = ctypes.POINTER(cm_rates)
+    lib.cm_cost_estimate.argtypes = [i32, i32, i32, i32, i64, i64, i64, rp, ctypes.POINTER(ctypes.c_double)]
+    lib.cm_cost_estimate.restype = i32
+    lib.cm_plan_choose.argtypes = [i32, i32, i64, i64, i64, rp, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                   ctypes.POINTER(ctypes.c_double)]
+    lib.cm_plan_choose.restype = i32
     _lib = lib
     return lib
 
@@ -200,6 +212,31 @@ def cm_check_status(ws, stream=None):
     info = (ctypes.c_int * 4)()
     st = load().cm_check_status(_ptr(ws), _stream_ptr(stream), info)
     return st, list(info)
+
+
+def _rates(rates):
+    if isinstance(rates, cm_rates):
+        return rates
+    return cm_rates(*(float(rates[k]) for k in ("gemm_tflops", "ring_gbs", "coll_gbs", "hop_us", "mem_gbs")))
+
+
+def cost_estimate(n_ranks, chunks, direction, op, rows, K, n, rates) -> float:
+    """Predicted time (us) of one candidate; direction "none" = native collective + GEMM."""
+    us = ctypes.c_double()
+    r = _rates(rates)
+    _check(load().cm_cost_estimate(n_ranks, chunks, DIRECTIONS[direction], op, rows, K, n, ctypes.byref(r),
+                                   ctypes.byref(us)), "cm_cost_estimate")
+    return us.value
+
+
+def plan_choose(n_ranks, op, rows, K, n, rates, max_chunks=CM_MAX_CHUNKS):
+    """The cost model's pick: (chunks, direction name, predicted us); "none" = decline."""
+    c, d, us = ctypes.c_int(), ctypes.c_int(), ctypes.c_double()
+    r = _rates(rates)
+    _check(load().cm_plan_choose(n_ranks, op, rows, K, n, ctypes.byref(r), max_chunks, ctypes.byref(c),
+                                 ctypes.byref(d), ctypes.byref(us)), "cm_plan_choose")
+    name = {v: k for k, v in DIRECTIONS.items()}[d.value]
+    return c.value, name, us.value
 
 
 def version() -> str:

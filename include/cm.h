@@ -245,6 +245,50 @@ typedef enum cm_option {
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);
 
+/*
+ * Cost model ("Overlap Communication with Dependent Computation via
+ * Decomposition in Large Deep Learning Models", section "The idea", knowing
+ * when to decline, and section "What it costs").  A peak-rate estimate of
+ * one rank's time for the decomposed ring and for the native collective
+ * followed by the undecomposed GEMM, from rates the caller measured.  Host
+ * only; no device work.
+ *
+ * cm_rates (all per rank, all > 0 except hop_us >= 0):
+ *   gemm_tflops  dense bf16 GEMM rate of one rank (TFLOP/s)
+ *   ring_gbs     one ring link in one direction (GB/s)
+ *   coll_gbs     algorithm bandwidth of the native AllGather / ReduceScatter
+ *                (GB/s); the ring drives fewer links, so usually ring_gbs
+ *                is below it
+ *   hop_us       fixed cost of one message (one chunk over one hop: the flag
+ *                round trip), in us; it holds the link
+ *   mem_gbs      local memory bandwidth, for the bidirectional ring's
+ *                realigning addition (GB/s)
+ *
+ * cm_cost_estimate -- predicted time in us of one candidate: n_ranks,
+ *   chunks (1..CM_MAX_CHUNKS) and direction (CM_RING_NONE = native
+ *   collective, then GEMM).  Shapes as the compute calls: AG rows = m (one
+ *   shard), K, n; RS rows = M (divisible by n_ranks), K = k, n.
+ *   Errors: CM_ERR_INVALID_ARG for a bad argument or rate, CM_ERR_SHAPE if
+ *   M is not divisible by n_ranks (RS).
+ * cm_plan_choose -- the fastest of: native, and one-way and bidirectional
+ *   rings with 1, 2, 4 ... max_chunks chunks that split the shard (AG) or
+ *   bucket (RS) evenly.  *dir = CM_RING_NONE means "decline: keep the
+ *   native collective".  Ties keep the simpler choice.  *us (optional)
+ *   receives the predicted time.
+ */
+typedef struct cm_rates {
+    double gemm_tflops;
+    double ring_gbs;
+    double coll_gbs;
+    double hop_us;
+    double mem_gbs;
+} cm_rates;
+
+cm_status cm_cost_estimate(int n_ranks, int chunks, cm_direction dir, cm_op op, int64_t rows, int64_t K,
+                           int64_t n, const cm_rates *rates, double *us);
+cm_status cm_plan_choose(int n_ranks, cm_op op, int64_t rows, int64_t K, int64_t n, const cm_rates *rates,
+                         int max_chunks, int *chunks, cm_direction *dir, double *us);
+
 /* Library version string. */
 const char *cm_version(void);
 
