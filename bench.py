@@ -232,10 +232,21 @@ class Step:
     def rs(self):
         self.cm.cm_gemm_rs(self.plan, self.x2, self.w2, self.y2, self.ws2, "nk")
 
+    def rs_pipe(self):
+        """The pipelined GEMM->ReduceScatter on the same inputs (own workspace)."""
+        if not hasattr(self, "ws3"):
+            import torch
+            r = self.x2.shape
+            n = self.y2.shape[2]
+            self.ws3 = torch.empty(self.plan.rs_pipelined_workspace_size(r[1], n), dtype=torch.uint8,
+                                   device=self.x2.device)
+        self.cm.cm_gemm_rs_pipelined(self.plan, self.x2, self.w2, self.y2, self.ws3, "nk")
+
     def check(self, ops=("ag", "rs")):
         """Device status of the last call of each op in `ops` (only ops that ran)."""
         for op in ops:
-            st, info = self.cm.cm_check_status(self.ws1 if op == "ag" else self.ws2)
+            ws = {"ag": self.ws1, "rs": self.ws2, "rs_pipe": getattr(self, "ws3", None)}[op]
+            st, info = self.cm.cm_check_status(ws)
             if st != 0:
                 raise RuntimeError(f"{op}: device status {st} {info}")
 
@@ -529,6 +540,16 @@ def run_sweep(args):
                                       "ms": ms, "tflops": tf, "frac_of_peak": tf / peak,
                                       "vs_undecomposed_time": ms / t_none[op], "peak_source": kind}), flush=True)
                 del st
+        # pipeline-chunk ReduceScatter ([HTP] section 6) next to the moving bucket
+        for chunks in (1, 2, 4):
+            st = Step(N, chunks, "uni", data, device)
+            ms = time_loop(st.rs_pipe, args.steps, torch, warmup=args.warmup)
+            st.check(("rs_pipe",))
+            tf = f_rs / (ms / 1e3) / 1e12
+            print(json.dumps({"sweep": WORKLOAD, "op": "rs", "N": N, "chunks": chunks, "ring": "pipelined",
+                              "ms": ms, "tflops": tf, "frac_of_peak": tf / peak,
+                              "vs_undecomposed_time": ms / t_none["rs"], "peak_source": kind}), flush=True)
+            del st
         del data
         torch.cuda.empty_cache()
     return 0

@@ -6,4 +6,4 @@ library behind include/cm.h.  This package is its Python binding.
 """
 
 from .cm import (CMError, Plan, cm_ag_gemm, cm_check_status, cm_gemm_rs,  # noqa: F401
-                 load, version)
+                 cm_gemm_rs_pipelined, cost_estimate, load, plan_choose, version)

@@ -14,7 +14,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libcm.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-SOURCES = ["cm_kernel.cu", "cm_kernel_pair.cu", "cm_api.cu", "cm_plan.cpp", "cm_noalloc.cu", "cm_cost.cpp"]
+SOURCES = ["cm_kernel.cu", "cm_kernel_pair.cu", "cm_api.cu", "cm_plan.cpp", "cm_noalloc.cu", "cm_cost.cpp", "cm_reduce.cu"]
 HEADERS = ["cm_internal.h", "cm_kernel.cuh", "cm_device.cuh", "cm_kernel_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -31,7 +31,8 @@ LAYOUTS = {"kn": CM_W_KN, "nk": CM_W_NK}
 EXPORTS = ["cm_plan", "cm_plan_destroy", "cm_plan_steps", "cm_plan_step", "cm_plan_tasks",
            "cm_ag_gemm_workspace_size", "cm_gemm_rs_workspace_size", "cm_ag_gemm", "cm_gemm_rs",
            "cm_check_status", "cm_status_string", "cm_plan_set_option", "cm_version",
-           "cm_ag_gemm_noalloc", "cm_cost_estimate", "cm_plan_choose"]
+           "cm_ag_gemm_noalloc", "cm_cost_estimate", "cm_plan_choose",
+           "cm_gemm_rs_pipelined_workspace_size", "cm_gemm_rs_pipelined"]
 CM_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -98,6 +99,10 @@ def load():
     lib.cm_version.restype = ctypes.c_char_p
     lib.cm_ag_gemm_noalloc.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p]
     lib.cm_ag_gemm_noalloc.restype = i32
+    lib.cm_gemm_rs_pipelined_workspace_size.argtypes = [p, i64, i64]
+    lib.cm_gemm_rs_pipelined_workspace_size.restype = sz
+    lib.cm_gemm_rs_pipelined.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p, sz, p]
+    lib.cm_gemm_rs_pipelined.restype = i32
     rp = ctypes.POINTER(cm_rates)
     lib.cm_cost_estimate.argtypes = [i32, i32, i32, i32, i64, i64, i64, rp, ctypes.POINTER(ctypes.c_double)]
     lib.cm_cost_estimate.restype = i32
@@ -155,6 +160,9 @@ class Plan:
     def ag_workspace_size(self, m: int, K: int) -> int:
         return int(load().cm_ag_gemm_workspace_size(self.handle, int(m), int(K)))
 
+    def rs_pipelined_workspace_size(self, M: int, n: int) -> int:
+        return load().cm_gemm_rs_pipelined_workspace_size(self.handle, M, n)
+
     def rs_workspace_size(self, M: int, n: int) -> int:
         return int(load().cm_gemm_rs_workspace_size(self.handle, int(M), int(n)))
 
@@ -205,6 +213,15 @@ def cm_gemm_rs(plan: Plan, x, w, y, ws, w_layout: str = "nk", stream=None):
     st = load().cm_gemm_rs(plan.handle, _ptr(x), _ptr(w), LAYOUTS[w_layout], _ptr(y), _ydtype(y),
                            M, k, n, _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream))
     _check(st, "cm_gemm_rs")
+
+
+def cm_gemm_rs_pipelined(plan: Plan, x, w, y, ws, w_layout: str = "nk", stream=None):
+    """GEMM->ReduceScatter with pipeline chunks: x [N][M][k], w per rank, y [N][M/N][n]."""
+    N, M, k = x.shape
+    n = w.shape[1] if w_layout == "nk" else w.shape[2]
+    st = load().cm_gemm_rs_pipelined(plan.handle, _ptr(x), _ptr(w), LAYOUTS[w_layout], _ptr(y), _ydtype(y),
+                                     M, k, n, _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream))
+    _check(st, "cm_gemm_rs_pipelined")
 
 
 def cm_check_status(ws, stream=None):

@@ -46,6 +46,16 @@ WsLayout rs_layout(const PlanImpl &p, int64_t M, int64_t n) {
     return l;
 }
 
+// Pipelined RS: the status block, then every rank's fp32 partial product of
+// every bucket, [N*N][M/N][n] (buffer r*N + o).
+WsLayout rs_pipe_layout(const PlanImpl &p, int64_t M, int64_t n) {
+    WsLayout l;
+    l.buf_off = align_up(l.flags_off, 1024);
+    l.buf_bytes = size_t(p.N) * size_t(M) * size_t(n) * sizeof(float);
+    l.total = l.buf_off + l.buf_bytes;
+    return l;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -120,15 +130,29 @@ void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int
     }
 }
 
-cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, const WsLayout &l, void *ws,
-              bool b_mn, cudaStream_t stream) {
+// Launch geometry of the selected kernel for `tiles` tiles.
+cudaError_t launch_tiles(const PlanImpl &pl, const KernelChoice &kc, const KParams &kp, bool b_mn, int64_t tiles,
+                         int max_clusters, int sms, cudaStream_t stream) {
+    if (kc.pair) {
+        int clusters = pl.grid > 0 ? std::min(pl.grid / kc.cluster_ctas, max_clusters) : max_clusters;
+        clusters = std::max(1, clusters);
+        if (tiles < clusters) clusters = int(tiles);
+        return launch_pair(kp, b_mn, kc.cluster_ctas, clusters, stream);
+    }
+    int grid = pl.grid > 0 ? std::min(pl.grid, sms) : sms;
+    if (tiles < grid) grid = int(tiles);
+    return launch_persistent(kp, b_mn, grid, stream);
+}
+
+// Per-call parameters shared by every launch: status, flags, bounds, tile order.
+cm_status setup_launch(const PlanImpl &pl, const KernelChoice &kc, KParams &kp, const WsLayout &l, void *ws,
+                       int *sms, int *max_clusters) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return CM_ERR_CUDA;
-    int sms = 0;
-    if (prepare_device(dev, &sms) != cudaSuccess) return CM_ERR_CUDA;
-    int max_clusters = 0;
-    if (kc.pair && prepare_pair(dev, kc.cluster_ctas, &max_clusters) != cudaSuccess) return CM_ERR_CUDA;
-    if (kc.pair && max_clusters <= 0) return CM_ERR_UNSUPPORTED;
+    if (prepare_device(dev, sms) != cudaSuccess) return CM_ERR_CUDA;
+    *max_clusters = 0;
+    if (kc.pair && prepare_pair(dev, kc.cluster_ctas, max_clusters) != cudaSuccess) return CM_ERR_CUDA;
+    if (kc.pair && *max_clusters <= 0) return CM_ERR_UNSUPPORTED;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     kp.status = reinterpret_cast<uint32_t *>(w8);
     kp.flags = reinterpret_cast<uint32_t *>(w8 + l.flags_off);
@@ -144,12 +168,21 @@ cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, c
         const int64_t tile_bytes = int64_t(kc.pair ? pair_rows() : kBM) * kp.kblocks * kBK * 2;
         kp.row_band = int(std::max<int64_t>(1, kRowBandBytes / tile_bytes));
     }
+    return CM_OK;
+}
+
+cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, const WsLayout &l, void *ws,
+              bool b_mn, cudaStream_t stream) {
+    int sms = 0, max_clusters = 0;
+    cm_status st = setup_launch(pl, kc, kp, l, ws, &sms, &max_clusters);
+    if (st != CM_OK) return st;
     const auto &tasks = pl.tasks[op];
     const int ntasks = int(tasks.size());
     if (ntasks > kMaxTasks) return CM_ERR_UNSUPPORTED;
     std::memcpy(kp.tasks, tasks.data(), sizeof(cm_task) * size_t(ntasks));
     // status word and flags start at zero for every call
     if (cudaMemsetAsync(ws, 0, l.buf_off, stream) != cudaSuccess) return CM_ERR_CUDA;
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
     const auto &sb = pl.step_begin[op];
     const int nsteps = int(sb.size()) - 1;
     const int launches = pl.serial_steps ? nsteps : 1;
@@ -160,18 +193,29 @@ cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, c
         kp.task_end = pl.serial_steps ? sb[size_t(i) + 1] : ntasks;
         if (kp.task_end <= kp.task_begin) continue;
         const int64_t tiles = int64_t(kp.task_end - kp.task_begin) * kp.tiles_per_task;
-        if (kc.pair) {
-            int clusters = pl.grid > 0 ? std::min(pl.grid / kc.cluster_ctas, max_clusters) : max_clusters;
-            clusters = std::max(1, clusters);
-            if (tiles < clusters) clusters = int(tiles);
-            if (launch_pair(kp, b_mn, kc.cluster_ctas, clusters, stream) != cudaSuccess) return CM_ERR_CUDA;
-        } else {
-            int grid = pl.grid > 0 ? std::min(pl.grid, sms) : sms;
-            if (tiles < grid) grid = int(tiles);
-            if (launch_persistent(kp, b_mn, grid, stream) != cudaSuccess) return CM_ERR_CUDA;
-        }
+        if (launch_tiles(pl, kc, kp, b_mn, tiles, max_clusters, sms, stream) != cudaSuccess) return CM_ERR_CUDA;
     }
     return CM_OK;
+}
+
+// The library's second stream per device (non-blocking) and its events: the
+// pipelined RS runs each chunk's reduction there, ordered after that chunk's
+// GEMM by an event; the caller's stream waits for the last reduction.
+constexpr int kMaxDevices = 64;
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t ev[CM_MAX_CHUNKS + 1] = {};
+};
+
+SideStream *side_stream(int dev) {   // caller holds the pipelined call's mutex
+    static SideStream ss[kMaxDevices];
+    SideStream &d = ss[dev];
+    if (!d.stream) {
+        if (cudaStreamCreateWithFlags(&d.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+        for (auto &e : d.ev)
+            if (cudaEventCreateWithFlags(&e, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+    }
+    return &d;
 }
 
 cm_status check_common(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl, void *y, cm_dtype yd,
@@ -222,6 +266,7 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
+    kp.q_only = -1;
     g_l2_promotion = pl.l2_promotion;
     const KernelChoice kc = choose_kernel(pl, n);
     // A box: a CTA's 128 rows, or a 64-row quarter when two pairs multicast it
@@ -283,6 +328,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     static std::mutex mu;
     std::lock_guard<std::mutex> lock(mu);
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
+    kp.q_only = -1;
     g_l2_promotion = pl.l2_promotion;
     const KernelChoice kc = choose_kernel(pl, n);
     const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
@@ -317,6 +363,111 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.a_box_rows = int(box_rows);
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n);
     return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t cm_gemm_rs_pipelined_workspace_size(cm_plan_t plan, int64_t M, int64_t n) {
+    if (!plan || M <= 0 || n <= 0) return 0;
+    return rs_pipe_layout(plan->impl, M, n).total;
+}
+
+cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y,
+                               cm_dtype y_dtype, int64_t M, int64_t k, int64_t n, void *ws, size_t ws_bytes,
+                               cm_stream_t stream) {
+    cm_status st = check_common(plan, x, w, wlayout, y, y_dtype, M, k, n);
+    if (st != CM_OK) return st;
+    const PlanImpl &pl = plan->impl;
+    const int N = pl.N;
+    if (M % N != 0) return CM_ERR_SHAPE;
+    const int64_t Mb = M / N;
+    const int c = pl.chunks;
+    if (Mb % c != 0) return CM_ERR_SHAPE;
+    const WsLayout l = rs_pipe_layout(pl, M, n);
+    if (!ws || ws_bytes < l.total) return CM_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return CM_ERR_ALIGNMENT;
+    const int64_t rows_c = Mb / c;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    static KParams kp;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CM_ERR_CUDA;
+    SideStream *ss = side_stream(dev);
+    if (!ss) return CM_ERR_CUDA;
+    std::memset(static_cast<void *>(&kp), 0, sizeof kp);
+    g_l2_promotion = pl.l2_promotion;
+    const KernelChoice kc = choose_kernel(pl, n);
+    const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(a_rows, rows_c));
+    // x [N][M][k] viewed as [N*N*c][rows_c][k]: slab (r*N + bucket)*c + chunk
+    if (!make_map(&kp.tmA0, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
+    kp.tmA1 = kp.tmA0;
+    const bool b_mn = wlayout == CM_W_KN;
+    const uint32_t b_rows = kc.pair ? kBN / 2 : kBN;
+    if (b_mn) {
+        if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(k), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+    } else {
+        if (!make_map(&kp.tmB, w, uint64_t(k), uint64_t(n), uint64_t(N), kBK, b_rows)) return CM_ERR_CUDA;
+    }
+    // partial products as [N*N*c][rows_c][n] fp32: slab (r*N + bucket)*c + chunk
+    float *P = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
+    if (!make_map(&kp.tmAcc, P, uint64_t(n), uint64_t(rows_c), uint64_t(N) * N * c, 32, 32, true)) return CM_ERR_CUDA;
+    kp.y = y;
+    kp.acc = P;
+    kp.y_rank_stride = 0;
+    kp.out_rows_per_idx = Mb;
+    kp.acc_buf_stride = Mb * n;
+    kp.op = 1;
+    kp.N = N;
+    kp.chunks = c;
+    kp.rows_c = int(rows_c);
+    kp.kblocks = int((k + kBK - 1) / kBK);
+    kp.n = int(n);
+    kp.y_f32 = y_dtype == CM_F32;
+    kp.a_box_rows = int(box_rows);
+    set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n);
+    kp.tiles_per_task = kp.mtiles_c * kp.ntile_groups;   // one chunk per launch
+    kp.tgt_in = kp.tgt_free = 0;
+    int sms = 0, max_clusters = 0;
+    st = setup_launch(pl, kc, kp, l, ws, &sms, &max_clusters);
+    if (st != CM_OK) return st;
+    // one task per (rank r, bucket o): X_r's rows of bucket o times W_r, stored
+    // as an fp32 partial; no ring, no flags
+    const int ntasks = N * N;
+    if (ntasks > kMaxTasks) return CM_ERR_UNSUPPORTED;
+    for (int r = 0; r < N; ++r)
+        for (int o = 0; o < N; ++o) {
+            cm_task &t = kp.tasks[r * N + o];
+            std::memset(&t, 0xff, sizeof t);   // every field -1 ...
+            t.rank = int16_t(r);
+            t.a_slab = int16_t(r * N + o);
+            t.a_src = 0;
+            t.out_idx = int16_t(o);
+            t.out_buf = int16_t(r * N + o);
+            t.step = 0;
+            t.stream = 0;
+            const int g = std::max(1, std::min(pl.tile_group, N));   // runs of one rank's buckets
+            const int first = (o / g) * g, size = std::min(g, N - first);
+            t.tile_group = int16_t((size << 8) | (o - first));
+        }
+    kp.task_begin = 0;
+    kp.task_end = ntasks;
+    if (cudaMemsetAsync(ws, 0, l.buf_off, s) != cudaSuccess) return CM_ERR_CUDA;
+    for (int j = 0; j < c; ++j) {
+        // GEMM of chunk j on the caller's stream; its reduction on the side
+        // stream, under the GEMM of chunk j + 1
+        kp.q_only = j;
+        kp.tile_counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + kCounterOff) + j;
+        const int64_t tiles = int64_t(ntasks) * kp.tiles_per_task;
+        if (launch_tiles(pl, kc, kp, b_mn, tiles, max_clusters, sms, s) != cudaSuccess) return CM_ERR_CUDA;
+        if (cudaEventRecord(ss->ev[j], s) != cudaSuccess) return CM_ERR_CUDA;
+        if (cudaStreamWaitEvent(ss->stream, ss->ev[j], 0) != cudaSuccess) return CM_ERR_CUDA;
+        if (launch_reduce_chunk(P, y, N, Mb, rows_c, n, j, y_dtype == CM_F32, sms, ss->stream) != cudaSuccess)
+            return CM_ERR_CUDA;
+    }
+    if (cudaEventRecord(ss->ev[CM_MAX_CHUNKS], ss->stream) != cudaSuccess) return CM_ERR_CUDA;
+    if (cudaStreamWaitEvent(s, ss->ev[CM_MAX_CHUNKS], 0) != cudaSuccess) return CM_ERR_CUDA;
+    return CM_OK;
 }
 
 cm_status cm_check_status(const void *ws, cm_stream_t stream, int32_t info[4]) {

@@ -44,9 +44,11 @@ struct KParams {
     uint32_t *flags;
     uint32_t *status;
     uint32_t *tile_counter;    // dynamic tile scheduler (CTA-pair kernel), zero at launch
-    int static_tiles;          // CTA-pair kernel: 1 = cluster c takes tiles c, c + clusters, ... instead
-    int l2_hint_a, l2_hint_b;
-    int row_band;              // row tiles per band of the tile order (0 = a whole task group)  // CTA-pair kernel: L2 priority of A / B loads (0 normal, 1 evict_last, 2 evict_first)
+    int static_tiles;          // CTA-pair kernel: 1 = cluster c takes tiles c, c + clusters, ...
+                               // instead of the next index of the global counter
+    int l2_hint_a, l2_hint_b;  // CTA-pair kernel: L2 priority of A / B loads (0 normal, 1 evict_last, 2 evict_first)
+    int row_band;              // row tiles per band of the tile order (0 = a whole task group)
+    int q_only;                // >= 0: this launch covers only chunk q_only of every task
     const uint8_t *x_bytes;    // AG: x and the receive slots as bytes (pair forwarder)
     uint8_t *slot_bytes;
     int64_t row_bytes;         // bytes per A row (K * 2)
@@ -78,5 +80,9 @@ cudaError_t prepare_device(int device, int *num_sms);
 int pair_rows();
 cudaError_t prepare_pair(int device, int cluster_ctas, int *max_clusters);
 cudaError_t launch_pair(const KParams &p, bool b_mn_major, int cluster_ctas, int clusters, cudaStream_t stream);
+// Pipelined GEMM -> ReduceScatter: y rows of chunk j of every bucket = the sum
+// over ranks of the fp32 partials P [N*N][Mb][n] (cm_reduce.cu).
+cudaError_t launch_reduce_chunk(const float *P, void *y, int N, int64_t Mb, int64_t rc, int64_t n, int j, bool y_f32,
+                                int sms, cudaStream_t stream);
 
 }  // namespace cm

@@ -35,6 +35,7 @@ __device__ __forceinline__ TileCoord decode_cl(const KParams &p, int t, uint32_t
     const int per_q = rows * p.ntile_groups;
     c.q = u / per_q;
     u -= c.q * per_q;
+    if (p.q_only >= 0) c.q = p.q_only;   // one chunk per launch: u never reaches a second one
     const int band = p.row_band > 0 && p.row_band < rows ? p.row_band : rows;
     const int full = rows / band;
     const int in_full = full * band * p.ntile_groups;

@@ -188,6 +188,29 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
                      void *ws, size_t ws_bytes, cm_stream_t stream);
 
 /*
+ * cm_gemm_rs_pipelined -- GEMM -> ReduceScatter with pipeline chunks instead
+ * of a moving bucket ("Hiding Tensor-Parallel Collectives: AG/RS Overlap in
+ * Megatron", section 6): every rank computes its full fp32 partial product
+ * X_r @ W_r, chunk by chunk, and the reduction of chunk j (owner o's rows of
+ * that chunk = the sum over ranks r = 0..N-1 of their partials, rounded once
+ * to y_dtype) runs on a second, library-owned stream while the GEMM computes
+ * chunk j + 1.  A chunk is a contiguous row block of every bucket, M/N/chunks
+ * rows (the plan's chunk count; its direction is not used).
+ *  Arguments, layouts and result: those of cm_gemm_rs (same output).
+ *  Workspace: cm_gemm_rs_pipelined_workspace_size(plan, M, n) bytes (the
+ *  partial products, N * M * n fp32, plus a status block), 256-byte aligned.
+ *  Stream: asynchronous on `stream`; the library's second stream waits on an
+ *  event after each chunk's GEMM and `stream` waits for the last reduction,
+ *  so work queued on `stream` afterwards sees the output.  Calls on one
+ *  device are serialised on the host (the second stream is shared).
+ *  Errors: as cm_gemm_rs.
+ */
+size_t cm_gemm_rs_pipelined_workspace_size(cm_plan_t plan, int64_t M, int64_t n);
+cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout,
+                               void *y, cm_dtype y_dtype, int64_t M, int64_t k, int64_t n,
+                               void *ws, size_t ws_bytes, cm_stream_t stream);
+
+/*
  * cm_check_status -- synchronise `stream` and read the device status word of
  * the last call that used `ws`.  Returns CM_OK, CM_ERR_TIMEOUT (a bounded
  * wait expired; the outputs of that call are undefined) or CM_ERR_CUDA.
