@@ -11,6 +11,9 @@ Contents
   the plain definitions, see its header.
     - AllGather->GEMM:   Y_r = concat_j(X_j) @ W_r
     - GEMM->ReduceScatter: Y_o = (sum_r X_r @ W_r)[rows of bucket o]
+    - weight gradient of the column-parallel layer (the backward pair's
+      wgrad): dW_r = dY_r^T @ concat_j(X_j); its data gradient is the
+      GEMM->ReduceScatter above with W_r read as [n][K]
 * ``ring.py``: a rank-by-rank simulation of the ring schedules the pages
   describe (shards / accumulating buckets handed to a neighbour each step),
   in fp64, with its own schedule derived from the pages -- a second,
@@ -64,6 +67,8 @@ def _load():
         lib.cm_oracle_ag_gemm_rows.argtypes = [i32, i64, i64, i64, p, p, i32, i64, p, p, p]
         lib.cm_oracle_gemm_rs.argtypes = [i32, i64, i64, i64, p, p, i32, p]
         lib.cm_oracle_gemm_rs_rows.argtypes = [i32, i64, i64, i64, p, p, i32, i64, p, p, p]
+        lib.cm_oracle_wgrad.argtypes = [i32, i64, i64, i64, p, p, p]
+        lib.cm_oracle_wgrad_rows.argtypes = [i32, i64, i64, i64, p, p, i64, p, p, p]
         lib.cm_oracle_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
@@ -129,6 +134,35 @@ def ag_gemm_rows(x_bits, w_bits, ranks, rows, w_layout: str = "nk") -> np.ndarra
     out = np.empty((len(rows), n), dtype=np.float64)
     _load().cm_oracle_ag_gemm_rows(N, m, K, n, _ptr(x), _ptr(w), W_LAYOUTS[w_layout],
                                    len(rows), _ptr(ranks), _ptr(rows), _ptr(out))
+    return out
+
+
+def _wgrad_dims(x, dy):
+    N, m, K = x.shape
+    assert dy.shape[0] == N and dy.shape[1] == N * m
+    return N, m, K, dy.shape[2]
+
+
+def wgrad(x_bits, dy_bits) -> np.ndarray:
+    """Weight gradient of the column-parallel layer: dW[r][i][k] = sum_t dY_r[t][i] * X_all[t][k],
+    x [N][m][K], dy [N][N*m][n] -> [N][n][K] fp64."""
+    x, dy = _bits(x_bits), _bits(dy_bits)
+    N, m, K, n = _wgrad_dims(x, dy)
+    out = np.empty((N, n, K), dtype=np.float64)
+    _load().cm_oracle_wgrad(N, m, K, n, _ptr(x), _ptr(dy), _ptr(out))
+    return out
+
+
+def wgrad_rows(x_bits, dy_bits, ranks, rows) -> np.ndarray:
+    """Sampled rows of the weight gradient: out[s] = dW[ranks[s]][rows[s]]."""
+    x, dy = _bits(x_bits), _bits(dy_bits)
+    N, m, K, n = _wgrad_dims(x, dy)
+    ranks = np.ascontiguousarray(ranks, dtype=np.int32)
+    rows = np.ascontiguousarray(rows, dtype=np.int64)
+    assert ranks.shape == rows.shape and ranks.ndim == 1
+    assert ((0 <= ranks) & (ranks < N)).all() and ((0 <= rows) & (rows < n)).all()
+    out = np.empty((len(rows), K), dtype=np.float64)
+    _load().cm_oracle_wgrad_rows(N, m, K, n, _ptr(x), _ptr(dy), len(rows), _ptr(ranks), _ptr(rows), _ptr(out))
     return out
 
 

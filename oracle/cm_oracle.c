@@ -162,6 +162,53 @@ void cm_oracle_gemm_rs(int N, int64_t M, int64_t k, int64_t n,
     (void)N;
 }
 
+/*
+ * Weight gradient of the column-parallel layer whose forward is the
+ * AllGather -> GEMM above.  "Tensor Parallelism > Communication Patterns":
+ * the gradient of a column-parallel weight shard is computed locally from the
+ * full input; "Hiding Tensor-Parallel Collectives", section 7: that full input
+ * is an AllGather the data-gradient GEMM does not need (bulk overlap).  With
+ * W_r stored [n][K] (Y_r[t][i] = sum_k X_all[t][k] * W_r[i][k]):
+ *
+ *   dW_r[i][k] = sum over tokens t = 0 .. N*m-1 of dY_r[t][i] * X_all[t][k],
+ *   X_all = concat_j(X_j), t ascending.
+ *
+ * x: [N][m][K], dy: [N][N*m][n], rows (r, i) sampled by `ranks`/`rows`;
+ * out: [count][K].
+ */
+void cm_oracle_wgrad_rows(int N, int64_t m, int64_t K, int64_t n,
+                          const uint16_t *x, const uint16_t *dy, int64_t count,
+                          const int32_t *ranks, const int64_t *rows, double *out) {
+    const int64_t T = (int64_t)N * m;            /* tokens: concat_j(X_j) rows */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t s = 0; s < count; ++s) {
+        const int r = ranks[s];
+        const int64_t i = rows[s];
+        double *o = out + s * K;
+        for (int64_t k = 0; k < K; ++k) o[k] = 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            const double d = bf16_to_f64(dy[((int64_t)r * T + t) * n + i]);
+            const uint16_t *xt = x + t * K;      /* row t of X_all (shards are contiguous) */
+            for (int64_t k = 0; k < K; ++k) o[k] += d * bf16_to_f64(xt[k]);
+        }
+    }
+}
+
+/* Every row of every rank's weight gradient: out [N][n][K]. */
+void cm_oracle_wgrad(int N, int64_t m, int64_t K, int64_t n,
+                     const uint16_t *x, const uint16_t *dy, double *out) {
+    const int64_t count = (int64_t)N * n;
+    int32_t *ranks = (int32_t *)malloc((size_t)count * sizeof(int32_t));
+    int64_t *rows = (int64_t *)malloc((size_t)count * sizeof(int64_t));
+    for (int64_t s = 0; s < count; ++s) {
+        ranks[s] = (int32_t)(s / n);
+        rows[s] = s % n;
+    }
+    cm_oracle_wgrad_rows(N, m, K, n, x, dy, count, ranks, rows, out);
+    free(ranks);
+    free(rows);
+}
+
 /* Threads OpenMP will use (reported next to the CPU timings). */
 int cm_oracle_threads(void) {
 #ifdef _OPENMP

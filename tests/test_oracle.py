@@ -287,3 +287,82 @@ def test_plant_wrong_neighbour_fails_ring(monkeypatch):
     except ring.RingTimeout:
         return                                  # caught: the schedule stalls
     assert not np.array_equal(got, ref)
+
+
+# --- the backward pair of the column-parallel layer ("Tensor Parallelism >
+# Communication Patterns": the backward pass is the forward's dual; "Hiding
+# Tensor-Parallel Collectives", section 7: the weight gradient needs an
+# AllGather of the input that the data gradient does not) -----------------
+
+def _brute_wgrad(x, dy):
+    """Pure-Python exact sums: dW_r[i][k] = sum_t dY_r[t][i] * X_all[t][k]."""
+    N, m, K = x.shape
+    n = dy.shape[2]
+    x_all = x.reshape(N * m, K)
+    out = np.zeros((N, n, K), dtype=np.int64)
+    for r, i, k in itertools.product(range(N), range(n), range(K)):
+        s = 0
+        for t in range(N * m):
+            s += int(dy[r, t, i]) * int(x_all[t, k])
+        out[r, i, k] = s
+    return out
+
+
+@pytest.mark.parametrize("N,m,K,n", [(1, 3, 5, 4), (2, 4, 6, 3), (3, 2, 7, 5), (4, 3, 4, 2)])
+def test_wgrad_brute_force_exact(N, m, K, n):
+    x, _ = gen.int_inputs((N, m, K), (1, 1), -8, 8, seed=N * 31 + m)
+    dy, _ = gen.int_inputs((N, N * m, n), (1, 1), -8, 8, seed=N * 37 + n)
+    ref = _brute_wgrad(x.to(torch.int64).numpy(), dy.to(torch.int64).numpy())
+    got = oracle.wgrad(gen.bf16_bits(x), gen.bf16_bits(dy))
+    assert np.array_equal(got, ref.astype(np.float64))
+
+
+def test_wgrad_all_ones_gradient_is_column_sums():
+    N, m, K, n = 3, 5, 7, 4
+    x, _ = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=8)
+    dy = torch.ones((N, N * m, n), dtype=torch.bfloat16)
+    got = oracle.wgrad(gen.bf16_bits(x), gen.bf16_bits(dy))
+    colsum = _f64(x).reshape(N * m, K).sum(axis=0)
+    assert np.allclose(got, np.broadcast_to(colsum, (N, n, K)), rtol=1e-13, atol=1e-12)
+
+
+def test_wgrad_equals_numpy_transpose_matmul():
+    N, m, K, n = 4, 6, 9, 5
+    x, _ = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=9)
+    dy, _ = gen.ag_inputs(N, N * m, n, 1, gen.NORMAL1, gen.NORMAL002, seed=10)
+    got = oracle.wgrad(gen.bf16_bits(x), gen.bf16_bits(dy))
+    x_all = _f64(x).reshape(N * m, K)
+    for r in range(N):
+        assert np.allclose(got[r], _f64(dy)[r].T @ x_all, rtol=1e-12, atol=1e-12)
+    rows = oracle.wgrad_rows(gen.bf16_bits(x), gen.bf16_bits(dy), [0, 3, 2], [4, 0, 2])
+    assert np.array_equal(rows, got[[0, 3, 2], [4, 0, 2]])
+
+
+@pytest.mark.parametrize("N", [1, 2, 4])
+def test_backward_pair_adjoint_identities(N):
+    """<dY, dL/dY-linear map> identities: for Y_r = X_all @ W_r^T,
+    sum_r <dY_r, Y_r> = sum_r <dW_r, W_r> (wgrad) = sum_j <dX_j, X_j> (dgrad,
+    the GEMM->ReduceScatter of dY_r @ W_r)."""
+    m, K, n = 4, 6, 5
+    x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL1, seed=20 + N, w_layout="nk")   # W_r [n][K]
+    dy, _ = gen.ag_inputs(N, N * m, n, 1, gen.NORMAL1, gen.NORMAL1, seed=30 + N)
+    xb, wb, dyb = gen.bf16_bits(x), gen.bf16_bits(w), gen.bf16_bits(dy)
+    y = oracle.ag_gemm(xb, wb, "nk")                           # [N][N*m][n]
+    lhs = float((_f64(dy) * y).sum())
+    dw = oracle.wgrad(xb, dyb)                                  # [N][n][K]
+    assert float((dw * _f64(w)).sum()) == pytest.approx(lhs, rel=1e-12, abs=1e-12)
+    dx = oracle.gemm_rs(dyb, wb, "kn")                          # W_r [n][K] is [k][n_out]: dX [N][m][K]
+    assert dx.shape == (N, m, K)
+    assert float((dx * _f64(x)).sum()) == pytest.approx(lhs, rel=1e-12, abs=1e-12)
+
+
+def test_plant_wgrad_wrong_token_order_fails_identity():
+    """A gradient that pairs dY rows with the wrong token (shard order reversed)
+    breaks the adjoint identity."""
+    N, m, K, n = 3, 4, 5, 3
+    x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL1, seed=41, w_layout="nk")
+    dy, _ = gen.ag_inputs(N, N * m, n, 1, gen.NORMAL1, gen.NORMAL1, seed=42)
+    xb, wb, dyb = gen.bf16_bits(x), gen.bf16_bits(w), gen.bf16_bits(dy)
+    lhs = float((_f64(dy) * oracle.ag_gemm(xb, wb, "nk")).sum())
+    bad = oracle.wgrad(xb[::-1].copy(), dyb)                   # X_all built from reversed shards
+    assert abs(float((bad * _f64(w)).sum()) - lhs) > 1e-6 * max(1.0, abs(lhs))
