@@ -638,6 +638,51 @@ def run_gate(args):
     return 0
 
 
+def run_backward(args):
+    """The backward pair of the MLP fc1 (column-parallel) layer at N ranks: data
+    gradient (GEMM-RS of dY_r @ W_r) and weight gradient (dY_r^T @ gathered X),
+    with the gather on a second stream under the GEMM-RS (bulk overlap) and
+    without; the data gradient alone next to them."""
+    import torch
+    import __graft_entry__
+    from collective_matmul_decomposition_gb300 import cm
+    from collective_matmul_decomposition_gb300 import inputs as gen
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    peaks, kind = load_peaks()
+    for N in (4, 8, 16):
+        sh = gen.mlp_shapes(N)["ag"]
+        m, K, n = sh["m"], sh["K"], sh["n"]
+        T = N * m
+        x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=6000, w_layout="nk")
+        dy, _ = gen.ag_inputs(N, T, n, 1, gen.NORMAL1, gen.NORMAL1, seed=6001)
+        x, w, dy = x.to(device), w.to(device), dy.to(device)
+        dx = torch.empty(N, m, K, dtype=torch.bfloat16, device=device)
+        dw = torch.empty(N, n, K, dtype=torch.bfloat16, device=device)
+        plan = cm.Plan(N, 1, "uni")
+        ws = torch.empty(plan.backward_pair_workspace_size(m, K, n), dtype=torch.uint8, device=device)
+        flops = 4.0 * N * T * n * K
+        res = {}
+        for overlap in (1, 0):
+            plan.set_option(cm.CM_OPT_BULK_OVERLAP, overlap)
+            ms = time_loop(lambda: cm.cm_backward_pair(plan, x, w, dy, dx, dw, ws), args.steps, torch,
+                           warmup=args.warmup)
+            st, info = cm.cm_check_status(ws)
+            if st != 0:
+                raise RuntimeError(f"backward pair: device status {st} {info}")
+            res["overlap" if overlap else "serial"] = ms
+        ms_dgrad = time_loop(lambda: cm.cm_gemm_rs(plan, dy, w, dx, ws, "kn"), args.steps, torch, warmup=args.warmup)
+        print(json.dumps({"backward_pair": WORKLOAD, "N": N, "m": m, "K": K, "n": n,
+                          "ms_bulk_overlap": res["overlap"], "ms_serial_gather": res["serial"],
+                          "ms_dgrad_alone": ms_dgrad,
+                          "tflops_bulk_overlap": flops / (res["overlap"] / 1e3) / 1e12,
+                          "frac_of_peak": flops / (res["overlap"] / 1e3) / 1e12 / float(peaks["bf16_tflops"]),
+                          "gather_bytes": N * N * m * K * 2, "peak_source": kind}), flush=True)
+        del x, w, dy, dx, dw, ws
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_profile_case(args):
     """A few calls of one op of one workload, nothing else: the command ncu captures."""
     import torch
@@ -680,6 +725,7 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--gate", action="store_true", help="the cost model's choices against measurement")
+    ap.add_argument("--backward", action="store_true", help="the backward pair of the MLP fc1 layer")
     ap.add_argument("--profile", choices=["ag", "rs"], default=None,
                     help="run only --steps calls of one op (for ncu captures)")
     ap.add_argument("--workload", default=WORKLOAD)
@@ -705,6 +751,8 @@ def main(argv=None):
         return run_sweep(args)
     if args.gate:
         return run_gate(args)
+    if args.backward:
+        return run_backward(args)
     if args.profile:
         return run_profile_case(args)
     return run_ours(args)

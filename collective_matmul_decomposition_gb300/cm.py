@@ -22,6 +22,7 @@ CM_W_KN, CM_W_NK = 0, 1
 CM_OP_AG_GEMM, CM_OP_GEMM_RS = 0, 1
 CM_OPT_TIMEOUT_NS, CM_OPT_SERIAL_STEPS, CM_OPT_GRID, CM_OPT_SKIP_SIGNAL, CM_OPT_KERNEL = 0, 1, 2, 3, 4
 CM_OPT_STATIC_TILES, CM_OPT_TILE_GROUP, CM_OPT_L2_HINTS, CM_OPT_L2_PROMOTION, CM_OPT_ROW_BAND = 5, 6, 7, 8, 9
+CM_OPT_BULK_OVERLAP = 10
 CM_MAX_RANKS, CM_MAX_CHUNKS = 16, 8
 
 DIRECTIONS = {"uni": CM_RING_UNI, "bidi": CM_RING_BIDI, "none": CM_RING_NONE}
@@ -32,7 +33,8 @@ EXPORTS = ["cm_plan", "cm_plan_destroy", "cm_plan_steps", "cm_plan_step", "cm_pl
            "cm_ag_gemm_workspace_size", "cm_gemm_rs_workspace_size", "cm_ag_gemm", "cm_gemm_rs",
            "cm_check_status", "cm_status_string", "cm_plan_set_option", "cm_version",
            "cm_ag_gemm_noalloc", "cm_cost_estimate", "cm_plan_choose",
-           "cm_gemm_rs_pipelined_workspace_size", "cm_gemm_rs_pipelined"]
+           "cm_gemm_rs_pipelined_workspace_size", "cm_gemm_rs_pipelined",
+           "cm_backward_pair_workspace_size", "cm_backward_pair"]
 CM_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -103,6 +105,10 @@ def load():
     lib.cm_gemm_rs_pipelined_workspace_size.restype = sz
     lib.cm_gemm_rs_pipelined.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p, sz, p]
     lib.cm_gemm_rs_pipelined.restype = i32
+    lib.cm_backward_pair_workspace_size.argtypes = [p, i64, i64, i64]
+    lib.cm_backward_pair_workspace_size.restype = sz
+    lib.cm_backward_pair.argtypes = [p, p, p, p, p, i32, p, i32, i64, i64, i64, p, sz, p]
+    lib.cm_backward_pair.restype = i32
     rp = ctypes.POINTER(cm_rates)
     lib.cm_cost_estimate.argtypes = [i32, i32, i32, i32, i64, i64, i64, rp, ctypes.POINTER(ctypes.c_double)]
     lib.cm_cost_estimate.restype = i32
@@ -159,6 +165,9 @@ class Plan:
 
     def ag_workspace_size(self, m: int, K: int) -> int:
         return int(load().cm_ag_gemm_workspace_size(self.handle, int(m), int(K)))
+
+    def backward_pair_workspace_size(self, m: int, K: int, n: int) -> int:
+        return load().cm_backward_pair_workspace_size(self.handle, m, K, n)
 
     def rs_pipelined_workspace_size(self, M: int, n: int) -> int:
         return load().cm_gemm_rs_pipelined_workspace_size(self.handle, M, n)
@@ -222,6 +231,17 @@ def cm_gemm_rs_pipelined(plan: Plan, x, w, y, ws, w_layout: str = "nk", stream=N
     st = load().cm_gemm_rs_pipelined(plan.handle, _ptr(x), _ptr(w), LAYOUTS[w_layout], _ptr(y), _ydtype(y),
                                      M, k, n, _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream))
     _check(st, "cm_gemm_rs_pipelined")
+
+
+def cm_backward_pair(plan: Plan, x, w, dy, dx, dw, ws, stream=None):
+    """Backward pair of the column-parallel layer: dx [N][m][K] = GEMM-RS of dy_r @ W_r,
+    dw [N][n][K] = dy_r^T @ concat_j(x_j) (its AllGather overlapped with the GEMM-RS)."""
+    N, m, K = x.shape
+    n = w.shape[1]
+    st = load().cm_backward_pair(plan.handle, _ptr(x), _ptr(w), _ptr(dy), _ptr(dx), _ydtype(dx), _ptr(dw),
+                                 _ydtype(dw), m, K, n, _ptr(ws), ws.numel() * ws.element_size(),
+                                 _stream_ptr(stream))
+    _check(st, "cm_backward_pair")
 
 
 def cm_check_status(ws, stream=None):

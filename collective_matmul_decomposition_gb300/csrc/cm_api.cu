@@ -131,17 +131,19 @@ void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int
 }
 
 // Launch geometry of the selected kernel for `tiles` tiles.
-cudaError_t launch_tiles(const PlanImpl &pl, const KernelChoice &kc, const KParams &kp, bool b_mn, int64_t tiles,
+// layout: bit 0 = B MN-major, bit 1 = A MN-major (CTA pairs only).
+cudaError_t launch_tiles(const PlanImpl &pl, const KernelChoice &kc, const KParams &kp, int layout, int64_t tiles,
                          int max_clusters, int sms, cudaStream_t stream) {
     if (kc.pair) {
         int clusters = pl.grid > 0 ? std::min(pl.grid / kc.cluster_ctas, max_clusters) : max_clusters;
         clusters = std::max(1, clusters);
         if (tiles < clusters) clusters = int(tiles);
-        return launch_pair(kp, b_mn, kc.cluster_ctas, clusters, stream);
+        return launch_pair(kp, layout, kc.cluster_ctas, clusters, stream);
     }
+    if (layout & 2) return cudaErrorInvalidValue;
     int grid = pl.grid > 0 ? std::min(pl.grid, sms) : sms;
     if (tiles < grid) grid = int(tiles);
-    return launch_persistent(kp, b_mn, grid, stream);
+    return launch_persistent(kp, (layout & 1) != 0, grid, stream);
 }
 
 // Per-call parameters shared by every launch: status, flags, bounds, tile order.
@@ -193,7 +195,8 @@ cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, c
         kp.task_end = pl.serial_steps ? sb[size_t(i) + 1] : ntasks;
         if (kp.task_end <= kp.task_begin) continue;
         const int64_t tiles = int64_t(kp.task_end - kp.task_begin) * kp.tiles_per_task;
-        if (launch_tiles(pl, kc, kp, b_mn, tiles, max_clusters, sms, stream) != cudaSuccess) return CM_ERR_CUDA;
+        if (launch_tiles(pl, kc, kp, b_mn ? 1 : 0, tiles, max_clusters, sms, stream) != cudaSuccess)
+            return CM_ERR_CUDA;
     }
     return CM_OK;
 }
@@ -207,9 +210,11 @@ struct SideStream {
     cudaEvent_t ev[CM_MAX_CHUNKS + 1] = {};
 };
 
-SideStream *side_stream(int dev) {   // caller holds the pipelined call's mutex
-    static SideStream ss[kMaxDevices];
-    SideStream &d = ss[dev];
+enum SideUser { kSidePipelinedRs = 0, kSideBackwardPair = 1 };
+
+SideStream *side_stream(int dev, SideUser user) {   // caller holds that user's call mutex
+    static SideStream ss[2][kMaxDevices];
+    SideStream &d = ss[user][dev];
     if (!d.stream) {
         if (cudaStreamCreateWithFlags(&d.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
         for (auto &e : d.ev)
@@ -392,7 +397,7 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     std::lock_guard<std::mutex> lock(mu);
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CM_ERR_CUDA;
-    SideStream *ss = side_stream(dev);
+    SideStream *ss = side_stream(dev, kSidePipelinedRs);
     if (!ss) return CM_ERR_CUDA;
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
     g_l2_promotion = pl.l2_promotion;
@@ -459,7 +464,7 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
         kp.q_only = j;
         kp.tile_counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + kCounterOff) + j;
         const int64_t tiles = int64_t(ntasks) * kp.tiles_per_task;
-        if (launch_tiles(pl, kc, kp, b_mn, tiles, max_clusters, sms, s) != cudaSuccess) return CM_ERR_CUDA;
+        if (launch_tiles(pl, kc, kp, b_mn ? 1 : 0, tiles, max_clusters, sms, s) != cudaSuccess) return CM_ERR_CUDA;
         if (cudaEventRecord(ss->ev[j], s) != cudaSuccess) return CM_ERR_CUDA;
         if (cudaStreamWaitEvent(ss->stream, ss->ev[j], 0) != cudaSuccess) return CM_ERR_CUDA;
         if (launch_reduce_chunk(P, y, N, Mb, rows_c, n, j, y_dtype == CM_F32, sms, ss->stream) != cudaSuccess)
@@ -467,6 +472,128 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     }
     if (cudaEventRecord(ss->ev[CM_MAX_CHUNKS], ss->stream) != cudaSuccess) return CM_ERR_CUDA;
     if (cudaStreamWaitEvent(s, ss->ev[CM_MAX_CHUNKS], 0) != cudaSuccess) return CM_ERR_CUDA;
+    return CM_OK;
+}
+
+// Backward pair workspace: the data gradient's GEMM-RS workspace, a status
+// block for the weight-gradient launch, then every rank's gathered input.
+struct BwdLayout {
+    size_t rs_bytes = 0, wg_off = 0, xg_off = 0, total = 0;
+};
+
+BwdLayout bwd_layout(const PlanImpl &p, int64_t m, int64_t K, int64_t n) {
+    (void)n;
+    BwdLayout b;
+    b.rs_bytes = rs_layout(p, int64_t(p.N) * m, K).total;
+    b.wg_off = align_up(b.rs_bytes, 1024);
+    b.xg_off = b.wg_off + 1024;
+    b.total = b.xg_off + size_t(p.N) * size_t(p.N) * size_t(m) * size_t(K) * 2;
+    return b;
+}
+
+size_t cm_backward_pair_workspace_size(cm_plan_t plan, int64_t m, int64_t K, int64_t n) {
+    if (!plan || m <= 0 || K <= 0 || n <= 0) return 0;
+    return bwd_layout(plan->impl, m, K, n).total;
+}
+
+cm_status cm_backward_pair(cm_plan_t plan, const void *x, const void *w, const void *dy, void *dx, cm_dtype dx_dtype,
+                           void *dw, cm_dtype dw_dtype, int64_t m, int64_t K, int64_t n, void *ws, size_t ws_bytes,
+                           cm_stream_t stream) {
+    if (!plan || !x || !w || !dy || !dx || !dw) return CM_ERR_INVALID_ARG;
+    if ((dx_dtype != CM_BF16 && dx_dtype != CM_F32) || (dw_dtype != CM_BF16 && dw_dtype != CM_F32))
+        return CM_ERR_INVALID_ARG;
+    const PlanImpl &pl = plan->impl;
+    const int N = pl.N;
+    const int64_t T = int64_t(N) * m;   // tokens: the gathered rows
+    if (m <= 0 || K <= 0 || n <= 0) return CM_ERR_SHAPE;
+    if (K % 8 != 0 || n % 8 != 0) return CM_ERR_ALIGNMENT;
+    if (n < 64 || K < 64 || T < 64 || m % pl.chunks != 0) return CM_ERR_SHAPE;
+    if (!aligned16(x) || !aligned16(w) || !aligned16(dy) || !aligned16(dx) || !aligned16(dw)) return CM_ERR_ALIGNMENT;
+    const BwdLayout bl = bwd_layout(pl, m, K, n);
+    if (!ws || ws_bytes < bl.total) return CM_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return CM_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    uint8_t *xg = w8 + bl.xg_off;   // [N ranks][T][K] bf16
+
+    static KParams kp;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CM_ERR_CUDA;
+    SideStream *ss = side_stream(dev, kSideBackwardPair);
+    if (!ss) return CM_ERR_CUDA;
+
+    // 1. the weight gradient's AllGather: every rank's copy of concat_j(X_j),
+    //    on the second stream (after the work already queued on `stream`)
+    const size_t shard = size_t(m) * size_t(K) * 2;
+    cudaStream_t ag = pl.bulk_overlap ? ss->stream : s;
+    if (pl.bulk_overlap) {
+        if (cudaEventRecord(ss->ev[0], s) != cudaSuccess) return CM_ERR_CUDA;
+        if (cudaStreamWaitEvent(ag, ss->ev[0], 0) != cudaSuccess) return CM_ERR_CUDA;
+    }
+    for (int r = 0; r < N; ++r)
+        for (int j = 0; j < N; ++j)
+            if (cudaMemcpyAsync(xg + (size_t(r) * N + j) * shard, static_cast<const uint8_t *>(x) + size_t(j) * shard,
+                                shard, cudaMemcpyDeviceToDevice, ag) != cudaSuccess)
+                return CM_ERR_CUDA;
+    if (pl.bulk_overlap && cudaEventRecord(ss->ev[1], ag) != cudaSuccess) return CM_ERR_CUDA;
+
+    // 2. the data gradient: GEMM -> ReduceScatter of dY_r @ W_r on the ring
+    cm_status st = cm_gemm_rs(plan, dy, w, CM_W_KN, dx, dx_dtype, T, n, K, ws, bl.rs_bytes, stream);
+    if (st != CM_OK) return st;
+
+    // 3. the weight gradient once the gather has landed: one GEMM per rank,
+    //    A = dY_r^T (MN-major) and B = the rank's gathered input (MN-major)
+    if (pl.bulk_overlap && cudaStreamWaitEvent(s, ss->ev[1], 0) != cudaSuccess) return CM_ERR_CUDA;
+    std::memset(static_cast<void *>(&kp), 0, sizeof kp);
+    kp.q_only = -1;
+    g_l2_promotion = pl.l2_promotion;
+    KernelChoice kc;
+    kc.pair = true;
+    kc.cluster_ctas = 2;
+    if (!make_map(&kp.tmA0, dy, uint64_t(n), uint64_t(T), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+    kp.tmA1 = kp.tmA0;
+    if (!make_map(&kp.tmB, xg, uint64_t(K), uint64_t(T), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+    kp.y = dw;
+    kp.y_rank_stride = n * K;
+    kp.out_rows_per_idx = n;
+    kp.op = 0;
+    kp.N = N;
+    kp.chunks = 1;
+    kp.rows_c = int(n);
+    kp.kblocks = int((T + kBK - 1) / kBK);
+    kp.n = int(K);
+    kp.y_f32 = dw_dtype == CM_F32;
+    kp.a_box_rows = kBM;   // an MN-major half is always two full 64-wide boxes
+    set_tiling(kc, CM_OP_AG_GEMM, kp, n, K);
+    kp.tgt_in = kp.tgt_free = 0;
+    for (int r = 0; r < N; ++r) {
+        cm_task &t = kp.tasks[r];
+        std::memset(&t, 0xff, sizeof t);   // every field -1 ...
+        t.rank = int16_t(r);
+        t.a_slab = int16_t(r);
+        t.a_src = 0;
+        t.out_idx = 0;
+        t.step = 0;
+        t.stream = 0;
+        t.tile_group = int16_t(1 << 8);
+    }
+    kp.task_begin = 0;
+    kp.task_end = N;
+    WsLayout l;   // the weight-gradient launch's own status block and counters
+    l.flags_off = 0;
+    l.buf_off = 256;
+    int sms = 0, max_clusters = 0;
+    st = setup_launch(pl, kc, kp, l, w8 + bl.wg_off, &sms, &max_clusters);
+    if (st != CM_OK) return st;
+    // failures go to the call's status word (cleared by the GEMM-RS above),
+    // so cm_check_status(ws) covers both launches; the tile counter is fresh
+    kp.status = reinterpret_cast<uint32_t *>(w8);
+    kp.tile_counter = reinterpret_cast<uint32_t *>(w8 + bl.wg_off + kCounterOff);
+    if (cudaMemsetAsync(w8 + bl.wg_off, 0, 256, s) != cudaSuccess) return CM_ERR_CUDA;
+    if (launch_tiles(pl, kc, kp, 3, int64_t(N) * kp.tiles_per_task, max_clusters, sms, s) != cudaSuccess)
+        return CM_ERR_CUDA;
     return CM_OK;
 }
 

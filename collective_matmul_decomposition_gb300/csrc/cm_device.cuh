@@ -165,10 +165,10 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo_byte
 
 // Instruction descriptor of tcgen05.mma.kind::f16: D f32 (bits 4-5 = 1),
 // A bf16 (7-9 = 1), B bf16 (10-12 = 1), A K-major (15 = 0), B K-major or
-// MN-major (16), N >> 3 in 17-22, M >> 4 in 24-28.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major) {
-    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(b_mn_major) << 16) | (uint32_t(N >> 3) << 17) |
-           (uint32_t(M >> 4) << 24);
+// MN-major (16), N >> 3 in 17-22, M >> 4 in 24-28; A MN-major is bit 15.
+__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major, bool a_mn_major = false) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(a_mn_major) << 15) | (uint32_t(b_mn_major) << 16) |
+           (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
 // ---- gpu-scope flags ----------------------------------------------------------

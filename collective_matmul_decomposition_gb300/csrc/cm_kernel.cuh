@@ -79,7 +79,8 @@ cudaError_t prepare_device(int device, int *num_sms);
 // that share the A tile by TMA multicast).
 int pair_rows();
 cudaError_t prepare_pair(int device, int cluster_ctas, int *max_clusters);
-cudaError_t launch_pair(const KParams &p, bool b_mn_major, int cluster_ctas, int clusters, cudaStream_t stream);
+// layout: bit 0 = B MN-major, bit 1 = A MN-major (bit 1 only with cluster_ctas == 2).
+cudaError_t launch_pair(const KParams &p, int layout, int cluster_ctas, int clusters, cudaStream_t stream);
 // Pipelined GEMM -> ReduceScatter: y rows of chunk j of every bucket = the sum
 // over ranks of the fp32 partials P [N*N][Mb][n] (cm_reduce.cu).
 cudaError_t launch_reduce_chunk(const float *P, void *y, int N, int64_t Mb, int64_t rc, int64_t n, int j, bool y_f32,

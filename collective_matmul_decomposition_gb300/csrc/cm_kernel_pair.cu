@@ -107,8 +107,12 @@ __device__ __forceinline__ bool ring_wait(const KParams &p, volatile int *abort,
     return wait_mbar<false>(p, abort, bar, parity, site, task, q);
 }
 
-template <bool B_MN, int CL>
+// LAYOUT bit 0: B is MN-major (W stored [K][n]); bit 1: A is MN-major (A
+// stored [K][rows], rows contiguous -- a transposed activation, as in a
+// weight-gradient GEMM).  An MN-major operand half is two 64-wide boxes.
+template <int LAYOUT, int CL>
 __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &cl) {
+    constexpr bool B_MN = (LAYOUT & 1) != 0, A_MN = (LAYOUT & 2) != 0;
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued = 0;   // ring stages filled so far
@@ -197,7 +201,10 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
             const uint32_t sa = a_smem0 + uint32_t(stage) * kHalfA, sb = b_smem0 + uint32_t(stage) * kHalfB;
             const int k0 = kb * kBK;
             if (cl.pos == 0) mbar_expect_tx(s.full + stage, tx_pair);
-            if (CL == 4)
+            if (A_MN) {
+                for (int j = 0; j < kCtaRows / 64; ++j)
+                    tma_load_3d_pair_a(sa + uint32_t(j * (64 * kBK * 2)), tm_a, fb, a_row + 64 * j, k0, slab);
+            } else if (CL == 4)
                 tma_load_3d_pair_mc_a(sa, tm_a, fb, k0, a_row, slab, mc_mask);
             else if (hinted)
                 tma_load_3d_pair_hint_a(sa, tm_a, fb, k0, a_row, slab, pol_a);
@@ -239,14 +246,19 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
             if (uint32_t(i) < issued) drain_mbar<true>(p, &s.full[i], i < stage ? phase : phase ^ 1u);
 }
 
-template <bool B_MN, int CL>
+template <int LAYOUT, int CL>
 __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
-    constexpr uint32_t kIdesc = idesc_bf16(kPairRows, kBN, B_MN);
+    constexpr bool B_MN = (LAYOUT & 1) != 0, A_MN = (LAYOUT & 2) != 0;
+    constexpr uint32_t kIdesc = idesc_bf16(kPairRows, kBN, B_MN, A_MN);
+    // SW128 descriptors: K-major halves step 32 bytes per K=16 MMA; MN-major
+    // halves are two 64-wide blocks 8 KB apart and step 16 rows of 128 bytes
+    constexpr uint32_t kALbo = A_MN ? 64 * kBK * 2 : 16;
+    constexpr uint32_t kAStep = A_MN ? (16 * 128) >> 4 : 32 >> 4;
     constexpr uint32_t kBLbo = B_MN ? 64 * kBK * 2 : 16;
     constexpr uint32_t kBStep = B_MN ? (16 * 128) >> 4 : 32 >> 4;
     // descriptors of ring stage 0; stage i adds its byte offset / 16 to the
     // start-address field (shared addresses stay below 2^18, so no carry)
-    const uint64_t ad0 = desc_sw128(smem_u32(s.a0), 16, 1024);
+    const uint64_t ad0 = desc_sw128(smem_u32(s.a0), kALbo, 1024);
     const uint64_t bd0 = desc_sw128(smem_u32(s.b0), kBLbo, 1024);
     QueueReader qr;
     qr.init(s);
@@ -275,7 +287,7 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
             const uint64_t bd = bd0 + uint64_t((uint32_t(stage) * kHalfB) >> 4);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-                mma_bf16_pair(d, ad + uint64_t(2 * k), bd + uint64_t(kBStep * k), kIdesc, (kk | k) != 0 ? 1u : 0u);
+                mma_bf16_pair(d, ad + uint64_t(kAStep * k), bd + uint64_t(kBStep * k), kIdesc, (kk | k) != 0 ? 1u : 0u);
             mma_commit_pair_mc(s.empty + stage, uint16_t((1u << CL) - 1u));   // every CTA's stage s
             if (++stage == kPStages) {
                 stage = 0;
@@ -619,7 +631,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
     if (lane == 0) bulk_wait<0>();
 }
 
-template <bool B_MN, int CL>
+template <int LAYOUT, int CL>
 __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_constant__ KParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -687,10 +699,10 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     const int total = (p.task_end - p.task_begin) * p.tiles_per_task;
 
     if (warp == 0) {
-        if (lane == 0) producer<B_MN, CL>(p, s, total, cl);
+        if (lane == 0) producer<LAYOUT, CL>(p, s, total, cl);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && cl.pos == 0) mma_issuer<B_MN, CL>(p, s, tmem_base, cl);
+        if (lane == 0 && cl.pos == 0) mma_issuer<LAYOUT, CL>(p, s, tmem_base, cl);
         __syncwarp();
     } else if (warp == 2) {
         if (lane == 0 && p.op == 0) forwarder<CL>(p, s, cl);
@@ -714,8 +726,10 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
 
 template <int CL>
 cudaError_t prepare_one(int device, int *max_clusters) {
-    for (int v = 0; v < 2; ++v) {
-        auto fn = v ? cm_pair_kernel<true, CL> : cm_pair_kernel<false, CL>;
+    // layouts built for this cluster size: K-major / MN-major B, and (one pair
+    // per cluster) both operands MN-major
+    void (*fns[3])(KParams) = {cm_pair_kernel<0, CL>, cm_pair_kernel<1, CL>, cm_pair_kernel<CL == 2 ? 3 : 1, CL>};
+    for (auto fn : fns) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
         if (e != cudaSuccess) return e;
     }
@@ -734,14 +748,14 @@ cudaError_t prepare_one(int device, int *max_clusters) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, cm_pair_kernel<false, CL>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, cm_pair_kernel<0, CL>, &cfg);
     if (e != cudaSuccess) return e;
     *max_clusters = n;
     return cudaSuccess;
 }
 
 template <int CL>
-cudaError_t launch_one(const KParams &p, bool b_mn_major, int clusters, cudaStream_t stream) {
+cudaError_t launch_one(const KParams &p, int layout, int clusters, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(CL * clusters), 1, 1);
     cfg.blockDim = dim3(kPThreads, 1, 1);
@@ -754,8 +768,14 @@ cudaError_t launch_one(const KParams &p, bool b_mn_major, int clusters, cudaStre
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (b_mn_major) return cudaLaunchKernelEx(&cfg, cm_pair_kernel<true, CL>, p);
-    return cudaLaunchKernelEx(&cfg, cm_pair_kernel<false, CL>, p);
+    switch (layout) {
+        case 0: return cudaLaunchKernelEx(&cfg, cm_pair_kernel<0, CL>, p);
+        case 1: return cudaLaunchKernelEx(&cfg, cm_pair_kernel<1, CL>, p);
+        case 3:
+            if (CL == 2) return cudaLaunchKernelEx(&cfg, cm_pair_kernel<CL == 2 ? 3 : 1, CL>, p);
+            return cudaErrorInvalidValue;   // both operands MN-major: one pair per cluster only
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -776,9 +796,9 @@ cudaError_t prepare_pair(int device, int cluster_ctas, int *max_clusters) {
     return cudaSuccess;
 }
 
-cudaError_t launch_pair(const KParams &p, bool b_mn_major, int cluster_ctas, int clusters, cudaStream_t stream) {
-    if (cluster_ctas == 4) return launch_one<4>(p, b_mn_major, clusters, stream);
-    return launch_one<2>(p, b_mn_major, clusters, stream);
+cudaError_t launch_pair(const KParams &p, int layout, int cluster_ctas, int clusters, cudaStream_t stream) {
+    if (cluster_ctas == 4) return launch_one<4>(p, layout, clusters, stream);
+    return launch_one<2>(p, layout, clusters, stream);
 }
 
 }  // namespace cm

@@ -211,6 +211,37 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
                                void *ws, size_t ws_bytes, cm_stream_t stream);
 
 /*
+ * cm_backward_pair -- the backward pass of the column-parallel layer whose
+ * forward is cm_ag_gemm (Y_r = concat_j(X_j) @ W_r^T, W_r stored [n][K]):
+ *   data gradient   dX_o = rows [o*m, (o+1)*m) of sum_r dY_r @ W_r
+ *                   -- a GEMM -> ReduceScatter, run as the decomposed ring
+ *                   of cm_gemm_rs with W_r read as [k = n][K];
+ *   weight gradient dW_r = dY_r^T @ concat_j(X_j)
+ *                   -- it needs every rank's gathered input, an AllGather the
+ *                   data gradient does not need, so it runs on a second,
+ *                   library-owned stream under the GEMM-RS ("bulk overlap").
+ * ("Tensor Parallelism > Communication Patterns": the backward pass is the
+ * forward's dual; "Hiding Tensor-Parallel Collectives: AG/RS Overlap in
+ * Megatron", section 7.)
+ *  x   [N][m][K] bf16: the forward input shards (read by the AllGather)
+ *  w   [N][n][K] bf16: the forward weights
+ *  dy  [N][N*m][n] bf16: each rank's output gradient
+ *  dx  [N][m][K]: the sequence-sharded input gradient (dx_dtype)
+ *  dw  [N][n][K]: the weight gradients (dw_dtype)
+ *  Buffers: the caller must not write x or dy until `stream` has passed
+ *  this call (the second stream reads x; `stream` waits for it before the
+ *  weight-gradient GEMM).  The gathered inputs live in the workspace,
+ *  cm_backward_pair_workspace_size(plan, m, K, n) bytes, 256-byte aligned.
+ *  Shapes: n, K and N*m at least 64; K and n multiples of 8; m divisible
+ *  by the plan's chunks.  Errors as cm_gemm_rs.
+ */
+size_t cm_backward_pair_workspace_size(cm_plan_t plan, int64_t m, int64_t K, int64_t n);
+cm_status cm_backward_pair(cm_plan_t plan, const void *x, const void *w, const void *dy,
+                           void *dx, cm_dtype dx_dtype, void *dw, cm_dtype dw_dtype,
+                           int64_t m, int64_t K, int64_t n, void *ws, size_t ws_bytes,
+                           cm_stream_t stream);
+
+/*
  * cm_check_status -- synchronise `stream` and read the device status word of
  * the last call that used `ws`.  Returns CM_OK, CM_ERR_TIMEOUT (a bounded
  * wait expired; the outputs of that call are undefined) or CM_ERR_CUDA.
@@ -252,6 +283,9 @@ const char *cm_status_string(cm_status status);
  *                        tiles runs through every column tile before the
  *                        next band starts; 4096 puts a whole group in one
  *                        band.
+ *  CM_OPT_BULK_OVERLAP   cm_backward_pair: 1 (default) runs the weight
+ *                        gradient's AllGather on a second stream under the
+ *                        data-gradient GEMM-RS; 0 runs it first on `stream`.
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
@@ -263,7 +297,8 @@ typedef enum cm_option {
     CM_OPT_TILE_GROUP = 6,
     CM_OPT_L2_HINTS = 7,
     CM_OPT_L2_PROMOTION = 8,
-    CM_OPT_ROW_BAND = 9
+    CM_OPT_ROW_BAND = 9,
+    CM_OPT_BULK_OVERLAP = 10
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);
