@@ -17,7 +17,10 @@ Contents
 * ``ring.py``: a rank-by-rank simulation of the ring schedules the pages
   describe (shards / accumulating buckets handed to a neighbour each step),
   in fp64, with its own schedule derived from the pages -- a second,
-  independent path that checks the schedule rather than the arithmetic.
+  independent path that checks the schedule rather than the arithmetic --
+  and of Cannon-style 2-D rotation on a q x q grid (A blocks move left, B
+  blocks move up), whose definition is the plain GEMM of the assembled
+  blocks.
 
 Parity pins (what each function is checked against, in ``tests/``) are listed
 in the test files; every function here has at least one pin.

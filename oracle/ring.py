@@ -220,3 +220,48 @@ def gemm_rs_ring(x_bits, w_bits, w_layout="nk", chunks=1, direction="uni",
 
     _run(N, rank)
     return (y, net.log) if return_log else y
+
+
+def cannon_gemm(a_bits, b_bits, q, b_layout="nk", drop=None, timeout=5.0, return_log=False):
+    """Cannon-style 2-D rotation ("Overlap Communication with Dependent
+    Computation via Decomposition ...", section "What people did before":
+    shard rotation interleaved with partial products, operands split along
+    the contracting dimension) on a q x q grid of ranks.
+
+    a_bits: [q*q][bm][bk], block A_{i,k} at index i*q + k.
+    b_bits: [q*q] blocks of B, B_{k,j} at index k*q + j, each [bn][bk]
+            ("nk") or [bk][bn] ("kn").
+    Rank (i, j) starts with A_{i,(i+j) mod q} and B_{(i+j) mod q, j} (the
+    skew: with every block in one memory the rank simply starts from those),
+    then for q steps multiplies what it holds into C_{i,j}, sends its A block
+    to the left neighbour (i, j-1) and its B block to the upper neighbour
+    (i-1, j), and receives the next ones from the right and from below.
+    Returns C [q*q][bm][bn] fp64, C_{i,j} at index i*q + j.
+    """
+    a = np.ascontiguousarray(a_bits)
+    b = np.ascontiguousarray(b_bits)
+    P = q * q
+    assert a.shape[0] == P and b.shape[0] == P
+    bm = a.shape[1]
+    bn = b.shape[1] if b_layout == "nk" else b.shape[2]
+    c = np.full((P, bm, bn), np.nan)
+    net = _Net(P, ["a", "b"], drop, timeout)
+
+    def rank(rho):
+        i, j = divmod(rho, q)
+        k0 = (i + j) % q
+        a_id, a_blk = (i, k0), a[i * q + k0]
+        b_id, b_blk = (k0, j), b[k0 * q + j]
+        acc = np.zeros((bm, bn))
+        for s in range(q):
+            assert a_id[1] == b_id[0], "the held blocks share the contraction index"
+            acc += _gemm(a_blk, b_blk, b_layout)
+            if s + 1 < q:
+                net.send(rho, i * q + (j - 1) % q, "a", s, a_id, 0, a_blk)
+                net.send(rho, ((i - 1) % q) * q + j, "b", s, b_id, 0, b_blk)
+                a_id, _, a_blk = net.recv(rho, "a", s + 1)
+                b_id, _, b_blk = net.recv(rho, "b", s + 1)
+        c[rho] = acc
+
+    _run(P, rank)
+    return (c, net.log) if return_log else c

@@ -366,3 +366,80 @@ def test_plant_wgrad_wrong_token_order_fails_identity():
     lhs = float((_f64(dy) * oracle.ag_gemm(xb, wb, "nk")).sum())
     bad = oracle.wgrad(xb[::-1].copy(), dyb)                   # X_all built from reversed shards
     assert abs(float((bad * _f64(w)).sum()) - lhs) > 1e-6 * max(1.0, abs(lhs))
+
+
+# --- Cannon-style 2-D rotation ("Overlap Communication with Dependent
+# Computation via Decomposition ...", section "What people did before") ----
+
+def _cannon_blocks(q, bm, bk, bn, seed, layout="nk"):
+    a, _ = gen.ag_inputs(q * q, bm, bk, 1, gen.NORMAL1, gen.NORMAL002, seed=seed)
+    bshape = (q * q, bn, bk) if layout == "nk" else (q * q, bk, bn)
+    b, _ = gen.ag_inputs(bshape[0], bshape[1], bshape[2], 1, gen.NORMAL1, gen.NORMAL002, seed=seed + 1)
+    return a, b
+
+
+def _assemble(a, b, q, layout):
+    """Plain matrices: A [q*bm][q*bk] and B as a [q*bk][q*bn] "kn" operand."""
+    P, bm, bk = a.shape
+    A = a.reshape(q, q, bm, bk).permute(0, 2, 1, 3).reshape(q * bm, q * bk)
+    bb = b if layout == "kn" else b.transpose(1, 2)          # blocks as [bk][bn]
+    bn = bb.shape[2]
+    B = bb.reshape(q, q, bk, bn).permute(0, 2, 1, 3).reshape(q * bk, q * bn)
+    return A.contiguous(), B.contiguous()
+
+
+@pytest.mark.parametrize("q", [1, 2, 3, 4])
+@pytest.mark.parametrize("layout", ["nk", "kn"])
+def test_cannon_ring_equals_definition(q, layout):
+    bm, bk, bn = 5, 6, 4
+    a, b = _cannon_blocks(q, bm, bk, bn, seed=50 + q, layout=layout)
+    c = ring.cannon_gemm(gen.bf16_bits(a), gen.bf16_bits(b), q, layout)
+    A, B = _assemble(a, b, q, layout)
+    ref = oracle.gemm(gen.bf16_bits(A), gen.bf16_bits(B), "kn")      # [q*bm][q*bn]
+    got = c.reshape(q, q, bm, bn).transpose(0, 2, 1, 3).reshape(q * bm, q * bn)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+@pytest.mark.parametrize("q", [2, 3, 4])
+def test_cannon_schedule_properties(q):
+    """A moves only to the left neighbour, B only up; every rank holds every
+    contraction block exactly once."""
+    a, b = _cannon_blocks(q, 2, 3, 2, seed=60)
+    _, log = ring.cannon_gemm(gen.bf16_bits(a), gen.bf16_bits(b), q, "nk", return_log=True)
+    held = {rho: set() for rho in range(q * q)}
+    for rho in range(q * q):
+        i, j = divmod(rho, q)
+        held[rho].add((i + j) % q)
+    for step, stream, src, dst, obj, _ in log:
+        si, sj = divmod(src, q)
+        di, dj = divmod(dst, q)
+        if stream == "a":
+            assert (di, dj) == (si, (sj - 1) % q) and obj[0] == di
+            held[dst].add(obj[1])
+        else:
+            assert (di, dj) == ((si - 1) % q, sj) and obj[1] == dj
+    assert all(h == set(range(q)) for h in held.values())
+    assert len(log) == 2 * q * q * (q - 1)
+
+
+def test_cannon_dropped_message_times_out():
+    a, b = _cannon_blocks(2, 2, 2, 2, seed=70)
+    with pytest.raises(ring.RingTimeout):
+        ring.cannon_gemm(gen.bf16_bits(a), gen.bf16_bits(b), 2, "nk", drop={(0, 0, "a")}, timeout=0.5)
+
+
+def test_plant_cannon_without_skew_fails_definition(monkeypatch):
+    """Starting every rank from k = 0 (no skew) pairs mismatched blocks."""
+    q, bm, bk, bn = 3, 3, 4, 2
+    a, b = _cannon_blocks(q, bm, bk, bn, seed=80)
+    src = open(ring.__file__).read()
+    assert "k0 = (i + j) % q" in src
+    bad_ns = {"__name__": "oracle.ring", "__package__": "oracle"}
+    exec(compile(src.replace("k0 = (i + j) % q", "k0 = 0").replace(
+        'assert a_id[1] == b_id[0], "the held blocks share the contraction index"', "pass"),
+        ring.__file__, "exec"), bad_ns)
+    c = bad_ns["cannon_gemm"](gen.bf16_bits(a), gen.bf16_bits(b), q, "nk")
+    A, B = _assemble(a, b, q, "nk")
+    ref = oracle.gemm(gen.bf16_bits(A), gen.bf16_bits(B), "kn")
+    got = c.reshape(q, q, bm, bn).transpose(0, 2, 1, 3).reshape(q * bm, q * bn)
+    assert not np.allclose(got, ref, rtol=1e-6, atol=1e-6)
