@@ -683,6 +683,47 @@ def run_backward(args):
     return 0
 
 
+def run_cannon(args):
+    """Cannon-style 2-D rotation on q x q logical ranks for C = A @ B with
+    A, B, C of 8192 x 8192 (bf16 in, bf16 out), against the same GEMM as one
+    launch of this kernel (N=1) and torch.matmul."""
+    import torch
+    import __graft_entry__
+    from collective_matmul_decomposition_gb300 import cm
+    from collective_matmul_decomposition_gb300 import inputs as gen
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    peaks, kind = load_peaks()
+    S = 8192
+    for q in (2, 4):
+        b_ = S // q
+        a, _ = gen.ag_inputs(q * q, b_, b_, 1, gen.NORMAL1, gen.NORMAL002, seed=7000)
+        b, _ = gen.ag_inputs(q * q, b_, b_, 1, gen.NORMAL1, gen.NORMAL002, seed=7001)   # blocks [bn][bk]
+        a, b = a.to(device), b.to(device)
+        c = torch.empty(q * q, b_, b_, dtype=torch.bfloat16, device=device)
+        plan = cm.Plan(q * q, 1, "uni")
+        ws = torch.empty(plan.cannon_workspace_size(b_, b_, b_), dtype=torch.uint8, device=device)
+        ms = time_loop(lambda: cm.cm_cannon_gemm(plan, a, b, c, ws, "nk"), args.steps, torch, warmup=args.warmup)
+        st, info = cm.cm_check_status(ws)
+        if st != 0:
+            raise RuntimeError(f"cannon: device status {st} {info}")
+        A = a.reshape(q, q, b_, b_).permute(0, 2, 1, 3).reshape(S, S).contiguous()
+        Bt = b.reshape(q, q, b_, b_).permute(1, 2, 0, 3).reshape(S, S).contiguous()   # [n][K]
+        one = cm.Plan(1, 1, "uni")
+        y1 = torch.empty(1, S, S, dtype=torch.bfloat16, device=device)
+        ws1 = torch.empty(one.ag_workspace_size(S, S), dtype=torch.uint8, device=device)
+        ms_mono = time_loop(lambda: cm.cm_ag_gemm(one, A[None], Bt[None], y1, ws1, "nk"), args.steps, torch,
+                            warmup=args.warmup)
+        ms_torch = time_loop(lambda: torch.matmul(A, Bt.t()), args.steps, torch, warmup=args.warmup)
+        fl = 2.0 * S ** 3
+        print(json.dumps({"cannon": f"{S}x{S}x{S}", "q": q, "ms": ms, "tflops": fl / (ms / 1e3) / 1e12,
+                          "ms_monolithic_same_kernel": ms_mono, "ms_torch": ms_torch,
+                          "rotation_bytes_per_step": 2 * q * q * b_ * b_ * 2, "peak_source": kind}), flush=True)
+        del a, b, c, ws, A, Bt, y1, ws1
+        torch.cuda.empty_cache()
+    return 0
+
+
 def run_profile_case(args):
     """A few calls of one op of one workload, nothing else: the command ncu captures."""
     import torch
@@ -726,6 +767,7 @@ def main(argv=None):
     ap.add_argument("--sweep", action="store_true")
     ap.add_argument("--gate", action="store_true", help="the cost model's choices against measurement")
     ap.add_argument("--backward", action="store_true", help="the backward pair of the MLP fc1 layer")
+    ap.add_argument("--cannon", action="store_true", help="Cannon-style 2-D rotation, 8192^3")
     ap.add_argument("--profile", choices=["ag", "rs"], default=None,
                     help="run only --steps calls of one op (for ncu captures)")
     ap.add_argument("--workload", default=WORKLOAD)
@@ -753,6 +795,8 @@ def main(argv=None):
         return run_gate(args)
     if args.backward:
         return run_backward(args)
+    if args.cannon:
+        return run_cannon(args)
     if args.profile:
         return run_profile_case(args)
     return run_ours(args)

@@ -34,7 +34,8 @@ EXPORTS = ["cm_plan", "cm_plan_destroy", "cm_plan_steps", "cm_plan_step", "cm_pl
            "cm_check_status", "cm_status_string", "cm_plan_set_option", "cm_version",
            "cm_ag_gemm_noalloc", "cm_cost_estimate", "cm_plan_choose",
            "cm_gemm_rs_pipelined_workspace_size", "cm_gemm_rs_pipelined",
-           "cm_backward_pair_workspace_size", "cm_backward_pair"]
+           "cm_backward_pair_workspace_size", "cm_backward_pair",
+           "cm_cannon_workspace_size", "cm_cannon_gemm"]
 CM_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -109,6 +110,10 @@ def load():
     lib.cm_backward_pair_workspace_size.restype = sz
     lib.cm_backward_pair.argtypes = [p, p, p, p, p, i32, p, i32, i64, i64, i64, p, sz, p]
     lib.cm_backward_pair.restype = i32
+    lib.cm_cannon_workspace_size.argtypes = [p, i64, i64, i64]
+    lib.cm_cannon_workspace_size.restype = sz
+    lib.cm_cannon_gemm.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p, sz, p]
+    lib.cm_cannon_gemm.restype = i32
     rp = ctypes.POINTER(cm_rates)
     lib.cm_cost_estimate.argtypes = [i32, i32, i32, i32, i64, i64, i64, rp, ctypes.POINTER(ctypes.c_double)]
     lib.cm_cost_estimate.restype = i32
@@ -165,6 +170,9 @@ class Plan:
 
     def ag_workspace_size(self, m: int, K: int) -> int:
         return int(load().cm_ag_gemm_workspace_size(self.handle, int(m), int(K)))
+
+    def cannon_workspace_size(self, bm: int, bk: int, bn: int) -> int:
+        return load().cm_cannon_workspace_size(self.handle, bm, bk, bn)
 
     def backward_pair_workspace_size(self, m: int, K: int, n: int) -> int:
         return load().cm_backward_pair_workspace_size(self.handle, m, K, n)
@@ -242,6 +250,15 @@ def cm_backward_pair(plan: Plan, x, w, dy, dx, dw, ws, stream=None):
                                  _ydtype(dw), m, K, n, _ptr(ws), ws.numel() * ws.element_size(),
                                  _stream_ptr(stream))
     _check(st, "cm_backward_pair")
+
+
+def cm_cannon_gemm(plan: Plan, a, b, c, ws, b_layout: str = "nk", stream=None):
+    """Cannon-style 2-D rotation: a [q*q][bm][bk], b blocks, c [q*q][bm][bn]."""
+    P, bm, bk = a.shape
+    bn = b.shape[1] if b_layout == "nk" else b.shape[2]
+    st = load().cm_cannon_gemm(plan.handle, _ptr(a), _ptr(b), LAYOUTS[b_layout], _ptr(c), _ydtype(c), bm, bk, bn,
+                               _ptr(ws), ws.numel() * ws.element_size(), _stream_ptr(stream))
+    _check(st, "cm_cannon_gemm")
 
 
 def cm_check_status(ws, stream=None):

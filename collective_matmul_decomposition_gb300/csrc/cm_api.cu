@@ -210,10 +210,10 @@ struct SideStream {
     cudaEvent_t ev[CM_MAX_CHUNKS + 1] = {};
 };
 
-enum SideUser { kSidePipelinedRs = 0, kSideBackwardPair = 1 };
+enum SideUser { kSidePipelinedRs = 0, kSideBackwardPair = 1, kSideCannon = 2 };
 
 SideStream *side_stream(int dev, SideUser user) {   // caller holds that user's call mutex
-    static SideStream ss[2][kMaxDevices];
+    static SideStream ss[3][kMaxDevices];
     SideStream &d = ss[user][dev];
     if (!d.stream) {
         if (cudaStreamCreateWithFlags(&d.stream, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
@@ -594,6 +594,153 @@ cm_status cm_backward_pair(cm_plan_t plan, const void *x, const void *w, const v
     if (cudaMemsetAsync(w8 + bl.wg_off, 0, 256, s) != cudaSuccess) return CM_ERR_CUDA;
     if (launch_tiles(pl, kc, kp, 3, int64_t(N) * kp.tiles_per_task, max_clusters, sms, s) != cudaSuccess)
         return CM_ERR_CUDA;
+    return CM_OK;
+}
+
+// Cannon workspace: the status block, two fp32 accumulators per rank
+// (ping-pong across steps), then two sets of rotated A blocks and two of B.
+struct CannonLayout {
+    size_t acc_off = 0, a_off = 0, b_off = 0, total = 0;
+};
+
+CannonLayout cannon_layout(int P, int64_t bm, int64_t bk, int64_t bn) {
+    CannonLayout c;
+    c.acc_off = 1024;
+    c.a_off = align_up(c.acc_off + size_t(P) * 2 * size_t(bm) * size_t(bn) * 4, 1024);
+    c.b_off = align_up(c.a_off + 2 * size_t(P) * size_t(bm) * size_t(bk) * 2, 1024);
+    c.total = c.b_off + 2 * size_t(P) * size_t(bk) * size_t(bn) * 2;
+    return c;
+}
+
+int grid_side(int P) {   // q with q * q == P, else 0
+    for (int q = 1; q * q <= P; ++q)
+        if (q * q == P) return q;
+    return 0;
+}
+
+size_t cm_cannon_workspace_size(cm_plan_t plan, int64_t bm, int64_t bk, int64_t bn) {
+    if (!plan || bm <= 0 || bk <= 0 || bn <= 0 || grid_side(plan->impl.N) == 0) return 0;
+    return cannon_layout(plan->impl.N, bm, bk, bn).total;
+}
+
+cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayout blayout, void *c, cm_dtype c_dtype,
+                         int64_t bm, int64_t bk, int64_t bn, void *ws, size_t ws_bytes, cm_stream_t stream) {
+    cm_status st = check_common(plan, a, b, blayout, c, c_dtype, bm, bk, bn);
+    if (st != CM_OK) return st;
+    const PlanImpl &pl = plan->impl;
+    const int P = pl.N, q = grid_side(P);
+    if (q == 0) return CM_ERR_SHAPE;
+    const CannonLayout cl = cannon_layout(P, bm, bk, bn);
+    if (!ws || ws_bytes < cl.total) return CM_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return CM_ERR_ALIGNMENT;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t *w8 = static_cast<uint8_t *>(ws);
+    float *acc = reinterpret_cast<float *>(w8 + cl.acc_off);
+    const size_t a_blk = size_t(bm) * size_t(bk) * 2, b_blk = size_t(bk) * size_t(bn) * 2;
+    uint8_t *aset[2] = {w8 + cl.a_off, w8 + cl.a_off + size_t(P) * a_blk};
+    uint8_t *bset[2] = {w8 + cl.b_off, w8 + cl.b_off + size_t(P) * b_blk};
+    const uint8_t *a_in = static_cast<const uint8_t *>(a), *b_in = static_cast<const uint8_t *>(b);
+
+    static KParams kp;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CM_ERR_CUDA;
+    SideStream *ss = side_stream(dev, kSideCannon);
+    if (!ss) return CM_ERR_CUDA;
+    // events: ev[0] start, ev[1 + s] rotation into step s ready (s >= 1),
+    // ev[1 + q + s] GEMM of step s done -- 1 + 2q <= CM_MAX_CHUNKS + 1 for q <= 4
+    cudaEvent_t *ev = ss->ev;
+    std::memset(static_cast<void *>(&kp), 0, sizeof kp);
+    kp.q_only = -1;
+    g_l2_promotion = pl.l2_promotion;
+    const KernelChoice kc = choose_kernel(pl, bn);
+    const bool b_mn = blayout == CM_W_KN;
+    const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(a_rows, bm));
+    if (!make_map(&kp.tmAcc, acc, uint64_t(bn), uint64_t(bm), uint64_t(P) * 2, 32, 32, true)) return CM_ERR_CUDA;
+    kp.y = c;
+    kp.acc = acc;
+    kp.out_rows_per_idx = bm;
+    kp.acc_buf_stride = bm * bn;
+    kp.op = 1;
+    kp.N = P;
+    kp.chunks = 1;
+    kp.rows_c = int(bm);
+    kp.kblocks = int((bk + kBK - 1) / kBK);
+    kp.n = int(bn);
+    kp.y_f32 = c_dtype == CM_F32;
+    kp.a_box_rows = int(box_rows);
+    set_tiling(kc, CM_OP_GEMM_RS, kp, bm, bn);
+    kp.tgt_in = kp.tgt_free = 0;
+    WsLayout l;
+    l.flags_off = 256;
+    l.buf_off = 1024;
+    int sms = 0, max_clusters = 0;
+    st = setup_launch(pl, kc, kp, l, ws, &sms, &max_clusters);
+    if (st != CM_OK) return st;
+    if (cudaMemsetAsync(ws, 0, 256, s) != cudaSuccess) return CM_ERR_CUDA;
+    if (cudaEventRecord(ev[0], s) != cudaSuccess) return CM_ERR_CUDA;
+    auto held_k = [q](int i, int j, int step) { return (i + j + step) % q; };
+    for (int step = 0; step < q; ++step) {
+        // GEMM of this step: rank (i, j) multiplies A_{i,k} B_{k,j}, k = (i+j+step) mod q,
+        // adding the accumulator of the previous step; the last step writes C
+        if (step > 0 && cudaStreamWaitEvent(s, ev[1 + step], 0) != cudaSuccess) return CM_ERR_CUDA;
+        const void *asrc = step == 0 ? static_cast<const void *>(a_in) : aset[step % 2];
+        const void *bsrc = step == 0 ? static_cast<const void *>(b_in) : bset[step % 2];
+        if (!make_map(&kp.tmA0, asrc, uint64_t(bk), uint64_t(bm), uint64_t(P), kBK, box_rows)) return CM_ERR_CUDA;
+        kp.tmA1 = kp.tmA0;
+        if (b_mn) {
+            if (!make_map(&kp.tmB, bsrc, uint64_t(bn), uint64_t(bk), uint64_t(P), 64, kBK)) return CM_ERR_CUDA;
+        } else {
+            const uint32_t b_rows = kc.pair ? kBN / 2 : kBN;
+            if (!make_map(&kp.tmB, bsrc, uint64_t(bk), uint64_t(bn), uint64_t(P), kBK, b_rows)) return CM_ERR_CUDA;
+        }
+        for (int rho = 0; rho < P; ++rho) {
+            const int i = rho / q, j = rho % q, k = held_k(i, j, 0);
+            cm_task &t = kp.tasks[rho];
+            std::memset(&t, 0xff, sizeof t);   // every field -1 ...
+            t.a_src = 0;
+            t.a_slab = int16_t(step == 0 ? i * q + k : rho);    // skewed input block, or the rotated one
+            t.rank = int16_t(step == 0 ? k * q + j : rho);      // B slab
+            t.out_idx = int16_t(rho);
+            t.in_buf[0] = int16_t(step > 0 ? rho * 2 + (step - 1) % 2 : -1);
+            t.out_buf = int16_t(step + 1 < q ? rho * 2 + step % 2 : -1);
+            t.step = int16_t(step);
+            t.stream = 0;
+            t.tile_group = int16_t(1 << 8);
+        }
+        kp.task_begin = 0;
+        kp.task_end = P;
+        kp.tile_counter = reinterpret_cast<uint32_t *>(w8 + kCounterOff) + step;
+        if (launch_tiles(pl, kc, kp, b_mn ? 1 : 0, int64_t(P) * kp.tiles_per_task, max_clusters, sms, s) !=
+            cudaSuccess)
+            return CM_ERR_CUDA;
+        if (cudaEventRecord(ev[1 + q + step], s) != cudaSuccess) return CM_ERR_CUDA;
+        // rotation into step + 1 on the second stream, under this GEMM: rank
+        // (i, j) receives A from (i, j+1) and B from (i+1, j).  It writes the
+        // set the GEMM of step - 1 read, so it waits for that GEMM.
+        if (step + 1 < q) {
+            const int nx = step + 1;
+            if (step == 0 && cudaStreamWaitEvent(ss->stream, ev[0], 0) != cudaSuccess) return CM_ERR_CUDA;
+            if (step >= 1 && cudaStreamWaitEvent(ss->stream, ev[1 + q + step - 1], 0) != cudaSuccess)
+                return CM_ERR_CUDA;
+            for (int rho = 0; rho < P; ++rho) {
+                const int i = rho / q, j = rho % q;
+                const int ra = i * q + (j + 1) % q, rb = ((i + 1) % q) * q + j;   // right and lower neighbours
+                const uint8_t *sa = step == 0 ? a_in + size_t(i * q + held_k(i, (j + 1) % q, 0)) * a_blk
+                                              : aset[step % 2] + size_t(ra) * a_blk;
+                const uint8_t *sb = step == 0 ? b_in + size_t(held_k((i + 1) % q, j, 0) * q + j) * b_blk
+                                              : bset[step % 2] + size_t(rb) * b_blk;
+                if (cudaMemcpyAsync(aset[nx % 2] + size_t(rho) * a_blk, sa, a_blk, cudaMemcpyDeviceToDevice,
+                                    ss->stream) != cudaSuccess ||
+                    cudaMemcpyAsync(bset[nx % 2] + size_t(rho) * b_blk, sb, b_blk, cudaMemcpyDeviceToDevice,
+                                    ss->stream) != cudaSuccess)
+                    return CM_ERR_CUDA;
+            }
+            if (cudaEventRecord(ev[1 + nx], ss->stream) != cudaSuccess) return CM_ERR_CUDA;
+        }
+    }
     return CM_OK;
 }
 

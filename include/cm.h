@@ -242,6 +242,33 @@ cm_status cm_backward_pair(cm_plan_t plan, const void *x, const void *w, const v
                            cm_stream_t stream);
 
 /*
+ * cm_cannon_gemm -- Cannon-style 2-D rotation on a q x q grid of logical
+ * ranks (q * q = the plan's rank count: 1, 4, 9 or 16), the contracting-
+ * dimension-sharded special case of the decomposition ("Overlap
+ * Communication with Dependent Computation via Decomposition in Large Deep
+ * Learning Models", section "What people did before": shard rotation
+ * interleaved with partial products).  C = A @ B with every operand in
+ * q x q blocks:
+ *   a  [q*q][bm][bk] bf16, block A_{i,k} at index i*q + k
+ *   b  [q*q] blocks of B, B_{k,j} at index k*q + j, each [bn][bk]
+ *      (CM_W_NK) or [bk][bn] (CM_W_KN)
+ *   c  [q*q][bm][bn] (c_dtype), block C_{i,j} at index i*q + j
+ * Rank (i, j) starts from A_{i,(i+j) mod q} and B_{(i+j) mod q, j} (the
+ * skew, read in place), then for q steps multiplies what it holds into an
+ * fp32 accumulator while the next blocks rotate in -- A from the right
+ * neighbour (i, j+1), B from below (i+1, j) -- by copies on a second,
+ * library-owned stream under the step's GEMM.  One kernel launch per step.
+ *  Workspace: cm_cannon_workspace_size(plan, bm, bk, bn) bytes, 256-byte
+ *  aligned (accumulators and two sets of rotated blocks).
+ *  Errors: CM_ERR_SHAPE if the rank count is not a square; otherwise as
+ *  cm_gemm_rs (bk and bn multiples of 8).
+ */
+size_t cm_cannon_workspace_size(cm_plan_t plan, int64_t bm, int64_t bk, int64_t bn);
+cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayout b_layout,
+                         void *c, cm_dtype c_dtype, int64_t bm, int64_t bk, int64_t bn,
+                         void *ws, size_t ws_bytes, cm_stream_t stream);
+
+/*
  * cm_check_status -- synchronise `stream` and read the device status word of
  * the last call that used `ws`.  Returns CM_OK, CM_ERR_TIMEOUT (a bounded
  * wait expired; the outputs of that call are undefined) or CM_ERR_CUDA.
