@@ -16,18 +16,20 @@
 // Both pairs' MMA commits release every CTA's ring stage, so a multicast
 // never lands in a stage still being read.
 //
-// Tiles are handed out dynamically: the leader's producer takes the next
-// tile index from a global counter and publishes it to both CTAs through a
-// small shared-memory queue, so clusters that finish early take the next
+// Tiles are handed out dynamically: a scheduler thread of the cluster leader
+// takes the next tile index from a global counter and publishes it to every
+// CTA through a small shared-memory queue, so clusters that finish early take the next
 // tile in order (the tiles running at any time stay close together, which
 // keeps their operands in L2) and a tile's dependencies are always on tiles
 // handed out earlier.
 //
 // Roles (384 threads per CTA):
-//   warp 0    producer: leader = scheduler + TMA loads of its halves;
-//             peer = TMA loads of its halves.  All loads complete on the
-//             leader's ring barrier; the leader posts the byte count.  The
-//             leader takes the next tile index while the current tile loads.
+//   warp 0    producer: TMA loads of this CTA's halves.  All loads complete
+//             on the pair leader's ring barrier; the leader posts the byte
+//             count.
+//   warp 3    scheduler (cluster leader only): takes tile j + 1 from the
+//             global counter once the producer has started tile j, and
+//             publishes it to every CTA of the cluster.
 //   warp 1    MMA issuer (leader only): pair MMAs; commits each stage and,
 //             per tile, the accumulator to the barriers of both CTAs.
 //   warp 2    AG forwarder (both CTAs): every tile copies a slice of its CTA's
@@ -72,7 +74,7 @@ struct Cl {
 struct PSmem {
     uint8_t *a0, *b0;   // ring stage 0 of A and B; stage i is kHalfA (kHalfB) bytes further
     uint8_t *fbuf[2];   // AG: forwarder copy buffers; RS: the same 32 KB as 8 epilogue-warp buffers
-    uint64_t *full, *empty, *tfull, *tempty, *drain, *fbar, *qfull, *qempty, *ebar;
+    uint64_t *full, *empty, *tfull, *tempty, *drain, *fbar, *qfull, *qempty, *ebar, *started;
     volatile int32_t *qtile;
     uint32_t *tmem_slot;
     volatile int *abort;
@@ -133,41 +135,10 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
     const uint64_t tm_b = reinterpret_cast<uint64_t>(&p.tmB);
     QueueReader qr;
     qr.init(s);
-    int qslot = 0;
-    uint32_t qphase = 0;
-    // Tile indices: the cluster leader takes them from the global counter (or
-    // the next of its static round-robin share) and publishes them to every
-    // CTA of the cluster through the queue; the others read the queue.  The
-    // leader takes the index of the next tile while the first slices of the
-    // current one are already loading and publishes it a few slices later, so
-    // the counter's round trip never sits between two tiles' loads; the other
-    // CTAs read it at the tile boundary, long after it was published.
-    const int cid = int(blockIdx.x) / CL, ncl = int(gridDim.x) / CL;
-    int static_next = cid;
-    auto take = [&]() -> int {
-        if (p.static_tiles) {
-            const int t = static_next;
-            static_next += ncl;
-            return t;
-        }
-        return int(atomic_add_relaxed(p.tile_counter, 1u));
-    };
-    auto publish = [&](int t) -> int {
-        if (!wait_mbar<true>(p, s.abort, &s.qempty[qslot], qphase ^ 1u, kSiteEmpty, -1, -1)) return -1;
-        if (t >= total) t = -1;
-        s.qtile[qslot] = t;
-        for (uint32_t r = 1; r < uint32_t(CL); ++r)
-            st_shared_cluster(mapa_shared(smem_u32(const_cast<int32_t *>(&s.qtile[qslot])), r), uint32_t(t));
-        mbar_arrive(&s.qfull[qslot]);
-        for (uint32_t r = 1; r < uint32_t(CL); ++r) mbar_arrive_cluster(mapa_shared(smem_u32(&s.qfull[qslot]), r));
-        if (++qslot == kQueue) {
-            qslot = 0;
-            qphase ^= 1u;
-        }
-        return t;
-    };
-    const bool leads = cl.rank == 0;
-    int cur = leads ? publish(take()) : qr.next(p, s);
+    // tile indices come from the cluster leader's scheduler thread through
+    // the queue; this CTA's producer tells it when a tile starts loading
+    const bool signals = cl.rank == 0;
+    int cur = qr.next(p, s);
     while (cur >= 0 && !*s.abort) {
         const TileCoord c = decode_cl(p, cur, cl.pair, CL / 2);
         const cm_task &tk = p.tasks[c.task];
@@ -188,8 +159,7 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
         const int a_row = c.mt * kPairRows + int(cl.pos) * kCtaRows + (CL == 4 ? int(cl.pair) * (kCtaRows / 2) : 0);
         const int n0 = c.nt * kBN + int(cl.pos) * (kBN / 2);
         const int nk = kslices(p, tk);
-        const int publish_at = min(3, nk - 1);
-        int taken = 0, nxt = -1, kb = 0;
+        int kb = 0;
         bool ok = true;
         bool free_ready = mbar_test_wait(s.empty + stage, phase ^ 1u);
         for (int kk = 0; kk < nk; ++kk) {
@@ -229,13 +199,10 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
                 ++rr;
                 slab += slab_step;
             }
-            if (leads) {
-                if (kk == 0) taken = take();   // the result is not needed until publish_at
-                if (kk == publish_at) nxt = publish(taken);
-            }
+            if (signals && kk == 0) mbar_arrive(s.started);
         }
         if (!ok) break;
-        cur = leads ? nxt : qr.next(p, s);
+        cur = qr.next(p, s);
     }
     // a pair leader's ring barriers count every load into its pair: once they
     // complete, no load is still writing this pair's shared memory.  Stage i
@@ -244,6 +211,44 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
     if (cl.pos == 0)
         for (int i = 0; i < kPStages; ++i)
             if (uint32_t(i) < issued) drain_mbar<true>(p, &s.full[i], i < stage ? phase : phase ^ 1u);
+}
+
+// The cluster leader's scheduler (warp 3): takes tile indices from the
+// global counter (or the next of its static round-robin share) and publishes
+// them to every CTA of the cluster through the queue.  Tile j + 1 is taken
+// once the leader's producer has started loading tile j, so a cluster holds at
+// most one tile beyond the one loading, while the counter's round trip and
+// the cluster-scope publication stay off the producer's path.
+template <int CL>
+__device__ void scheduler(const KParams &p, const PSmem &s, int total) {
+    const int cid = int(blockIdx.x) / CL, ncl = int(gridDim.x) / CL;
+    int static_next = cid, slot = 0;
+    uint32_t qphase = 0, sphase = 0;
+    for (int j = 0;; ++j) {
+        if (j > 0) {
+            if (!wait_mbar<false>(p, s.abort, s.started, sphase, kSiteEmpty, -1, -1)) return;
+            sphase ^= 1u;
+        }
+        int t;
+        if (p.static_tiles) {
+            t = static_next;
+            static_next += ncl;
+        } else {
+            t = int(atomic_add_relaxed(p.tile_counter, 1u));
+        }
+        if (t >= total) t = -1;
+        if (!wait_mbar<true>(p, s.abort, &s.qempty[slot], qphase ^ 1u, kSiteEmpty, -1, -1)) return;
+        s.qtile[slot] = t;
+        for (uint32_t r = 1; r < uint32_t(CL); ++r)
+            st_shared_cluster(mapa_shared(smem_u32(const_cast<int32_t *>(&s.qtile[slot])), r), uint32_t(t));
+        mbar_arrive(&s.qfull[slot]);
+        for (uint32_t r = 1; r < uint32_t(CL); ++r) mbar_arrive_cluster(mapa_shared(smem_u32(&s.qfull[slot]), r));
+        if (++slot == kQueue) {
+            slot = 0;
+            qphase ^= 1u;
+        }
+        if (t < 0) return;
+    }
 }
 
 template <int LAYOUT, int CL>
@@ -271,7 +276,9 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
         if (t < 0 || *s.abort) break;
         const TileCoord c = decode_cl(p, t, cl.pair, CL / 2);
         const cm_task &tk = p.tasks[c.task];
-        if (!wait_mbar<true>(p, s.abort, &s.tempty[accb], acc_phase ^ 1u, kSiteTmemEmpty, c.task, c.q)) break;
+        if (!mbar_try_wait_cluster(&s.tempty[accb], acc_phase ^ 1u) &&
+            !wait_mbar<true>(p, s.abort, &s.tempty[accb], acc_phase ^ 1u, kSiteTmemEmpty, c.task, c.q))
+            break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(accb * kBN);
         const int nk = kslices(p, tk);
@@ -650,7 +657,8 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     s.qfull = s.fbar + 2;
     s.qempty = s.qfull + kQueue;
     s.ebar = s.qempty + kQueue;
-    s.qtile = reinterpret_cast<volatile int32_t *>(s.ebar + kPEpiWarps);
+    s.started = s.ebar + kPEpiWarps;
+    s.qtile = reinterpret_cast<volatile int32_t *>(s.started + 1);
     s.tmem_slot = reinterpret_cast<uint32_t *>(const_cast<int32_t *>(s.qtile) + kQueue);
     s.abort = reinterpret_cast<volatile int *>(s.tmem_slot + 1);
 
@@ -671,9 +679,10 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
             mbar_init(&s.fbar[i], 1);
         }
         mbar_init(s.drain, 1);
-        // queue readers: the pair leaders' MMA threads, the other CTAs'
-        // producers, 8 epilogue warps per CTA and (AG) every forwarder
-        const uint32_t readers = CL / 2 + (CL - 1) + CL * kPEpiWarps + (p.op == 0 ? CL : 0);
+        mbar_init(s.started, 1);
+        // queue readers: the pair leaders' MMA threads, every producer, 8
+        // epilogue warps per CTA and (AG) every forwarder
+        const uint32_t readers = CL / 2 + CL + CL * kPEpiWarps + (p.op == 0 ? CL : 0);
         for (int i = 0; i < kQueue; ++i) {
             mbar_init(&s.qfull[i], 1);
             mbar_init(&s.qempty[i], readers);
@@ -706,6 +715,9 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
         __syncwarp();
     } else if (warp == 2) {
         if (lane == 0 && p.op == 0) forwarder<CL>(p, s, cl);
+        __syncwarp();
+    } else if (warp == 3) {
+        if (lane == 0 && cl.rank == 0) scheduler<CL>(p, s, total);
         __syncwarp();
     } else if (warp >= 4) {
         if (p.op == 0)
