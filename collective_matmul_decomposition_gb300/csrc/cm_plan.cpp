@@ -28,7 +28,8 @@
 // -- each rank's steps run in order right after its predecessor's, and a
 // rank's weight shard W_r is streamed in two runs instead of once per step.
 // Bidirectional rings (two predecessors, one each way), the undecomposed op
-// and the step-serial mode: step-major, and inside a step by shard / bucket.
+// and the step-serial mode: step-major, and inside a step by rank, so that a
+// rank's clockwise and counter-clockwise tasks share one pass over W_r.
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -148,10 +149,14 @@ void order_and_index(PlanImpl &p, int op, std::vector<cm_task> &tasks) {
             return rank_blocked_key(N, x.rank, x.step) < rank_blocked_key(N, y.rank, y.step);
         });
     } else {
+        // inside a step, a rank's tasks (its clockwise and counter-clockwise
+        // shard or bucket) sit together: they share W_r and form one tile
+        // group; tasks of one step never depend on each other
         std::stable_sort(tasks.begin(), tasks.end(), [](const cm_task &x, const cm_task &y) {
             if (x.step != y.step) return x.step < y.step;
-            if (x.out_idx != y.out_idx) return x.out_idx < y.out_idx;
-            return x.stream < y.stream;
+            if (x.rank != y.rank) return x.rank < y.rank;
+            if (x.stream != y.stream) return x.stream < y.stream;
+            return x.out_idx < y.out_idx;
         });
     }
     // tile groups: runs of consecutive same-rank tasks, at most tile_group long
