@@ -75,28 +75,47 @@ struct PSmem {
     uint8_t *a0, *b0;   // ring stage 0 of A and B; stage i is kHalfA (kHalfB) bytes further
     uint8_t *fbuf[2];   // AG: forwarder copy buffers; RS: the same 32 KB as 8 epilogue-warp buffers
     uint64_t *full, *empty, *tfull, *tempty, *drain, *fbar, *qfull, *qempty, *ebar, *started;
-    volatile int32_t *qtile;
+    int32_t *qent;      // tile queue: kQueue entries of kQWords words, each CTA its own (see QTile)
     uint32_t *tmem_slot;
     volatile int *abort;
 };
 
 // Consumer side of the tile queue: returns the next tile index (-1 = no more
 // work or failure) and releases the slot on the leader.
+// One published tile as a CTA sees it, worked out once by the cluster
+// leader's scheduler: the tile (-1 = no more work or failure), where it lies,
+// and this CTA's load coordinates for its first K slice.
+struct QTile {
+    int t, task, q, mt, nt, nk, a_src, a_row, n0, slab, rr, sig;
+};
+constexpr int kQWords = 12;
+
+// Consumer side of the tile queue.  Slots are released by the epilogue
+// warps and (AG) the forwarders only: an epilogue warp reads entry j after
+// the MMAs of tile j completed, which needed the producers' loads and the
+// MMA thread's reads of that entry, so its release covers theirs.
 struct QueueReader {
     int slot = 0;
     uint32_t phase = 0;
     uint32_t qempty_leader0;   // slot i's release barrier on the leader: 8*i bytes further
 
     __device__ void init(const PSmem &s) { qempty_leader0 = mapa_shared(smem_u32(&s.qempty[0]), 0); }
-    __device__ int next(const KParams &p, const PSmem &s) {
-        int t = -1;
-        if (wait_mbar<true>(p, s.abort, &s.qfull[slot], phase, kSiteEmpty, -1, -1)) t = s.qtile[slot];
-        mbar_arrive_cluster(qempty_leader0 + 8u * uint32_t(slot));
+    __device__ QTile next(const KParams &p, const PSmem &s, bool release) {
+        QTile e;
+        e.t = -1;
+        if (mbar_try_wait_cluster(&s.qfull[slot], phase) ||
+            wait_mbar<true>(p, s.abort, &s.qfull[slot], phase, kSiteEmpty, -1, -1)) {
+            const volatile int4 *v = reinterpret_cast<const volatile int4 *>(s.qent + kQWords * slot);
+            const int4 a = const_cast<const int4 &>(v[0]), b = const_cast<const int4 &>(v[1]),
+                       c = const_cast<const int4 &>(v[2]);
+            e = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+        }
+        if (release) mbar_arrive_cluster(qempty_leader0 + 8u * uint32_t(slot));
         if (++slot == kQueue) {
             slot = 0;
             phase ^= 1u;
         }
-        return t;
+        return e;
     }
 };
 
@@ -138,27 +157,19 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
     // tile indices come from the cluster leader's scheduler thread through
     // the queue; this CTA's producer tells it when a tile starts loading
     const bool signals = cl.rank == 0;
-    int cur = qr.next(p, s);
-    while (cur >= 0 && !*s.abort) {
-        const TileCoord c = decode_cl(p, cur, cl.pair, CL / 2);
-        const cm_task &tk = p.tasks[c.task];
-        if (p.op == 0 && tk.wait_in[0] >= 0) {
-            if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q))
-                break;
-            fence_proxy_async_global();
-        }
+    const uint64_t tm_a0 = reinterpret_cast<uint64_t>(&p.tmA0), tm_a1 = reinterpret_cast<uint64_t>(&p.tmA1);
+    const int slab_step = p.N * p.chunks;
+    QTile c = qr.next(p, s, false);
+    while (c.t >= 0 && !*s.abort) {
+        // A rows that arrived by the ring were acquired by the scheduler
+        // before it published this entry; order them before our TMA reads
+        if (c.a_src == 1) fence_proxy_async_global();
         // Slice coordinates.  A: (K offset, row, slab); B: (K offset, column,
         // rank), or (column, K offset, rank) when W is MN-major.  A tile that
         // sums over ranks (a_src 2) walks rank by rank through the K slices.
-        const bool sum_ranks = tk.a_src == 2;
-        int rr = sum_ranks ? 0 : tk.rank;
-        int slab = (sum_ranks ? tk.out_idx : tk.a_slab) * p.chunks + c.q;
-        const int slab_step = p.N * p.chunks;
-        const uint64_t tm_a = reinterpret_cast<uint64_t>(tk.a_src == 1 ? &p.tmA1 : &p.tmA0);
-        // two-pair clusters: this CTA loads quarter `pair` of its A half (multicast)
-        const int a_row = c.mt * kPairRows + int(cl.pos) * kCtaRows + (CL == 4 ? int(cl.pair) * (kCtaRows / 2) : 0);
-        const int n0 = c.nt * kBN + int(cl.pos) * (kBN / 2);
-        const int nk = kslices(p, tk);
+        int rr = c.rr, slab = c.slab;
+        const uint64_t tm_a = c.a_src == 1 ? tm_a1 : tm_a0;
+        const int a_row = c.a_row, n0 = c.n0, nk = c.nk;
         int kb = 0;
         bool ok = true;
         bool free_ready = mbar_test_wait(s.empty + stage, phase ^ 1u);
@@ -202,7 +213,7 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
             if (signals && kk == 0) mbar_arrive(s.started);
         }
         if (!ok) break;
-        cur = qr.next(p, s);
+        c = qr.next(p, s, false);
     }
     // a pair leader's ring barriers count every load into its pair: once they
     // complete, no load is still writing this pair's shared memory.  Stage i
@@ -214,11 +225,12 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
 }
 
 // The cluster leader's scheduler (warp 3): takes tile indices from the
-// global counter (or the next of its static round-robin share) and publishes
-// them to every CTA of the cluster through the queue.  Tile j + 1 is taken
-// once the leader's producer has started loading tile j, so a cluster holds at
-// most one tile beyond the one loading, while the counter's round trip and
-// the cluster-scope publication stay off the producer's path.
+// global counter (or the next of its static round-robin share), decodes each
+// once, works out every CTA's load coordinates, waits until an AG tile's A
+// rows have arrived, and publishes a ready-to-use entry to every CTA of the
+// cluster.  Tile j + 1 is taken once the leader's producer has started
+// loading tile j, so a cluster holds at most one tile beyond the one loading,
+// and none of this sits on the producer's path between two tiles.
 template <int CL>
 __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
     const int cid = int(blockIdx.x) / CL, ncl = int(gridDim.x) / CL;
@@ -237,10 +249,35 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
             t = int(atomic_add_relaxed(p.tile_counter, 1u));
         }
         if (t >= total) t = -1;
+        TileCoord c = {0, 0, 0, 0};
+        if (t >= 0) c = decode_cl(p, t, 0, CL / 2);
+        const cm_task &tk = p.tasks[c.task];
+        // AG: the tile's A rows arrive by the ring; the producers that read
+        // this entry see them (acquire here, release to them by the queue)
+        if (t >= 0 && p.op == 0 && tk.wait_in[0] >= 0 &&
+            !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q))
+            return;
         if (!wait_mbar<true>(p, s.abort, &s.qempty[slot], qphase ^ 1u, kSiteEmpty, -1, -1)) return;
-        s.qtile[slot] = t;
-        for (uint32_t r = 1; r < uint32_t(CL); ++r)
-            st_shared_cluster(mapa_shared(smem_u32(const_cast<int32_t *>(&s.qtile[slot])), r), uint32_t(t));
+        const bool sum_ranks = tk.a_src == 2;
+        const int slab = (sum_ranks ? tk.out_idx : tk.a_slab) * p.chunks + c.q;
+        const int rr = sum_ranks ? 0 : tk.rank;
+        const int nk = kslices(p, tk), sig = p.op == 0 ? tk.sig_done : -1;
+        for (uint32_t r = 0; r < uint32_t(CL); ++r) {
+            const int pos = int(r & 1u), pair = int(r >> 1);
+            const int nt = c.nt + pair;   // c.nt is the group's first column tile
+            const int a_row = c.mt * kPairRows + pos * kCtaRows + (CL == 4 ? pair * (kCtaRows / 2) : 0);
+            const int n0 = nt * kBN + pos * (kBN / 2);
+            int32_t *e = s.qent + kQWords * slot;
+            const uint32_t w[kQWords] = {uint32_t(t),   uint32_t(c.task), uint32_t(c.q), uint32_t(c.mt),
+                                         uint32_t(nt),  uint32_t(nk),     uint32_t(tk.a_src), uint32_t(a_row),
+                                         uint32_t(n0),  uint32_t(slab),   uint32_t(rr),       uint32_t(sig)};
+            if (r == 0) {
+                for (int i = 0; i < kQWords; ++i) e[i] = int32_t(w[i]);
+            } else {
+                const uint32_t ra = mapa_shared(smem_u32(e), r);
+                for (int i = 0; i < kQWords; i += 4) st_shared_cluster_v4(ra + 4u * i, w[i], w[i + 1], w[i + 2], w[i + 3]);
+            }
+        }
         mbar_arrive(&s.qfull[slot]);
         for (uint32_t r = 1; r < uint32_t(CL); ++r) mbar_arrive_cluster(mapa_shared(smem_u32(&s.qfull[slot]), r));
         if (++slot == kQueue) {
@@ -272,16 +309,14 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
     int accb = 0;
     uint32_t acc_phase = 0;
     for (;;) {
-        const int t = qr.next(p, s);
-        if (t < 0 || *s.abort) break;
-        const TileCoord c = decode_cl(p, t, cl.pair, CL / 2);
-        const cm_task &tk = p.tasks[c.task];
+        const QTile c = qr.next(p, s, false);
+        if (c.t < 0 || *s.abort) break;
         if (!mbar_try_wait_cluster(&s.tempty[accb], acc_phase ^ 1u) &&
             !wait_mbar<true>(p, s.abort, &s.tempty[accb], acc_phase ^ 1u, kSiteTmemEmpty, c.task, c.q))
             break;
         tc_fence_after();
         const uint32_t d = tmem_base + uint32_t(accb * kBN);
-        const int nk = kslices(p, tk);
+        const int nk = c.nk;
         bool ok = true;
         bool full_ready = mbar_test_wait(s.full + stage, phase);
         for (int kk = 0; kk < nk; ++kk) {
@@ -305,7 +340,7 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
         if (!ok) break;
         mma_commit_pair_mc(&s.tfull[accb], uint16_t(3u << (2u * cl.pair)));   // this pair's CTAs
         // AG: both CTAs' A slices of this tile have landed; the slot rows may be reused
-        if (p.op == 0 && tk.sig_done >= 0) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
+        if (c.sig >= 0) red_release_add(flag_ptr(p, c.sig, c.q), 1u);
         if (++accb == 2) {
             accb = 0;
             acc_phase ^= 1u;
@@ -325,9 +360,8 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
     // moves while all its tiles run instead of one tile doing all of it
     const int per = (kCtaRows + p.ntiles - 1) / p.ntiles;
     for (;;) {
-        const int t = qr.next(p, s);
-        if (t < 0 || *s.abort) break;
-        const TileCoord c = decode_cl(p, t, cl.pair, CL / 2);
+        const QTile c = qr.next(p, s, true);
+        if (c.t < 0 || *s.abort) break;
         const cm_task &tk = p.tasks[c.task];
         if (!(tk.fwd_slot[0] >= 0 || tk.fwd_slot[1] >= 0) || c.nt >= p.ntiles) continue;
         bool ok = true;
@@ -434,12 +468,15 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
     int accb = 0;
     uint32_t acc_phase = 0;
     for (;;) {
-        int t = -1;
-        if (lane == 0) t = qr.next(p, s);
-        t = __shfl_sync(0xffffffffu, t, 0);
+        QTile e;
+        if (lane == 0) e = qr.next(p, s, true);
+        const int t = __shfl_sync(0xffffffffu, e.t, 0);
         bool bad = t < 0;
-        TileCoord c = {0, 0, 0, 0};
-        if (!bad) c = decode_cl(p, t, cl.pair, CL / 2);
+        TileCoord c;
+        c.task = bad ? 0 : __shfl_sync(0xffffffffu, e.task, 0);
+        c.q = __shfl_sync(0xffffffffu, e.q, 0);
+        c.mt = __shfl_sync(0xffffffffu, e.mt, 0);
+        c.nt = __shfl_sync(0xffffffffu, e.nt, 0);
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
         if (p.op == 1 && leader_thread && !bad) {
@@ -523,12 +560,15 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
     int accb = 0;
     uint32_t acc_phase = 0;
     for (;;) {
-        int t = -1;
-        if (lane == 0) t = qr.next(p, s);
-        t = __shfl_sync(0xffffffffu, t, 0);
+        QTile e;
+        if (lane == 0) e = qr.next(p, s, true);
+        const int t = __shfl_sync(0xffffffffu, e.t, 0);
         bool bad = t < 0;
-        TileCoord c = {0, 0, 0, 0};
-        if (!bad) c = decode_cl(p, t, cl.pair, CL / 2);
+        TileCoord c;
+        c.task = bad ? 0 : __shfl_sync(0xffffffffu, e.task, 0);
+        c.q = __shfl_sync(0xffffffffu, e.q, 0);
+        c.mt = __shfl_sync(0xffffffffu, e.mt, 0);
+        c.nt = __shfl_sync(0xffffffffu, e.nt, 0);
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
         const bool real = c.nt < p.ntiles;   // a cluster's second pair may have no column tile
@@ -658,8 +698,8 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     s.qempty = s.qfull + kQueue;
     s.ebar = s.qempty + kQueue;
     s.started = s.ebar + kPEpiWarps;
-    s.qtile = reinterpret_cast<volatile int32_t *>(s.started + 1);
-    s.tmem_slot = reinterpret_cast<uint32_t *>(const_cast<int32_t *>(s.qtile) + kQueue);
+    s.qent = reinterpret_cast<int32_t *>(s.started + 1);   // 16-byte aligned: 40 barriers precede it
+    s.tmem_slot = reinterpret_cast<uint32_t *>(s.qent + kQWords * kQueue);
     s.abort = reinterpret_cast<volatile int *>(s.tmem_slot + 1);
 
     const int warp = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
@@ -680,9 +720,8 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
         }
         mbar_init(s.drain, 1);
         mbar_init(s.started, 1);
-        // queue readers: the pair leaders' MMA threads, every producer, 8
-        // epilogue warps per CTA and (AG) every forwarder
-        const uint32_t readers = CL / 2 + CL + CL * kPEpiWarps + (p.op == 0 ? CL : 0);
+        // queue slot releases: 8 epilogue warps per CTA and (AG) every forwarder
+        const uint32_t readers = CL * kPEpiWarps + (p.op == 0 ? CL : 0);
         for (int i = 0; i < kQueue; ++i) {
             mbar_init(&s.qfull[i], 1);
             mbar_init(&s.qempty[i], readers);
