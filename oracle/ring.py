@@ -54,17 +54,20 @@ def hop_split(N: int):
 class _Net:
     """Point-to-point links between neighbouring ranks, one inbox per (rank, stream)."""
 
-    def __init__(self, N, streams, drop=None, timeout=5.0):
+    def __init__(self, N, streams, drop=None, timeout=5.0, trace=None):
         self.N = N
         self.boxes = {(r, s): queue.Queue() for r in range(N) for s in streams}
         self.drop = set(drop or ())   # {(sender, step, stream)}
         self.timeout = timeout
         self.log = []                 # (step, stream, src, dst, object id, chunk)
+        self.trace = trace            # optional list: the log entries with a copy of each payload
         self.lock = threading.Lock()
 
     def send(self, src, dst, stream, step, obj, chunk, payload):
         with self.lock:
             self.log.append((step, stream, src, dst, obj, chunk))
+            if self.trace is not None:
+                self.trace.append((step, stream, src, dst, obj, chunk, np.array(payload, copy=True)))
         if (src, step, stream) in self.drop:
             return
         self.boxes[(dst, stream)].put((obj, chunk, payload))
@@ -102,7 +105,7 @@ def _chunks(rows: int, chunks: int):
 
 
 def ag_gemm_ring(x_bits, w_bits, w_layout="nk", chunks=1, direction="uni",
-                 drop=None, timeout=5.0, return_log=False):
+                 drop=None, timeout=5.0, return_log=False, trace=None):
     """AllGather->GEMM by the ring schedule; returns y [N][N*m][n] fp64."""
     x = np.ascontiguousarray(x_bits)
     w = np.ascontiguousarray(w_bits)
@@ -118,7 +121,7 @@ def ag_gemm_ring(x_bits, w_bits, w_layout="nk", chunks=1, direction="uni",
     else:
         raise ValueError(direction)
     nxt = {"cw": lambda r: (r + 1) % N, "ccw": lambda r: (r - 1) % N}
-    net = _Net(N, list(hops), drop, timeout)
+    net = _Net(N, list(hops), drop, timeout, trace)
 
     def rank(r):
         # step 0: multiply the own shard, chunk by chunk, forwarding each chunk
@@ -144,7 +147,7 @@ def ag_gemm_ring(x_bits, w_bits, w_layout="nk", chunks=1, direction="uni",
 
 
 def gemm_rs_ring(x_bits, w_bits, w_layout="nk", chunks=1, direction="uni",
-                 drop=None, timeout=5.0, return_log=False):
+                 drop=None, timeout=5.0, return_log=False, trace=None):
     """GEMM->ReduceScatter by the circulating-bucket schedule; y [N][M/N][n] fp64."""
     x = np.ascontiguousarray(x_bits)
     w = np.ascontiguousarray(w_bits)
@@ -165,7 +168,7 @@ def gemm_rs_ring(x_bits, w_bits, w_layout="nk", chunks=1, direction="uni",
         streams = ["cw", "ccw"]
     else:
         raise ValueError(direction)
-    net = _Net(N, streams, drop, timeout)
+    net = _Net(N, streams, drop, timeout, trace)
 
     if direction == "uni":
         def rank(r):
