@@ -251,6 +251,92 @@ class Step:
                 raise RuntimeError(f"{op}: device status {st} {info}")
 
 
+class EndToEnd:
+    """One step through the C ABI starting from pinned host buffers.
+
+    Serial: H2D of the four inputs, both calls, D2H of both outputs, then the
+    host reads the result. Pipelined: the same per-step work, but the H2D of
+    step i+1 (into the other device buffer set) and the D2H of step i-1 run on
+    their own streams while step i computes; the host reads step i-1's result
+    once its copy has landed. Every step still moves all of its inputs and
+    outputs across the host link."""
+
+    def __init__(self, st, data, torch):
+        self.torch = torch
+        self.st = st
+        self.host_in = [t.pin_memory() for t in data["cpu"]]
+        self.host_out = [[torch.empty(st.y1.shape, dtype=st.y1.dtype).pin_memory(),
+                          torch.empty(st.y2.shape, dtype=st.y2.dtype).pin_memory()] for _ in range(2)]
+        self.dev_in = [[st.x1, st.w1, st.x2, st.w2], [torch.empty_like(t) for t in (st.x1, st.w1, st.x2, st.w2)]]
+        self.dev_out = [[st.y1, st.y2], [torch.empty_like(st.y1), torch.empty_like(st.y2)]]
+        self.h2d = sum(t.numel() * t.element_size() for t in self.host_in)
+        self.d2h = sum(t.numel() * t.element_size() for t in self.host_out[0])
+        self.s_in = torch.cuda.Stream()
+        self.s_out = torch.cuda.Stream()
+
+    def compute(self, b):
+        cm, st = self.st.cm, self.st
+        x1, w1, x2, w2 = self.dev_in[b]
+        y1, y2 = self.dev_out[b]
+        cm.cm_ag_gemm(st.plan, x1, w1, y1, st.ws1, "nk")
+        cm.cm_gemm_rs(st.plan, x2, w2, y2, st.ws2, "nk")
+
+    def run_serial(self, n):
+        torch = self.torch
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(n):
+            for d, h in zip(self.dev_in[0], self.host_in):
+                d.copy_(h, non_blocking=True)
+            self.compute(0)
+            for h, d in zip(self.host_out[0], self.dev_out[0]):
+                h.copy_(d, non_blocking=True)
+            torch.cuda.synchronize()
+            float(self.host_out[0][1][0, 0, 0])
+        return time.perf_counter() - t0
+
+    def run_pipelined(self, n):
+        torch = self.torch
+        main = torch.cuda.current_stream()
+        ev = lambda: torch.cuda.Event()
+        in_ready, comp_done, out_done = [ev() for _ in range(n)], [ev() for _ in range(n)], [ev() for _ in range(n)]
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+
+        def load(i):
+            b = i % 2
+            with torch.cuda.stream(self.s_in):
+                if i >= 2:
+                    self.s_in.wait_event(comp_done[i - 2])      # step i-2 has read this buffer set
+                for d, h in zip(self.dev_in[b], self.host_in):
+                    d.copy_(h, non_blocking=True)
+                in_ready[i].record(self.s_in)
+
+        load(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                load(i + 1)
+            main.wait_event(in_ready[i])
+            if i >= 2:
+                main.wait_event(out_done[i - 2])               # step i-2's outputs have left
+            self.compute(b)
+            comp_done[i].record(main)
+            with torch.cuda.stream(self.s_out):
+                self.s_out.wait_event(comp_done[i])
+                for h, d in zip(self.host_out[b], self.dev_out[b]):
+                    h.copy_(d, non_blocking=True)
+                out_done[i].record(self.s_out)
+            if i >= 1:
+                out_done[i - 1].synchronize()
+                float(self.host_out[(i - 1) % 2][1][0, 0, 0])
+        out_done[n - 1].synchronize()
+        float(self.host_out[(n - 1) % 2][1][0, 0, 0])
+        dt = time.perf_counter() - t0
+        torch.cuda.synchronize()
+        return dt
+
+
 def time_loop(fn, iters, torch, warmup=3):
     """Mean ms per call of fn() over iters calls after `warmup` untimed calls
     (CUDA events, synchronised)."""
@@ -264,6 +350,36 @@ def time_loop(fn, iters, torch, warmup=3):
     b.record()
     torch.cuda.synchronize()
     return a.elapsed_time(b) / iters
+
+
+def time_interleaved(fns, iters, torch, warmup=3):
+    """Mean ms per call of each fn in the dict `fns`, calling them in turn
+    (one of each per round, `iters` rounds) so that all see the same clocks
+    and power state. CUDA events around every call, synchronised once."""
+    for _ in range(warmup):
+        for fn in fns.values():
+            fn()
+    torch.cuda.synchronize()
+    ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(iters)] for k in fns}
+    for i in range(iters):
+        for k, fn in fns.items():
+            ev[k][i][0].record()
+            fn()
+            ev[k][i][1].record()
+    torch.cuda.synchronize()
+    return {k: statistics.mean(a.elapsed_time(b) for a, b in ev[k]) for k in fns}
+
+
+def concat_operands(st, shapes, N):
+    """The undecomposed operands of one step for torch.matmul: fc1 X [N*m, K] and
+    W [N*n, K]; fc2 X [M, N*k] and W [n, N*k] (contiguous copies)."""
+    a, r = shapes["ag"], shapes["rs"]
+    X1 = st.x1.reshape(N * a["m"], a["K"])
+    W1 = st.w1.reshape(N * a["n"], a["K"])
+    X2 = st.x2.permute(1, 0, 2).reshape(r["M"], N * r["k"]).contiguous()
+    W2 = st.w2.permute(1, 0, 2).reshape(r["n"], N * r["k"]).contiguous()
+    return X1, W1, X2, W2
 
 
 def oracle_sample(cpu, shapes, N, seconds: float, seed=0):
@@ -414,29 +530,14 @@ def run_ours(args):
     if rank == 0:
         iters = max(5, min(20, K))
         mono = Step(N, 1, "none", {"shapes": shapes, "cpu": data["cpu"]}, device)
-        a, r = shapes["ag"], shapes["rs"]
-        X1 = st.x1.reshape(N * a["m"], a["K"])
-        W1 = st.w1.reshape(N * a["n"], a["K"])
-        X2 = st.x2.permute(1, 0, 2).reshape(r["M"], N * r["k"]).contiguous()
-        W2 = st.w2.permute(1, 0, 2).reshape(r["n"], N * r["k"]).contiguous()
+        X1, W1, X2, W2 = concat_operands(st, shapes, N)
         variants = {"ag": st.ag, "none_ag": mono.ag, "torch_ag": lambda: torch.matmul(X1, W1.t()),
                     "rs": st.rs, "none_rs": mono.rs, "torch_rs": lambda: torch.matmul(X2, W2.t())}
-        for fn in variants.values():
-            for _ in range(3):
-                fn()
-        torch.cuda.synchronize()
-        ev = {k: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                  for _ in range(iters)] for k in variants}
-        for i in range(iters):
-            for k, fn in variants.items():
-                ev[k][i][0].record()
-                fn()
-                ev[k][i][1].record()
-        torch.cuda.synchronize()
+        ms = time_interleaved(variants, iters, torch)
         st.check()
         mono.check()
         for k in variants:
-            detail[f"{k}_ms_interleaved"] = statistics.mean(e[0].elapsed_time(e[1]) for e in ev[k])
+            detail[f"{k}_ms_interleaved"] = ms[k]
         detail["ag_ms"] = statistics.mean(ag_ms)
         detail["rs_ms"] = statistics.mean(rs_ms)
         detail["ag_tflops"] = f_ag / (detail["ag_ms"] / 1e3) / 1e12
@@ -449,38 +550,29 @@ def run_ours(args):
                                  f"concatenated operands, interleaved {iters} times after the timed region")
         del X2, W2, mono, variants
 
-    # end to end through the C ABI with host buffers: pinned H2D of every input,
-    # both calls, D2H of both outputs, host reads the result
+    # end to end through the C ABI with host buffers: every step copies all four
+    # inputs from pinned host memory, runs both calls and copies both outputs
+    # back, and the host reads each step's result
     e2e = None
     if rank == 0 or world > 1:
-        host_in = [t.pin_memory() for t in data["cpu"]]
-        host_out = [torch.empty(st.y1.shape, dtype=st.y1.dtype).pin_memory(),
-                    torch.empty(st.y2.shape, dtype=st.y2.dtype).pin_memory()]
-        dev_in = [st.x1, st.w1, st.x2, st.w2]
-        h2d = sum(t.numel() * t.element_size() for t in host_in)
-        d2h = sum(t.numel() * t.element_size() for t in host_out)
         n_e2e = max(3, min(10, K))
-
-        def e2e_step():
-            for d, h in zip(dev_in, host_in):
-                d.copy_(h, non_blocking=True)
-            step()
-            host_out[0].copy_(st.y1, non_blocking=True)
-            host_out[1].copy_(st.y2, non_blocking=True)
-            torch.cuda.synchronize()
-            return float(host_out[1][0, 0, 0])
-
-        e2e_step()
+        runner = EndToEnd(st, data, torch)
+        runner.run_serial(1)
+        runner.run_pipelined(2)
         dist_barrier()
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step()
-        dt = time.perf_counter() - t0
+        dt_serial = runner.run_serial(n_e2e)
+        dist_barrier()
+        dt = runner.run_pipelined(n_e2e)
         dt_max = dist_max(dt, device)
         e2e = {"value": aggregate(f_ag + f_rs, n_e2e, world, dt_max), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": dt / n_e2e * 1e3, "steps": n_e2e}
+               "h2d_bytes_per_step": runner.h2d, "d2h_bytes_per_step": runner.d2h,
+               "ms_per_step": dt / n_e2e * 1e3, "steps": n_e2e,
+               "how": ("copies of step i+1's inputs and of step i-1's outputs overlap step i's calls "
+                       "(two device buffer sets, one copy stream each way)"),
+               "serial_ms_per_step": dt_serial / n_e2e * 1e3,
+               "serial_value": (f_ag + f_rs) * world / (dt_serial / n_e2e) / 1e12}
         st.check()
+        del runner
 
     cpu_baseline = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -525,31 +617,39 @@ def run_sweep(args):
         data = make_step_inputs(N, device)
         shapes = data["shapes"]
         f_ag, f_rs = flops(shapes, N)
+        fl = {"ag": f_ag, "rs": f_rs}
+        # every point runs interleaved with the undecomposed op in this kernel
+        # and with torch.matmul on the concatenated operands, so that the
+        # ratios compare calls made under the same clocks
         mono = Step(N, 1, "none", data, device)
-        t_none = {"ag": time_loop(mono.ag, args.steps, torch), "rs": time_loop(mono.rs, args.steps, torch)}
-        mono.check()
-        del mono
+        X1, W1, X2, W2 = concat_operands(mono, shapes, N)
+        comp = {"ag": {"none": mono.ag, "torch": lambda: torch.matmul(X1, W1.t())},
+                "rs": {"none": mono.rs, "torch": lambda: torch.matmul(X2, W2.t())}}
+
+        def emit(op, chunks, ring, fn, check):
+            t = time_interleaved({"dec": fn, **comp[op]}, args.steps, torch, warmup=args.warmup)
+            check()
+            tf = fl[op] / (t["dec"] / 1e3) / 1e12
+            print(json.dumps({"sweep": WORKLOAD, "op": op, "N": N, "chunks": chunks, "ring": ring,
+                              "ms": t["dec"], "tflops": tf, "frac_of_peak": tf / peak,
+                              "vs_undecomposed_time": t["dec"] / t["none"],
+                              "vs_torch_time": t["dec"] / t["torch"],
+                              "ms_undecomposed": t["none"], "ms_torch": t["torch"],
+                              "peak_source": kind}), flush=True)
+
         for direction in ("uni", "bidi"):
             for chunks in (1, 2, 4):
                 st = Step(N, chunks, direction, data, device)
-                for op, fn, fl in (("ag", st.ag, f_ag), ("rs", st.rs, f_rs)):
-                    ms = time_loop(fn, args.steps, torch, warmup=args.warmup)
-                    st.check((op,))
-                    tf = fl / (ms / 1e3) / 1e12
-                    print(json.dumps({"sweep": WORKLOAD, "op": op, "N": N, "chunks": chunks, "ring": direction,
-                                      "ms": ms, "tflops": tf, "frac_of_peak": tf / peak,
-                                      "vs_undecomposed_time": ms / t_none[op], "peak_source": kind}), flush=True)
+                emit("ag", chunks, direction, st.ag, lambda: st.check(("ag",)))
+                emit("rs", chunks, direction, st.rs, lambda: st.check(("rs",)))
                 del st
         # pipeline-chunk ReduceScatter ([HTP] section 6) next to the moving bucket
         for chunks in (1, 2, 4):
             st = Step(N, chunks, "uni", data, device)
-            ms = time_loop(st.rs_pipe, args.steps, torch, warmup=args.warmup)
-            st.check(("rs_pipe",))
-            tf = f_rs / (ms / 1e3) / 1e12
-            print(json.dumps({"sweep": WORKLOAD, "op": "rs", "N": N, "chunks": chunks, "ring": "pipelined",
-                              "ms": ms, "tflops": tf, "frac_of_peak": tf / peak,
-                              "vs_undecomposed_time": ms / t_none["rs"], "peak_source": kind}), flush=True)
+            emit("rs", chunks, "pipelined", st.rs_pipe, lambda: st.check(("rs_pipe",)))
             del st
+        mono.check()
+        del mono, X1, W1, X2, W2, comp
         del data
         torch.cuda.empty_cache()
     return 0
