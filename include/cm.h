@@ -125,9 +125,15 @@ cm_status cm_plan_step(cm_plan_t plan, cm_op op, int rank, int step, int stream,
 
 /*
  * One entry of the task table the persistent kernel executes, in execution
- * order (step-major).  A task is one partial GEMM of one rank at one step;
- * flag ids name per-chunk device counters (word = id * chunks + chunk).
- * Exposed so tests can check the table's dependency structure on the host.
+ * order.  A task is one partial GEMM of one rank at one step; flag ids name
+ * per-chunk device counters (word = id * chunks + chunk).  Order: for a
+ * one-way ring, rank-blocked -- rank 0's step 0, rank 1's steps 0..1, ...,
+ * rank N-1's steps 0..N-1, then rank 0's steps 1..N-1, rank 1's steps
+ * 2..N-1, ... -- so each rank's weight shard is streamed in two runs; for a
+ * bidirectional ring, CM_RING_NONE and the step-serial mode, step-major and
+ * by rank inside a step.  Every flag a task waits on is raised by an earlier
+ * task.  Exposed so tests can check the table's dependency structure on the
+ * host.
  */
 typedef struct cm_task {
     int16_t rank;          /* r: selects W_r (and Y_r for AG) */
@@ -154,11 +160,15 @@ typedef struct cm_task {
 int cm_plan_tasks(cm_plan_t plan, cm_op op, cm_task *out, int capacity);
 
 /*
- * Workspace bytes for one call; 0 for a bad plan.  Holds a status word, the
- * per-chunk flags and, for AG, the receive slots (2 per rank and stream, each
- * [m][K] bf16); for RS, the circulating fp32 accumulators (2 per rank and
- * stream, each [M/N][n]).  The caller allocates it (256-byte aligned); its
- * contents need no initialisation.
+ * Workspace bytes for one call; 0 for a bad plan or a non-positive size.
+ * Holds a 256-byte status block (status word, tile counters), the per-chunk
+ * flags and, for a ring with N > 1: for AG, one receive slot per (rank, ring
+ * stream, step), each [m][K] bf16; for RS, one fp32 accumulator per (rank,
+ * ring stream, step), each [M/N][n].  Every slot is written once per call, so
+ * no task waits for one to be freed.  The caller allocates it (256-byte
+ * aligned) and owns it; its contents need no initialisation (each call clears
+ * the status block and flags with one memset on its stream).  Calls that
+ * share a workspace must be ordered on the GPU (one stream).
  */
 size_t cm_ag_gemm_workspace_size(cm_plan_t plan, int64_t m, int64_t K);
 size_t cm_gemm_rs_workspace_size(cm_plan_t plan, int64_t M, int64_t n);
@@ -168,8 +178,16 @@ size_t cm_gemm_rs_workspace_size(cm_plan_t plan, int64_t M, int64_t n);
  *  x  [N][m][K] bf16: shard X_j at x + j*m*K (the gathered X is x itself).
  *  w  N weight shards, bf16: W_r at w + r*K*n, laid out per `wlayout`.
  *  y  [N][N*m][n] (y_dtype): Y_r at y + r*N*m*n; rows j*m..j*m+m-1 hold X_j @ W_r.
- *  m % chunks == 0; K and n multiples of 8.  Outputs must not alias inputs
- *  or the workspace.  Enqueued on `stream`.
+ *  ws, ws_bytes: workspace of at least cm_ag_gemm_workspace_size(plan, m, K)
+ *  bytes.  Outputs must not alias inputs or the workspace; inputs are not
+ *  modified.  Enqueued on `stream`; returns before the GPU work runs.
+ *  Errors (synchronous, nothing enqueued): CM_ERR_INVALID_ARG for a null
+ *  plan/pointer or a bad enum; CM_ERR_SHAPE if m, K or n is not positive,
+ *  exceeds 2^30, or m % chunks != 0; CM_ERR_ALIGNMENT if K or n is not a
+ *  multiple of 8 or a pointer is not 16-byte aligned; CM_ERR_WORKSPACE if
+ *  ws_bytes is too small; CM_ERR_UNSUPPORTED if the device cannot run the
+ *  kernel; CM_ERR_CUDA if a launch or tensor-map encoding fails.  Device-side
+ *  failures (a bounded wait that timed out) come from cm_check_status.
  */
 cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout,
                      void *y, cm_dtype y_dtype, int64_t m, int64_t K, int64_t n,
@@ -180,8 +198,11 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
  *  x  [N][M][k] bf16: X_r at x + r*M*k.
  *  w  N weight shards, bf16: W_r at w + r*k*n, laid out per `wlayout`.
  *  y  [N][M/N][n] (y_dtype): bucket o = rows o*M/N.. of sum_r X_r @ W_r.
- *  M % N == 0, (M/N) % chunks == 0; k and n multiples of 8.  Accumulation
- *  across ranks is fp32; the home rank rounds once to y_dtype.
+ *  ws, ws_bytes: workspace of at least cm_gemm_rs_workspace_size(plan, M, n)
+ *  bytes.  Accumulation across ranks is fp32; the home rank rounds once to
+ *  y_dtype.  Outputs must not alias inputs or the workspace.
+ *  Errors: as cm_ag_gemm, with CM_ERR_SHAPE also for M % N != 0 or
+ *  (M/N) % chunks != 0, and k in the role of K.
  */
 cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout,
                      void *y, cm_dtype y_dtype, int64_t M, int64_t k, int64_t n,

@@ -108,6 +108,21 @@ def test_compute_calls_reject_bad_arguments_without_device_work(lib):
     assert lib.cm_check_status(None, None, None) == cm.CM_ERR_INVALID_ARG
 
 
+def test_empty_shapes_are_rejected(lib):
+    """Empty problems (a zero size) are shape errors, returned before any
+    device work; their workspace size is 0."""
+    p = cm.Plan(2, 1, "uni")
+    fake = ctypes.c_void_p(1 << 20)
+    ws = p.ag_workspace_size(64, 256)
+    for m, K, n in ((0, 256, 512), (64, 0, 512), (64, 256, 0)):
+        assert lib.cm_ag_gemm(p.handle, fake, fake, 1, fake, 0, m, K, n, fake, ws, None) == cm.CM_ERR_SHAPE
+    wsr = p.rs_workspace_size(128, 512)
+    for M, k, n in ((0, 128, 512), (128, 0, 512), (128, 128, 0)):
+        assert lib.cm_gemm_rs(p.handle, fake, fake, 1, fake, 0, M, k, n, fake, wsr, None) == cm.CM_ERR_SHAPE
+    assert p.ag_workspace_size(0, 256) == 0
+    assert p.rs_workspace_size(0, 512) == 0
+
+
 def test_no_oracle_in_product_path():
     """The product package never imports the oracle."""
     pkg = os.path.join(ROOT, "collective_matmul_decomposition_gb300")
