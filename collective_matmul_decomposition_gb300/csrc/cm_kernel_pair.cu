@@ -409,36 +409,18 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
     bulk_wait<0>();
 }
 
-// One 32-column slice of one row: add received partial buckets (RS), then
-// store to the next accumulator or to the output (bf16 RNE or fp32).
-__device__ __forceinline__ void epi_slice(const KParams &p, const cm_task &tk, int64_t crow, int col0,
-                                          const uint32_t (&v)[32], const float4 (&in)[2][8]) {
-    float f[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-    int64_t orow;
-    bool to_acc = false;
-    if (p.op == 0) {
-        orow = int64_t(tk.rank) * p.y_rank_stride + (int64_t(tk.out_idx) * p.out_rows_per_idx + crow) * p.n;
-    } else {
-#pragma unroll
-        for (int j = 0; j < 2; ++j)
-            if (tk.in_buf[j] >= 0) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) add4(f + 4 * i, in[j][i]);
-            }
-        if (tk.out_buf >= 0) {
-            to_acc = true;
-            orow = int64_t(tk.out_buf) * p.acc_buf_stride + crow * p.n;
-        } else {
-            orow = (int64_t(tk.out_idx) * p.out_rows_per_idx + crow) * p.n;
-        }
-    }
-    if (to_acc || p.y_f32) {
-        float4 *dst = reinterpret_cast<float4 *>((to_acc ? p.acc : static_cast<float *>(p.y)) + orow + col0);
+// One 32-column slice of one row of an AG tile: the shard's rows of Y_r
+// (DynamicUpdateSlice), bf16 (RNE) or fp32.
+__device__ __forceinline__ void ag_store_slice(const KParams &p, const cm_task &tk, int64_t crow, int col0,
+                                               const uint32_t (&v)[32]) {
+    const int64_t orow = int64_t(tk.rank) * p.y_rank_stride + (int64_t(tk.out_idx) * p.out_rows_per_idx + crow) * p.n;
+    if (p.y_f32) {
+        float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + orow + col0);
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            if (col0 + 4 * i < p.n) dst[i] = make_float4(f[4 * i], f[4 * i + 1], f[4 * i + 2], f[4 * i + 3]);
+            if (col0 + 4 * i < p.n)
+                dst[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                     __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
     } else {
         uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(p.y) + orow + col0);
 #pragma unroll
@@ -447,7 +429,8 @@ __device__ __forceinline__ void epi_slice(const KParams &p, const cm_task &tk, i
             uint32_t w[4];
 #pragma unroll
             for (int h = 0; h < 4; ++h) {
-                __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * i + 2 * h], f[8 * i + 2 * h + 1]);
+                __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[8 * i + 2 * h]),
+                                                          __uint_as_float(v[8 * i + 2 * h + 1]));
                 w[h] = *reinterpret_cast<uint32_t *>(&b2);
             }
             dst[i] = make_uint4(w[0], w[1], w[2], w[3]);
@@ -455,13 +438,14 @@ __device__ __forceinline__ void epi_slice(const KParams &p, const cm_task &tk, i
     }
 }
 
+// AllGather -> GEMM epilogue: each warp reads its 32 TMEM lanes x 128
+// columns in 32-column slices and stores them into the shard's rows of Y_r.
 template <int CL>
 __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     const int e = int(threadIdx.x) / 32 - 4;   // 0..7
     const int lane = int(threadIdx.x) & 31;
     const int quad = e & 3;                      // TMEM lanes 32*quad.. (warp % 4)
     const int half = e >> 2;                     // columns 128*half..
-    const bool leader_thread = e == 0 && lane == 0;
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&s.tempty[0]), cl.leader);   // buffer b: +8*b
     QueueReader qr;
     if (lane == 0) qr.init(s);
@@ -479,15 +463,6 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
         c.nt = __shfl_sync(0xffffffffu, e.nt, 0);
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
-        if (p.op == 1 && leader_thread && !bad) {
-            for (int j = 0; j < 2 && !bad; ++j)
-                if (tk.wait_in[j] >= 0)
-                    bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q), p.tgt_in, kSiteEpilogueFlag, c.task,
-                                     c.q);
-            if (!bad && tk.wait_free[0] >= 0)
-                bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[0], c.q), p.tgt_free, kSiteEpilogueFlag, c.task,
-                                 c.q);
-        }
         bad = bar_or(1, kPEpiWarps * 32, bad || *s.abort != 0);
         if (bad) break;
         tc_fence_after();
@@ -495,37 +470,18 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
         const int row = c.mt * kPairRows + int(cl.pos) * kCtaRows + quad * 32 + lane;   // row inside the chunk
         const bool row_ok = row < p.rows_c;
         const int64_t crow = int64_t(c.q) * p.rows_c + row;
-        const bool rs_in = p.op == 1 && (tk.in_buf[0] >= 0 || tk.in_buf[1] >= 0);
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
             const int col_local = half * 128 + cb * 32;
             const int col0 = c.nt * kBN + col_local;
-            float4 in[2][8];
-            const bool live = row_ok && col0 < p.n;
-            if (rs_in && live) {   // issue the partial-bucket loads before the TMEM read
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    if (tk.in_buf[j] >= 0) {
-                        const float4 *src = reinterpret_cast<const float4 *>(
-                            p.acc + int64_t(tk.in_buf[j]) * p.acc_buf_stride + crow * p.n + col0);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            in[j][i] = col0 + 4 * i < p.n ? __ldcg(src + i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-            }
             uint32_t v[32];
             tmem_ld32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN + col_local), v);
             tmem_wait_ld();
-            if (live) epi_slice(p, tk, crow, col0, v, in);
+            if (row_ok && col0 < p.n) ag_store_slice(p, tk, crow, col0, v);
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * uint32_t(accb));
-        if (p.op == 1 && tk.sig_done >= 0) {
-            __threadfence();
-            bar_sync(1, kPEpiWarps * 32);
-            if (leader_thread) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
-        }
         if (++accb == 2) {
             accb = 0;
             acc_phase ^= 1u;
