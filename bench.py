@@ -561,10 +561,10 @@ def run_ours(args):
         runner.run_pipelined(2)
         dist_barrier()
         dt_serial = runner.run_serial(n_e2e)
-        # three rounds of n_e2e pipelined steps; the median round is reported
+        # five rounds of n_e2e pipelined steps; the median round is reported
         # (host-link throughput varies from round to round), every round listed
         rounds = []
-        for _ in range(3):
+        for _ in range(5):
             dist_barrier()
             rounds.append(dist_max(runner.run_pipelined(n_e2e), device))
         dt_max = statistics.median(rounds)
@@ -572,7 +572,7 @@ def run_ours(args):
                "h2d_bytes_per_step": runner.h2d, "d2h_bytes_per_step": runner.d2h,
                "ms_per_step": dt_max / n_e2e * 1e3, "steps": n_e2e,
                "how": ("copies of step i+1's inputs and of step i-1's outputs overlap step i's calls "
-                       "(two device buffer sets, one copy stream each way); median of 3 rounds"),
+                       "(two device buffer sets, one copy stream each way); median of 5 rounds"),
                "round_ms_per_step": [r / n_e2e * 1e3 for r in rounds],
                "serial_ms_per_step": dt_serial / n_e2e * 1e3,
                "serial_value": (f_ag + f_rs) * world / (dt_serial / n_e2e) / 1e12}
@@ -852,13 +852,15 @@ def run_profile_case(args):
         st.plan.set_option(st.cm.CM_OPT_L2_PROMOTION, args.l2_promotion)
     if args.row_band >= 0:
         st.plan.set_option(st.cm.CM_OPT_ROW_BAND, args.row_band)
+    if args.rs_preload >= 0:
+        st.plan.set_option(st.cm.CM_OPT_RS_PRELOAD, args.rs_preload)
     fn = st.ag if args.profile == "ag" else st.rs
     f_ag, f_rs = flops(data["shapes"], N)
     ms = time_loop(fn, args.steps, torch, warmup=args.warmup)
     st.check((args.profile,))
     fl = f_ag if args.profile == "ag" else f_rs
     print(json.dumps({"profile_case": args.workload, "op": args.profile, "N": N, "chunks": args.chunks,
-                      "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group, "l2_hints": args.l2_hints, "l2_promotion": args.l2_promotion, "row_band": args.row_band,
+                      "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group, "l2_hints": args.l2_hints, "l2_promotion": args.l2_promotion, "row_band": args.row_band, "rs_preload": args.rs_preload,
                       "ms": ms, "tflops": fl / (ms / 1e3) / 1e12}), flush=True)
     return 0
 
@@ -885,6 +887,7 @@ def main(argv=None):
     ap.add_argument("--l2-hints", type=int, default=-1, help="CM_OPT_L2_HINTS for --profile (-1 = default)")
     ap.add_argument("--l2-promotion", type=int, default=-1, help="CM_OPT_L2_PROMOTION for --profile (-1 = default)")
     ap.add_argument("--row-band", type=int, default=-1, help="CM_OPT_ROW_BAND for --profile (-1 = default)")
+    ap.add_argument("--rs-preload", type=int, default=-1, help="CM_OPT_RS_PRELOAD for --profile (-1 = default)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="oracle seconds for the cpu_baseline of the default arm")
     ap.add_argument("--ref-seconds", type=float, default=120.0,

@@ -23,6 +23,7 @@ CM_OP_AG_GEMM, CM_OP_GEMM_RS = 0, 1
 CM_OPT_TIMEOUT_NS, CM_OPT_SERIAL_STEPS, CM_OPT_GRID, CM_OPT_SKIP_SIGNAL, CM_OPT_KERNEL = 0, 1, 2, 3, 4
 CM_OPT_STATIC_TILES, CM_OPT_TILE_GROUP, CM_OPT_L2_HINTS, CM_OPT_L2_PROMOTION, CM_OPT_ROW_BAND = 5, 6, 7, 8, 9
 CM_OPT_BULK_OVERLAP = 10
+CM_OPT_RS_PRELOAD = 11
 CM_MAX_RANKS, CM_MAX_CHUNKS = 16, 8
 
 DIRECTIONS = {"uni": CM_RING_UNI, "bidi": CM_RING_BIDI, "none": CM_RING_NONE}

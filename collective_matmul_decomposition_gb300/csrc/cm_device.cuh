@@ -333,6 +333,13 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
 }
 // arrive on the mbarrier at this offset in every CTA of `cta_mask` once the
 // pair MMAs issued so far by this thread are complete
+// Copy 128 rows x 256 bits (8 fp32 columns) from shared memory (the SW128
+// matrix `desc` describes) into TMEM lanes 0..127 at column address `taddr`,
+// in both CTAs of the pair, each from its own shared memory.  Issued by the
+// pair leader; ordered with its MMAs, tracked by its commits.
+__device__ __forceinline__ void tmem_cp_pair_128x256b(uint32_t taddr, uint64_t desc) {
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
+}
 __device__ __forceinline__ void mma_commit_pair_mc(uint64_t *bar, uint16_t cta_mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(

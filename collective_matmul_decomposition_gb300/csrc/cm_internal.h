@@ -43,6 +43,7 @@ struct PlanImpl {
     int l2_promotion = 3;   // see CM_OPT_L2_PROMOTION
     int row_band = 0;       // see CM_OPT_ROW_BAND
     int bulk_overlap = 1;   // see CM_OPT_BULK_OVERLAP
+    int rs_preload = 2;     // see CM_OPT_RS_PRELOAD
     int64_t skip_signal = -1;
     Schedule sched[2];                    // per cm_op
     std::vector<cm_task> tasks[2];        // per cm_op, execution order

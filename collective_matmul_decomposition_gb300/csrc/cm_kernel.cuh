@@ -39,6 +39,8 @@ struct KParams {
     CUtensorMap tmA1;   // AG workspace receive slots, same view (loads and forward stores)
     CUtensorMap tmB;    // weights: [N][n][K] (K-major) or [N][K][n] (n-major)
     CUtensorMap tmAcc;  // RS fp32 accumulators as [bufs*chunks][rows_c][n], 32 x 32 boxes (CTA pairs)
+    CUtensorMap tmAccIn;  // the same view, 32-column x pre_box_rows boxes: received buckets
+                          // loaded through the operand ring (rs_preload)
     void *y;
     float *acc;                // RS circulating accumulators
     uint32_t *flags;
@@ -64,6 +66,8 @@ struct KParams {
     int n;
     int y_f32;
     int a_box_rows;
+    int rs_preload;            // RS, CTA pairs of one cluster: received buckets preloaded into TMEM
+    int pre_box_rows;          // rows of a tmAccIn box (128, or rows_c if smaller)
     int tiles_per_task, task_begin, task_end;
     uint32_t tgt_in, tgt_free;
     cm_task tasks[kMaxTasks];

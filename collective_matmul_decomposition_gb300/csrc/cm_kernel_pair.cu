@@ -61,6 +61,8 @@ constexpr int kHalfA = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kHalfB = (kBN / 2) * kBK * 2;  // 16 KB
 constexpr int kFwdPiece = 16384;             // forwarder copy granule
 constexpr int kQueue = 6;                    // tile-index queue depth
+constexpr int kPreStages = kBN * 4 / (2 * 128);   // RS preload: a CTA's 256 fp32 columns as two
+                                                  // 32-column boxes per ring stage
 constexpr int kPSmemBytes = kPStages * (kHalfA + kHalfB) + 2 * kFwdPiece + 1024 + 1024;
 
 // Position of this CTA in its cluster.
@@ -87,8 +89,10 @@ struct PSmem {
 // and this CTA's load coordinates for its first K slice.
 struct QTile {
     int t, task, q, mt, nt, nk, a_src, a_row, n0, slab, rr, sig;
+    int pre;        // RS preload: accumulator buffer whose bucket is loaded before the K slices, -1 none
+    int pad[3];
 };
-constexpr int kQWords = 12;
+constexpr int kQWords = 16;
 
 // Consumer side of the tile queue.  Slots are released by the epilogue
 // warps and (AG) the forwarders only: an epilogue warp reads entry j after
@@ -107,8 +111,8 @@ struct QueueReader {
             wait_mbar<true>(p, s.abort, &s.qfull[slot], phase, kSiteEmpty, -1, -1)) {
             const volatile int4 *v = reinterpret_cast<const volatile int4 *>(s.qent + kQWords * slot);
             const int4 a = const_cast<const int4 &>(v[0]), b = const_cast<const int4 &>(v[1]),
-                       c = const_cast<const int4 &>(v[2]);
-            e = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+                       c = const_cast<const int4 &>(v[2]), d = const_cast<const int4 &>(v[3]);
+            e = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, {d.y, d.z, d.w}};
         }
         if (release) mbar_arrive_cluster(qempty_leader0 + 8u * uint32_t(slot));
         if (++slot == kQueue) {
@@ -173,7 +177,34 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
         int kb = 0;
         bool ok = true;
         bool free_ready = mbar_test_wait(s.empty + stage, phase ^ 1u);
-        for (int kk = 0; kk < nk; ++kk) {
+        if (c.pre >= 0) {
+            // RS preload: this CTA's 128 rows x 256 columns of the received
+            // bucket, ahead of the K slices, through the same ring; the
+            // scheduler acquired its flag before publishing this entry
+            fence_proxy_async_global();
+            const uint32_t tx_pre = 2u * 2u * uint32_t(p.pre_box_rows) * 128u;   // two boxes on each CTA
+            const uint64_t tm_pre = reinterpret_cast<uint64_t>(&p.tmAccIn);
+            const int pslab = c.pre * p.chunks + c.q;
+            for (int ps = 0; ps < kPreStages; ++ps) {
+                if (!ring_wait(p, s.abort, s.empty + stage, phase ^ 1u, free_ready, kSiteEmpty, c.task, c.q)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t fb = full_leader0 + 8u * uint32_t(stage);
+                const uint32_t sa = a_smem0 + uint32_t(stage) * kHalfA, sb = b_smem0 + uint32_t(stage) * kHalfB;
+                const int col = c.nt * kBN + 64 * ps;
+                if (cl.pos == 0) mbar_expect_tx(s.full + stage, tx_pre);
+                tma_load_3d_pair_a(sa, tm_pre, fb, col, a_row, pslab);
+                tma_load_3d_pair_a(sb, tm_pre, fb, col + 32, a_row, pslab);
+                ++issued;
+                if (++stage == kPStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+                free_ready = mbar_test_wait(s.empty + stage, phase ^ 1u);
+            }
+        }
+        for (int kk = 0; kk < nk && ok; ++kk) {
             if (!ring_wait(p, s.abort, s.empty + stage, phase ^ 1u, free_ready, kSiteEmpty, c.task, c.q)) {
                 ok = false;
                 break;
@@ -257,6 +288,12 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
         if (t >= 0 && p.op == 0 && tk.wait_in[0] >= 0 &&
             !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q))
             return;
+        // RS preload: the received bucket is read before the partial GEMM, so
+        // its producers must be done before this tile is published
+        const bool pre = t >= 0 && p.op == 1 && p.rs_preload && CL == 2 && tk.in_buf[0] >= 0;
+        if (pre && tk.wait_in[0] >= 0 &&
+            !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q))
+            return;
         if (!wait_mbar<true>(p, s.abort, &s.qempty[slot], qphase ^ 1u, kSiteEmpty, -1, -1)) return;
         const bool sum_ranks = tk.a_src == 2;
         const int slab = (sum_ranks ? tk.out_idx : tk.a_slab) * p.chunks + c.q;
@@ -270,7 +307,8 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
             int32_t *e = s.qent + kQWords * slot;
             const uint32_t w[kQWords] = {uint32_t(t),   uint32_t(c.task), uint32_t(c.q), uint32_t(c.mt),
                                          uint32_t(nt),  uint32_t(nk),     uint32_t(tk.a_src), uint32_t(a_row),
-                                         uint32_t(n0),  uint32_t(slab),   uint32_t(rr),       uint32_t(sig)};
+                                         uint32_t(n0),  uint32_t(slab),   uint32_t(rr),       uint32_t(sig),
+                                         uint32_t(pre ? int(tk.in_buf[0]) : -1), 0u, 0u, 0u};
             if (r == 0) {
                 for (int i = 0; i < kQWords; ++i) e[i] = int32_t(w[i]);
             } else {
@@ -302,6 +340,9 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
     // start-address field (shared addresses stay below 2^18, so no carry)
     const uint64_t ad0 = desc_sw128(smem_u32(s.a0), kALbo, 1024);
     const uint64_t bd0 = desc_sw128(smem_u32(s.b0), kBLbo, 1024);
+    // RS preload stages hold fp32 boxes of 128 rows x 128 bytes, SW128
+    const uint64_t pd_a0 = desc_sw128(smem_u32(s.a0), 16, 1024);
+    const uint64_t pd_b0 = desc_sw128(smem_u32(s.b0), 16, 1024);
     QueueReader qr;
     qr.init(s);
     int stage = 0;
@@ -319,7 +360,31 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
         const int nk = c.nk;
         bool ok = true;
         bool full_ready = mbar_test_wait(s.full + stage, phase);
-        for (int kk = 0; kk < nk; ++kk) {
+        // RS preload: copy the received bucket into the accumulator; the
+        // partial GEMM then adds onto it
+        const int npre = c.pre >= 0 ? kPreStages : 0;
+        for (int ps = 0; ps < npre; ++ps) {
+            if (!ring_wait(p, s.abort, s.full + stage, phase, full_ready, kSiteFull, c.task, c.q)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint64_t pa = pd_a0 + uint64_t((uint32_t(stage) * kHalfA) >> 4);
+            const uint64_t pb = pd_b0 + uint64_t((uint32_t(stage) * kHalfB) >> 4);
+            const uint32_t col = d + uint32_t(64 * ps);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tmem_cp_pair_128x256b(col + uint32_t(8 * j), pa + uint64_t(2 * j));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) tmem_cp_pair_128x256b(col + 32u + uint32_t(8 * j), pb + uint64_t(2 * j));
+            mma_commit_pair_mc(s.empty + stage, uint16_t((1u << CL) - 1u));
+            if (++stage == kPStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+            full_ready = mbar_test_wait(s.full + stage, phase);
+        }
+        const uint32_t acc0 = npre > 0 ? 1u : 0u;
+        for (int kk = 0; kk < nk && ok; ++kk) {
             if (!ring_wait(p, s.abort, s.full + stage, phase, full_ready, kSiteFull, c.task, c.q)) {
                 ok = false;
                 break;
@@ -329,7 +394,7 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
             const uint64_t bd = bd0 + uint64_t((uint32_t(stage) * kHalfB) >> 4);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
-                mma_bf16_pair(d, ad + uint64_t(kAStep * k), bd + uint64_t(kBStep * k), kIdesc, (kk | k) != 0 ? 1u : 0u);
+                mma_bf16_pair(d, ad + uint64_t(kAStep * k), bd + uint64_t(kBStep * k), kIdesc, (kk | k) != 0 ? 1u : acc0);
             mma_commit_pair_mc(s.empty + stage, uint16_t((1u << CL) - 1u));   // every CTA's stage s
             if (++stage == kPStages) {
                 stage = 0;
@@ -525,6 +590,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         c.q = __shfl_sync(0xffffffffu, e.q, 0);
         c.mt = __shfl_sync(0xffffffffu, e.mt, 0);
         c.nt = __shfl_sync(0xffffffffu, e.nt, 0);
+        const int pre = __shfl_sync(0xffffffffu, e.pre, 0);   // in_buf[0] already in the accumulator
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
         const bool real = c.nt < p.ntiles;   // a cluster's second pair may have no column tile
@@ -558,7 +624,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
             for (int j = 0; j < 2; ++j) {
-                if (tk.in_buf[j] < 0) continue;
+                if (tk.in_buf[j] < 0 || (j == 0 && pre >= 0)) continue;
                 if (lane == 0) {
                     if (store_pending) {
                         bulk_wait_read<0>();

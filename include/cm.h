@@ -334,6 +334,16 @@ const char *cm_status_string(cm_status status);
  *  CM_OPT_BULK_OVERLAP   cm_backward_pair: 1 (default) runs the weight
  *                        gradient's AllGather on a second stream under the
  *                        data-gradient GEMM-RS; 0 runs it first on `stream`.
+ *  CM_OPT_RS_PRELOAD     cm_gemm_rs on the CTA-pair kernel (one pair per
+ *                        cluster): 1 brings a tile's received partial bucket
+ *                        in through the operand ring and copies it into the
+ *                        tile's tensor-memory accumulator before the partial
+ *                        GEMM adds onto it, so the epilogue only stores;
+ *                        0 adds the received bucket in the epilogue; 2 (the
+ *                        default) preloads when a tile has at most 8 K
+ *                        slices of 64 (k <= 512), where the epilogue, not
+ *                        the GEMM, sets the pace.  The same sum, in a
+ *                        different fp32 order.
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
@@ -346,7 +356,8 @@ typedef enum cm_option {
     CM_OPT_L2_HINTS = 7,
     CM_OPT_L2_PROMOTION = 8,
     CM_OPT_ROW_BAND = 9,
-    CM_OPT_BULK_OVERLAP = 10
+    CM_OPT_BULK_OVERLAP = 10,
+    CM_OPT_RS_PRELOAD = 11
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);
