@@ -854,7 +854,7 @@ def run_profile_case(args):
         st.plan.set_option(st.cm.CM_OPT_ROW_BAND, args.row_band)
     if args.rs_preload >= 0:
         st.plan.set_option(st.cm.CM_OPT_RS_PRELOAD, args.rs_preload)
-    fn = st.ag if args.profile == "ag" else st.rs
+    fn = {"ag": st.ag, "rs": st.rs, "rs_pipe": st.rs_pipe}[args.profile]
     f_ag, f_rs = flops(data["shapes"], N)
     ms = time_loop(fn, args.steps, torch, warmup=args.warmup)
     st.check((args.profile,))
@@ -875,7 +875,7 @@ def main(argv=None):
     ap.add_argument("--gate", action="store_true", help="the cost model's choices against measurement")
     ap.add_argument("--backward", action="store_true", help="the backward pair of the MLP fc1 layer")
     ap.add_argument("--cannon", action="store_true", help="Cannon-style 2-D rotation, 8192^3")
-    ap.add_argument("--profile", choices=["ag", "rs"], default=None,
+    ap.add_argument("--profile", choices=["ag", "rs", "rs_pipe"], default=None,
                     help="run only --steps calls of one op (for ncu captures)")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--ranks", type=int, default=8)
