@@ -14,10 +14,22 @@ namespace {
 
 constexpr size_t kStatusBytes = 256;   // status word at 0, tile counters at kCounterOff
 constexpr size_t kCounterOff = 64;
-// CM_OPT_RS_PRELOAD automatic choice: preload a tile's received bucket when
-// the tile has at most this many K slices (measured: 4 slices 12 % faster,
-// 24 and more 4-7 % slower than adding it in the epilogue)
-constexpr int64_t kPreloadMaxKSlices = 8;
+// CM_OPT_RS_PRELOAD automatic choice, by the K slices of a tile: up to
+// kPreloadAllKSlices the whole received bucket is preloaded (the epilogue
+// sets the pace there: 4 slices measured 13 % faster); beyond that none
+// (24 to 112 slices measured 2-7 % slower with all or half preloaded: a
+// preloaded tile cannot start its MMAs before the bucket is complete).
+constexpr int64_t kPreloadAllKSlices = 8;
+
+// Ring stages of received bucket per tile for CM_OPT_RS_PRELOAD = mode.
+int preload_stages(int mode, int64_t kslices) {
+    switch (mode) {
+        case 1: return 4;
+        case 3: return 2;
+        case 2: return kslices <= kPreloadAllKSlices ? 4 : 0;
+        default: return 0;
+    }
+}
 static_assert(kCounterOff + 4 * (CM_MAX_RANKS + 1) <= kStatusBytes, "tile counters fit the status block");
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
@@ -360,12 +372,13 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
             return CM_ERR_CUDA;
         // received buckets through the operand ring: each CTA of a pair loads
         // its 128 rows of the tile as 32-column boxes (one per 16 KB stage half)
-        const bool short_k = (k + kBK - 1) / kBK <= kPreloadMaxKSlices;
-        if ((pl.rs_preload == 1 || (pl.rs_preload == 2 && short_k)) && kc.pair && kc.cluster_ctas == 2) {
+        const int pre_stages = preload_stages(pl.rs_preload, (k + kBK - 1) / kBK);
+        if (pre_stages > 0 && kc.pair && kc.cluster_ctas == 2) {
             const uint32_t pre_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
             if (!make_map(&kp.tmAccIn, kp.acc, uint64_t(n), uint64_t(rows_c), uint64_t(nbufs * c), 32, pre_rows, true))
                 return CM_ERR_CUDA;
             kp.rs_preload = 1;
+            kp.pre_stages = pre_stages;
             kp.pre_box_rows = int(pre_rows);
         }
     }

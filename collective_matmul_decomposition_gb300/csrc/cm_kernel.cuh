@@ -67,6 +67,8 @@ struct KParams {
     int y_f32;
     int a_box_rows;
     int rs_preload;            // RS, CTA pairs of one cluster: received buckets preloaded into TMEM
+    int pre_stages;            // ... as this many ring stages per tile (4: every slice, 2: the first two
+                               //     32-column slices of each epilogue warp)
     int pre_box_rows;          // rows of a tmAccIn box (128, or rows_c if smaller)
     int tiles_per_task, task_begin, task_end;
     uint32_t tgt_in, tgt_free;

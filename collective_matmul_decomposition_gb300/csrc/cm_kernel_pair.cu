@@ -61,8 +61,9 @@ constexpr int kHalfA = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kHalfB = (kBN / 2) * kBK * 2;  // 16 KB
 constexpr int kFwdPiece = 16384;             // forwarder copy granule
 constexpr int kQueue = 6;                    // tile-index queue depth
-constexpr int kPreStages = kBN * 4 / (2 * 128);   // RS preload: a CTA's 256 fp32 columns as two
-                                                  // 32-column boxes per ring stage
+// RS preload: ring stage ps carries the 32-column fp32 boxes at columns
+// 32*ps and 128 + 32*ps of the tile (slice ps of both epilogue column
+// halves); p.pre_stages of them (2 or 4) precede the K slices.
 constexpr int kPSmemBytes = kPStages * (kHalfA + kHalfB) + 2 * kFwdPiece + 1024 + 1024;
 
 // Position of this CTA in its cluster.
@@ -185,17 +186,17 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
             const uint32_t tx_pre = 2u * 2u * uint32_t(p.pre_box_rows) * 128u;   // two boxes on each CTA
             const uint64_t tm_pre = reinterpret_cast<uint64_t>(&p.tmAccIn);
             const int pslab = c.pre * p.chunks + c.q;
-            for (int ps = 0; ps < kPreStages; ++ps) {
+            for (int ps = 0; ps < p.pre_stages; ++ps) {
                 if (!ring_wait(p, s.abort, s.empty + stage, phase ^ 1u, free_ready, kSiteEmpty, c.task, c.q)) {
                     ok = false;
                     break;
                 }
                 const uint32_t fb = full_leader0 + 8u * uint32_t(stage);
                 const uint32_t sa = a_smem0 + uint32_t(stage) * kHalfA, sb = b_smem0 + uint32_t(stage) * kHalfB;
-                const int col = c.nt * kBN + 64 * ps;
+                const int col = c.nt * kBN + 32 * ps;
                 if (cl.pos == 0) mbar_expect_tx(s.full + stage, tx_pre);
                 tma_load_3d_pair_a(sa, tm_pre, fb, col, a_row, pslab);
-                tma_load_3d_pair_a(sb, tm_pre, fb, col + 32, a_row, pslab);
+                tma_load_3d_pair_a(sb, tm_pre, fb, col + kBN / 2, a_row, pslab);
                 ++issued;
                 if (++stage == kPStages) {
                     stage = 0;
@@ -290,7 +291,7 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
             return;
         // RS preload: the received bucket is read before the partial GEMM, so
         // its producers must be done before this tile is published
-        const bool pre = t >= 0 && p.op == 1 && p.rs_preload && CL == 2 && tk.in_buf[0] >= 0;
+        const bool pre = t >= 0 && p.op == 1 && p.rs_preload && p.pre_stages > 0 && CL == 2 && tk.in_buf[0] >= 0;
         if (pre && tk.wait_in[0] >= 0 &&
             !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q))
             return;
@@ -362,7 +363,7 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
         bool full_ready = mbar_test_wait(s.full + stage, phase);
         // RS preload: copy the received bucket into the accumulator; the
         // partial GEMM then adds onto it
-        const int npre = c.pre >= 0 ? kPreStages : 0;
+        const int npre = c.pre >= 0 ? p.pre_stages : 0;
         for (int ps = 0; ps < npre; ++ps) {
             if (!ring_wait(p, s.abort, s.full + stage, phase, full_ready, kSiteFull, c.task, c.q)) {
                 ok = false;
@@ -371,11 +372,11 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
             tc_fence_after();
             const uint64_t pa = pd_a0 + uint64_t((uint32_t(stage) * kHalfA) >> 4);
             const uint64_t pb = pd_b0 + uint64_t((uint32_t(stage) * kHalfB) >> 4);
-            const uint32_t col = d + uint32_t(64 * ps);
+            const uint32_t col = d + uint32_t(32 * ps);
 #pragma unroll
             for (int j = 0; j < 4; ++j) tmem_cp_pair_128x256b(col + uint32_t(8 * j), pa + uint64_t(2 * j));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) tmem_cp_pair_128x256b(col + 32u + uint32_t(8 * j), pb + uint64_t(2 * j));
+            for (int j = 0; j < 4; ++j) tmem_cp_pair_128x256b(col + uint32_t(kBN / 2 + 8 * j), pb + uint64_t(2 * j));
             mma_commit_pair_mc(s.empty + stage, uint16_t((1u << CL) - 1u));
             if (++stage == kPStages) {
                 stage = 0;
@@ -590,7 +591,8 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         c.q = __shfl_sync(0xffffffffu, e.q, 0);
         c.mt = __shfl_sync(0xffffffffu, e.mt, 0);
         c.nt = __shfl_sync(0xffffffffu, e.nt, 0);
-        const int pre = __shfl_sync(0xffffffffu, e.pre, 0);   // in_buf[0] already in the accumulator
+        const int pre = __shfl_sync(0xffffffffu, e.pre, 0);   // in_buf[0]'s slices cb < p.pre_stages are
+                                                              // already in the accumulator
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
         const bool real = c.nt < p.ntiles;   // a cluster's second pair may have no column tile
@@ -624,7 +626,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
             for (int j = 0; j < 2; ++j) {
-                if (tk.in_buf[j] < 0 || (j == 0 && pre >= 0)) continue;
+                if (tk.in_buf[j] < 0 || (j == 0 && pre >= 0 && cb < p.pre_stages)) continue;
                 if (lane == 0) {
                     if (store_pending) {
                         bulk_wait_read<0>();
@@ -678,6 +680,13 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
                     }
                 }
             }
+        }
+        // half preload: the next tile in this buffer accumulates onto every
+        // column, so the columns it will not preload must read zero
+        if (p.pre_stages > 0 && p.pre_stages < 4) {
+            for (int cb = p.pre_stages; cb < 4; ++cb)
+                tmem_zero32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN + half * 128 + cb * 32));
+            tmem_wait_st();
         }
         tc_fence_before();
         __syncwarp();
@@ -767,6 +776,22 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem_base = *s.tmem_slot;
     const int total = (p.task_end - p.task_begin) * p.tiles_per_task;
+    if (p.op == 1 && p.pre_stages > 0 && p.pre_stages < 4) {
+        // half preload: both accumulators start with zeros in the columns
+        // that are not preloaded (see the RS epilogue), before any MMA
+        if (warp >= 4) {
+            const int e = warp - 4;
+            for (int b = 0; b < 2; ++b)
+                for (int cb = p.pre_stages; cb < 4; ++cb)
+                    tmem_zero32(tmem_base + (uint32_t((e & 3) * 32) << 16) +
+                                uint32_t(b * kBN + (e >> 2) * 128 + cb * 32));
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncthreads();
+        cluster_sync();
+        tc_fence_after();
+    }
 
     if (warp == 0) {
         if (lane == 0) producer<LAYOUT, CL>(p, s, total, cl);

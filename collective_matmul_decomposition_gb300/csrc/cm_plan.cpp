@@ -399,7 +399,7 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
             p.bulk_overlap = int(value);
             return CM_OK;
         case CM_OPT_RS_PRELOAD:
-            if (value < 0 || value > 2) return CM_ERR_INVALID_ARG;
+            if (value < 0 || value > 3) return CM_ERR_INVALID_ARG;
             p.rs_preload = int(value);
             return CM_OK;
         case CM_OPT_ROW_BAND:

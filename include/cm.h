@@ -339,11 +339,15 @@ const char *cm_status_string(cm_status status);
  *                        in through the operand ring and copies it into the
  *                        tile's tensor-memory accumulator before the partial
  *                        GEMM adds onto it, so the epilogue only stores;
- *                        0 adds the received bucket in the epilogue; 2 (the
- *                        default) preloads when a tile has at most 8 K
- *                        slices of 64 (k <= 512), where the epilogue, not
- *                        the GEMM, sets the pace.  The same sum, in a
- *                        different fp32 order.
+ *                        0 adds the received bucket in the epilogue; 3
+ *                        preloads half of it (the first two of each
+ *                        epilogue warp's four 32-column slices) and adds the
+ *                        rest in the epilogue; 2 (the default) preloads all
+ *                        of it when a tile has at most 8 K slices of 64
+ *                        (k <= 512), where the epilogue sets the pace, and
+ *                        none beyond (the epilogue then hides under the
+ *                        partial GEMM).  The same sum, in a different fp32
+ *                        order.
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,

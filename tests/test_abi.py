@@ -56,10 +56,10 @@ def test_plan_arguments(lib):
     for opt, bad in ((cm.CM_OPT_L2_HINTS, -1), (cm.CM_OPT_L2_HINTS, 256),
                      (cm.CM_OPT_L2_PROMOTION, -1), (cm.CM_OPT_L2_PROMOTION, 4),
                      (cm.CM_OPT_ROW_BAND, -1), (cm.CM_OPT_ROW_BAND, 4097),
-                     (cm.CM_OPT_RS_PRELOAD, -1), (cm.CM_OPT_RS_PRELOAD, 3)):
+                     (cm.CM_OPT_RS_PRELOAD, -1), (cm.CM_OPT_RS_PRELOAD, 4)):
         with pytest.raises(cm.CMError):
             p.set_option(opt, bad)
-    for v in (0, 1, 2):
+    for v in (0, 1, 2, 3):
         p.set_option(cm.CM_OPT_RS_PRELOAD, v)
     p.set_option(cm.CM_OPT_L2_HINTS, 0x21)
     p.set_option(cm.CM_OPT_L2_PROMOTION, 0)

@@ -1,9 +1,9 @@
 """GEMM->ReduceScatter with the received partial bucket preloaded into the
-tile's tensor-memory accumulator (CM_OPT_RS_PRELOAD = 1, forced on): the same
-result as the epilogue-add path (0), against the oracle, exactly on integer
-inputs, and at the full MLP sweep size on sampled rows.  The automatic
-choice (2, the default) picks one of the two by the tile's K-slice count;
-both sides of that choice are checked here and by the default-path tests."""
+tile's tensor-memory accumulator (CM_OPT_RS_PRELOAD = 1: all of it; 3: half,
+the rest added in the epilogue): the same result as the epilogue-add path
+(0), against the oracle, exactly on integer inputs, and at the full MLP
+sweep size on sampled rows.  The automatic choice (2, the default) picks one
+of the first two by the tile's K-slice count; it is checked against both."""
 
 import numpy as np
 import pytest
@@ -33,17 +33,19 @@ def _plan(N, chunks, direction, preload, kernel=0):
 ])
 @pytest.mark.parametrize("layout", ["nk", "kn"])
 @pytest.mark.parametrize("ydtype", [torch.float32, torch.bfloat16])
-def test_preload_vs_oracle(N, M, k, n, chunks, direction, layout, ydtype):
+@pytest.mark.parametrize("mode", [1, 3])
+def test_preload_vs_oracle(N, M, k, n, chunks, direction, layout, ydtype, mode):
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=M + k, w_layout=layout)
     ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), layout)
-    y, _, _ = run_rs(_plan(N, chunks, direction, 1), x, w, layout, ydtype)
+    y, _, _ = run_rs(_plan(N, chunks, direction, mode), x, w, layout, ydtype)
     e = oracle.normwise_max_rel_err(_np(y), ref)
     assert np.isfinite(_np(y)).all()
     assert e <= (TOL_F32 if ydtype == torch.float32 else TOL), e
 
 
 @pytest.mark.parametrize("direction", ["uni", "bidi"])
-def test_preload_exact_on_integers(direction):
+@pytest.mark.parametrize("mode", [1, 3])
+def test_preload_exact_on_integers(direction, mode):
     """Small-integer inputs keep every fp32 partial sum exact, so both paths
     and the oracle agree bit for bit whatever the summation order."""
     N, M, k, n = 6, 1536, 256, 640
@@ -51,7 +53,7 @@ def test_preload_exact_on_integers(direction):
     x = torch.randint(-3, 4, (N, M, k), generator=g).to(torch.bfloat16)
     w = torch.randint(-2, 3, (N, n, k), generator=g).to(torch.bfloat16)
     ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
-    y1, _, _ = run_rs(_plan(N, 2, direction, 1), x, w, "nk")
+    y1, _, _ = run_rs(_plan(N, 2, direction, mode), x, w, "nk")
     y0, _, _ = run_rs(_plan(N, 2, direction, 0), x, w, "nk")
     assert np.array_equal(_np(y1), ref)
     assert torch.equal(y1, y0)
@@ -76,14 +78,13 @@ def test_preload_matches_epilogue_add_and_repeats():
     assert (ya - y0).abs().max().item() <= 1e-4 * y0.abs().max().item()
 
 
-@pytest.mark.parametrize("k", [256, 1024])
-def test_automatic_choice_matches_both_paths(k):
+@pytest.mark.parametrize("k,picked", [(256, 1), (512, 1), (1024, 0), (4096, 0)])
+def test_automatic_choice_matches_the_path_it_picks(k, picked):
     """The default (automatic) setting gives the bits of the path it picks:
-    preload for k = 256 (4 K slices), epilogue add for k = 1024 (16)."""
+    all preloaded for at most 8 K slices, none beyond."""
     N, M, n = 4, 2048, 512
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=k, w_layout="nk")
     auto, _, _ = run_rs(cm.Plan(N, 1, "uni"), x, w, "nk")
-    picked = 1 if k <= 512 else 0
     y, _, _ = run_rs(_plan(N, 1, "uni", picked), x, w, "nk")
     assert torch.equal(auto, y)
 
@@ -104,13 +105,13 @@ def test_preload_skipped_signal_times_out():
     assert oracle.normwise_max_rel_err(_np(y), ref) <= TOL_F32
 
 
-@pytest.mark.parametrize("N", [8, 16])
-def test_preload_full_size_sampled(N):
+@pytest.mark.parametrize("N,mode", [(8, 1), (16, 3)])
+def test_preload_full_size_sampled(N, mode):
     """The MLP h=8192, ffn=28672, s=8192 fc2 GEMM-RS at full size, sampled rows."""
     s = gen.mlp_shapes(N)["rs"]
     wl = gen.WORKLOADS["mlp_h8192_ffn28672_s8192"]["rs"]
     x, w = gen.rs_inputs(N, s["M"], s["k"], s["n"], wl["x"], wl["w"], wl["seed"], "nk")
-    y, _, _ = run_rs(_plan(N, 1, "uni", 1), x, w, "nk", torch.bfloat16)
+    y, _, _ = run_rs(_plan(N, 1, "uni", mode), x, w, "nk", torch.bfloat16)
     Mb = s["M"] // N
     rng = np.random.default_rng(N)
     pairs = [(o, r) for o in range(N) for r in (0, 255, 256, Mb - 1)]
