@@ -41,6 +41,13 @@
 //             column half = (warp - 4) / 4.  AG writes shard rows of Y_r; RS
 //             moves the fp32 bucket through a 4 KB swizzled buffer per warp
 //             with TMA loads and stores.
+//
+// RS preload (p.pre_stages > 0): for a tile that receives a bucket, the
+// scheduler acquires the bucket's flag before publishing the tile, the
+// producer loads the CTA's rows of that bucket through the ring ahead of the
+// K slices, and the MMA thread copies them into the accumulator
+// (tcgen05.cp) and accumulates the partial GEMM onto them; the epilogue then
+// only stores the preloaded slices.
 // All waits are bounded; see cm_kernel.cu for the failure protocol.
 #include <cuda_bf16.h>
 
