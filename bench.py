@@ -708,8 +708,10 @@ def run_gate(args):
         dec, mono = Step(N, chunks, direction, data, device), Step(N, 1, "none", data, device)
         for op in ops:
             fl = f_ag if op == "ag" else f_rs
-            ms_dec = time_loop(getattr(dec, op), args.steps, torch, warmup=args.warmup)
-            ms_none = time_loop(getattr(mono, op), args.steps, torch, warmup=args.warmup)
+            # interleaved, so that both forms run under the same clocks
+            t = time_interleaved({"dec": getattr(dec, op), "none": getattr(mono, op)}, args.steps, torch,
+                                 warmup=args.warmup)
+            ms_dec, ms_none = t["dec"], t["none"]
             dec.check((op,))
             mono.check((op,))
             sh = data["shapes"][op]
