@@ -127,14 +127,20 @@ KernelChoice choose_kernel(const PlanImpl &pl, int64_t n) {
 constexpr int64_t kRowBandBytes = int64_t(32) << 20;   // A bytes per row band of the tile order
 
 // Row tiles, column tiles and flag targets for the selected kernel.
-void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int64_t n) {
+// pair_chunks: a ring call on CTA pairs of one cluster whose chunks have at
+// most 128 rows puts two chunks in one 256-row pair tile, one per CTA,
+// instead of leaving half of every tile on zero rows.
+void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int64_t n, bool pair_chunks = false) {
     const int tm = kc.pair ? pair_rows() : kBM;
-    const int per_tile = kc.pair ? 2 : 1;   // signals per tile (one per CTA of a pair)
+    kp.chunk_pair = pair_chunks && kc.pair && kc.cluster_ctas == 2 && kp.chunks % 2 == 0 && rows_c <= kBM;
+    // signals per chunk and tile: one per CTA of a pair whose CTAs share the
+    // chunk; one when each CTA of the pair has a chunk of its own
+    const int per_tile = kc.pair && !kp.chunk_pair ? 2 : 1;
     kp.mtiles_c = int((rows_c + tm - 1) / tm);
     kp.ntiles = int((n + kBN - 1) / kBN);
     const int pairs = kc.pair ? kc.cluster_ctas / 2 : 1;
     kp.ntile_groups = (kp.ntiles + pairs - 1) / pairs;   // single CTAs: one column tile per group
-    kp.tiles_per_task = kp.chunks * kp.mtiles_c * kp.ntile_groups;
+    kp.tiles_per_task = (kp.chunk_pair ? kp.chunks / 2 : kp.chunks) * kp.mtiles_c * kp.ntile_groups;
     if (op == CM_OP_AG_GEMM) {
         // forwards per chunk: CTA pairs forward a row slice from every tile
         // (2 CTAs each); single CTAs forward whole row tiles from column tile 0
@@ -325,7 +331,7 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    set_tiling(kc, CM_OP_AG_GEMM, kp, rows_c, n);
+    set_tiling(kc, CM_OP_AG_GEMM, kp, rows_c, n, true);
     return run(pl, kc, CM_OP_AG_GEMM, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -393,7 +399,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n);
+    set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
     return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
 }
 

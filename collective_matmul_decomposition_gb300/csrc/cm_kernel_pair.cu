@@ -98,7 +98,8 @@ struct PSmem {
 struct QTile {
     int t, task, q, mt, nt, nk, a_src, a_row, n0, slab, rr, sig;
     int pre;        // RS preload: accumulator buffer whose bucket is loaded before the K slices, -1 none
-    int pad[3];
+    int row0;       // this CTA's first output row inside its chunk q
+    int pad[2];
 };
 constexpr int kQWords = 16;
 
@@ -120,7 +121,7 @@ struct QueueReader {
             const volatile int4 *v = reinterpret_cast<const volatile int4 *>(s.qent + kQWords * slot);
             const int4 a = const_cast<const int4 &>(v[0]), b = const_cast<const int4 &>(v[1]),
                        c = const_cast<const int4 &>(v[2]), d = const_cast<const int4 &>(v[3]);
-            e = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, {d.y, d.z, d.w}};
+            e = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, d.y, {d.z, d.w}};
         }
         if (release) mbar_arrive_cluster(qempty_leader0 + 8u * uint32_t(slot));
         if (++slot == kQueue) {
@@ -293,30 +294,38 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
         const cm_task &tk = p.tasks[c.task];
         // AG: the tile's A rows arrive by the ring; the producers that read
         // this entry see them (acquire here, release to them by the queue)
-        if (t >= 0 && p.op == 0 && tk.wait_in[0] >= 0 &&
-            !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q))
-            return;
+        // the chunks this tile reads: c.q, or 2*c.q and 2*c.q + 1 when a pair
+        // tile covers two chunks (one per CTA)
+        const int q0 = p.chunk_pair ? 2 * c.q : c.q, nq = p.chunk_pair ? 2 : 1;
+        if (t >= 0 && p.op == 0 && tk.wait_in[0] >= 0)
+            for (int qq = q0; qq < q0 + nq; ++qq)
+                if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], qq), p.tgt_in, kSiteProducerFlag, c.task, qq))
+                    return;
         // RS preload: the received bucket is read before the partial GEMM, so
         // its producers must be done before this tile is published
         const bool pre = t >= 0 && p.op == 1 && p.rs_preload && p.pre_stages > 0 && CL == 2 && tk.in_buf[0] >= 0;
-        if (pre && tk.wait_in[0] >= 0 &&
-            !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q))
-            return;
+        if (pre && tk.wait_in[0] >= 0)
+            for (int qq = q0; qq < q0 + nq; ++qq)
+                if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], qq), p.tgt_in, kSiteProducerFlag, c.task, qq))
+                    return;
         if (!wait_mbar<true>(p, s.abort, &s.qempty[slot], qphase ^ 1u, kSiteEmpty, -1, -1)) return;
         const bool sum_ranks = tk.a_src == 2;
-        const int slab = (sum_ranks ? tk.out_idx : tk.a_slab) * p.chunks + c.q;
+        const int slab0 = (sum_ranks ? tk.out_idx : tk.a_slab) * p.chunks;
         const int rr = sum_ranks ? 0 : tk.rank;
         const int nk = kslices(p, tk), sig = p.op == 0 ? tk.sig_done : -1;
         for (uint32_t r = 0; r < uint32_t(CL); ++r) {
             const int pos = int(r & 1u), pair = int(r >> 1);
             const int nt = c.nt + pair;   // c.nt is the group's first column tile
-            const int a_row = c.mt * kPairRows + pos * kCtaRows + (CL == 4 ? pair * (kCtaRows / 2) : 0);
+            const int q = p.chunk_pair ? q0 + pos : c.q;   // this CTA's chunk
+            const int row0 = p.chunk_pair ? 0 : c.mt * kPairRows + pos * kCtaRows;
+            const int a_row = row0 + (CL == 4 ? pair * (kCtaRows / 2) : 0);
+            const int slab = slab0 + q;
             const int n0 = nt * kBN + pos * (kBN / 2);
             int32_t *e = s.qent + kQWords * slot;
-            const uint32_t w[kQWords] = {uint32_t(t),   uint32_t(c.task), uint32_t(c.q), uint32_t(c.mt),
+            const uint32_t w[kQWords] = {uint32_t(t),   uint32_t(c.task), uint32_t(q),   uint32_t(c.mt),
                                          uint32_t(nt),  uint32_t(nk),     uint32_t(tk.a_src), uint32_t(a_row),
                                          uint32_t(n0),  uint32_t(slab),   uint32_t(rr),       uint32_t(sig),
-                                         uint32_t(pre ? int(tk.in_buf[0]) : -1), 0u, 0u, 0u};
+                                         uint32_t(pre ? int(tk.in_buf[0]) : -1), uint32_t(row0), 0u, 0u};
             if (r == 0) {
                 for (int i = 0; i < kQWords; ++i) e[i] = int32_t(w[i]);
             } else {
@@ -413,7 +422,10 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
         if (!ok) break;
         mma_commit_pair_mc(&s.tfull[accb], uint16_t(3u << (2u * cl.pair)));   // this pair's CTAs
         // AG: both CTAs' A slices of this tile have landed; the slot rows may be reused
-        if (c.sig >= 0) red_release_add(flag_ptr(p, c.sig, c.q), 1u);
+        if (c.sig >= 0) {
+            red_release_add(flag_ptr(p, c.sig, c.q), 1u);
+            if (p.chunk_pair) red_release_add(flag_ptr(p, c.sig, c.q + 1), 1u);   // the peer CTA's chunk
+        }
         if (++accb == 2) {
             accb = 0;
             acc_phase ^= 1u;
@@ -443,7 +455,7 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
         if (!ok) break;
         fence_proxy_async_global();
         const int lo = c.nt * per;
-        const int row0 = c.mt * kPairRows + int(cl.pos) * kCtaRows + lo;
+        const int row0 = c.row0 + lo;
         const int nrows = min(min(per, kCtaRows - lo), p.rows_c - row0);
         if (nrows > 0) {
             const int64_t rb = p.row_bytes;
@@ -534,13 +546,14 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
         c.q = __shfl_sync(0xffffffffu, e.q, 0);
         c.mt = __shfl_sync(0xffffffffu, e.mt, 0);
         c.nt = __shfl_sync(0xffffffffu, e.nt, 0);
+        const int row0 = __shfl_sync(0xffffffffu, e.row0, 0);   // this CTA's first row in chunk c.q
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
         bad = bar_or(1, kPEpiWarps * 32, bad || *s.abort != 0);
         if (bad) break;
         tc_fence_after();
 
-        const int row = c.mt * kPairRows + int(cl.pos) * kCtaRows + quad * 32 + lane;   // row inside the chunk
+        const int row = row0 + quad * 32 + lane;   // row inside the chunk
         const bool row_ok = row < p.rows_c;
         const int64_t crow = int64_t(c.q) * p.rows_c + row;
 #pragma unroll 1
@@ -598,6 +611,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         c.q = __shfl_sync(0xffffffffu, e.q, 0);
         c.mt = __shfl_sync(0xffffffffu, e.mt, 0);
         c.nt = __shfl_sync(0xffffffffu, e.nt, 0);
+        const int row0 = __shfl_sync(0xffffffffu, e.row0, 0);   // this CTA's first row in chunk c.q
         const int pre = __shfl_sync(0xffffffffu, e.pre, 0);   // in_buf[0]'s slices cb < p.pre_stages are
                                                               // already in the accumulator
         const cm_task &tk = p.tasks[c.task];
@@ -617,7 +631,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         if (lane == 0) fence_proxy_async_global();   // the received buckets were released by other CTAs
         tc_fence_after();
 
-        const int row_w = c.mt * kPairRows + int(cl.pos) * kCtaRows + quad * 32;   // warp's first row in the chunk
+        const int row_w = row0 + quad * 32;   // warp's first row in the chunk
         const int row = row_w + lane;
         const bool row_ok = row < p.rows_c;
         const int64_t crow = int64_t(c.q) * p.rows_c + row;
