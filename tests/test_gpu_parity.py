@@ -13,6 +13,8 @@ Bars (the arithmetic is bf16 products accumulated in fp32):
 Full-size workloads are checked on sampled rows the oracle computes one by one.
 """
 
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -265,9 +267,39 @@ def test_gpt3_layer_bidi():
     _check_rs_full(8, r["M"], r["k"], r["n"], "bidi", 1, r["seed"])
 
 
-@pytest.mark.parametrize("N,chunks,direction", [(8, 1, "uni"), (4, 4, "bidi"), (16, 2, "uni"), (16, 4, "bidi")])
-def test_mlp_h8192_sweep_points(N, chunks, direction):
+@functools.lru_cache(maxsize=1)
+def _mlp_case(N):
+    """Inputs of the MLP sweep at N ranks (they depend on N only) and the
+    oracle's sampled reference rows, made once for all chunk counts and rings."""
     s = gen.mlp_shapes(N)
     a, r = s["ag"], s["rs"]
-    _check_ag_full(N, a["m"], a["K"], a["n"], direction, chunks, 5000 + N)
-    _check_rs_full(N, r["M"], r["k"], r["n"], direction, chunks, 5002 + N)
+    xa, wa = gen.ag_inputs(N, a["m"], a["K"], a["n"], gen.NORMAL1, gen.NORMAL002, seed=5000 + N, w_layout="nk")
+    xr, wr = gen.rs_inputs(N, r["M"], r["k"], r["n"], gen.NORMAL1, gen.NORMAL002, seed=5002 + N, w_layout="nk")
+    rng = np.random.default_rng(5000 + N)
+    ranks, rows = _ag_rows(N, a["m"], rng)
+    ref_a = oracle.ag_gemm_rows(gen.bf16_bits(xa), gen.bf16_bits(wa), ranks, rows, "nk")
+    Mb = r["M"] // N
+    owners = np.concatenate([np.arange(N), np.arange(N), rng.integers(0, N, 24)])
+    orow = np.concatenate([np.zeros(N, int), np.full(N, Mb - 1), rng.integers(0, Mb, 24)])
+    ref_r = oracle.gemm_rs_rows(gen.bf16_bits(xr), gen.bf16_bits(wr), owners, orow, "nk")
+    return dict(xa=xa, wa=wa, xr=xr, wr=wr, ranks=ranks, rows=rows, ref_a=ref_a, owners=owners, orow=orow,
+                ref_r=ref_r)
+
+
+SWEEP = [(N, c, d) for N in (4, 8, 16) for d in ("uni", "bidi") for c in (1, 2, 4)]
+
+
+@pytest.mark.parametrize("N,chunks,direction", SWEEP)
+def test_mlp_h8192_sweep_points(N, chunks, direction):
+    """Every (N, chunks, ring) point of the MLP h=8192, ffn=28672, s=8192
+    chunk/ring sweep, both ops at full size, on sampled rows."""
+    c = _mlp_case(N)
+    y, _, _ = run_ag(cm.Plan(N, chunks, direction), c["xa"], c["wa"], "nk", torch.bfloat16)
+    got = y[torch.as_tensor(c["ranks"], device=DEV), torch.as_tensor(c["rows"], device=DEV)]
+    assert oracle.normwise_max_rel_err(_np(got), c["ref_a"]) <= TOL
+    assert torch.isfinite(y).all()
+    del y
+    y, _, _ = run_rs(cm.Plan(N, chunks, direction), c["xr"], c["wr"], "nk", torch.bfloat16)
+    got = y[torch.as_tensor(c["owners"], device=DEV), torch.as_tensor(c["orow"], device=DEV)]
+    assert oracle.normwise_max_rel_err(_np(got), c["ref_r"]) <= TOL
+    assert torch.isfinite(y).all()
