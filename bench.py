@@ -353,7 +353,7 @@ def time_loop(fn, iters, torch, warmup=3):
 
 
 def time_interleaved(fns, iters, torch, warmup=3):
-    """Mean ms per call of each fn in the dict `fns`, calling them in turn
+    """Median ms per call of each fn in the dict `fns`, calling them in turn
     (one of each per round, `iters` rounds) so that all see the same clocks
     and power state. CUDA events around every call, synchronised once."""
     for _ in range(warmup):
@@ -368,7 +368,7 @@ def time_interleaved(fns, iters, torch, warmup=3):
             fn()
             ev[k][i][1].record()
     torch.cuda.synchronize()
-    return {k: statistics.mean(a.elapsed_time(b) for a, b in ev[k]) for k in fns}
+    return {k: statistics.median(a.elapsed_time(b) for a, b in ev[k]) for k in fns}
 
 
 def concat_operands(st, shapes, N):
@@ -547,7 +547,7 @@ def run_ours(args):
             detail[f"{op}_vs_torch_time"] = mine / detail[f"torch_{op}_ms_interleaved"]
             detail[f"{op}_vs_none_time"] = mine / detail[f"none_{op}_ms_interleaved"]
         detail["comparators"] = ("each op, its undecomposed form in this kernel and torch.matmul on the "
-                                 f"concatenated operands, interleaved {iters} times after the timed region")
+                                 f"concatenated operands, interleaved {iters} times after the timed region (median)")
         del X2, W2, mono, variants
 
     # end to end through the C ABI with host buffers: every step copies all four
@@ -632,7 +632,7 @@ def run_sweep(args):
                 "rs": {"none": mono.rs, "torch": lambda: torch.matmul(X2, W2.t())}}
 
         def emit(op, chunks, ring, fn, check):
-            t = time_interleaved({"dec": fn, **comp[op]}, args.steps, torch, warmup=args.warmup)
+            t = time_interleaved({"dec": fn, **comp[op]}, max(20, args.steps), torch, warmup=args.warmup)
             check()
             tf = fl[op] / (t["dec"] / 1e3) / 1e12
             print(json.dumps({"sweep": WORKLOAD, "op": op, "N": N, "chunks": chunks, "ring": ring,
@@ -709,7 +709,7 @@ def run_gate(args):
         for op in ops:
             fl = f_ag if op == "ag" else f_rs
             # interleaved, so that both forms run under the same clocks
-            t = time_interleaved({"dec": getattr(dec, op), "none": getattr(mono, op)}, args.steps, torch,
+            t = time_interleaved({"dec": getattr(dec, op), "none": getattr(mono, op)}, max(20, args.steps), torch,
                                  warmup=args.warmup)
             ms_dec, ms_none = t["dec"], t["none"]
             dec.check((op,))
