@@ -24,6 +24,7 @@ CM_OPT_TIMEOUT_NS, CM_OPT_SERIAL_STEPS, CM_OPT_GRID, CM_OPT_SKIP_SIGNAL, CM_OPT_
 CM_OPT_STATIC_TILES, CM_OPT_TILE_GROUP, CM_OPT_L2_HINTS, CM_OPT_L2_PROMOTION, CM_OPT_ROW_BAND = 5, 6, 7, 8, 9
 CM_OPT_BULK_OVERLAP = 10
 CM_OPT_RS_PRELOAD = 11
+CM_OPT_RS_IN_PLACE = 12
 CM_MAX_RANKS, CM_MAX_CHUNKS = 16, 8
 
 DIRECTIONS = {"uni": CM_RING_UNI, "bidi": CM_RING_BIDI, "none": CM_RING_NONE}
@@ -33,7 +34,7 @@ LAYOUTS = {"kn": CM_W_KN, "nk": CM_W_NK}
 EXPORTS = ["cm_plan", "cm_plan_destroy", "cm_plan_steps", "cm_plan_step", "cm_plan_tasks",
            "cm_ag_gemm_workspace_size", "cm_gemm_rs_workspace_size", "cm_ag_gemm", "cm_gemm_rs",
            "cm_check_status", "cm_status_string", "cm_plan_set_option", "cm_version",
-           "cm_ag_gemm_noalloc", "cm_cost_estimate", "cm_plan_choose",
+           "cm_ag_gemm_noalloc", "cm_ag_gemm_noalloc_check_status", "cm_cost_estimate", "cm_plan_choose",
            "cm_gemm_rs_pipelined_workspace_size", "cm_gemm_rs_pipelined",
            "cm_backward_pair_workspace_size", "cm_backward_pair",
            "cm_cannon_workspace_size", "cm_cannon_gemm"]
@@ -103,6 +104,8 @@ def load():
     lib.cm_version.restype = ctypes.c_char_p
     lib.cm_ag_gemm_noalloc.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p]
     lib.cm_ag_gemm_noalloc.restype = i32
+    lib.cm_ag_gemm_noalloc_check_status.argtypes = [p, ctypes.POINTER(i32)]
+    lib.cm_ag_gemm_noalloc_check_status.restype = i32
     lib.cm_gemm_rs_pipelined_workspace_size.argtypes = [p, i64, i64]
     lib.cm_gemm_rs_pipelined_workspace_size.restype = sz
     lib.cm_gemm_rs_pipelined.argtypes = [p, p, p, i32, p, i32, i64, i64, i64, p, sz, p]
@@ -222,6 +225,13 @@ def cm_ag_gemm_noalloc(plan: Plan, x, w, y, w_layout: str = "nk", stream=None):
     st = load().cm_ag_gemm_noalloc(plan.handle, _ptr(x), _ptr(w), LAYOUTS[w_layout], _ptr(y), _ydtype(y),
                                    m, K, n, _stream_ptr(stream))
     _check(st, "cm_ag_gemm_noalloc")
+
+
+def cm_ag_gemm_noalloc_check_status(stream=None):
+    """Synchronise and return (status, info[4]) of the last cm_ag_gemm_noalloc call."""
+    info = (ctypes.c_int * 4)()
+    st = load().cm_ag_gemm_noalloc_check_status(_stream_ptr(stream), info)
+    return st, list(info)
 
 
 def cm_gemm_rs(plan: Plan, x, w, y, ws, w_layout: str = "nk", stream=None):

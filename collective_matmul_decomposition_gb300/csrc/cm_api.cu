@@ -51,13 +51,19 @@ WsLayout ag_layout(const PlanImpl &p, int64_t m, int64_t K) {
     return l;
 }
 
+// RS accumulator buffers of [M/N][n] fp32: one per (bucket, ring stream) when
+// buckets are accumulated in place, else one per (rank, ring stream, step).
+int64_t rs_bufs(const PlanImpl &p) {
+    if (p.dir == CM_RING_NONE || p.N <= 1) return 0;
+    const int64_t per = p.rs_in_place ? 1 : p.sched[CM_OP_GEMM_RS].steps;
+    return int64_t(p.N) * streams_of(p) * per;
+}
+
 WsLayout rs_layout(const PlanImpl &p, int64_t M, int64_t n) {
     WsLayout l;
     l.flags_bytes = size_t(p.flag_ids[CM_OP_GEMM_RS]) * size_t(p.chunks) * sizeof(uint32_t);
     l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
-    const bool ring = p.dir != CM_RING_NONE && p.N > 1;
-    const size_t bufs = ring ? size_t(p.N * streams_of(p) * p.sched[CM_OP_GEMM_RS].steps) : 0;
-    l.buf_bytes = bufs * size_t(M / p.N) * size_t(n) * sizeof(float);
+    l.buf_bytes = size_t(rs_bufs(p)) * size_t(M / p.N) * size_t(n) * sizeof(float);
     l.total = l.buf_off + l.buf_bytes;
     return l;
 }
@@ -86,11 +92,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// 3-D tensor [d2][d1][d0] (d0 contiguous) of bf16 (or fp32), 128-byte swizzled boxes of b0 x b1.
-int g_l2_promotion = 3;   // promotion of the maps being built (set per call under the call's lock)
-
-bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0, uint32_t b1,
-              bool f32 = false) {
+// 3-D tensor [d2][d1][d0] (d0 contiguous) of bf16 (or fp32), 128-byte swizzled boxes of b0 x b1;
+// l2_promotion is the plan's CM_OPT_L2_PROMOTION (0 none, 1 64 B, 2 128 B, 3 256 B).
+bool make_map(CUtensorMap *m, int l2_promotion, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t b0,
+              uint32_t b1, bool f32 = false) {
     auto enc = encode_fn();
     if (!enc) return false;
     const uint64_t es_bytes = f32 ? 4 : 2;
@@ -101,28 +106,19 @@ bool make_map(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64
     CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
                      const_cast<void *>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                     static_cast<CUtensorMapL2promotion>(g_l2_promotion),
+                     static_cast<CUtensorMapL2promotion>(l2_promotion),
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The kernel a call runs: single CTAs, or CTA pairs in clusters of 2 or 4.
+// The kernel a call runs: CTA pairs (one pair per cluster), or single CTAs.
 struct KernelChoice {
     bool pair;
-    int cluster_ctas;   // 2 or 4 for the pair kernel
 };
 
-KernelChoice choose_kernel(const PlanImpl &pl, int64_t n) {
-    (void)n;
-    switch (pl.kernel) {
-        case 1: return {false, 1};
-        case 2: return {true, 2};
-        case 3: return {true, 4};
-        default: return {true, 2};   // measured fastest: one pair per cluster
-    }
-}
+KernelChoice choose_kernel(const PlanImpl &pl) { return {pl.kernel != 1}; }
 
 constexpr int64_t kRowBandBytes = int64_t(32) << 20;   // A bytes per row band of the tile order
 
@@ -132,15 +128,13 @@ constexpr int64_t kRowBandBytes = int64_t(32) << 20;   // A bytes per row band o
 // instead of leaving half of every tile on zero rows.
 void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int64_t n, bool pair_chunks = false) {
     const int tm = kc.pair ? pair_rows() : kBM;
-    kp.chunk_pair = pair_chunks && kc.pair && kc.cluster_ctas == 2 && kp.chunks % 2 == 0 && rows_c <= kBM;
+    kp.chunk_pair = pair_chunks && kc.pair && kp.chunks % 2 == 0 && rows_c <= kBM;
     // signals per chunk and tile: one per CTA of a pair whose CTAs share the
     // chunk; one when each CTA of the pair has a chunk of its own
     const int per_tile = kc.pair && !kp.chunk_pair ? 2 : 1;
     kp.mtiles_c = int((rows_c + tm - 1) / tm);
     kp.ntiles = int((n + kBN - 1) / kBN);
-    const int pairs = kc.pair ? kc.cluster_ctas / 2 : 1;
-    kp.ntile_groups = (kp.ntiles + pairs - 1) / pairs;   // single CTAs: one column tile per group
-    kp.tiles_per_task = (kp.chunk_pair ? kp.chunks / 2 : kp.chunks) * kp.mtiles_c * kp.ntile_groups;
+    kp.tiles_per_task = (kp.chunk_pair ? kp.chunks / 2 : kp.chunks) * kp.mtiles_c * kp.ntiles;
     if (op == CM_OP_AG_GEMM) {
         // forwards per chunk: CTA pairs forward a row slice from every tile
         // (2 CTAs each); single CTAs forward whole row tiles from column tile 0
@@ -157,10 +151,10 @@ void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int
 cudaError_t launch_tiles(const PlanImpl &pl, const KernelChoice &kc, const KParams &kp, int layout, int64_t tiles,
                          int max_clusters, int sms, cudaStream_t stream) {
     if (kc.pair) {
-        int clusters = pl.grid > 0 ? std::min(pl.grid / kc.cluster_ctas, max_clusters) : max_clusters;
+        int clusters = pl.grid > 0 ? std::min(pl.grid / 2, max_clusters) : max_clusters;
         clusters = std::max(1, clusters);
         if (tiles < clusters) clusters = int(tiles);
-        return launch_pair(kp, layout, kc.cluster_ctas, clusters, stream);
+        return launch_pair(kp, layout, clusters, stream);
     }
     if (layout & 2) return cudaErrorInvalidValue;
     int grid = pl.grid > 0 ? std::min(pl.grid, sms) : sms;
@@ -175,7 +169,7 @@ cm_status setup_launch(const PlanImpl &pl, const KernelChoice &kc, KParams &kp, 
     if (cudaGetDevice(&dev) != cudaSuccess) return CM_ERR_CUDA;
     if (prepare_device(dev, sms) != cudaSuccess) return CM_ERR_CUDA;
     *max_clusters = 0;
-    if (kc.pair && prepare_pair(dev, kc.cluster_ctas, max_clusters) != cudaSuccess) return CM_ERR_CUDA;
+    if (kc.pair && prepare_pair(dev, max_clusters) != cudaSuccess) return CM_ERR_CUDA;
     if (kc.pair && *max_clusters <= 0) return CM_ERR_UNSUPPORTED;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     kp.status = reinterpret_cast<uint32_t *>(w8);
@@ -294,16 +288,15 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     std::lock_guard<std::mutex> lock(mu);
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
     kp.q_only = -1;
-    g_l2_promotion = pl.l2_promotion;
-    const KernelChoice kc = choose_kernel(pl, n);
-    // A box: a CTA's 128 rows, or a 64-row quarter when two pairs multicast it
-    const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
-    const uint32_t box_rows = uint32_t(std::min<int64_t>(a_rows, rows_c));
-    if (!make_map(&kp.tmA0, x, uint64_t(K), uint64_t(rows_c), uint64_t(slabs), kBK, box_rows)) return CM_ERR_CUDA;
+    const int promo = pl.l2_promotion;
+    const KernelChoice kc = choose_kernel(pl);
+    // A box: a CTA's 128 rows (fewer when a chunk is shorter)
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
+    if (!make_map(&kp.tmA0, promo, x, uint64_t(K), uint64_t(rows_c), uint64_t(slabs), kBK, box_rows)) return CM_ERR_CUDA;
     uint8_t *bufs = static_cast<uint8_t *>(ws) + l.buf_off;
     if (l.buf_bytes > 0) {
         const int64_t nslots = int64_t(N) * streams_of(pl) * pl.sched[CM_OP_AG_GEMM].steps;
-        if (!make_map(&kp.tmA1, bufs, uint64_t(K), uint64_t(rows_c), uint64_t(nslots * c), kBK, box_rows))
+        if (!make_map(&kp.tmA1, promo, bufs, uint64_t(K), uint64_t(rows_c), uint64_t(nslots * c), kBK, box_rows))
             return CM_ERR_CUDA;
     } else {
         kp.tmA1 = kp.tmA0;
@@ -311,9 +304,9 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     const bool b_mn = wlayout == CM_W_KN;
     const uint32_t b_rows = kc.pair ? kBN / 2 : kBN;   // a pair CTA stages half the columns
     if (b_mn) {
-        if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(K), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+        if (!make_map(&kp.tmB, promo, w, uint64_t(n), uint64_t(K), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     } else {
-        if (!make_map(&kp.tmB, w, uint64_t(K), uint64_t(n), uint64_t(N), kBK, b_rows)) return CM_ERR_CUDA;
+        if (!make_map(&kp.tmB, promo, w, uint64_t(K), uint64_t(n), uint64_t(N), kBK, b_rows)) return CM_ERR_CUDA;
     }
     kp.y = y;
     kp.acc = nullptr;
@@ -356,32 +349,31 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     std::lock_guard<std::mutex> lock(mu);
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
     kp.q_only = -1;
-    g_l2_promotion = pl.l2_promotion;
-    const KernelChoice kc = choose_kernel(pl, n);
-    const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
-    const uint32_t box_rows = uint32_t(std::min<int64_t>(a_rows, rows_c));
+    const int promo = pl.l2_promotion;
+    const KernelChoice kc = choose_kernel(pl);
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
     // x [N][M][k] viewed as [N*N*c][rows_c][k]: slab (r*N + bucket)*c + chunk
-    if (!make_map(&kp.tmA0, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
+    if (!make_map(&kp.tmA0, promo, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
     kp.tmA1 = kp.tmA0;
     const bool b_mn = wlayout == CM_W_KN;
     const uint32_t b_rows = kc.pair ? kBN / 2 : kBN;
     if (b_mn) {
-        if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(k), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+        if (!make_map(&kp.tmB, promo, w, uint64_t(n), uint64_t(k), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     } else {
-        if (!make_map(&kp.tmB, w, uint64_t(k), uint64_t(n), uint64_t(N), kBK, b_rows)) return CM_ERR_CUDA;
+        if (!make_map(&kp.tmB, promo, w, uint64_t(k), uint64_t(n), uint64_t(N), kBK, b_rows)) return CM_ERR_CUDA;
     }
     kp.y = y;
     kp.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
     if (l.buf_bytes > 0) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
-        const int64_t nbufs = int64_t(N) * streams_of(pl) * pl.sched[CM_OP_GEMM_RS].steps;
-        if (!make_map(&kp.tmAcc, kp.acc, uint64_t(n), uint64_t(rows_c), uint64_t(nbufs * c), 32, 32, true))
+        const int64_t nbufs = rs_bufs(pl);
+        if (!make_map(&kp.tmAcc, promo, kp.acc, uint64_t(n), uint64_t(rows_c), uint64_t(nbufs * c), 32, 32, true))
             return CM_ERR_CUDA;
         // received buckets through the operand ring: each CTA of a pair loads
         // its 128 rows of the tile as 32-column boxes (one per 16 KB stage half)
         const int pre_stages = preload_stages(pl.rs_preload, (k + kBK - 1) / kBK);
-        if (pre_stages > 0 && kc.pair && kc.cluster_ctas == 2) {
+        if (pre_stages > 0 && kc.pair) {
             const uint32_t pre_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
-            if (!make_map(&kp.tmAccIn, kp.acc, uint64_t(n), uint64_t(rows_c), uint64_t(nbufs * c), 32, pre_rows, true))
+            if (!make_map(&kp.tmAccIn, promo, kp.acc, uint64_t(n), uint64_t(rows_c), uint64_t(nbufs * c), 32, pre_rows, true))
                 return CM_ERR_CUDA;
             kp.rs_preload = 1;
             kp.pre_stages = pre_stages;
@@ -433,23 +425,22 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     SideStream *ss = side_stream(dev, kSidePipelinedRs);
     if (!ss) return CM_ERR_CUDA;
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
-    g_l2_promotion = pl.l2_promotion;
-    const KernelChoice kc = choose_kernel(pl, n);
-    const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
-    const uint32_t box_rows = uint32_t(std::min<int64_t>(a_rows, rows_c));
+    const int promo = pl.l2_promotion;
+    const KernelChoice kc = choose_kernel(pl);
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
     // x [N][M][k] viewed as [N*N*c][rows_c][k]: slab (r*N + bucket)*c + chunk
-    if (!make_map(&kp.tmA0, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
+    if (!make_map(&kp.tmA0, promo, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
     kp.tmA1 = kp.tmA0;
     const bool b_mn = wlayout == CM_W_KN;
     const uint32_t b_rows = kc.pair ? kBN / 2 : kBN;
     if (b_mn) {
-        if (!make_map(&kp.tmB, w, uint64_t(n), uint64_t(k), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+        if (!make_map(&kp.tmB, promo, w, uint64_t(n), uint64_t(k), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     } else {
-        if (!make_map(&kp.tmB, w, uint64_t(k), uint64_t(n), uint64_t(N), kBK, b_rows)) return CM_ERR_CUDA;
+        if (!make_map(&kp.tmB, promo, w, uint64_t(k), uint64_t(n), uint64_t(N), kBK, b_rows)) return CM_ERR_CUDA;
     }
     // partial products as [N*N*c][rows_c][n] fp32: slab (r*N + bucket)*c + chunk
     float *P = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
-    if (!make_map(&kp.tmAcc, P, uint64_t(n), uint64_t(rows_c), uint64_t(N) * N * c, 32, 32, true)) return CM_ERR_CUDA;
+    if (!make_map(&kp.tmAcc, promo, P, uint64_t(n), uint64_t(rows_c), uint64_t(N) * N * c, 32, 32, true)) return CM_ERR_CUDA;
     kp.y = y;
     kp.acc = P;
     kp.y_rank_stride = 0;
@@ -464,7 +455,7 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n);
-    kp.tiles_per_task = kp.mtiles_c * kp.ntile_groups;   // one chunk per launch
+    kp.tiles_per_task = kp.mtiles_c * kp.ntiles;   // one chunk per launch
     kp.tgt_in = kp.tgt_free = 0;
     int sms = 0, max_clusters = 0;
     st = setup_launch(pl, kc, kp, l, ws, &sms, &max_clusters);
@@ -581,13 +572,12 @@ cm_status cm_backward_pair(cm_plan_t plan, const void *x, const void *w, const v
     if (pl.bulk_overlap && cudaStreamWaitEvent(s, ss->ev[1], 0) != cudaSuccess) return CM_ERR_CUDA;
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
     kp.q_only = -1;
-    g_l2_promotion = pl.l2_promotion;
+    const int promo = pl.l2_promotion;
     KernelChoice kc;
     kc.pair = true;
-    kc.cluster_ctas = 2;
-    if (!make_map(&kp.tmA0, dy, uint64_t(n), uint64_t(T), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+    if (!make_map(&kp.tmA0, promo, dy, uint64_t(n), uint64_t(T), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     kp.tmA1 = kp.tmA0;
-    if (!make_map(&kp.tmB, xg, uint64_t(K), uint64_t(T), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
+    if (!make_map(&kp.tmB, promo, xg, uint64_t(K), uint64_t(T), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     kp.y = dw;
     kp.y_rank_stride = n * K;
     kp.out_rows_per_idx = n;
@@ -686,12 +676,11 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
     cudaEvent_t *ev = ss->ev;
     std::memset(static_cast<void *>(&kp), 0, sizeof kp);
     kp.q_only = -1;
-    g_l2_promotion = pl.l2_promotion;
-    const KernelChoice kc = choose_kernel(pl, bn);
+    const int promo = pl.l2_promotion;
+    const KernelChoice kc = choose_kernel(pl);
     const bool b_mn = blayout == CM_W_KN;
-    const int64_t a_rows = kc.pair && kc.cluster_ctas == 4 ? kBM / 2 : kBM;
-    const uint32_t box_rows = uint32_t(std::min<int64_t>(a_rows, bm));
-    if (!make_map(&kp.tmAcc, acc, uint64_t(bn), uint64_t(bm), uint64_t(P) * 2, 32, 32, true)) return CM_ERR_CUDA;
+    const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, bm));
+    if (!make_map(&kp.tmAcc, promo, acc, uint64_t(bn), uint64_t(bm), uint64_t(P) * 2, 32, 32, true)) return CM_ERR_CUDA;
     kp.y = c;
     kp.acc = acc;
     kp.out_rows_per_idx = bm;
@@ -721,13 +710,13 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
         if (step > 0 && cudaStreamWaitEvent(s, ev[1 + step], 0) != cudaSuccess) return CM_ERR_CUDA;
         const void *asrc = step == 0 ? static_cast<const void *>(a_in) : aset[step % 2];
         const void *bsrc = step == 0 ? static_cast<const void *>(b_in) : bset[step % 2];
-        if (!make_map(&kp.tmA0, asrc, uint64_t(bk), uint64_t(bm), uint64_t(P), kBK, box_rows)) return CM_ERR_CUDA;
+        if (!make_map(&kp.tmA0, promo, asrc, uint64_t(bk), uint64_t(bm), uint64_t(P), kBK, box_rows)) return CM_ERR_CUDA;
         kp.tmA1 = kp.tmA0;
         if (b_mn) {
-            if (!make_map(&kp.tmB, bsrc, uint64_t(bn), uint64_t(bk), uint64_t(P), 64, kBK)) return CM_ERR_CUDA;
+            if (!make_map(&kp.tmB, promo, bsrc, uint64_t(bn), uint64_t(bk), uint64_t(P), 64, kBK)) return CM_ERR_CUDA;
         } else {
             const uint32_t b_rows = kc.pair ? kBN / 2 : kBN;
-            if (!make_map(&kp.tmB, bsrc, uint64_t(bk), uint64_t(bn), uint64_t(P), kBK, b_rows)) return CM_ERR_CUDA;
+            if (!make_map(&kp.tmB, promo, bsrc, uint64_t(bk), uint64_t(bn), uint64_t(P), kBK, b_rows)) return CM_ERR_CUDA;
         }
         for (int rho = 0; rho < P; ++rho) {
             const int i = rho / q, j = rho % q, k = held_k(i, j, 0);

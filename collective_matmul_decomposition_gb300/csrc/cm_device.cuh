@@ -80,6 +80,17 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, const void *src, 
                  "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
                  : "memory");
 }
+// Element-wise add of a shared-memory box into the tensor map's box in global
+// memory, performed at L2: the destination elements are read there, the box's
+// elements added to them, and the sums written back.  Completion is tracked
+// by the bulk group.
+__device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, const void *src, int c0, int c1, int c2) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
@@ -276,14 +287,6 @@ __device__ __forceinline__ void tma_load_3d_pair_hint_a(uint32_t dst, uint64_t t
         "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr), "l"(policy)
         : "memory");
 }
-__device__ __forceinline__ void tma_load_3d_pair_mc_a(uint32_t dst, uint64_t tmap, uint32_t bar_cluster_addr, int c0,
-                                                      int c1, int c2, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
-        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr), "h"(cta_mask)
-        : "memory");
-}
 // Same, with an L2 eviction-priority policy for the loaded lines.
 __device__ __forceinline__ void tma_load_3d_pair_hint(void *dst, const void *tmap, uint32_t bar_cluster_addr, int c0,
                                                       int c1, int c2, uint64_t policy) {
@@ -307,17 +310,6 @@ __device__ __forceinline__ uint64_t policy_evict_normal() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
-}
-// Same, multicast: the box lands at the same shared-memory offset in every CTA
-// of `cta_mask`, and each landing counts on the ring barrier of that CTA's
-// pair leader.
-__device__ __forceinline__ void tma_load_3d_pair_mc(void *dst, const void *tmap, uint32_t bar_cluster_addr, int c0,
-                                                    int c1, int c2, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar_cluster_addr), "h"(cta_mask)
-        : "memory");
 }
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t *dst_smem, uint32_t ncols) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),

@@ -44,6 +44,7 @@ struct PlanImpl {
     int row_band = 0;       // see CM_OPT_ROW_BAND
     int bulk_overlap = 1;   // see CM_OPT_BULK_OVERLAP
     int rs_preload = 2;     // see CM_OPT_RS_PRELOAD
+    int rs_in_place = 1;    // see CM_OPT_RS_IN_PLACE
     int64_t skip_signal = -1;
     Schedule sched[2];                    // per cm_op
     std::vector<cm_task> tasks[2];        // per cm_op, execution order

@@ -62,7 +62,6 @@ struct KParams {
     int N, chunks;
     int rows_c;                // rows per chunk
     int mtiles_c, ntiles, kblocks;
-    int ntile_groups;          // CTA-pair kernel: column-tile groups (one column tile per pair of a cluster)
     int n;
     int y_f32;
     int a_box_rows;
@@ -83,12 +82,11 @@ cudaError_t launch_persistent(const KParams &p, bool b_mn_major, int grid, cudaS
 // One-time per-device kernel attributes; returns the SM count.
 cudaError_t prepare_device(int device, int *num_sms);
 
-// CTA-pair kernel (256 x 256 tiles; clusters of one pair, or of two pairs
-// that share the A tile by TMA multicast).
+// CTA-pair kernel (256 x 256 tiles; one pair per cluster).
 int pair_rows();
-cudaError_t prepare_pair(int device, int cluster_ctas, int *max_clusters);
-// layout: bit 0 = B MN-major, bit 1 = A MN-major (bit 1 only with cluster_ctas == 2).
-cudaError_t launch_pair(const KParams &p, int layout, int cluster_ctas, int clusters, cudaStream_t stream);
+cudaError_t prepare_pair(int device, int *max_clusters);
+// layout: bit 0 = B MN-major, bit 1 = A MN-major.
+cudaError_t launch_pair(const KParams &p, int layout, int clusters, cudaStream_t stream);
 // Pipelined GEMM -> ReduceScatter: y rows of chunk j of every bucket = the sum
 // over ranks of the fp32 partials P [N*N][Mb][n] (cm_reduce.cu).
 cudaError_t launch_reduce_chunk(const float *P, void *y, int N, int64_t Mb, int64_t rc, int64_t n, int j, bool y_f32,

@@ -17,14 +17,12 @@ struct TileCoord {
 
 // Linear tile index -> (task, chunk, row tile, column tile) of one CTA (or
 // one CTA pair).  Tiles run task group by task group (see cm_task.tile_group);
-// inside a group the order is chunk, row band, column-tile group, row tile of
-// the band.  The group's row tiles (task by task) are cut into bands of
+// inside a group the order is chunk, row band, column tile, row tile of the
+// band.  The group's row tiles (task by task) are cut into bands of
 // `row_band` row tiles (0: one band); each band runs through every column
 // tile before the next band starts, so the tiles running together share one
 // block of weight columns (W_r of the group's rank) and one band of A rows.
-// A column-tile group is `pairs` adjacent column tiles, one per CTA pair of a
-// cluster; `pair` selects this pair's.
-__device__ __forceinline__ TileCoord decode_cl(const KParams &p, int t, uint32_t pair, int pairs) {
+__device__ __forceinline__ TileCoord decode(const KParams &p, int t) {
     TileCoord c;
     const int task = p.task_begin + t / p.tiles_per_task;
     const int16_t grp = p.tasks[task].tile_group;
@@ -32,19 +30,19 @@ __device__ __forceinline__ TileCoord decode_cl(const KParams &p, int t, uint32_t
     const int gfirst = task - gpos;
     int u = t - (gfirst - p.task_begin) * p.tiles_per_task;   // tile index inside the group
     const int rows = gsize * p.mtiles_c;                       // row tiles of the group
-    const int per_q = rows * p.ntile_groups;
+    const int per_q = rows * p.ntiles;
     c.q = u / per_q;
     u -= c.q * per_q;
     if (p.q_only >= 0) c.q = p.q_only;   // one chunk per launch: u never reaches a second one
     const int band = p.row_band > 0 && p.row_band < rows ? p.row_band : rows;
     const int full = rows / band;
-    const int in_full = full * band * p.ntile_groups;
+    const int in_full = full * band * p.ntiles;
     int b0, bs;   // first row tile and row tiles of this tile's band
     if (u < in_full) {
-        const int b = u / (band * p.ntile_groups);
+        const int b = u / (band * p.ntiles);
         b0 = b * band;
         bs = band;
-        u -= b * band * p.ntile_groups;
+        u -= b * band * p.ntiles;
     } else {
         b0 = full * band;
         bs = rows - b0;
@@ -55,11 +53,9 @@ __device__ __forceinline__ TileCoord decode_cl(const KParams &p, int t, uint32_t
     const int off = rho / p.mtiles_c;
     c.mt = rho - off * p.mtiles_c;
     c.task = gfirst + off;
-    c.nt = g * pairs + int(pair);
+    c.nt = g;
     return c;
 }
-
-__device__ __forceinline__ TileCoord decode(const KParams &p, int t) { return decode_cl(p, t, 0, 1); }
 
 __device__ __forceinline__ uint32_t *flag_ptr(const KParams &p, int id, int q) {
     return p.flags + size_t(id) * size_t(p.chunks) + size_t(q);

@@ -9,12 +9,8 @@
 // operand bytes per MMA of the single-CTA tile, so a 6-stage ring of 32 KB
 // stages fits in shared memory.
 //
-// A cluster holds one pair (CL = 2) or two pairs (CL = 4).  With two pairs
-// they compute adjacent column tiles of the same rows, so their A tiles are
-// the same: each CTA loads a 64-row quarter of its A half and multicasts it
-// to its counterpart in the other pair, cutting L2 requests by a quarter.
-// Both pairs' MMA commits release every CTA's ring stage, so a multicast
-// never lands in a stage still being read.
+// A cluster is one pair.  Every operand load is an ordinary TMA tile load
+// into the loading CTA's own shared memory; no load is multicast.
 //
 // Tiles are handed out dynamically: a scheduler thread of the cluster leader
 // takes the next tile index from a global counter and publishes it to every
@@ -68,6 +64,7 @@ constexpr int kHalfA = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kHalfB = (kBN / 2) * kBK * 2;  // 16 KB
 constexpr int kFwdPiece = 16384;             // forwarder copy granule
 constexpr int kQueue = 6;                    // tile-index queue depth
+constexpr int CL = 2;                        // CTAs per cluster: one pair
 // RS preload: ring stage ps carries the 32-column fp32 boxes at columns
 // 32*ps and 128 + 32*ps of the tile (slice ps of both epilogue column
 // halves); p.pre_stages of them (2 or 4) precede the K slices.
@@ -75,10 +72,9 @@ constexpr int kPSmemBytes = kPStages * (kHalfA + kHalfB) + 2 * kFwdPiece + 1024 
 
 // Position of this CTA in its cluster.
 struct Cl {
-    uint32_t rank;     // %cluster_ctarank
-    uint32_t pair;     // which CTA pair of the cluster
-    uint32_t pos;      // 0 = pair leader (issues the MMAs), 1 = its peer
-    uint32_t leader;   // cluster rank of this pair's leader
+    uint32_t rank;     // %cluster_ctarank (0 = pair leader, issues the MMAs; 1 = its peer)
+    uint32_t pos;      // same as rank
+    uint32_t leader;   // cluster rank of the pair leader (0)
 };
 
 struct PSmem {
@@ -144,7 +140,7 @@ __device__ __forceinline__ bool ring_wait(const KParams &p, volatile int *abort,
 // LAYOUT bit 0: B is MN-major (W stored [K][n]); bit 1: A is MN-major (A
 // stored [K][rows], rows contiguous -- a transposed activation, as in a
 // weight-gradient GEMM).  An MN-major operand half is two 64-wide boxes.
-template <int LAYOUT, int CL>
+template <int LAYOUT>
 __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &cl) {
     constexpr bool B_MN = (LAYOUT & 1) != 0, A_MN = (LAYOUT & 2) != 0;
     int stage = 0;
@@ -152,13 +148,11 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
     uint32_t issued = 0;   // ring stages filled so far
     // the leader's ring barrier of stage i sits 8*i bytes after stage 0's
     const uint32_t full_leader0 = mapa_shared(smem_u32(&s.full[0]), cl.leader);
-    const uint32_t a_smem0 = smem_u32(s.a0) + (CL == 4 ? cl.pair * (kHalfA / 2) : 0u);
+    const uint32_t a_smem0 = smem_u32(s.a0);
     const uint32_t b_smem0 = smem_u32(s.b0);
-    // bytes per stage for the pair: each CTA's A half (one box, or two
-    // multicast quarters) and B half
-    const uint32_t a_half = uint32_t(p.a_box_rows) * kBK * 2 * (CL == 4 ? 2u : 1u);
+    // bytes per stage for the pair: each CTA's A half (one box) and B half
+    const uint32_t a_half = uint32_t(p.a_box_rows) * kBK * 2;
     const uint32_t tx_pair = 2u * (a_half + kHalfB);
-    const uint16_t mc_mask = uint16_t((1u << cl.rank) | (1u << (cl.rank ^ 2u)));
     auto policy = [](int h) {
         return h == 1 ? policy_evict_last() : h == 2 ? policy_evict_first() : policy_evict_normal();
     };
@@ -225,9 +219,7 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
             if (A_MN) {
                 for (int j = 0; j < kCtaRows / 64; ++j)
                     tma_load_3d_pair_a(sa + uint32_t(j * (64 * kBK * 2)), tm_a, fb, a_row + 64 * j, k0, slab);
-            } else if (CL == 4)
-                tma_load_3d_pair_mc_a(sa, tm_a, fb, k0, a_row, slab, mc_mask);
-            else if (hinted)
+            } else if (hinted)
                 tma_load_3d_pair_hint_a(sa, tm_a, fb, k0, a_row, slab, pol_a);
             else
                 tma_load_3d_pair_a(sa, tm_a, fb, k0, a_row, slab);
@@ -271,7 +263,6 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
 // cluster.  Tile j + 1 is taken once the leader's producer has started
 // loading tile j, so a cluster holds at most one tile beyond the one loading,
 // and none of this sits on the producer's path between two tiles.
-template <int CL>
 __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
     const int cid = int(blockIdx.x) / CL, ncl = int(gridDim.x) / CL;
     int static_next = cid, slot = 0;
@@ -290,7 +281,7 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
         }
         if (t >= total) t = -1;
         TileCoord c = {0, 0, 0, 0};
-        if (t >= 0) c = decode_cl(p, t, 0, CL / 2);
+        if (t >= 0) c = decode(p, t);
         const cm_task &tk = p.tasks[c.task];
         // AG: the tile's A rows arrive by the ring; the producers that read
         // this entry see them (acquire here, release to them by the queue)
@@ -303,7 +294,8 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
                     return;
         // RS preload: the received bucket is read before the partial GEMM, so
         // its producers must be done before this tile is published
-        const bool pre = t >= 0 && p.op == 1 && p.rs_preload && p.pre_stages > 0 && CL == 2 && tk.in_buf[0] >= 0;
+        const bool pre = t >= 0 && p.op == 1 && p.rs_preload && p.pre_stages > 0 && tk.in_buf[0] >= 0 &&
+                         tk.in_buf[0] != tk.out_buf;
         if (pre && tk.wait_in[0] >= 0)
             for (int qq = q0; qq < q0 + nq; ++qq)
                 if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], qq), p.tgt_in, kSiteProducerFlag, c.task, qq))
@@ -314,11 +306,11 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
         const int rr = sum_ranks ? 0 : tk.rank;
         const int nk = kslices(p, tk), sig = p.op == 0 ? tk.sig_done : -1;
         for (uint32_t r = 0; r < uint32_t(CL); ++r) {
-            const int pos = int(r & 1u), pair = int(r >> 1);
-            const int nt = c.nt + pair;   // c.nt is the group's first column tile
+            const int pos = int(r);
+            const int nt = c.nt;
             const int q = p.chunk_pair ? q0 + pos : c.q;   // this CTA's chunk
             const int row0 = p.chunk_pair ? 0 : c.mt * kPairRows + pos * kCtaRows;
-            const int a_row = row0 + (CL == 4 ? pair * (kCtaRows / 2) : 0);
+            const int a_row = row0;
             const int slab = slab0 + q;
             const int n0 = nt * kBN + pos * (kBN / 2);
             int32_t *e = s.qent + kQWords * slot;
@@ -343,7 +335,7 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
     }
 }
 
-template <int LAYOUT, int CL>
+template <int LAYOUT>
 __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     constexpr bool B_MN = (LAYOUT & 1) != 0, A_MN = (LAYOUT & 2) != 0;
     constexpr uint32_t kIdesc = idesc_bf16(kPairRows, kBN, B_MN, A_MN);
@@ -420,7 +412,7 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
             full_ready = mbar_test_wait(s.full + stage, phase);
         }
         if (!ok) break;
-        mma_commit_pair_mc(&s.tfull[accb], uint16_t(3u << (2u * cl.pair)));   // this pair's CTAs
+        mma_commit_pair_mc(&s.tfull[accb], uint16_t((1u << CL) - 1u));   // both CTAs' accumulators
         // AG: both CTAs' A slices of this tile have landed; the slot rows may be reused
         if (c.sig >= 0) {
             red_release_add(flag_ptr(p, c.sig, c.q), 1u);
@@ -435,7 +427,6 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
     drain_mbar<true>(p, s.drain, 0);
 }
 
-template <int CL>
 __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
     QueueReader qr;
     qr.init(s);
@@ -448,7 +439,7 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
         const QTile c = qr.next(p, s, true);
         if (c.t < 0 || *s.abort) break;
         const cm_task &tk = p.tasks[c.task];
-        if (!(tk.fwd_slot[0] >= 0 || tk.fwd_slot[1] >= 0) || c.nt >= p.ntiles) continue;
+        if (!(tk.fwd_slot[0] >= 0 || tk.fwd_slot[1] >= 0)) continue;
         bool ok = true;
         if (tk.a_src == 1 && tk.wait_in[0] >= 0)   // the shard chunk has arrived here
             ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteForwardFlag, c.task, c.q);
@@ -478,8 +469,14 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
                     bulk_load(s.fbuf[b ^ 1], src + int64_t(i + 1) * kFwdPiece, piece(i + 1), &s.fbar[b ^ 1]);
                 }
                 ok = wait_mbar<false>(p, s.abort, &s.fbar[b], fph[b], kSiteForwardFull, c.task, c.q);
+                if (!ok) {
+                    // leaving early: piece i, and piece i + 1 if it was
+                    // requested, may still be landing in this CTA's buffers
+                    drain_mbar<false>(p, &s.fbar[b], fph[b]);
+                    if (i + 1 < np) drain_mbar<false>(p, &s.fbar[b ^ 1], fph[b ^ 1]);
+                    break;
+                }
                 fph[b] ^= 1u;
-                if (!ok) break;
                 for (int j = 0; j < 2; ++j)
                     if (dst[j]) bulk_store(dst[j] + int64_t(i) * kFwdPiece, s.fbuf[b], piece(i));
                 bulk_commit();
@@ -525,7 +522,6 @@ __device__ __forceinline__ void ag_store_slice(const KParams &p, const cm_task &
 
 // AllGather -> GEMM epilogue: each warp reads its 32 TMEM lanes x 128
 // columns in 32-column slices and stores them into the shard's rows of Y_r.
-template <int CL>
 __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     const int e = int(threadIdx.x) / 32 - 4;   // 0..7
     const int lane = int(threadIdx.x) & 31;
@@ -580,12 +576,16 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
 // 16-byte chunk j of row r sits at chunk position j ^ (r & 7).
 __device__ __forceinline__ float4 *swz_row(uint8_t *buf, int row) { return reinterpret_cast<float4 *>(buf + row * 128); }
 
-// GEMM -> ReduceScatter epilogue.  The circulating fp32 bucket moves through
-// shared memory by TMA: per 32-column slice each warp loads the received
-// partial bucket(s) for its 32 rows (one 4 KB box), adds the TMEM slice, and
-// TMA-stores the sum to the next rank's receive buffer -- or, at the owner,
-// rounds it into the output.
-template <int CL>
+// GEMM -> ReduceScatter epilogue, per 32-column slice of each warp's 32 rows
+// (one 4 KB fp32 box staged in shared memory):
+//  - a bucket kept in place (in_buf[0] == out_buf): the TMEM slice is added
+//    into the bucket where it lies with a TMA reduce-add, so nothing comes
+//    back to the SM;
+//  - the first contributor (no input): the slice is TMA-stored as the bucket;
+//  - a bucket in per-step buffers: the received partial bucket is TMA-loaded,
+//    the slice added, and the sum TMA-stored to the next rank's buffer;
+//  - the owner: the received partial bucket(s) are TMA-loaded, the slice
+//    added, and the sum rounded into the output.
 __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     const int e = int(threadIdx.x) / 32 - 4;   // 0..7
     const int lane = int(threadIdx.x) & 31;
@@ -596,7 +596,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
     uint8_t *buf = s.fbuf[0] + e * 4096;
     uint64_t *eb = &s.ebar[e];
     uint32_t eph = 0;
-    bool store_pending = false;   // lane 0: a TMA store may still be reading buf
+    bool store_pending = false;   // lane 0: a TMA store / reduce may still be reading buf
     QueueReader qr;
     if (lane == 0) qr.init(s);
     int accb = 0;
@@ -616,8 +616,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
                                                               // already in the accumulator
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
-        const bool real = c.nt < p.ntiles;   // a cluster's second pair may have no column tile
-        if (leader_thread && !bad && real) {
+        if (leader_thread && !bad) {
             for (int j = 0; j < 2 && !bad; ++j)
                 if (tk.wait_in[j] >= 0)
                     bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q), p.tgt_in, kSiteEpilogueFlag, c.task,
@@ -635,6 +634,9 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         const int row = row_w + lane;
         const bool row_ok = row < p.rows_c;
         const int64_t crow = int64_t(c.q) * p.rows_c + row;
+        // the bucket is accumulated where it lies: its partial sum is not read here
+        const bool in_place = tk.out_buf >= 0 && tk.in_buf[0] == tk.out_buf;
+        bool skip = false;   // a bucket load failed (the kernel is aborting): no further copies this tile
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
             const int col_local = half * 128 + cb * 32;
@@ -642,12 +644,12 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
             uint32_t v[32];
             tmem_ld32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN + col_local), v);
             tmem_wait_ld();
-            if (col0 >= p.n) continue;   // the whole slice lies past the last column
+            if (skip || col0 >= p.n) continue;   // aborting, or the whole slice lies past the last column
             float f[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) f[i] = __uint_as_float(v[i]);
-            for (int j = 0; j < 2; ++j) {
-                if (tk.in_buf[j] < 0 || (j == 0 && pre >= 0 && cb < p.pre_stages)) continue;
+            for (int j = 0; j < 2 && !skip; ++j) {
+                if (tk.in_buf[j] < 0 || (j == 0 && (in_place || (pre >= 0 && cb < p.pre_stages)))) continue;
                 if (lane == 0) {
                     if (store_pending) {
                         bulk_wait_read<0>();
@@ -656,13 +658,20 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
                     mbar_expect_tx(eb, 32 * 32 * 4);
                     tma_load_3d(buf, &p.tmAcc, eb, col0, row_w, tk.in_buf[j] * p.chunks + c.q);
                 }
-                wait_mbar<false>(p, s.abort, eb, eph, kSiteEpilogueFlag, c.task, c.q);
+                const bool landed = wait_mbar<false>(p, s.abort, eb, eph, kSiteEpilogueFlag, c.task, c.q);
+                if (__any_sync(0xffffffffu, !landed)) {
+                    // the load may still be landing in buf: wait for it (bounded) and stop
+                    if (lane == 0) drain_mbar<false>(p, eb, eph);
+                    skip = true;
+                }
                 eph ^= 1u;
+                if (skip) break;
                 float4 *r = swz_row(buf, lane);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) add4(f + 4 * i, r[i ^ (lane & 7)]);
                 __syncwarp();
             }
+            if (skip) continue;
             if (tk.out_buf >= 0) {
                 if (lane == 0 && store_pending) {
                     bulk_wait_read<0>();
@@ -675,7 +684,11 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    tma_store_3d(&p.tmAcc, buf, col0, row_w, tk.out_buf * p.chunks + c.q);
+                    const int slab = tk.out_buf * p.chunks + c.q;
+                    if (in_place)
+                        tma_reduce_add_3d(&p.tmAcc, buf, col0, row_w, slab);
+                    else
+                        tma_store_3d(&p.tmAcc, buf, col0, row_w, slab);
                     bulk_commit();
                     store_pending = true;
                 }
@@ -712,15 +725,15 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * uint32_t(accb));
-        if (tk.sig_done >= 0 && real) {
+        if (tk.sig_done >= 0) {
             if (lane == 0) {
-                bulk_wait<0>();            // this warp's bucket slices are in global memory
+                bulk_wait<0>();            // this warp's bucket slices (stores or adds) are done in global memory
                 store_pending = false;
                 fence_proxy_async_global();
             }
             __threadfence();
             bar_sync(1, kPEpiWarps * 32);
-            if (leader_thread) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
+            if (leader_thread && !*s.abort) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
         }
         if (++accb == 2) {
             accb = 0;
@@ -730,7 +743,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
     if (lane == 0) bulk_wait<0>();
 }
 
-template <int LAYOUT, int CL>
+template <int LAYOUT>
 __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_constant__ KParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -757,13 +770,12 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     const int warp = int(threadIdx.x) >> 5, lane = int(threadIdx.x) & 31;
     Cl cl;
     cl.rank = cluster_ctarank();
-    cl.pair = cl.rank >> 1;
-    cl.pos = cl.rank & 1u;
-    cl.leader = cl.rank & ~1u;
+    cl.pos = cl.rank;
+    cl.leader = 0;
     if (threadIdx.x == 0) {
         for (int i = 0; i < kPStages; ++i) {
             mbar_init(&s.full[i], 1);
-            mbar_init(&s.empty[i], CL / 2);   // the commit of every pair's MMA
+            mbar_init(&s.empty[i], 1);   // the pair MMA's commit
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.tfull[i], 1);
@@ -772,7 +784,7 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
         }
         mbar_init(s.drain, 1);
         mbar_init(s.started, 1);
-        // queue slot releases: 8 epilogue warps per CTA and (AG) every forwarder
+        // queue slot releases: 8 epilogue warps per CTA and (AG) both forwarders
         const uint32_t readers = CL * kPEpiWarps + (p.op == 0 ? CL : 0);
         for (int i = 0; i < kQueue; ++i) {
             mbar_init(&s.qfull[i], 1);
@@ -815,22 +827,22 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     }
 
     if (warp == 0) {
-        if (lane == 0) producer<LAYOUT, CL>(p, s, total, cl);
+        if (lane == 0) producer<LAYOUT>(p, s, total, cl);
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && cl.pos == 0) mma_issuer<LAYOUT, CL>(p, s, tmem_base, cl);
+        if (lane == 0 && cl.pos == 0) mma_issuer<LAYOUT>(p, s, tmem_base, cl);
         __syncwarp();
     } else if (warp == 2) {
-        if (lane == 0 && p.op == 0) forwarder<CL>(p, s, cl);
+        if (lane == 0 && p.op == 0) forwarder(p, s, cl);
         __syncwarp();
     } else if (warp == 3) {
-        if (lane == 0 && cl.rank == 0) scheduler<CL>(p, s, total);
+        if (lane == 0 && cl.rank == 0) scheduler(p, s, total);
         __syncwarp();
     } else if (warp >= 4) {
         if (p.op == 0)
-            epilogue_ag<CL>(p, s, tmem_base, cl);
+            epilogue_ag(p, s, tmem_base, cl);
         else
-            epilogue_rs<CL>(p, s, tmem_base, cl);
+            epilogue_rs(p, s, tmem_base, cl);
     }
     tc_fence_before();
     __syncthreads();
@@ -843,11 +855,9 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
 }
 
 
-template <int CL>
 cudaError_t prepare_one(int device, int *max_clusters) {
-    // layouts built for this cluster size: K-major / MN-major B, and (one pair
-    // per cluster) both operands MN-major
-    void (*fns[3])(KParams) = {cm_pair_kernel<0, CL>, cm_pair_kernel<1, CL>, cm_pair_kernel<CL == 2 ? 3 : 1, CL>};
+    // layouts: K-major / MN-major B, and both operands MN-major
+    void (*fns[3])(KParams) = {cm_pair_kernel<0>, cm_pair_kernel<1>, cm_pair_kernel<3>};
     for (auto fn : fns) {
         cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kPSmemBytes);
         if (e != cudaSuccess) return e;
@@ -867,14 +877,30 @@ cudaError_t prepare_one(int device, int *max_clusters) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, cm_pair_kernel<0, CL>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&n, cm_pair_kernel<0>, &cfg);
     if (e != cudaSuccess) return e;
     *max_clusters = n;
     return cudaSuccess;
 }
 
-template <int CL>
-cudaError_t launch_one(const KParams &p, int layout, int clusters, cudaStream_t stream) {
+}  // namespace
+
+int pair_rows() { return kPairRows; }
+
+cudaError_t prepare_pair(int device, int *max_clusters) {
+    static int cached[64] = {0};
+    if (device < 0 || device >= 64) return cudaErrorInvalidValue;
+    if (cached[device] == 0) {
+        int n = 0;
+        cudaError_t e = prepare_one(device, &n);
+        if (e != cudaSuccess) return e;
+        cached[device] = n > 0 ? n : -1;
+    }
+    *max_clusters = cached[device] > 0 ? cached[device] : 0;
+    return cudaSuccess;
+}
+
+cudaError_t launch_pair(const KParams &p, int layout, int clusters, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(unsigned(CL * clusters), 1, 1);
     cfg.blockDim = dim3(kPThreads, 1, 1);
@@ -888,36 +914,11 @@ cudaError_t launch_one(const KParams &p, int layout, int clusters, cudaStream_t 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     switch (layout) {
-        case 0: return cudaLaunchKernelEx(&cfg, cm_pair_kernel<0, CL>, p);
-        case 1: return cudaLaunchKernelEx(&cfg, cm_pair_kernel<1, CL>, p);
-        case 3:
-            if (CL == 2) return cudaLaunchKernelEx(&cfg, cm_pair_kernel<CL == 2 ? 3 : 1, CL>, p);
-            return cudaErrorInvalidValue;   // both operands MN-major: one pair per cluster only
+        case 0: return cudaLaunchKernelEx(&cfg, cm_pair_kernel<0>, p);
+        case 1: return cudaLaunchKernelEx(&cfg, cm_pair_kernel<1>, p);
+        case 3: return cudaLaunchKernelEx(&cfg, cm_pair_kernel<3>, p);
         default: return cudaErrorInvalidValue;
     }
-}
-
-}  // namespace
-
-int pair_rows() { return kPairRows; }
-
-cudaError_t prepare_pair(int device, int cluster_ctas, int *max_clusters) {
-    static int cached[64][2] = {{0}};
-    if (device < 0 || device >= 64 || (cluster_ctas != 2 && cluster_ctas != 4)) return cudaErrorInvalidValue;
-    const int k = cluster_ctas == 4;
-    if (cached[device][k] == 0) {
-        int n = 0;
-        cudaError_t e = cluster_ctas == 4 ? prepare_one<4>(device, &n) : prepare_one<2>(device, &n);
-        if (e != cudaSuccess) return e;
-        cached[device][k] = n > 0 ? n : -1;
-    }
-    *max_clusters = cached[device][k] > 0 ? cached[device][k] : 0;
-    return cudaSuccess;
-}
-
-cudaError_t launch_pair(const KParams &p, int layout, int cluster_ctas, int clusters, cudaStream_t stream) {
-    if (cluster_ctas == 4) return launch_one<4>(p, layout, clusters, stream);
-    return launch_one<2>(p, layout, clusters, stream);
 }
 
 }  // namespace cm

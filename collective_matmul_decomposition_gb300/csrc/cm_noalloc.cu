@@ -19,6 +19,9 @@
 //    can overlap on the GPU (different streams, no ordering) race on it.
 //  - A problem whose scratch exceeds the array is rejected with
 //    CM_ERR_WORKSPACE before any device work.
+//  - The array's status word records a device-side wait that timed out in
+//    the last call; cm_ag_gemm_noalloc_check_status reads it (with the same
+//    device current), as cm_check_status does for a caller's workspace.
 //  - Nothing here calls cudaMalloc, cudaFree or an allocating library routine.
 #include <cuda_runtime.h>
 
@@ -60,4 +63,11 @@ extern "C" cm_status cm_ag_gemm_noalloc(cm_plan_t plan, const void *x, const voi
     const cm_status st = scratch_address(&ws);
     if (st != CM_OK) return st;
     return cm_ag_gemm(plan, x, w, wlayout, y, y_dtype, m, K, n, ws, need, stream);
+}
+
+extern "C" cm_status cm_ag_gemm_noalloc_check_status(cm_stream_t stream, int32_t info[4]) {
+    void *ws = nullptr;
+    const cm_status st = scratch_address(&ws);
+    if (st != CM_OK) return st;
+    return cm_check_status(ws, stream, info);
 }

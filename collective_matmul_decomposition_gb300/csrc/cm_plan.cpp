@@ -16,12 +16,17 @@
 //     the owner adds both partials and its own product (the realigning add).
 //
 // Task table: one task per (rank, step, stream) that multiplies.  Every
-// (rank, stream, step) has its own receive slot (AG) or accumulator buffer
-// (RS), written once, so the only dependency is readiness: task (r, i) needs
-// what its ring predecessor produced at step i-1.  Every flag a task waits on
-// is signalled by a task earlier in the table, which makes the in-order tile
-// hand-out of the kernels free of deadlock (the earliest unfinished tile
-// never waits).
+// (rank, stream, step) has its own receive slot (AG), written once.  RS
+// buckets live either in one fp32 buffer per (bucket, stream) that every
+// contributor after the first accumulates into in place (in_buf[0] ==
+// out_buf: the kernels add their partial product to it where it lies), or --
+// CM_OPT_RS_IN_PLACE = 0 -- in one buffer per (rank, stream, step), written
+// once and read by the next rank.  Either way the only dependency is
+// readiness: task (r, i) needs what its ring predecessor produced at step
+// i-1, and that predecessor is the buffer's only other user at the time.
+// Every flag a task waits on is signalled by a task earlier in the table,
+// which makes the in-order tile hand-out of the kernels free of deadlock (the
+// earliest unfinished tile never waits).
 //
 // Order.  One ring (uni): rank-blocked --
 //   (0,0) | (1,0..1) | (2,0..2) | ... | (N-1,0..N-1) | (0,1..N-1) | (1,2..N-1) | ...
@@ -227,7 +232,13 @@ void build_rs_tasks(PlanImpl &p) {
     Ids ids{N, S};
     p.flag_ids[CM_OP_GEMM_RS] = N * S * 2;
     std::vector<cm_task> tasks;
-    auto acc = [&](int r, int d, int step) { return (r * D + d) * S + step; };   // written once
+    // accumulator buffer that (rank r, stream d, step) reads and a step-i
+    // contributor to bucket o writes: one per bucket and stream (in place),
+    // or one per (rank, stream, step) (written once)
+    const bool in_place = p.rs_in_place != 0;
+    auto acc = [&](int r, int d, int step, int bucket) {
+        return in_place ? bucket * D + d : (r * D + d) * S + step;
+    };
     if (p.dir == CM_RING_NONE) {
         for (int o = 0; o < N; ++o) {
             cm_task t = blank_task(o, 0, 0);
@@ -246,27 +257,30 @@ void build_rs_tasks(PlanImpl &p) {
                     t.a_src = 0; t.a_slab = int16_t(r * N + e.obj); t.out_idx = int16_t(e.obj);
                     t.sig_done = int16_t(ids.fid(kFlagDone, r, i, d));
                     const bool owner = e.dst < 0;
+                    const int o = e.obj;
                     if (!owner) {
                         // partial bucket goes to the next rank of this stream
-                        t.out_buf = int16_t(acc(e.dst, d, i + 1));
+                        // (in place: the bucket's one buffer, which this
+                        // task starts at step 0 and adds to after that)
+                        t.out_buf = int16_t(acc(e.dst, d, i + 1, o));
                         if (i > 0) {
-                            t.in_buf[0] = int16_t(acc(r, d, i));
+                            t.in_buf[0] = int16_t(acc(r, d, i, o));
                             t.wait_in[0] = int16_t(ids.fid(kFlagDone, e.src, i - 1, d));
                         }
                     } else if (p.dir == CM_RING_UNI) {
                         if (i > 0) {
-                            t.in_buf[0] = int16_t(acc(r, 0, i));
+                            t.in_buf[0] = int16_t(acc(r, 0, i, o));
                             t.wait_in[0] = int16_t(ids.fid(kFlagDone, e.src, i - 1, 0));
                         }
                     } else {
                         // realigning addition: clockwise partial arrived at step a,
                         // counter-clockwise partial at step b
                         if (a >= 1) {
-                            t.in_buf[0] = int16_t(acc(r, 0, a));
+                            t.in_buf[0] = int16_t(acc(r, 0, a, o));
                             t.wait_in[0] = int16_t(ids.fid(kFlagDone, md(r - 1, N), a - 1, 0));
                         }
                         if (b >= 1) {
-                            t.in_buf[1] = int16_t(acc(r, 1, b));
+                            t.in_buf[1] = int16_t(acc(r, 1, b, o));
                             t.wait_in[1] = int16_t(ids.fid(kFlagDone, md(r + 1, N), b - 1, 1));
                         }
                     }
@@ -378,7 +392,7 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
             p.grid = int(value);
             return CM_OK;
         case CM_OPT_KERNEL:
-            if (value < 0 || value > 3) return CM_ERR_INVALID_ARG;
+            if (value < 0 || value > 2) return CM_ERR_INVALID_ARG;
             p.kernel = int(value);
             return CM_OK;
         case CM_OPT_TILE_GROUP:
@@ -412,6 +426,15 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
             return CM_OK;
         case CM_OPT_STATIC_TILES:
             p.static_tiles = value != 0;
+            return CM_OK;
+        case CM_OPT_RS_IN_PLACE:
+            if (value != 0 && value != 1) return CM_ERR_INVALID_ARG;
+            p.rs_in_place = int(value);
+            try {
+                cm::rebuild(p);
+            } catch (...) {
+                return CM_ERR_INVALID_ARG;
+            }
             return CM_OK;
         case CM_OPT_SKIP_SIGNAL:
             p.skip_signal = value < 0 ? -1 : value;

@@ -163,9 +163,10 @@ int cm_plan_tasks(cm_plan_t plan, cm_op op, cm_task *out, int capacity);
  * Workspace bytes for one call; 0 for a bad plan or a non-positive size.
  * Holds a 256-byte status block (status word, tile counters), the per-chunk
  * flags and, for a ring with N > 1: for AG, one receive slot per (rank, ring
- * stream, step), each [m][K] bf16; for RS, one fp32 accumulator per (rank,
- * ring stream, step), each [M/N][n].  Every slot is written once per call, so
- * no task waits for one to be freed.  The caller allocates it (256-byte
+ * stream, step), each [m][K] bf16, written once per call, so no task waits
+ * for one to be freed; for RS, one fp32 accumulator [M/N][n] per (bucket,
+ * ring stream) -- or per (rank, ring stream, step) with CM_OPT_RS_IN_PLACE =
+ * 0.  The caller allocates it (256-byte
  * aligned) and owns it; its contents need no initialisation (each call clears
  * the status block and flags with one memset on its stream).  Calls that
  * share a workspace must be ordered on the GPU (one stream).
@@ -312,9 +313,8 @@ const char *cm_status_string(cm_status status);
  *                        its consumers time out.  -1 clears it.
  *  CM_OPT_KERNEL         tile kernel.  0 (default) and 2: 256 x 256 tiles on
  *                        CTA pairs (tcgen05 cta_group::2), one pair per
- *                        cluster; 1: 128 x 256 tiles on single CTAs; 3: CTA
- *                        pairs, two pairs per cluster sharing the A tile by
- *                        TMA multicast.
+ *                        cluster; 1: 128 x 256 tiles on single CTAs.  Other
+ *                        values: CM_ERR_INVALID_ARG.
  *  CM_OPT_STATIC_TILES   CTA-pair kernel: 0 (default) hands tiles out in
  *                        order from a global counter as clusters free up;
  *                        1 gives cluster c the tiles c, c + clusters, ...
@@ -347,7 +347,21 @@ const char *cm_status_string(cm_status status);
  *                        (k <= 512), where the epilogue sets the pace, and
  *                        none beyond (the epilogue then hides under the
  *                        partial GEMM).  The same sum, in a different fp32
- *                        order.
+ *                        order.  Buckets accumulated in place (below) are
+ *                        never preloaded: only the owner's tile, which reads
+ *                        its bucket, can be.
+ *  CM_OPT_RS_IN_PLACE    cm_gemm_rs (and the backward pair's data gradient)
+ *                        on a ring: 1 (default) keeps each bucket in one fp32
+ *                        buffer per ring stream that the first contributor
+ *                        writes and every later one adds its partial product
+ *                        into where it lies (a TMA reduce-add at L2 on the
+ *                        CTA-pair kernel), in ring order, each after its
+ *                        predecessor's flag; 0 gives every (rank, stream,
+ *                        step) its own buffer, written once by the previous
+ *                        rank and read by the next.  The same fp32 sums in
+ *                        the same order.  Changes the workspace size (N
+ *                        buffers per stream instead of N per stream and
+ *                        step), so size the workspace after setting it.
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
@@ -361,7 +375,8 @@ typedef enum cm_option {
     CM_OPT_L2_PROMOTION = 8,
     CM_OPT_ROW_BAND = 9,
     CM_OPT_BULK_OVERLAP = 10,
-    CM_OPT_RS_PRELOAD = 11
+    CM_OPT_RS_PRELOAD = 11,
+    CM_OPT_RS_IN_PLACE = 12
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);
@@ -427,14 +442,27 @@ const char *cm_version(void);
  *  The first call on a device looks up the array's address with that device
  *  current; make it outside any stream capture.  Every call shares the array:
  *  its status word, flags and counters are cleared on `stream` at the start
- *  of each call, and calls that may overlap on the GPU race on it.  Only
- *  argument and launch errors are returned; the array's device status word
- *  is not exposed, so a device-side wait that expires (which leaves the
- *  outputs undefined) is not reported to this caller.  Never allocates.
+ *  of each call, and calls that may overlap on the GPU race on it.  Argument
+ *  and launch errors are returned; a device-side wait that expires (which
+ *  leaves the outputs undefined) is recorded in the array's status word, which
+ *  cm_ag_gemm_noalloc_check_status reads.  Never allocates.
  */
 #define CM_NOALLOC_SCRATCH_BYTES (64u << 20)
 cm_status cm_ag_gemm_noalloc(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y,
                              cm_dtype y_dtype, int64_t m, int64_t K, int64_t n, cm_stream_t stream);
+
+/*
+ * cm_ag_gemm_noalloc_check_status -- cm_check_status for the allocation-free
+ * entry point: synchronise `stream` and read the status word of the last
+ * cm_ag_gemm_noalloc call on the current device (the library's scratch array
+ * is that call's workspace).  Returns CM_OK, CM_ERR_TIMEOUT (a bounded wait
+ * expired; that call's outputs are undefined) or CM_ERR_CUDA; info as for
+ * cm_check_status.  Call it with the same device current as the call it
+ * checks.  Never allocates.  No counterpart on the pages: like the entry
+ * point it checks, it only repackages the library for callers that cannot
+ * allocate.
+ */
+cm_status cm_ag_gemm_noalloc_check_status(cm_stream_t stream, int32_t info[4]);
 
 #ifdef __cplusplus
 }

@@ -56,7 +56,8 @@ def test_plan_arguments(lib):
     for opt, bad in ((cm.CM_OPT_L2_HINTS, -1), (cm.CM_OPT_L2_HINTS, 256),
                      (cm.CM_OPT_L2_PROMOTION, -1), (cm.CM_OPT_L2_PROMOTION, 4),
                      (cm.CM_OPT_ROW_BAND, -1), (cm.CM_OPT_ROW_BAND, 4097),
-                     (cm.CM_OPT_RS_PRELOAD, -1), (cm.CM_OPT_RS_PRELOAD, 4)):
+                     (cm.CM_OPT_RS_PRELOAD, -1), (cm.CM_OPT_RS_PRELOAD, 4),
+                     (cm.CM_OPT_KERNEL, -1), (cm.CM_OPT_KERNEL, 3)):
         with pytest.raises(cm.CMError):
             p.set_option(opt, bad)
     for v in (0, 1, 2, 3):
@@ -77,7 +78,12 @@ def test_workspace_sizes(lib):
     p = cm.Plan(8, 1, "uni")
     m, K = 1024, 8192
     assert p.ag_workspace_size(m, K) >= 2 * 8 * m * K * 2
-    assert p.rs_workspace_size(8192, 8192) >= 2 * 8 * 1024 * 8192 * 4
+    # RS buckets in place: one [M/N][n] fp32 buffer per bucket
+    assert 8 * 1024 * 8192 * 4 <= p.rs_workspace_size(8192, 8192) < 9 * 1024 * 8192 * 4
+    p.set_option(cm.CM_OPT_RS_IN_PLACE, 0)     # one per (rank, step)
+    assert p.rs_workspace_size(8192, 8192) >= 8 * 8 * 1024 * 8192 * 4
+    with pytest.raises(cm.CMError):
+        p.set_option(cm.CM_OPT_RS_IN_PLACE, 2)
     b = cm.Plan(8, 1, "bidi")
     assert b.ag_workspace_size(m, K) >= 4 * 8 * m * K * 2
     assert cm.Plan(8, 1, "none").ag_workspace_size(m, K) < 1 << 20
@@ -135,3 +141,14 @@ def test_no_oracle_in_product_path():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "cm_oracle" not in text, f
+
+
+def test_no_multicast_load_in_the_kernels():
+    """No TMA load of the library is a cluster-multicast load: every operand
+    tile is loaded into the loading CTA's own shared memory.  (The tcgen05
+    commit that arrives on both CTAs' barriers is not a load.)"""
+    csrc = os.path.join(ROOT, "collective_matmul_decomposition_gb300", "csrc")
+    for f in os.listdir(csrc):
+        for line in open(os.path.join(csrc, f)):
+            if "multicast::cluster" in line:
+                assert "cp.async" not in line and "tcgen05.commit" in line, (f, line)

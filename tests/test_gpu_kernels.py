@@ -1,6 +1,5 @@
-"""Every tile kernel -- CTA pairs (tcgen05 cta_group::2) with one or two pairs
-per cluster (two pairs share the A tile by TMA multicast), and single CTAs --
-against the oracle and against each other."""
+"""Every tile kernel -- CTA pairs (tcgen05 cta_group::2, one pair per
+cluster) and single CTAs -- against the oracle and against each other."""
 
 import numpy as np
 import pytest
@@ -13,8 +12,8 @@ from test_gpu_parity import TOL_F32, _np, run_ag, run_rs
 
 pytestmark = pytest.mark.gpu
 
-PAIR, SINGLE, PAIR_CL2, PAIR_CL4 = 0, 1, 2, 3
-KERNELS = [PAIR, SINGLE, PAIR_CL2, PAIR_CL4]
+PAIR, SINGLE, PAIR_CL2 = 0, 1, 2
+KERNELS = [PAIR, SINGLE, PAIR_CL2]
 
 
 def _plan(N, chunks, direction, kernel):
@@ -28,8 +27,8 @@ def _plan(N, chunks, direction, kernel):
     (2, 64, 256, 512, 1, "uni"),        # rows per chunk below one CTA's 128
     (3, 200, 200, 296, 2, "bidi"),      # ragged rows / columns / K
     (4, 384, 320, 768, 1, "uni"),       # row tiles straddling the pair split; 3 column tiles
-    (5, 136, 72, 520, 1, "none"),       # odd column-tile count: a cluster's second pair idles
-    (2, 48, 64, 256, 1, "uni"),         # rows below one multicast quarter, one column tile
+    (5, 136, 72, 520, 1, "none"),       # odd column-tile count
+    (2, 48, 64, 256, 1, "uni"),         # rows below half a CTA's 128, one column tile
 ])
 @pytest.mark.parametrize("layout", ["nk", "kn"])
 def test_kernel_vs_oracle(kernel, N, m, K, n, chunks, direction, layout):
@@ -47,7 +46,7 @@ def test_kernels_agree_bitwise_on_ag():
     N, m, K, n = 4, 512, 1024, 1280
     x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=99, w_layout="nk")
     base, _, _ = run_ag(_plan(N, 1, "uni", SINGLE), x, w, "nk")
-    for k in (PAIR, PAIR_CL2, PAIR_CL4):
+    for k in (PAIR, PAIR_CL2):
         y, _, _ = run_ag(_plan(N, 1, "uni", k), x, w, "nk")
         assert torch.equal(y, base), k
 
@@ -69,7 +68,7 @@ def test_l2_options_change_no_bits(hints, promotion):
     assert torch.equal(yr, base_r)
 
 
-@pytest.mark.parametrize("kernel", [PAIR, SINGLE, PAIR_CL4])
+@pytest.mark.parametrize("kernel", [PAIR, SINGLE])
 @pytest.mark.parametrize("band", [1, 3])
 def test_row_bands_change_no_bits(kernel, band):
     """The row-band tile order only reorders tiles: same bits out."""
@@ -115,3 +114,4 @@ def test_timeout_each_kernel(kernel):
     ref = oracle.ag_gemm(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
     y, _, _ = run_ag(p, x, w, "nk")
     assert oracle.normwise_max_rel_err(_np(y), ref) <= TOL_F32
+

@@ -132,13 +132,55 @@ def test_tile_groups(group):
 
 
 def test_slots_written_once():
-    """Every receive slot (AG) and accumulator buffer (RS) has one writer."""
+    """Every receive slot (AG) has one writer; so does every RS accumulator
+    buffer when buckets live in per-step buffers."""
     for d in ("uni", "bidi"):
         p = cm.Plan(8, 1, d)
         ag = [s_ for t in p.tasks(AG) for s_ in t.fwd_slot if s_ >= 0]
         assert len(ag) == len(set(ag))
+        p.set_option(cm.CM_OPT_RS_IN_PLACE, 0)
         rs = [t.out_buf for t in p.tasks(RS) if t.out_buf >= 0]
         assert len(rs) == len(set(rs))
+        assert all(t.in_buf[0] != t.out_buf or t.out_buf < 0 for t in p.tasks(RS))
+
+
+@pytest.mark.parametrize("N", [2, 3, 4, 5, 8, 16])
+@pytest.mark.parametrize("direction", ["uni", "bidi"])
+def test_in_place_buckets_form_one_chain_each(N, direction):
+    """Buckets accumulated in place: each (bucket, stream) buffer is started by
+    one task (no input), then updated in place (in_buf[0] == out_buf) by one
+    task per later ring step, each waiting on its predecessor's flag, and read
+    by the owner last -- a chain along the ring, one rank at a time."""
+    p = cm.Plan(N, 1, direction)
+    tasks = p.tasks(RS)
+    streams = 2 if direction == "bidi" else 1
+    users = {}
+    for t in tasks:
+        if t.out_buf >= 0:
+            assert t.in_buf[1] < 0
+            assert t.in_buf[0] in (-1, t.out_buf)
+            assert t.out_buf // streams == t.out_idx and t.out_buf % streams == t.stream
+            users.setdefault(t.out_buf, []).append(t)
+        else:
+            for j in range(2):
+                if t.in_buf[j] >= 0:
+                    assert t.in_buf[j] // streams == t.out_idx == t.rank
+                    users.setdefault(t.in_buf[j], []).append(t)
+    bufs_per_stream = set(b for b in users)
+    assert len(bufs_per_stream) <= N * streams
+    sig_of = {t.sig_done: t for t in tasks if t.sig_done >= 0}
+    for b, ts in users.items():
+        chain = sorted(ts, key=lambda t: t.step)
+        # contributors at steps 0, 1, ...; the owner (step a of a two-way ring) last
+        assert [t.step for t in chain[:-1]] == list(range(len(chain) - 1))
+        assert chain[-1].step > chain[-2].step if len(chain) > 1 else True
+        assert chain[0].in_buf[0] == -1 and chain[0].wait_in[0] < 0 and chain[0].out_buf == b
+        for prev, cur in zip(chain, chain[1:]):
+            j = 0 if cur.out_buf >= 0 or cur.in_buf[0] == b else 1
+            assert cur.wait_in[j] == prev.sig_done and sig_of[prev.sig_done] is prev
+        ranks = [t.rank for t in chain]
+        assert len(set(ranks)) == len(ranks)
+        assert chain[-1].out_buf < 0 and chain[-1].rank == b // streams   # the owner reads it last
 
 
 def kernel_tile_order(tasks, c, mtiles, ntiles, band=0):
@@ -264,9 +306,13 @@ def _simulate(p, op, mtiles, ntiles, grid, seed, band=0):
 @pytest.mark.parametrize("chunks", [1, 2, 4])
 @pytest.mark.parametrize("grid", [1, 3, 16])
 @pytest.mark.parametrize("group", [1, 4])
-def test_protocol_simulation(N, direction, chunks, grid, group):
+@pytest.mark.parametrize("in_place", [1, 0])
+def test_protocol_simulation(N, direction, chunks, grid, group, in_place):
+    if not in_place and (grid == 3 or group == 1):
+        pytest.skip("per-step RS buffers: a subset of the grid")
     p = cm.Plan(N, chunks, direction)
     p.set_option(cm.CM_OPT_TILE_GROUP, group)
+    p.set_option(cm.CM_OPT_RS_IN_PLACE, in_place)
     c = p.chunks
     mtiles, ntiles = 2, 2
     for seed in range(3):
@@ -321,8 +367,9 @@ def test_skip_signal_starves_consumer():
 @pytest.mark.parametrize("which", ["wait_in"])
 def test_simulation_catches_a_missing_wait(op, which):
     """Planted mistake: a task table without its readiness waits must fail
-    the simulation for some interleaving (slots are written once, so
-    readiness is the only dependency)."""
+    the simulation for some interleaving (readiness is the only dependency:
+    AG slots are written once, and an in-place bucket's predecessor is its
+    only other user)."""
     p = cm.Plan(5, 1, "uni")
     real = p.tasks
 
