@@ -113,7 +113,7 @@ def test_worked_examples_on_gpu(direction):
     x = pad(g["x"], (N, m, 8))
     w = pad(g["w"], (N, 8, 8))             # [K][n] per rank
     plan = cm.Plan(N, 1, direction)
-    ws = torch.empty(plan.ag_workspace_size(m, 8), dtype=torch.uint8, device=dev)
+    ws = torch.full((plan.ag_workspace_size(m, 8),), 0xFF, dtype=torch.uint8, device=dev)
     y = torch.full((N, N * m, 8), float("nan"), dtype=torch.float32, device=dev)
     cm.cm_ag_gemm(plan, x, w, y, ws, "kn")
     assert cm.cm_check_status(ws)[0] == 0
@@ -125,7 +125,7 @@ def test_worked_examples_on_gpu(direction):
     N, M = g["N"], len(g["x"][0])
     x = pad(g["x"], (N, M, 8))
     w = pad(g["w"], (N, 8, 8))
-    ws = torch.empty(plan.rs_workspace_size(M, 8), dtype=torch.uint8, device=dev)
+    ws = torch.full((plan.rs_workspace_size(M, 8),), 0xFF, dtype=torch.uint8, device=dev)
     y = torch.full((N, M // N, 8), float("nan"), dtype=torch.float32, device=dev)
     cm.cm_gemm_rs(plan, x, w, y, ws, "kn")
     assert cm.cm_check_status(ws)[0] == 0

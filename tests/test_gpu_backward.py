@@ -32,7 +32,7 @@ def run_backward(plan, x, w, dy, dtype=torch.float32, stream=None, overlap=1):
     N, m, K = x.shape
     n = w.shape[1]
     plan.set_option(cm.CM_OPT_BULK_OVERLAP, overlap)
-    ws = torch.empty(plan.backward_pair_workspace_size(m, K, n), dtype=torch.uint8, device=DEV)
+    ws = torch.full((plan.backward_pair_workspace_size(m, K, n),), 0xFF, dtype=torch.uint8, device=DEV)
     dx = torch.full((N, m, K), float("nan"), dtype=dtype, device=DEV)
     dw = torch.full((N, n, K), float("nan"), dtype=dtype, device=DEV)
     cm.cm_backward_pair(plan, x.to(DEV), w.to(DEV), dy.to(DEV), dx, dw, ws, stream)
@@ -93,7 +93,7 @@ def test_back_to_back_on_a_user_stream():
     sets = [backward_inputs(N, m, K, n, seed=s) for s in (11, 12)]
     refs = [oracle_backward(*t) for t in sets]
     plan = cm.Plan(N, 1, "uni")
-    ws = torch.empty(plan.backward_pair_workspace_size(m, K, n), dtype=torch.uint8, device=DEV)
+    ws = torch.full((plan.backward_pair_workspace_size(m, K, n),), 0xFF, dtype=torch.uint8, device=DEV)
     outs = [(torch.empty(N, m, K, device=DEV), torch.empty(N, n, K, device=DEV)) for _ in sets]
     dev_in = [tuple(t.to(DEV) for t in s_) for s_ in sets]
     s = torch.cuda.Stream()
@@ -114,7 +114,7 @@ def test_shape_errors():
     x = torch.zeros(2, 16, 64, dtype=torch.bfloat16, device=DEV)     # 32 tokens < 64
     w = torch.zeros(2, 64, 64, dtype=torch.bfloat16, device=DEV)
     dy = torch.zeros(2, 32, 64, dtype=torch.bfloat16, device=DEV)
-    ws = torch.empty(plan.backward_pair_workspace_size(16, 64, 64), dtype=torch.uint8, device=DEV)
+    ws = torch.full((plan.backward_pair_workspace_size(16, 64, 64),), 0xFF, dtype=torch.uint8, device=DEV)
     dx, dw = torch.empty(2, 16, 64, device=DEV), torch.empty(2, 64, 64, device=DEV)
     with pytest.raises(cm.CMError):
         cm.cm_backward_pair(plan, x, w, dy, dx, dw, ws)

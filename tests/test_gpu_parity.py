@@ -10,7 +10,19 @@ Bars (the arithmetic is bf16 products accumulated in fp32):
 * AllGather->GEMM is bit-identical across chunk counts, ring directions, the
   step-serial mode and the undecomposed path (each output element is the same
   tensor-core dot product whichever tile computes it).
-Full-size workloads are checked on sampled rows the oracle computes one by one.
+Every workspace starts filled with 0xFF bytes (NaN as bf16 and as fp32), so a
+tile that reads a receive slot or a bucket before its producer wrote it
+yields NaN and fails (the ordering hazards of "Hiding Tensor-Parallel
+Collectives: AG/RS Overlap in Megatron", sections 5 and 7: nothing is read
+before its producer has written it).
+
+Full-size workloads: the Megatron-SP fc1 and fc2 layers and the GPT-3 layer
+are compared with the oracle in full; the MLP sweep on rows the oracle
+computes one by one -- at least one in every 128-row block of every (rank,
+shard) pair for AllGather->GEMM and of every bucket for GEMM->ReduceScatter,
+so every CTA half of every pair tile of every task, for every chunk count,
+is compared element by element -- and in full against torch.matmul on the
+concatenated operands on the device (a second, independent computation).
 """
 
 import functools
@@ -42,7 +54,7 @@ DEV = "cuda:0"
 def run_ag(plan, x, w, layout="nk", ydtype=torch.float32, check=True):
     N, m, K = x.shape
     n = w.shape[1] if layout == "nk" else w.shape[2]
-    ws = torch.empty(plan.ag_workspace_size(m, K), dtype=torch.uint8, device=DEV)
+    ws = torch.full((plan.ag_workspace_size(m, K),), 0xFF, dtype=torch.uint8, device=DEV)
     y = torch.full((N, N * m, n), float("nan"), dtype=ydtype, device=DEV)
     cm.cm_ag_gemm(plan, x.to(DEV), w.to(DEV), y, ws, layout)
     st, info = cm.cm_check_status(ws)
@@ -54,7 +66,7 @@ def run_ag(plan, x, w, layout="nk", ydtype=torch.float32, check=True):
 def run_rs(plan, x, w, layout="nk", ydtype=torch.float32, check=True):
     N, M, k = x.shape
     n = w.shape[1] if layout == "nk" else w.shape[2]
-    ws = torch.empty(plan.rs_workspace_size(M, n), dtype=torch.uint8, device=DEV)
+    ws = torch.full((plan.rs_workspace_size(M, n),), 0xFF, dtype=torch.uint8, device=DEV)
     y = torch.full((N, M // N, n), float("nan"), dtype=ydtype, device=DEV)
     cm.cm_gemm_rs(plan, x.to(DEV), w.to(DEV), y, ws, layout)
     st, info = cm.cm_check_status(ws)
@@ -212,59 +224,110 @@ def test_skipped_signal_times_out_and_context_survives():
     _assert_close(y, ref, torch.float32)
 
 
-# ---- full-size workloads, sampled rows -----------------------------------------
+# ---- full-size workloads ----------------------------------------------------------
 
-def _ag_rows(N, m, rng, extra=48):
-    """(rank, gathered row) samples: every shard's first/last row, tile edges, random."""
-    rows = []
-    for j in range(N):
-        for i in {0, m - 1, min(127, m - 1), min(128, m - 1), m // 2}:
-            rows.append(j * m + i)
-    rows += list(rng.integers(0, N * m, size=extra))
-    ranks = list(rng.integers(0, N, size=len(rows)))
-    ranks[:N] = list(range(N))
+BLOCK = 128   # rows of one CTA's half of a 256-row pair tile
+
+
+def _block_rows(rows, rng):
+    """One random row in every BLOCK-row block of [0, rows), plus the first and last row."""
+    out = [b + int(rng.integers(0, min(BLOCK, rows - b))) for b in range(0, rows, BLOCK)]
+    return sorted(set(out) | {0, rows - 1})
+
+
+def _ag_rows(N, m, rng):
+    """(rank, gathered row) samples: for every (rank r, shard j) pair, one row
+    in every 128-row block of the shard (and its first and last row).  Every
+    task (r, j) of every ring schedule writes rows j*m.. of Y_r, and every CTA
+    half of every pair tile of that task covers one such block, whatever the
+    chunk count (chunks are multiples of 128 rows here)."""
+    ranks, rows = [], []
+    for r in range(N):
+        for j in range(N):
+            for i in _block_rows(m, rng):
+                ranks.append(r)
+                rows.append(j * m + i)
     return np.array(ranks), np.array(rows)
 
 
-def _check_ag_full(N, m, K, n, direction, chunks, seed, layout="nk"):
+def _rs_rows(N, Mb, rng):
+    """(owner, row) samples: one row in every 128-row block of every bucket
+    (and its first and last row) -- every chunk and pair-tile half of every
+    bucket, each of which is the sum of every rank's contribution."""
+    owners, rows = [], []
+    for o in range(N):
+        for i in _block_rows(Mb, rng):
+            owners.append(o)
+            rows.append(i)
+    return np.array(owners), np.array(rows)
+
+
+def _torch_ag(x, w, layout="nk"):
+    """Y_r = concat_j(X_j) @ W_r by torch.matmul (cuBLAS, bf16 in, fp32 accumulate), on the device."""
+    N, m, K = x.shape
+    X = x.reshape(N * m, K)
+    return torch.stack([X @ (w[r].t() if layout == "nk" else w[r]) for r in range(N)])
+
+
+def _torch_rs(x, w, layout="nk"):
+    """sum_r X_r @ W_r as one torch.matmul over the contraction-concatenated operands."""
+    N, M, k = x.shape
+    X = x.permute(1, 0, 2).reshape(M, N * k)
+    W = (w.transpose(1, 2) if layout == "nk" else w).reshape(N * k, -1)
+    return (X @ W).reshape(N, M // N, -1)
+
+
+def _check_ag_full(N, m, K, n, direction, chunks, seed, layout="nk", full_oracle=False):
     x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=seed, w_layout=layout)
     y, _, _ = run_ag(cm.Plan(N, chunks, direction), x, w, layout, torch.bfloat16)
-    rng = np.random.default_rng(seed)
-    ranks, rows = _ag_rows(N, m, rng)
+    assert torch.isfinite(y).all()
+    xd, wd = x.to(DEV), w.to(DEV)
+    assert _err(y, _np(_torch_ag(xd, wd, layout))) <= TOL
+    if full_oracle:
+        ref = oracle.ag_gemm(gen.bf16_bits(x), gen.bf16_bits(w), layout)
+        assert _err(y, ref) <= TOL
+        return
+    ranks, rows = _ag_rows(N, m, np.random.default_rng(seed))
     ref = oracle.ag_gemm_rows(gen.bf16_bits(x), gen.bf16_bits(w), ranks, rows, layout)
     got = y[torch.as_tensor(ranks, device=DEV), torch.as_tensor(rows, device=DEV)]
     assert oracle.normwise_max_rel_err(_np(got), ref) <= TOL
-    assert torch.isfinite(y).all()
 
 
-def _check_rs_full(N, M, k, n, direction, chunks, seed, layout="nk"):
+def _check_rs_full(N, M, k, n, direction, chunks, seed, layout="nk", full_oracle=False):
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=seed, w_layout=layout)
     y, _, _ = run_rs(cm.Plan(N, chunks, direction), x, w, layout, torch.bfloat16)
-    rng = np.random.default_rng(seed)
-    Mb = M // N
-    owners = np.concatenate([np.arange(N), np.arange(N), rng.integers(0, N, 24)])
-    rows = np.concatenate([np.zeros(N, int), np.full(N, Mb - 1), rng.integers(0, Mb, 24)])
+    assert torch.isfinite(y).all()
+    xd, wd = x.to(DEV), w.to(DEV)
+    assert _err(y, _np(_torch_rs(xd, wd, layout))) <= TOL
+    if full_oracle:
+        ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), layout)
+        assert _err(y, ref) <= TOL
+        return
+    owners, rows = _rs_rows(N, M // N, np.random.default_rng(seed))
     ref = oracle.gemm_rs_rows(gen.bf16_bits(x), gen.bf16_bits(w), owners, rows, layout)
     got = y[torch.as_tensor(owners, device=DEV), torch.as_tensor(rows, device=DEV)]
     assert oracle.normwise_max_rel_err(_np(got), ref) <= TOL
-    assert torch.isfinite(y).all()
 
 
 def test_sp_mlp_fc1_ag_n8():
+    """Megatron-SP MLP fc1 AllGather->GEMM, every output element against the oracle."""
     a = gen.WORKLOADS["sp_mlp_fc1_ag_n8"]["ag"]
-    _check_ag_full(8, a["m"], a["K"], a["n"], "uni", 1, a["seed"])
+    _check_ag_full(8, a["m"], a["K"], a["n"], "uni", 1, a["seed"], full_oracle=True)
 
 
 def test_sp_mlp_fc2_rs_n8():
+    """Megatron-SP MLP fc2 GEMM->ReduceScatter, every output element against the oracle."""
     r = gen.WORKLOADS["sp_mlp_fc2_rs_n8"]["rs"]
-    _check_rs_full(8, r["M"], r["k"], r["n"], "uni", 1, r["seed"])
+    _check_rs_full(8, r["M"], r["k"], r["n"], "uni", 1, r["seed"], full_oracle=True)
 
 
 def test_gpt3_layer_bidi():
+    """GPT-3 layer (QKV AllGather->GEMM, attention-out GEMM->ReduceScatter),
+    bidirectional ring, every output element against the oracle."""
     wl = gen.WORKLOADS["gpt3_h12288_s2048_n8"]
     a, r = wl["ag"], wl["rs"]
-    _check_ag_full(8, a["m"], a["K"], a["n"], "bidi", 1, a["seed"])
-    _check_rs_full(8, r["M"], r["k"], r["n"], "bidi", 1, r["seed"])
+    _check_ag_full(8, a["m"], a["K"], a["n"], "bidi", 1, a["seed"], full_oracle=True)
+    _check_rs_full(8, r["M"], r["k"], r["n"], "bidi", 1, r["seed"], full_oracle=True)
 
 
 @functools.lru_cache(maxsize=1)
@@ -278,12 +341,17 @@ def _mlp_case(N):
     rng = np.random.default_rng(5000 + N)
     ranks, rows = _ag_rows(N, a["m"], rng)
     ref_a = oracle.ag_gemm_rows(gen.bf16_bits(xa), gen.bf16_bits(wa), ranks, rows, "nk")
-    Mb = r["M"] // N
-    owners = np.concatenate([np.arange(N), np.arange(N), rng.integers(0, N, 24)])
-    orow = np.concatenate([np.zeros(N, int), np.full(N, Mb - 1), rng.integers(0, Mb, 24)])
+    owners, orow = _rs_rows(N, r["M"] // N, rng)
     ref_r = oracle.gemm_rs_rows(gen.bf16_bits(xr), gen.bf16_bits(wr), owners, orow, "nk")
     return dict(xa=xa, wa=wa, xr=xr, wr=wr, ranks=ranks, rows=rows, ref_a=ref_a, owners=owners, orow=orow,
                 ref_r=ref_r)
+
+
+@functools.lru_cache(maxsize=1)
+def _mlp_torch(N):
+    """torch.matmul results of the MLP sweep at N ranks (every element), on the device."""
+    c = _mlp_case(N)
+    return _torch_ag(c["xa"].to(DEV), c["wa"].to(DEV)), _torch_rs(c["xr"].to(DEV), c["wr"].to(DEV))
 
 
 SWEEP = [(N, c, d) for N in (4, 8, 16) for d in ("uni", "bidi") for c in (1, 2, 4)]
@@ -292,14 +360,18 @@ SWEEP = [(N, c, d) for N in (4, 8, 16) for d in ("uni", "bidi") for c in (1, 2, 
 @pytest.mark.parametrize("N,chunks,direction", SWEEP)
 def test_mlp_h8192_sweep_points(N, chunks, direction):
     """Every (N, chunks, ring) point of the MLP h=8192, ffn=28672, s=8192
-    chunk/ring sweep, both ops at full size, on sampled rows."""
+    chunk/ring sweep, both ops at full size: the oracle's rows in every
+    128-row block of every task, and every element against torch.matmul."""
     c = _mlp_case(N)
+    t_ag, t_rs = _mlp_torch(N)
     y, _, _ = run_ag(cm.Plan(N, chunks, direction), c["xa"], c["wa"], "nk", torch.bfloat16)
+    assert torch.isfinite(y).all()
     got = y[torch.as_tensor(c["ranks"], device=DEV), torch.as_tensor(c["rows"], device=DEV)]
     assert oracle.normwise_max_rel_err(_np(got), c["ref_a"]) <= TOL
-    assert torch.isfinite(y).all()
+    assert ((y.float() - t_ag.float()).abs().max() / t_ag.float().abs().max()).item() <= TOL
     del y
     y, _, _ = run_rs(cm.Plan(N, chunks, direction), c["xr"], c["wr"], "nk", torch.bfloat16)
+    assert torch.isfinite(y).all()
     got = y[torch.as_tensor(c["owners"], device=DEV), torch.as_tensor(c["orow"], device=DEV)]
     assert oracle.normwise_max_rel_err(_np(got), c["ref_r"]) <= TOL
-    assert torch.isfinite(y).all()
+    assert ((y.float() - t_rs.float()).abs().max() / t_rs.float().abs().max()).item() <= TOL

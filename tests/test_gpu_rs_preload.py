@@ -66,7 +66,7 @@ def test_preload_matches_epilogue_add_and_repeats():
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=11, w_layout="nk")
     p1 = _plan(N, 1, "uni", 1)
     dev = "cuda:0"
-    ws = torch.empty(p1.rs_workspace_size(M, n), dtype=torch.uint8, device=dev)
+    ws = torch.full((p1.rs_workspace_size(M, n),), 0xFF, dtype=torch.uint8, device=dev)
     xd, wd = x.to(dev), w.to(dev)
     ya = torch.empty(N, M // N, n, dtype=torch.float32, device=dev)
     yb = torch.empty_like(ya)
