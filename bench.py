@@ -14,6 +14,7 @@ timed region.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--sweep]   # the N x chunks x ring sweep, one JSON line per point
+                  [--configs] # every configuration's ops with roofline fractions
 
 For --gpus N > 1 (launched by torch.distributed.run), every rank runs an
 independent replica of the step on its own GPU (the path does not shard
@@ -210,7 +211,7 @@ def flops(s, N):
 class Step:
     """Device buffers and plans of one step; run() enqueues both ops."""
 
-    def __init__(self, N, chunks, direction, data, device):
+    def __init__(self, N, chunks, direction, data, device, y_dtype=None):
         import torch
         from collective_matmul_decomposition_gb300 import cm
         self.cm = cm
@@ -218,10 +219,11 @@ class Step:
         s = data["shapes"]
         a, r = s["ag"], s["rs"]
         x1, w1, x2, w2 = data["cpu"]
+        yd = y_dtype or torch.bfloat16
         self.x1, self.w1 = x1.to(device), w1.to(device)
         self.x2, self.w2 = x2.to(device), w2.to(device)
-        self.y1 = torch.empty(N, N * a["m"], a["n"], dtype=torch.bfloat16, device=device)
-        self.y2 = torch.empty(N, r["M"] // N, r["n"], dtype=torch.bfloat16, device=device)
+        self.y1 = torch.empty(N, N * a["m"], a["n"], dtype=yd, device=device)
+        self.y2 = torch.empty(N, r["M"] // N, r["n"], dtype=yd, device=device)
         self.plan = cm.Plan(N, chunks, direction)
         self.ws1 = torch.empty(self.plan.ag_workspace_size(a["m"], a["K"]), dtype=torch.uint8, device=device)
         self.ws2 = torch.empty(self.plan.rs_workspace_size(r["M"], r["n"]), dtype=torch.uint8, device=device)
@@ -453,6 +455,22 @@ def run_reference(args):
     return 0
 
 
+def choose_peak(peaks, timed_s, clocks):
+    """The measured dense bf16 peak that matches how the kernel ran: the burst
+    figure (a GEMM timed alone, clocks at their maximum) for a short timed
+    region or one whose median SM clock under load stayed at the maximum; the
+    sustained figure (seconds under the power cap) only for a region of a
+    second or more whose clocks came down."""
+    burst, sust = float(peaks["bf16_tflops"]), float(peaks["bf16_tflops_sustained"])
+    sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    at_max = sm is not None and mx and sm >= 0.97 * mx
+    if timed_s < 1.0:
+        return burst, "burst", f"timed region {timed_s:.3f} s < 1 s"
+    if at_max or sm is None:
+        return burst, "burst", f"median SM clock {sm} MHz of max {mx}"
+    return sust, "sustained", f"timed region {timed_s:.2f} s, median SM clock {sm} of max {mx} MHz"
+
+
 def step_config(N, chunks, direction, shapes):
     a, r = shapes["ag"], shapes["rs"]
     return {"workload": WORKLOAD, "logical_ranks": N, "chunks": chunks, "ring": direction,
@@ -514,13 +532,13 @@ def run_ours(args):
     clocks = clk.summary()
 
     peaks, peak_kind = load_peaks()
-    # the kernel is timed inside a long run of back-to-back steps (power-capped
-    # clocks), so the sustained dense bf16 figure is the denominator; the
-    # burst-relative fraction is reported beside it
-    peak = float(peaks["bf16_tflops_sustained"])
+    peak, peak_which, peak_why = choose_peak(peaks, elapsed_max, clocks)
     peak_burst = float(peaks["bf16_tflops"])
+    peak_sust = float(peaks["bf16_tflops_sustained"])
     launch_ms = statistics.mean(ag_ms + rs_ms)
     achieved = (f_ag + f_rs) / 2 / (launch_ms / 1e3) / 1e12
+    ach_ag = f_ag / (statistics.mean(ag_ms) / 1e3) / 1e12
+    ach_rs = f_rs / (statistics.mean(rs_ms) / 1e3) / 1e12
     traffic = ncu_traffic()
 
     # comparators on the same data -- the undecomposed op in this kernel and
@@ -595,10 +613,13 @@ def run_ours(args):
         "pct_of_peak": value / peak,
         "pct_of_burst_peak": value / peak_burst,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "frac_of_burst": achieved / peak_burst,
+                     "frac": achieved / peak,
+                     "frac_ag": ach_ag / peak, "frac_rs": ach_rs / peak,
+                     "achieved_ag": ach_ag, "achieved_rs": ach_rs,
+                     "frac_of_burst": achieved / peak_burst, "frac_of_sustained": achieved / peak_sust,
                      "traffic": traffic["bytes_per_launch"] if traffic else None,
                      "kernel": "cm_pair_kernel (one launch per op; AG and RS averaged)",
-                     "peak_source": f"bf16_tflops_sustained of {peak_kind} (burst {peak_burst})"},
+                     "peak_source": f"{peak_which} dense bf16 of {peak_kind} ({peak_why})"},
         "clocks": clocks,
         "e2e": e2e,
         "gpu_launches": 2 * K,
@@ -672,6 +693,87 @@ def named_workload_inputs(name):
     x2, w2 = gen.rs_inputs(N, r["M"], r["k"], r["n"], r["x"], r["w"], r["seed"], "nk")
     return N, {"shapes": {"ag": dict(m=a["m"], K=a["K"], n=a["n"]), "rs": dict(M=r["M"], k=r["k"], n=r["n"])},
                "cpu": (x1, w1, x2, w2)}
+
+
+def algorithmic_bytes(op, N, sh, out_bytes):
+    """Bytes an op must move at least: the ring's traffic (AG: every shard
+    written into N - 1 receive slots and read back; RS: every partial bucket
+    of N - 1 hops written and read as fp32) plus reading the operands and
+    writing the output once."""
+    if op == "ag":
+        m, K, n = sh["m"], sh["K"], sh["n"]
+        ring = 2 * N * (N - 1) * m * K * 2
+        return ring, ring + N * m * K * 2 + N * K * n * 2 + N * N * m * n * out_bytes
+    M, k, n = sh["M"], sh["k"], sh["n"]
+    ring = 2 * N * (N - 1) * (M // N) * n * 4
+    return ring, ring + N * M * k * 2 + N * k * n * 2 + M * n * out_bytes
+
+
+# The five workloads, each op with the ring the configuration names, plus the
+# other ring for the GPT-3 layer (its configuration names the bidirectional one).
+CONFIG_RUNS = [
+    ("tiny_n2", "ag", "uni", 1), ("tiny_n2", "rs", "uni", 1),
+    ("sp_mlp_fc1_ag_n8", "ag", "uni", 1), ("sp_mlp_fc2_rs_n8", "rs", "uni", 1),
+    ("gpt3_h12288_s2048_n8", "ag", "bidi", 1), ("gpt3_h12288_s2048_n8", "rs", "bidi", 1),
+    ("gpt3_h12288_s2048_n8", "ag", "uni", 1), ("gpt3_h12288_s2048_n8", "rs", "uni", 1),
+    (WORKLOAD, "ag", "uni", 1), (WORKLOAD, "rs", "uni", 1),
+]
+
+
+def run_configs(args):
+    """Every configuration's ops: ms per call (median of interleaved rounds
+    with the undecomposed op in this kernel and torch.matmul on the
+    concatenated operands), TFLOP/s, and the roofline fractions (tensor
+    against the measured burst bf16 peak -- each call is short and timed
+    between others -- and HBM against the measured copy bandwidth for the
+    algorithmic bytes), one JSON line each."""
+    import torch
+    import __graft_entry__
+    from collective_matmul_decomposition_gb300 import inputs as gen
+    __graft_entry__.build()
+    device = torch.device("cuda", 0)
+    peaks, kind = load_peaks()
+    burst, hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    cache = {}
+    for name, op, ring, chunks in CONFIG_RUNS:
+        if name not in cache:
+            cache.clear()
+            torch.cuda.empty_cache()
+            if name == WORKLOAD:
+                N, data = 8, make_step_inputs(8, device)
+            else:
+                N, data = named_workload_inputs(name)
+            yd = torch.float32 if gen.WORKLOADS[name]["y_dtype"] == "f32" else torch.bfloat16
+            mono = Step(N, 1, "none", data, device, yd)
+            X1, W1, X2, W2 = concat_operands(mono, data["shapes"], N)
+            cache[name] = (N, data, yd, mono, X1, W1, X2, W2)
+        N, data, yd, mono, X1, W1, X2, W2 = cache[name]
+        st = Step(N, chunks, ring, data, device, yd)
+        torch_fn = (lambda: torch.matmul(X1, W1.t())) if op == "ag" else (lambda: torch.matmul(X2, W2.t()))
+        with ClockSampler(physical_gpu_id(0)) as clk:
+            t = time_interleaved({"dec": getattr(st, op), "none": getattr(mono, op), "torch": torch_fn},
+                                 max(20, args.steps), torch, warmup=args.warmup)
+        st.check((op,))
+        mono.check((op,))
+        f_ag, f_rs = flops(data["shapes"], N)
+        fl = f_ag if op == "ag" else f_rs
+        tf = fl / (t["dec"] / 1e3) / 1e12
+        ring_b, alg_b = algorithmic_bytes(op, N, data["shapes"][op], 4 if yd == torch.float32 else 2)
+        gbs = alg_b / (t["dec"] / 1e3) / 1e9
+        ai = fl / alg_b
+        bound = "tensor" if ai >= burst * 1e12 / (hbm * 1e9) else "hbm"
+        print(json.dumps({
+            "config": name, "op": op, "N": N, "chunks": chunks, "ring": ring,
+            "ms": t["dec"], "tflops": tf, "bound": bound,
+            "frac_tensor": tf / burst, "algorithmic_bytes": alg_b, "ring_bytes": ring_b,
+            "achieved_gbs": gbs, "frac_hbm": gbs / hbm, "flop_per_byte": ai,
+            "frac": tf / burst if bound == "tensor" else gbs / hbm,
+            "ms_undecomposed": t["none"], "ms_torch": t["torch"],
+            "vs_undecomposed_time": t["dec"] / t["none"], "vs_torch_time": t["dec"] / t["torch"],
+            "rounds": max(20, args.steps), "clocks": clk.summary(),
+            "peak_source": f"bf16_tflops (burst) {burst} and hbm_gbs {hbm} of {kind}"}), flush=True)
+        del st
+    return 0
 
 
 # NVLink-class per-GPU rates for the gate's projection (one direction of one
@@ -877,6 +979,8 @@ def main(argv=None):
     ap.add_argument("--gate", action="store_true", help="the cost model's choices against measurement")
     ap.add_argument("--backward", action="store_true", help="the backward pair of the MLP fc1 layer")
     ap.add_argument("--cannon", action="store_true", help="Cannon-style 2-D rotation, 8192^3")
+    ap.add_argument("--configs", action="store_true",
+                    help="every configuration's ops with roofline fractions, one JSON line each")
     ap.add_argument("--profile", choices=["ag", "rs", "rs_pipe"], default=None,
                     help="run only --steps calls of one op (for ncu captures)")
     ap.add_argument("--workload", default=WORKLOAD)
@@ -907,6 +1011,8 @@ def main(argv=None):
         return run_backward(args)
     if args.cannon:
         return run_cannon(args)
+    if args.configs:
+        return run_configs(args)
     if args.profile:
         return run_profile_case(args)
     return run_ours(args)
