@@ -228,6 +228,14 @@ class Step:
         self.ws1 = torch.empty(self.plan.ag_workspace_size(a["m"], a["K"]), dtype=torch.uint8, device=device)
         self.ws2 = torch.empty(self.plan.rs_workspace_size(r["M"], r["n"]), dtype=torch.uint8, device=device)
 
+    def set_rs_in_place(self, v):
+        """CM_OPT_RS_IN_PLACE for this step's plan (the RS workspace is resized)."""
+        import torch
+        self.plan.set_option(self.cm.CM_OPT_RS_IN_PLACE, int(v))
+        M, n = self.x2.shape[1], self.y2.shape[2]
+        self.ws2 = torch.empty(self.plan.rs_workspace_size(M, n), dtype=torch.uint8, device=self.x2.device)
+        return self
+
     def ag(self):
         self.cm.cm_ag_gemm(self.plan, self.x1, self.w1, self.y1, self.ws1, "nk")
 
@@ -750,11 +758,17 @@ def run_configs(args):
         N, data, yd, mono, X1, W1, X2, W2 = cache[name]
         st = Step(N, chunks, ring, data, device, yd)
         torch_fn = (lambda: torch.matmul(X1, W1.t())) if op == "ag" else (lambda: torch.matmul(X2, W2.t()))
+        fns = {"dec": getattr(st, op), "none": getattr(mono, op), "torch": torch_fn}
+        alt = None
+        if op == "rs" and ring != "none":   # the same ring with one buffer per (rank, step)
+            alt = Step(N, chunks, ring, data, device, yd).set_rs_in_place(0)
+            fns["per_step"] = alt.rs
         with ClockSampler(physical_gpu_id(0)) as clk:
-            t = time_interleaved({"dec": getattr(st, op), "none": getattr(mono, op), "torch": torch_fn},
-                                 max(20, args.steps), torch, warmup=args.warmup)
+            t = time_interleaved(fns, max(20, args.steps), torch, warmup=args.warmup)
         st.check((op,))
         mono.check((op,))
+        if alt is not None:
+            alt.check(("rs",))
         f_ag, f_rs = flops(data["shapes"], N)
         fl = f_ag if op == "ag" else f_rs
         tf = fl / (t["dec"] / 1e3) / 1e12
@@ -770,9 +784,10 @@ def run_configs(args):
             "frac": tf / burst if bound == "tensor" else gbs / hbm,
             "ms_undecomposed": t["none"], "ms_torch": t["torch"],
             "vs_undecomposed_time": t["dec"] / t["none"], "vs_torch_time": t["dec"] / t["torch"],
+            "ms_rs_per_step_buffers": t.get("per_step"),
             "rounds": max(20, args.steps), "clocks": clk.summary(),
             "peak_source": f"bf16_tflops (burst) {burst} and hbm_gbs {hbm} of {kind}"}), flush=True)
-        del st
+        del st, alt
     return 0
 
 
@@ -958,13 +973,15 @@ def run_profile_case(args):
         st.plan.set_option(st.cm.CM_OPT_ROW_BAND, args.row_band)
     if args.rs_preload >= 0:
         st.plan.set_option(st.cm.CM_OPT_RS_PRELOAD, args.rs_preload)
+    if args.rs_in_place >= 0:
+        st.set_rs_in_place(args.rs_in_place)
     fn = {"ag": st.ag, "rs": st.rs, "rs_pipe": st.rs_pipe}[args.profile]
     f_ag, f_rs = flops(data["shapes"], N)
     ms = time_loop(fn, args.steps, torch, warmup=args.warmup)
     st.check((args.profile,))
     fl = f_ag if args.profile == "ag" else f_rs
     print(json.dumps({"profile_case": args.workload, "op": args.profile, "N": N, "chunks": args.chunks,
-                      "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group, "l2_hints": args.l2_hints, "l2_promotion": args.l2_promotion, "row_band": args.row_band, "rs_preload": args.rs_preload,
+                      "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group, "l2_hints": args.l2_hints, "l2_promotion": args.l2_promotion, "row_band": args.row_band, "rs_preload": args.rs_preload, "rs_in_place": args.rs_in_place,
                       "ms": ms, "tflops": fl / (ms / 1e3) / 1e12}), flush=True)
     return 0
 
@@ -994,6 +1011,7 @@ def main(argv=None):
     ap.add_argument("--l2-promotion", type=int, default=-1, help="CM_OPT_L2_PROMOTION for --profile (-1 = default)")
     ap.add_argument("--row-band", type=int, default=-1, help="CM_OPT_ROW_BAND for --profile (-1 = default)")
     ap.add_argument("--rs-preload", type=int, default=-1, help="CM_OPT_RS_PRELOAD for --profile (-1 = default)")
+    ap.add_argument("--rs-in-place", type=int, default=-1, help="CM_OPT_RS_IN_PLACE for --profile (-1 = default)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="oracle seconds for the cpu_baseline of the default arm")
     ap.add_argument("--ref-seconds", type=float, default=120.0,

@@ -25,6 +25,8 @@ CM_OPT_STATIC_TILES, CM_OPT_TILE_GROUP, CM_OPT_L2_HINTS, CM_OPT_L2_PROMOTION, CM
 CM_OPT_BULK_OVERLAP = 10
 CM_OPT_RS_PRELOAD = 11
 CM_OPT_RS_IN_PLACE = 12
+CM_OPT_TASK_ORDER = 13
+CM_OPT_RS_EPILOGUE = 14
 CM_MAX_RANKS, CM_MAX_CHUNKS = 16, 8
 
 DIRECTIONS = {"uni": CM_RING_UNI, "bidi": CM_RING_BIDI, "none": CM_RING_NONE}

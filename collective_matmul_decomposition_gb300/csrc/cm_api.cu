@@ -21,6 +21,22 @@ constexpr size_t kCounterOff = 64;
 // preloaded tile cannot start its MMAs before the bucket is complete).
 constexpr int64_t kPreloadAllKSlices = 8;
 
+// CM_OPT_RS_EPILOGUE: 1 = every epilogue warp on every tile, TMA copies
+// through shared memory; 2 = two warp groups, one per accumulator, with
+// vector reductions; 0 = automatic.
+// The automatic choice, measured over the MLP sweep (h=8192, ffn=28672,
+// s=8192) and the GPT-3 attention-out GEMM-RS with both interleaved: two
+// groups were 2-6 % faster on one-way rings of 8 and 16 ranks with at least
+// 28 K slices per tile and on two-way rings of 16 ranks; the TMA epilogue
+// was as fast or faster everywhere else (6-11 % on the GPT-3 layer, 24 K
+// slices; 1-3 % at 4 ranks and on two-way rings of 8).
+int rs_groups(const PlanImpl &pl, int64_t k) {
+    if (pl.rs_epilogue != 0) return pl.rs_epilogue == 2 ? 1 : 0;
+    const int64_t kslices = (k + kBK - 1) / kBK;
+    const bool many_ranks = pl.N >= 16 || (pl.N >= 8 && pl.dir == CM_RING_UNI);
+    return many_ranks && kslices >= 28 ? 1 : 0;
+}
+
 // Ring stages of received bucket per tile for CM_OPT_RS_PRELOAD = mode.
 int preload_stages(int mode, int64_t kslices) {
     switch (mode) {
@@ -40,9 +56,15 @@ struct WsLayout {
 
 int streams_of(const PlanImpl &p) { return p.dir == CM_RING_BIDI ? 2 : 1; }
 
+// Readiness counters: AG one per (flag id, chunk, row tile), RS one per (flag
+// id, chunk, row tile, column tile) -- sized for the smaller (128-row) tiles
+// of the two kernels, so either kernel's indices fit.
+size_t row_tiles(int64_t rows_c) { return size_t((rows_c + kBM - 1) / kBM); }
+
 WsLayout ag_layout(const PlanImpl &p, int64_t m, int64_t K) {
     WsLayout l;
-    l.flags_bytes = size_t(p.flag_ids[CM_OP_AG_GEMM]) * size_t(p.chunks) * sizeof(uint32_t);
+    const int64_t rows_c = p.dir == CM_RING_NONE ? int64_t(p.N) * m : (m + p.chunks - 1) / p.chunks;
+    l.flags_bytes = size_t(p.flag_ids[CM_OP_AG_GEMM]) * size_t(p.chunks) * row_tiles(rows_c) * sizeof(uint32_t);
     l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
     const bool ring = p.dir != CM_RING_NONE && p.N > 1;
     const size_t slots = ring ? size_t(p.N * streams_of(p) * p.sched[CM_OP_AG_GEMM].steps) : 0;   // one per (rank, stream, step)
@@ -61,7 +83,9 @@ int64_t rs_bufs(const PlanImpl &p) {
 
 WsLayout rs_layout(const PlanImpl &p, int64_t M, int64_t n) {
     WsLayout l;
-    l.flags_bytes = size_t(p.flag_ids[CM_OP_GEMM_RS]) * size_t(p.chunks) * sizeof(uint32_t);
+    const int64_t rows_c = (M / p.N + p.chunks - 1) / p.chunks;
+    l.flags_bytes = size_t(p.flag_ids[CM_OP_GEMM_RS]) * size_t(p.chunks) * row_tiles(rows_c) *
+                    size_t((n + kBN - 1) / kBN) * sizeof(uint32_t);
     l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
     l.buf_bytes = size_t(rs_bufs(p)) * size_t(M / p.N) * size_t(n) * sizeof(float);
     l.total = l.buf_off + l.buf_bytes;
@@ -113,6 +137,12 @@ bool make_map(CUtensorMap *m, int l2_promotion, const void *base, uint64_t d0, u
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// fp32 accumulators [slabs][rows][n] in 32 x 32 boxes (128-byte swizzle):
+// the CTA-pair TMA epilogue's loads, stores and adds of bucket slices.
+bool make_acc_maps(KParams &kp, int promo, const float *acc, int64_t n, int64_t rows, int64_t slabs) {
+    return make_map(&kp.tmAcc, promo, acc, uint64_t(n), uint64_t(rows), uint64_t(slabs), 32, 32, true);
+}
+
 // The kernel a call runs: CTA pairs (one pair per cluster), or single CTAs.
 struct KernelChoice {
     bool pair;
@@ -136,12 +166,16 @@ void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int
     kp.ntiles = int((n + kBN - 1) / kBN);
     kp.tiles_per_task = (kp.chunk_pair ? kp.chunks / 2 : kp.chunks) * kp.mtiles_c * kp.ntiles;
     if (op == CM_OP_AG_GEMM) {
-        // forwards per chunk: CTA pairs forward a row slice from every tile
-        // (2 CTAs each); single CTAs forward whole row tiles from column tile 0
-        kp.tgt_in = uint32_t(kc.pair ? per_tile * kp.mtiles_c * kp.ntiles : kp.mtiles_c);
+        // forwards per (chunk, row tile): CTA pairs forward a row slice from
+        // every column tile (from each CTA that holds the chunk); single CTAs
+        // forward the whole row tile from column tile 0
+        kp.tgt_in = uint32_t(kc.pair ? per_tile * kp.ntiles : 1);
         kp.tgt_free = 0;   // receive slots are written once: nothing waits for a slot to be free
     } else {
-        kp.tgt_in = uint32_t(per_tile * kp.mtiles_c * kp.ntiles);   // finished tile halves per chunk
+        // signals of the same bucket tile: CTA pairs, one per warp of the
+        // epilogue group that drains it (two groups) or one per CTA (TMA
+        // epilogue), in each CTA holding the chunk; single CTAs, one per tile
+        kp.tgt_in = uint32_t(kc.pair ? (kp.rs_groups ? per_tile * (kPairEpiWarps / 2) : per_tile) : 1);
         kp.tgt_free = kp.tgt_in;
     }
 }
@@ -189,19 +223,32 @@ cm_status setup_launch(const PlanImpl &pl, const KernelChoice &kc, KParams &kp, 
     return CM_OK;
 }
 
+// CM_OPT_TASK_ORDER automatic choice: a one-way ring runs step-major when the
+// weight shards of all ranks together take at most this many bytes (they
+// stay in L2 whichever order streams them, and step-major puts every task
+// furthest from the tasks it depends on); rank-blocked otherwise (each rank's
+// weight shard streamed in two runs instead of once per step).
+constexpr int64_t kStepMajorWeightBytes = int64_t(48) << 20;
+
+bool use_step_major(const PlanImpl &pl, int64_t weight_bytes) {
+    if (pl.task_order == 2) return true;
+    if (pl.task_order == 1) return false;
+    return weight_bytes <= kStepMajorWeightBytes;
+}
+
 cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, const WsLayout &l, void *ws,
-              bool b_mn, cudaStream_t stream) {
+              bool b_mn, bool step_major, cudaStream_t stream) {
     int sms = 0, max_clusters = 0;
     cm_status st = setup_launch(pl, kc, kp, l, ws, &sms, &max_clusters);
     if (st != CM_OK) return st;
-    const auto &tasks = pl.tasks[op];
+    const auto &tasks = step_major ? pl.tasks_sm[op] : pl.tasks[op];
     const int ntasks = int(tasks.size());
     if (ntasks > kMaxTasks) return CM_ERR_UNSUPPORTED;
     std::memcpy(kp.tasks, tasks.data(), sizeof(cm_task) * size_t(ntasks));
     // status word and flags start at zero for every call
     if (cudaMemsetAsync(ws, 0, l.buf_off, stream) != cudaSuccess) return CM_ERR_CUDA;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
-    const auto &sb = pl.step_begin[op];
+    const auto &sb = step_major ? pl.step_begin_sm[op] : pl.step_begin[op];
     const int nsteps = int(sb.size()) - 1;
     const int launches = pl.serial_steps ? nsteps : 1;
     for (int i = 0; i < launches; ++i) {
@@ -325,7 +372,8 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
     set_tiling(kc, CM_OP_AG_GEMM, kp, rows_c, n, true);
-    return run(pl, kc, CM_OP_AG_GEMM, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
+    const bool sm = use_step_major(pl, int64_t(N) * K * n * 2);
+    return run(pl, kc, CM_OP_AG_GEMM, kp, l, ws, b_mn, sm, reinterpret_cast<cudaStream_t>(stream));
 }
 
 cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y, cm_dtype y_dtype,
@@ -366,10 +414,10 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
     if (l.buf_bytes > 0) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
         const int64_t nbufs = rs_bufs(pl);
-        if (!make_map(&kp.tmAcc, promo, kp.acc, uint64_t(n), uint64_t(rows_c), uint64_t(nbufs * c), 32, 32, true))
-            return CM_ERR_CUDA;
+        if (!make_acc_maps(kp, promo, kp.acc, n, rows_c, nbufs * c)) return CM_ERR_CUDA;
         // received buckets through the operand ring: each CTA of a pair loads
-        // its 128 rows of the tile as 32-column boxes (one per 16 KB stage half)
+        // its 128 rows of the tile as 32-column boxes (one per 16 KB stage
+        // half); with buckets kept in place only the owner's tiles read one
         const int pre_stages = preload_stages(pl.rs_preload, (k + kBK - 1) / kBK);
         if (pre_stages > 0 && kc.pair) {
             const uint32_t pre_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
@@ -391,8 +439,10 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
+    kp.rs_groups = rs_groups(pl, k);
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
-    return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, reinterpret_cast<cudaStream_t>(stream));
+    const bool sm = use_step_major(pl, int64_t(N) * k * n * 2);
+    return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, sm, reinterpret_cast<cudaStream_t>(stream));
 }
 
 size_t cm_gemm_rs_pipelined_workspace_size(cm_plan_t plan, int64_t M, int64_t n) {
@@ -440,7 +490,7 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     }
     // partial products as [N*N*c][rows_c][n] fp32: slab (r*N + bucket)*c + chunk
     float *P = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
-    if (!make_map(&kp.tmAcc, promo, P, uint64_t(n), uint64_t(rows_c), uint64_t(N) * N * c, 32, 32, true)) return CM_ERR_CUDA;
+    if (!make_acc_maps(kp, promo, P, n, rows_c, int64_t(N) * N * c)) return CM_ERR_CUDA;
     kp.y = y;
     kp.acc = P;
     kp.y_rank_stride = 0;
@@ -454,6 +504,7 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
+    kp.rs_groups = rs_groups(pl, k);
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n);
     kp.tiles_per_task = kp.mtiles_c * kp.ntiles;   // one chunk per launch
     kp.tgt_in = kp.tgt_free = 0;
@@ -680,7 +731,7 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
     const KernelChoice kc = choose_kernel(pl);
     const bool b_mn = blayout == CM_W_KN;
     const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, bm));
-    if (!make_map(&kp.tmAcc, promo, acc, uint64_t(bn), uint64_t(bm), uint64_t(P) * 2, 32, 32, true)) return CM_ERR_CUDA;
+    if (!make_acc_maps(kp, promo, acc, bn, bm, int64_t(P) * 2)) return CM_ERR_CUDA;
     kp.y = c;
     kp.acc = acc;
     kp.out_rows_per_idx = bm;
@@ -693,6 +744,7 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
     kp.n = int(bn);
     kp.y_f32 = c_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
+    kp.rs_groups = rs_groups(pl, bk);
     set_tiling(kc, CM_OP_GEMM_RS, kp, bm, bn);
     kp.tgt_in = kp.tgt_free = 0;
     WsLayout l;

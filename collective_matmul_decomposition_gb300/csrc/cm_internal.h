@@ -45,11 +45,15 @@ struct PlanImpl {
     int bulk_overlap = 1;   // see CM_OPT_BULK_OVERLAP
     int rs_preload = 2;     // see CM_OPT_RS_PRELOAD
     int rs_in_place = 1;    // see CM_OPT_RS_IN_PLACE
+    int task_order = 0;     // see CM_OPT_TASK_ORDER
+    int rs_epilogue = 0;    // see CM_OPT_RS_EPILOGUE
     int64_t skip_signal = -1;
     Schedule sched[2];                    // per cm_op
-    std::vector<cm_task> tasks[2];        // per cm_op, execution order
+    std::vector<cm_task> tasks[2];        // per cm_op, the ring's own execution order
+    std::vector<cm_task> tasks_sm[2];     // per cm_op, step-major execution order
     int flag_ids[2] = {0, 0};             // ids used per op (before * chunks)
     std::vector<int> step_begin[2];       // first task index of each step (+ end sentinel)
+    std::vector<int> step_begin_sm[2];    // the same for tasks_sm
 };
 
 }  // namespace cm

@@ -59,7 +59,7 @@ __device__ void producer(const KParams &p, const Smem &s, int total) {
         const TileCoord c = decode(p, t);
         const cm_task &tk = p.tasks[c.task];
         if (p.op == 0 && tk.wait_in[0] >= 0) {
-            if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteProducerFlag, c.task, c.q)) break;
+            if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q, c.mt, 0), p.tgt_in, kSiteProducerFlag, c.task, c.q)) break;
             fence_proxy_async_global();
         }
         const void *tmA = tk.a_src == 1 ? static_cast<const void *>(&p.tmA1) : static_cast<const void *>(&p.tmA0);
@@ -141,7 +141,7 @@ __device__ void mma_issuer(const KParams &p, const Smem &s, int total, uint32_t 
         mma_commit(&s.tfull[accb]);
         // AG: every K slice of this tile's A rows has landed in shared memory,
         // so the slot rows it read may be overwritten by the next forward.
-        if (p.op == 0 && tk.sig_done >= 0) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
+        if (p.op == 0 && tk.sig_done >= 0) red_release_add(flag_ptr(p, tk.sig_done, c.q, c.mt, 0), 1u);
         if (++accb == 2) {
             accb = 0;
             acc_phase ^= 1u;
@@ -164,7 +164,7 @@ __device__ void forwarder(const KParams &p, const Smem &s, int total) {
         if (fwd) {
             for (int j = 0; j < 2 && ok; ++j)
                 if (tk.fwd_slot[j] >= 0 && tk.wait_free[j] >= 0)
-                    ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[j], c.q), p.tgt_free, kSiteForwardFlag, c.task, c.q);
+                    ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[j], c.q, c.mt, 0), p.tgt_free, kSiteForwardFlag, c.task, c.q);
             if (!ok) break;
             fence_proxy_async_global();
         }
@@ -200,7 +200,7 @@ __device__ void forwarder(const KParams &p, const Smem &s, int total) {
             bulk_wait<0>();               // the stores are complete in global memory
             fence_proxy_async_global();
             for (int j = 0; j < 2; ++j)
-                if (tk.fwd_slot[j] >= 0 && tk.sig_fwd[j] >= 0) red_release_add(flag_ptr(p, tk.sig_fwd[j], c.q), 1u);
+                if (tk.fwd_slot[j] >= 0 && tk.sig_fwd[j] >= 0) red_release_add(flag_ptr(p, tk.sig_fwd[j], c.q, c.mt, 0), 1u);
         }
     }
     bulk_wait<0>();
@@ -218,9 +218,9 @@ __device__ void epilogue(const KParams &p, const Smem &s, int total, uint32_t tm
         if (p.op == 1 && et == 0 && !bad) {
             for (int j = 0; j < 2 && !bad; ++j)
                 if (tk.wait_in[j] >= 0)
-                    bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q), p.tgt_in, kSiteEpilogueFlag, c.task, c.q);
+                    bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q, c.mt, c.nt), p.tgt_in, kSiteEpilogueFlag, c.task, c.q);
             if (!bad && tk.wait_free[0] >= 0)
-                bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[0], c.q), p.tgt_free, kSiteEpilogueFlag, c.task, c.q);
+                bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[0], c.q, c.mt, c.nt), p.tgt_free, kSiteEpilogueFlag, c.task, c.q);
         }
         bad = bar_or(1, 128, bad || *s.abort != 0);
         if (bad) break;
@@ -290,7 +290,7 @@ __device__ void epilogue(const KParams &p, const Smem &s, int total, uint32_t tm
         if (p.op == 1 && tk.sig_done >= 0) {
             __threadfence();
             bar_sync(1, 128);
-            if (et == 0) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
+            if (et == 0) red_release_add(flag_ptr(p, tk.sig_done, c.q, c.mt, c.nt), 1u);
         }
         if (++accb == 2) {
             accb = 0;

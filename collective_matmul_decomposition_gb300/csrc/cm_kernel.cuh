@@ -21,6 +21,10 @@ constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBN * kBK * 2;
 constexpr uint32_t kTmemCols = 512;   // two 128 x 256 fp32 accumulators
 constexpr int kSmemBytes = kStages * (kABytes + kBBytes) + 1024 /*barriers*/ + 1024 /*align slack*/;
+// Epilogue warps of each CTA of the pair kernel.  In GEMM -> ReduceScatter
+// they form two groups of half of them, one per accumulator, and each warp
+// of a group signals its share of a finished tile on its own.
+constexpr int kPairEpiWarps = 8;
 
 // Status word sites (which wait gave up), reported by cm_check_status.
 enum Site : uint32_t {
@@ -69,6 +73,8 @@ struct KParams {
     int pre_stages;            // ... as this many ring stages per tile (4: every slice, 2: the first two
                                //     32-column slices of each epilogue warp)
     int pre_box_rows;          // rows of a tmAccIn box (128, or rows_c if smaller)
+    int rs_groups;             // CTA pairs, RS: 1 = two epilogue warp groups (one per accumulator) with
+                               // vector reductions; 0 = every epilogue warp on every tile, TMA copies
     int chunk_pair;            // CTA pairs: a pair tile covers chunks 2g and 2g+1 (one per CTA; chunks
                                // of at most 128 rows), and the tile decode's chunk index is g
     int tiles_per_task, task_begin, task_end;

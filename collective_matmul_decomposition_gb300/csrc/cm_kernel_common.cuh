@@ -57,8 +57,15 @@ __device__ __forceinline__ TileCoord decode(const KParams &p, int t) {
     return c;
 }
 
-__device__ __forceinline__ uint32_t *flag_ptr(const KParams &p, int id, int q) {
-    return p.flags + size_t(id) * size_t(p.chunks) + size_t(q);
+// Readiness counter of flag `id` for the tile region a task reads or writes:
+// AG, one per (id, chunk, row tile) -- the shard rows of one row tile arrive
+// together (every column tile of the forwarding task sends a slice of them);
+// RS, one per (id, chunk, row tile, column tile) -- the bucket tile a task
+// adds to depends only on its predecessor's same tile.
+__device__ __forceinline__ uint32_t *flag_ptr(const KParams &p, int id, int q, int mt, int nt) {
+    size_t w = (size_t(id) * size_t(p.chunks) + size_t(q)) * size_t(p.mtiles_c) + size_t(mt);
+    if (p.op == 1) w = w * size_t(p.ntiles) + size_t(nt);
+    return p.flags + w;
 }
 
 __device__ __forceinline__ int kslices(const KParams &p, const cm_task &tk) {

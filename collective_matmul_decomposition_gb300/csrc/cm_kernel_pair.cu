@@ -59,7 +59,7 @@ constexpr int kPairRows = 256;          // output rows per pair tile
 constexpr int kCtaRows = 128;           // rows staged per CTA
 constexpr int kPStages = 6;
 constexpr int kPThreads = 384;
-constexpr int kPEpiWarps = 8;
+constexpr int kPEpiWarps = kPairEpiWarps;
 constexpr int kHalfA = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kHalfB = (kBN / 2) * kBK * 2;  // 16 KB
 constexpr int kFwdPiece = 16384;             // forwarder copy granule
@@ -95,7 +95,8 @@ struct QTile {
     int t, task, q, mt, nt, nk, a_src, a_row, n0, slab, rr, sig;
     int pre;        // RS preload: accumulator buffer whose bucket is loaded before the K slices, -1 none
     int row0;       // this CTA's first output row inside its chunk q
-    int pad[2];
+    int ready;      // RS: the scheduler found every input flag of the tile already at its target
+    int pad;
 };
 constexpr int kQWords = 16;
 
@@ -117,7 +118,7 @@ struct QueueReader {
             const volatile int4 *v = reinterpret_cast<const volatile int4 *>(s.qent + kQWords * slot);
             const int4 a = const_cast<const int4 &>(v[0]), b = const_cast<const int4 &>(v[1]),
                        c = const_cast<const int4 &>(v[2]), d = const_cast<const int4 &>(v[3]);
-            e = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, d.y, {d.z, d.w}};
+            e = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, d.x, d.y, d.z, d.w};
         }
         if (release) mbar_arrive_cluster(qempty_leader0 + 8u * uint32_t(slot));
         if (++slot == kQueue) {
@@ -290,7 +291,8 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
         const int q0 = p.chunk_pair ? 2 * c.q : c.q, nq = p.chunk_pair ? 2 : 1;
         if (t >= 0 && p.op == 0 && tk.wait_in[0] >= 0)
             for (int qq = q0; qq < q0 + nq; ++qq)
-                if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], qq), p.tgt_in, kSiteProducerFlag, c.task, qq))
+                if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], qq, c.mt, c.nt), p.tgt_in, kSiteProducerFlag,
+                               c.task, qq))
                     return;
         // RS preload: the received bucket is read before the partial GEMM, so
         // its producers must be done before this tile is published
@@ -298,8 +300,19 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
                          tk.in_buf[0] != tk.out_buf;
         if (pre && tk.wait_in[0] >= 0)
             for (int qq = q0; qq < q0 + nq; ++qq)
-                if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], qq), p.tgt_in, kSiteProducerFlag, c.task, qq))
+                if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], qq, c.mt, c.nt), p.tgt_in, kSiteProducerFlag,
+                               c.task, qq))
                     return;
+        // RS: one look (no waiting) at the flags the tile's epilogue would wait
+        // for; if all are complete the epilogue skips its wait
+        int ready = 1;
+        if (t >= 0 && p.op == 1) {
+            for (int jj = 0; jj < 2 && ready; ++jj)
+                if (tk.wait_in[jj] >= 0 && !(pre && jj == 0))
+                    for (int qq = q0; qq < q0 + nq && ready; ++qq)
+                        if (ld_acquire(flag_ptr(p, tk.wait_in[jj], qq, c.mt, c.nt)) < p.tgt_in) ready = 0;
+            if (tk.wait_free[0] >= 0) ready = 0;
+        }
         if (!wait_mbar<true>(p, s.abort, &s.qempty[slot], qphase ^ 1u, kSiteEmpty, -1, -1)) return;
         const bool sum_ranks = tk.a_src == 2;
         const int slab0 = (sum_ranks ? tk.out_idx : tk.a_slab) * p.chunks;
@@ -317,7 +330,7 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
             const uint32_t w[kQWords] = {uint32_t(t),   uint32_t(c.task), uint32_t(q),   uint32_t(c.mt),
                                          uint32_t(nt),  uint32_t(nk),     uint32_t(tk.a_src), uint32_t(a_row),
                                          uint32_t(n0),  uint32_t(slab),   uint32_t(rr),       uint32_t(sig),
-                                         uint32_t(pre ? int(tk.in_buf[0]) : -1), uint32_t(row0), 0u, 0u};
+                                         uint32_t(pre ? int(tk.in_buf[0]) : -1), uint32_t(row0), uint32_t(ready), 0u};
             if (r == 0) {
                 for (int i = 0; i < kQWords; ++i) e[i] = int32_t(w[i]);
             } else {
@@ -415,8 +428,8 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
         mma_commit_pair_mc(&s.tfull[accb], uint16_t((1u << CL) - 1u));   // both CTAs' accumulators
         // AG: both CTAs' A slices of this tile have landed; the slot rows may be reused
         if (c.sig >= 0) {
-            red_release_add(flag_ptr(p, c.sig, c.q), 1u);
-            if (p.chunk_pair) red_release_add(flag_ptr(p, c.sig, c.q + 1), 1u);   // the peer CTA's chunk
+            red_release_add(flag_ptr(p, c.sig, c.q, c.mt, c.nt), 1u);
+            if (p.chunk_pair) red_release_add(flag_ptr(p, c.sig, c.q + 1, c.mt, c.nt), 1u);   // the peer CTA's chunk
         }
         if (++accb == 2) {
             accb = 0;
@@ -442,7 +455,8 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
         if (!(tk.fwd_slot[0] >= 0 || tk.fwd_slot[1] >= 0)) continue;
         bool ok = true;
         if (tk.a_src == 1 && tk.wait_in[0] >= 0)   // the shard chunk has arrived here
-            ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q), p.tgt_in, kSiteForwardFlag, c.task, c.q);
+            ok = wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q, c.mt, c.nt), p.tgt_in, kSiteForwardFlag,
+                           c.task, c.q);
         if (!ok) break;
         fence_proxy_async_global();
         const int lo = c.nt * per;
@@ -486,7 +500,8 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
         }
         fence_proxy_async_global();
         for (int j = 0; j < 2; ++j)
-            if (tk.fwd_slot[j] >= 0 && tk.sig_fwd[j] >= 0) red_release_add(flag_ptr(p, tk.sig_fwd[j], c.q), 1u);
+            if (tk.fwd_slot[j] >= 0 && tk.sig_fwd[j] >= 0)
+                red_release_add(flag_ptr(p, tk.sig_fwd[j], c.q, c.mt, c.nt), 1u);
     }
     bulk_wait<0>();
 }
@@ -576,8 +591,10 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
 // 16-byte chunk j of row r sits at chunk position j ^ (r & 7).
 __device__ __forceinline__ float4 *swz_row(uint8_t *buf, int row) { return reinterpret_cast<float4 *>(buf + row * 128); }
 
-// GEMM -> ReduceScatter epilogue, per 32-column slice of each warp's 32 rows
-// (one 4 KB fp32 box staged in shared memory):
+// GEMM -> ReduceScatter epilogue through the TMA unit (CM_OPT_RS_EPILOGUE =
+// 1).  All eight warps drain every tile: warp e takes 32 rows (TMEM lanes
+// 32*(e % 4)..) x 128 columns (half e / 4), per 32-column slice (one 4 KB
+// fp32 box staged in shared memory):
 //  - a bucket kept in place (in_buf[0] == out_buf): the TMEM slice is added
 //    into the bucket where it lies with a TMA reduce-add, so nothing comes
 //    back to the SM;
@@ -586,7 +603,7 @@ __device__ __forceinline__ float4 *swz_row(uint8_t *buf, int row) { return reint
 //    the slice added, and the sum TMA-stored to the next rank's buffer;
 //  - the owner: the received partial bucket(s) are TMA-loaded, the slice
 //    added, and the sum rounded into the output.
-__device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
+__device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     const int e = int(threadIdx.x) / 32 - 4;   // 0..7
     const int lane = int(threadIdx.x) & 31;
     const int quad = e & 3;
@@ -614,16 +631,17 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         const int row0 = __shfl_sync(0xffffffffu, e.row0, 0);   // this CTA's first row in chunk c.q
         const int pre = __shfl_sync(0xffffffffu, e.pre, 0);   // in_buf[0]'s slices cb < p.pre_stages are
                                                               // already in the accumulator
+        const int ready = __shfl_sync(0xffffffffu, e.ready, 0);   // inputs found complete by the scheduler
         const cm_task &tk = p.tasks[c.task];
         if (!bad) bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
-        if (leader_thread && !bad) {
+        if (leader_thread && !bad && !ready) {
             for (int j = 0; j < 2 && !bad; ++j)
                 if (tk.wait_in[j] >= 0)
-                    bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q), p.tgt_in, kSiteEpilogueFlag, c.task,
-                                     c.q);
+                    bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[j], c.q, c.mt, c.nt), p.tgt_in,
+                                     kSiteEpilogueFlag, c.task, c.q);
             if (!bad && tk.wait_free[0] >= 0)
-                bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[0], c.q), p.tgt_free, kSiteEpilogueFlag, c.task,
-                                 c.q);
+                bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[0], c.q, c.mt, c.nt), p.tgt_free,
+                                 kSiteEpilogueFlag, c.task, c.q);
         }
         bad = bar_or(1, kPEpiWarps * 32, bad || *s.abort != 0);
         if (bad) break;
@@ -733,7 +751,7 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
             }
             __threadfence();
             bar_sync(1, kPEpiWarps * 32);
-            if (leader_thread && !*s.abort) red_release_add(flag_ptr(p, tk.sig_done, c.q), 1u);
+            if (leader_thread && !*s.abort) red_release_add(flag_ptr(p, tk.sig_done, c.q, c.mt, c.nt), 1u);
         }
         if (++accb == 2) {
             accb = 0;
@@ -741,6 +759,173 @@ __device__ void epilogue_rs(const KParams &p, const PSmem &s, uint32_t tmem_base
         }
     }
     if (lane == 0) bulk_wait<0>();
+}
+
+// GEMM -> ReduceScatter epilogue in two warp groups (CM_OPT_RS_EPILOGUE =
+// 2).  The eight epilogue warps form two groups of four, one per TMEM
+// accumulator: group g takes every other tile (the ones
+// the MMA thread put in accumulator g), so two tiles' epilogues -- and their
+// latencies (input flags, the wait for a tile's adds to be performed) --
+// overlap.  In a group, warp w reads TMEM lanes 32*(w % 4).. and handles those
+// 32 rows x 256 columns of the tile in eight 32-column slices.  A slice read
+// from TMEM (one row per lane) is turned round through the warp's 4 KB
+// buffer, so that each lane then holds four consecutive columns of 8 rows and
+// 8 lanes cover a row's 128 bytes: every global access below is a coalesced
+// 16-byte vector, and none goes through the TMA unit, which stays free for
+// the operand loads.
+//  - a bucket kept in place (in_buf[0] == out_buf): the slice is added into
+//    the bucket where it lies (red.global.add.v4.f32, performed at L2);
+//  - the first contributor (no input): the slice is stored as the bucket;
+//  - a bucket in per-step buffers: the received partial bucket is loaded,
+//    the slice added, and the sum stored to the next rank's buffer;
+//  - the owner: the received partial bucket(s) are loaded, the slice added,
+//    and the sum rounded into the output.
+// TMEM slices are loaded one ahead.  Each warp signals its share of a tile
+// on its own, once its lanes' accesses are ordered before the signal (a
+// fence in every lane, a warp barrier, a release by lane 0): a consumer waits
+// for all four warps of the group in each CTA, and no warp waits for another.
+
+__device__ void epilogue_rs_grp(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
+    const int e = int(threadIdx.x) / 32 - 4;   // 0..7
+    const int lane = int(threadIdx.x) & 31;
+    const int quad = e & 3;                    // TMEM lanes 32*quad.. (warp % 4)
+    const int grp = e >> 2;                    // accumulator (and tile parity) of this warp's group
+    const uint32_t tempty_leader0 = mapa_shared(smem_u32(&s.tempty[0]), cl.leader);   // buffer b: +8*b
+    uint8_t *buf = s.fbuf[0] + e * 4096;   // 32 rows x 128 bytes; 16-byte chunk j of row r at j ^ (r & 7)
+    const int tr = lane >> 3, tc = lane & 7;   // turned round: rows 4i + tr, columns 4tc..4tc+3 of the slice
+    QueueReader qr;
+    if (lane == 0) qr.init(s);
+    const int accb = grp;
+    uint32_t acc_phase = 0;
+    for (int j = 0;; ++j) {
+        QTile e;
+        if (lane == 0) e = qr.next(p, s, true);   // every warp reads (and releases) every entry
+        const int t = __shfl_sync(0xffffffffu, e.t, 0);
+        if (t < 0) break;
+        if ((j & 1) != grp) continue;   // the other group's tile
+        TileCoord c;
+        c.task = __shfl_sync(0xffffffffu, e.task, 0);
+        c.q = __shfl_sync(0xffffffffu, e.q, 0);
+        c.mt = __shfl_sync(0xffffffffu, e.mt, 0);
+        c.nt = __shfl_sync(0xffffffffu, e.nt, 0);
+        const int row0 = __shfl_sync(0xffffffffu, e.row0, 0);   // this CTA's first row in chunk c.q
+        const int pre = __shfl_sync(0xffffffffu, e.pre, 0);   // in_buf[0]'s slices with (slice % 4) <
+                                                              // p.pre_stages are already in the accumulator
+        const int ready = __shfl_sync(0xffffffffu, e.ready, 0);   // inputs found complete by the scheduler
+        const cm_task &tk = p.tasks[c.task];
+        bool bad = !wait_mbar<true>(p, s.abort, &s.tfull[accb], acc_phase, kSiteTmemFull, c.task, c.q);
+        // each warp acquires the tile's input flags itself (unless the
+        // scheduler already found them complete): no barrier across warps
+        if (lane == 0 && !bad && !ready) {
+            for (int jj = 0; jj < 2 && !bad; ++jj)
+                if (tk.wait_in[jj] >= 0)
+                    bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[jj], c.q, c.mt, c.nt), p.tgt_in,
+                                     kSiteEpilogueFlag, c.task, c.q);
+            if (!bad && tk.wait_free[0] >= 0)
+                bad = !wait_flag(p, s.abort, flag_ptr(p, tk.wait_free[0], c.q, c.mt, c.nt), p.tgt_free,
+                                 kSiteEpilogueFlag, c.task, c.q);
+        }
+        bad = __any_sync(0xffffffffu, bad || *s.abort != 0);
+        __syncwarp();   // lane 0's acquire orders the whole warp's accesses below
+        if (bad) break;
+        tc_fence_after();
+
+        const int row_w = row0 + quad * 32;   // warp's first row in the chunk
+        // the bucket is accumulated where it lies: its partial sum is not read here
+        const bool in_place = tk.out_buf >= 0 && tk.in_buf[0] == tk.out_buf;
+        const int64_t brow0 = int64_t(c.q) * p.rows_c + row_w;   // warp's first row in the bucket
+        const uint32_t tcol = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN);
+        uint32_t v[2][32];
+        tmem_ld32(tcol, v[0]);
+        tmem_wait_ld_regs(v[0]);
+#pragma unroll
+        for (int cb = 0; cb < kBN / 32; ++cb) {
+            uint32_t(&cur)[32] = v[cb & 1];
+            if (cb + 1 < kBN / 32) tmem_ld32(tcol + uint32_t((cb + 1) * 32), v[(cb + 1) & 1]);   // in flight
+            const int col0 = c.nt * kBN + cb * 32;
+            if (col0 < p.n) {
+                float4 *wr = reinterpret_cast<float4 *>(buf + lane * 128);
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    wr[k ^ (lane & 7)] = make_float4(__uint_as_float(cur[4 * k]), __uint_as_float(cur[4 * k + 1]),
+                                                     __uint_as_float(cur[4 * k + 2]), __uint_as_float(cur[4 * k + 3]));
+                __syncwarp();
+                float4 x[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int r = 4 * i + tr;
+                    x[i] = reinterpret_cast<const float4 *>(buf + r * 128)[tc ^ (r & 7)];
+                }
+                __syncwarp();   // every lane has read the buffer before the next slice is written
+                const int col = col0 + 4 * tc;
+                const bool col_ok = col < p.n;   // n is a multiple of 8: a vector is all in or all out
+                for (int jj = 0; jj < 2; ++jj) {
+                    if (tk.in_buf[jj] < 0 || (jj == 0 && (in_place || (pre >= 0 && (cb & 3) < p.pre_stages))))
+                        continue;
+                    const float *src = p.acc + int64_t(tk.in_buf[jj]) * p.acc_buf_stride + brow0 * p.n + col;
+                    float4 a[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (col_ok && row_w + 4 * i + tr < p.rows_c)
+                            a[i] = __ldcg(reinterpret_cast<const float4 *>(src + int64_t(4 * i + tr) * p.n));
+                        else
+                            a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        x[i].x += a[i].x;
+                        x[i].y += a[i].y;
+                        x[i].z += a[i].z;
+                        x[i].w += a[i].w;
+                    }
+                }
+                if (tk.out_buf >= 0) {
+                    float *dst = p.acc + int64_t(tk.out_buf) * p.acc_buf_stride + brow0 * p.n + col;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (!col_ok || row_w + 4 * i + tr >= p.rows_c) continue;
+                        float *d = dst + int64_t(4 * i + tr) * p.n;
+                        if (in_place)
+                            red_add_v4(d, x[i]);
+                        else
+                            __stcg(reinterpret_cast<float4 *>(d), x[i]);
+                    }
+                } else {   // owner: the bucket is home
+                    const int64_t orow0 = (int64_t(tk.out_idx) * p.out_rows_per_idx + brow0) * p.n + col;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        if (!col_ok || row_w + 4 * i + tr >= p.rows_c) continue;
+                        const int64_t o = orow0 + int64_t(4 * i + tr) * p.n;
+                        if (p.y_f32) {
+                            *reinterpret_cast<float4 *>(static_cast<float *>(p.y) + o) = x[i];
+                        } else {
+                            __nv_bfloat162 lo = __floats2bfloat162_rn(x[i].x, x[i].y);
+                            __nv_bfloat162 hi = __floats2bfloat162_rn(x[i].z, x[i].w);
+                            *reinterpret_cast<uint2 *>(static_cast<__nv_bfloat16 *>(p.y) + o) =
+                                make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+                        }
+                    }
+                }
+            }
+            if (cb + 1 < kBN / 32) tmem_wait_ld_regs(v[(cb + 1) & 1]);
+        }
+        // half preload: the next tile in this accumulator adds onto every
+        // column, so the columns it will not preload must read zero
+        if (p.pre_stages > 0 && p.pre_stages < 4) {
+            for (int h = 0; h < 2; ++h)
+                for (int cb = p.pre_stages; cb < 4; ++cb)
+                    tmem_zero32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN + h * 128 + cb * 32));
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(tempty_leader0 + 8u * uint32_t(accb));
+        if (tk.sig_done >= 0) {
+            fence_acq_rel_gpu();   // this lane's adds / stores of the tile come before the signal
+            __syncwarp();
+            if (lane == 0 && !*s.abort) red_release_add(flag_ptr(p, tk.sig_done, c.q, c.mt, c.nt), 1u);
+        }
+        acc_phase ^= 1u;
+    }
 }
 
 template <int LAYOUT>
@@ -779,7 +964,9 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s.tfull[i], 1);
-            mbar_init(&s.tempty[i], 2 * kPEpiWarps);   // epilogue warps of both CTAs
+            // epilogue warps of both CTAs that drain accumulator i: all eight,
+            // or the four of the group that owns it (RS in two groups)
+            mbar_init(&s.tempty[i], 2 * (p.op == 1 && p.rs_groups ? kPEpiWarps / 2 : kPEpiWarps));
             mbar_init(&s.fbar[i], 1);
         }
         mbar_init(s.drain, 1);
@@ -841,8 +1028,10 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     } else if (warp >= 4) {
         if (p.op == 0)
             epilogue_ag(p, s, tmem_base, cl);
+        else if (p.rs_groups)
+            epilogue_rs_grp(p, s, tmem_base, cl);
         else
-            epilogue_rs(p, s, tmem_base, cl);
+            epilogue_rs_tma(p, s, tmem_base, cl);
     }
     tc_fence_before();
     __syncthreads();

@@ -147,8 +147,10 @@ int rank_blocked_key(int N, int r, int i) {
     return first + r * (N - 1) - r * (r - 1) / 2 + (i - r - 1);      // block (r, r+1..N-1)
 }
 
-void order_and_index(PlanImpl &p, int op, std::vector<cm_task> &tasks) {
-    if (p.dir == CM_RING_UNI && !p.serial_steps) {
+// Sort `tasks` into execution order -- rank-blocked (rank_blocked true) or
+// step-major -- and fill in the tile groups and the step index `sb`.
+void order_and_index(PlanImpl &p, int op, std::vector<cm_task> &tasks, bool rank_blocked, std::vector<int> &sb) {
+    if (rank_blocked) {
         const int N = p.N;
         std::stable_sort(tasks.begin(), tasks.end(), [N](const cm_task &x, const cm_task &y) {
             return rank_blocked_key(N, x.rank, x.step) < rank_blocked_key(N, y.rank, y.step);
@@ -174,10 +176,19 @@ void order_and_index(PlanImpl &p, int op, std::vector<cm_task> &tasks) {
         for (size_t j = t; j < e; ++j) tasks[j].tile_group = int16_t(((e - t) << 8) | (j - t));
         t = e;
     }
-    auto &sb = p.step_begin[op];
     sb.assign(size_t(p.sched[op].steps) + 1, int(tasks.size()));
     for (int t = int(tasks.size()) - 1; t >= 0; --t) sb[tasks[size_t(t)].step] = t;
     for (int i = int(sb.size()) - 2; i >= 0; --i) sb[size_t(i)] = std::min(sb[size_t(i)], sb[size_t(i) + 1]);
+}
+
+// Both execution orders of one op's tasks: the ring's own (rank-blocked for a
+// one-way ring, step-major otherwise and in the step-serial mode) and the
+// step-major one.
+void set_orders(PlanImpl &p, int op, const std::vector<cm_task> &tasks) {
+    p.tasks[op] = tasks;
+    order_and_index(p, op, p.tasks[op], p.dir == CM_RING_UNI && !p.serial_steps, p.step_begin[op]);
+    p.tasks_sm[op] = tasks;
+    order_and_index(p, op, p.tasks_sm[op], false, p.step_begin_sm[op]);
 }
 
 void build_ag_tasks(PlanImpl &p) {
@@ -221,8 +232,7 @@ void build_ag_tasks(PlanImpl &p) {
                 }
         }
     }
-    order_and_index(p, CM_OP_AG_GEMM, tasks);
-    p.tasks[CM_OP_AG_GEMM] = tasks;
+    set_orders(p, CM_OP_AG_GEMM, tasks);
 }
 
 void build_rs_tasks(PlanImpl &p) {
@@ -287,8 +297,7 @@ void build_rs_tasks(PlanImpl &p) {
                     tasks.push_back(t);
                 }
     }
-    order_and_index(p, CM_OP_GEMM_RS, tasks);
-    p.tasks[CM_OP_GEMM_RS] = tasks;
+    set_orders(p, CM_OP_GEMM_RS, tasks);
 }
 
 void apply_skip(PlanImpl &p) {
@@ -297,11 +306,12 @@ void apply_skip(PlanImpl &p) {
     const int rank = int((p.skip_signal >> 8) & 0xff);
     const int step = int(p.skip_signal & 0xff);
     if (op > 1) return;
-    for (cm_task &t : p.tasks[op])
-        if (t.rank == rank && t.step == step) {
-            t.sig_fwd[0] = t.sig_fwd[1] = -1;
-            t.sig_done = -1;
-        }
+    for (auto *v : {&p.tasks[op], &p.tasks_sm[op]})
+        for (cm_task &t : *v)
+            if (t.rank == rank && t.step == step) {
+                t.sig_fwd[0] = t.sig_fwd[1] = -1;
+                t.sig_done = -1;
+            }
 }
 
 }  // namespace
@@ -366,7 +376,7 @@ cm_status cm_plan_step(cm_plan_t plan, cm_op op, int rank, int step, int stream,
 
 int cm_plan_tasks(cm_plan_t plan, cm_op op, cm_task *out, int capacity) {
     if (!plan || (op != CM_OP_AG_GEMM && op != CM_OP_GEMM_RS)) return -1;
-    const auto &t = plan->impl.tasks[op];
+    const auto &t = plan->impl.task_order == 2 ? plan->impl.tasks_sm[op] : plan->impl.tasks[op];
     for (int i = 0; i < capacity && i < int(t.size()); ++i) out[i] = t[size_t(i)];
     return int(t.size());
 }
@@ -426,6 +436,14 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
             return CM_OK;
         case CM_OPT_STATIC_TILES:
             p.static_tiles = value != 0;
+            return CM_OK;
+        case CM_OPT_RS_EPILOGUE:
+            if (value < 0 || value > 2) return CM_ERR_INVALID_ARG;
+            p.rs_epilogue = int(value);
+            return CM_OK;
+        case CM_OPT_TASK_ORDER:
+            if (value < 0 || value > 2) return CM_ERR_INVALID_ARG;
+            p.task_order = int(value);
             return CM_OK;
         case CM_OPT_RS_IN_PLACE:
             if (value != 0 && value != 1) return CM_ERR_INVALID_ARG;

@@ -131,7 +131,8 @@ cm_status cm_plan_step(cm_plan_t plan, cm_op op, int rank, int step, int stream,
  * rank N-1's steps 0..N-1, then rank 0's steps 1..N-1, rank 1's steps
  * 2..N-1, ... -- so each rank's weight shard is streamed in two runs; for a
  * bidirectional ring, CM_RING_NONE and the step-serial mode, step-major and
- * by rank inside a step.  Every flag a task waits on is raised by an earlier
+ * by rank inside a step (CM_OPT_TASK_ORDER runs a one-way ring step-major
+ * too).  Every flag a task waits on is raised by an earlier
  * task.  Exposed so tests can check the table's dependency structure on the
  * host.
  */
@@ -347,9 +348,9 @@ const char *cm_status_string(cm_status status);
  *                        (k <= 512), where the epilogue sets the pace, and
  *                        none beyond (the epilogue then hides under the
  *                        partial GEMM).  The same sum, in a different fp32
- *                        order.  Buckets accumulated in place (below) are
- *                        never preloaded: only the owner's tile, which reads
- *                        its bucket, can be.
+ *                        order.  With buckets kept in place (below) only
+ *                        the owner's tiles read a bucket, so only they are
+ *                        preloaded.
  *  CM_OPT_RS_IN_PLACE    cm_gemm_rs (and the backward pair's data gradient)
  *                        on a ring: 1 (default) keeps each bucket in one fp32
  *                        buffer per ring stream that the first contributor
@@ -362,6 +363,30 @@ const char *cm_status_string(cm_status status);
  *                        the same order.  Changes the workspace size (N
  *                        buffers per stream instead of N per stream and
  *                        step), so size the workspace after setting it.
+ *  CM_OPT_TASK_ORDER     order of a one-way ring's tasks: 1 rank-blocked
+ *                        (see cm_task: each weight shard streamed in two
+ *                        runs), 2 step-major (every rank's step 0, then every
+ *                        rank's step 1, ...: a task is as far as possible from
+ *                        the ones it waits for), 0 (default) step-major when
+ *                        the weight shards of all ranks together take at most
+ *                        48 MB -- they stay in L2 either way -- and
+ *                        rank-blocked otherwise.  cm_plan_tasks lists the
+ *                        step-major table under 2 and the ring's own order
+ *                        under 0 and 1.  Bidirectional rings always run
+ *                        step-major.  The same results.
+ *  CM_OPT_RS_EPILOGUE    how the CTA-pair kernel moves GEMM -> ReduceScatter
+ *                        tiles out of tensor memory: 1 every epilogue warp
+ *                        on every tile, the bucket slices copied by TMA
+ *                        through shared memory (reduce-add, store or load);
+ *                        2 two groups of epilogue warps, one per tensor-memory
+ *                        accumulator, so that two tiles drain at once, with
+ *                        coalesced vector adds (red.global.add.v4.f32),
+ *                        stores and loads; 0 (default) two groups for rings
+ *                        of 8 ranks (one-way) or 16 (either) whose tiles
+ *                        have at least 28 K slices of 64, the TMA path
+ *                        otherwise (the faster of the two in measurement).
+ *                        The same fp32 additions in the same order: the same
+ *                        bits.
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
@@ -376,7 +401,9 @@ typedef enum cm_option {
     CM_OPT_ROW_BAND = 9,
     CM_OPT_BULK_OVERLAP = 10,
     CM_OPT_RS_PRELOAD = 11,
-    CM_OPT_RS_IN_PLACE = 12
+    CM_OPT_RS_IN_PLACE = 12,
+    CM_OPT_TASK_ORDER = 13,
+    CM_OPT_RS_EPILOGUE = 14
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);

@@ -30,15 +30,21 @@ pytestmark = pytest.mark.gpu
 PAIR, SINGLE = 0, 1
 
 
-def _plan(N, chunks, direction, in_place, kernel=PAIR, preload=0):
+def _plan(N, chunks, direction, in_place, kernel=PAIR, preload=0, epilogue=0):
     p = cm.Plan(N, chunks, direction)
     p.set_option(cm.CM_OPT_RS_IN_PLACE, in_place)
     p.set_option(cm.CM_OPT_KERNEL, kernel)
     p.set_option(cm.CM_OPT_RS_PRELOAD, preload)
+    p.set_option(cm.CM_OPT_RS_EPILOGUE, epilogue)
     return p
 
 
-@pytest.mark.parametrize("kernel", [PAIR, SINGLE])
+# the CTA-pair kernel with each RS epilogue (TMA copies / two warp groups
+# with vector adds), and the single-CTA kernel
+KERNEL_EPILOGUES = [(PAIR, 1), (PAIR, 2), (SINGLE, 0)]
+
+
+@pytest.mark.parametrize("kernel,epilogue", KERNEL_EPILOGUES)
 @pytest.mark.parametrize("N,M,k,n,chunks,direction", [
     (2, 256, 128, 512, 1, "uni"),
     (3, 768, 200, 296, 2, "uni"),       # ragged k and n
@@ -46,20 +52,40 @@ def _plan(N, chunks, direction, in_place, kernel=PAIR, preload=0):
     (5, 1280, 136, 520, 1, "bidi"),     # odd N: both streams equally long
     (8, 4096, 256, 1024, 4, "uni"),     # chunks of 128 rows: two chunks per pair tile
     (8, 2048, 64, 256, 1, "bidi"),
+    (4, 1536, 96, 1032, 1, "uni"),      # ragged last column tile, rows straddling the pair split
 ])
-def test_in_place_matches_per_step_buffers_bitwise(kernel, N, M, k, n, chunks, direction):
+def test_in_place_matches_per_step_buffers_bitwise(kernel, epilogue, N, M, k, n, chunks, direction):
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=N * 100 + k, w_layout="nk")
     ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
-    y0, _, _ = run_rs(_plan(N, chunks, direction, 0, kernel), x, w, "nk", torch.float32)
-    y1, _, _ = run_rs(_plan(N, chunks, direction, 1, kernel), x, w, "nk", torch.float32)
+    y0, _, _ = run_rs(_plan(N, chunks, direction, 0, kernel, 0, epilogue), x, w, "nk", torch.float32)
+    y1, _, _ = run_rs(_plan(N, chunks, direction, 1, kernel, 0, epilogue), x, w, "nk", torch.float32)
     assert torch.isfinite(y1).all()
     assert oracle.normwise_max_rel_err(_np(y1), ref) <= TOL_F32
     assert torch.equal(y0, y1)
 
 
+@pytest.mark.parametrize("in_place", [1, 0])
+@pytest.mark.parametrize("preload", [0, 1, 3])
+@pytest.mark.parametrize("direction", ["uni", "bidi"])
+def test_rs_epilogues_agree_bitwise(in_place, preload, direction):
+    """The two CTA-pair RS epilogues make the same fp32 additions in the same
+    order: the same bits, in both bucket modes and every preload mode."""
+    N, M, k, n = 8, 2048, 256, 1288
+    x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=71, w_layout="nk")
+    ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
+    ys = []
+    for epilogue in (1, 2):
+        for ydtype in (torch.float32, torch.bfloat16):
+            y, _, _ = run_rs(_plan(N, 2, direction, in_place, PAIR, preload, epilogue), x, w, "nk", ydtype)
+            assert oracle.normwise_max_rel_err(_np(y), ref) <= (TOL_F32 if ydtype == torch.float32 else TOL)
+            ys.append(y)
+    assert torch.equal(ys[0], ys[2]) and torch.equal(ys[1], ys[3])
+
+
 @pytest.mark.parametrize("preload", [0, 1, 2, 3])
 def test_in_place_with_owner_preload(preload):
-    """Only the owner's tile reads its bucket; every preload mode is legal."""
+    """Only the owner's tile reads its bucket, and only there does the
+    preload apply; every preload mode gives the oracle's result."""
     N, M, k, n = 8, 4096, 256, 2048
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=91, w_layout="kn")
     ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), "kn")
@@ -78,18 +104,19 @@ def test_in_place_exact_on_integers():
     x = torch.randint(-3, 4, (N, M, k), generator=g).to(torch.bfloat16)
     w = torch.randint(-3, 4, (N, n, k), generator=g).to(torch.bfloat16)
     ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
-    for kernel in (PAIR, SINGLE):
+    for kernel, epilogue in KERNEL_EPILOGUES:
         for direction in ("uni", "bidi"):
-            y, _, _ = run_rs(_plan(N, 2, direction, 1, kernel, 2), x, w, "nk", torch.float32)
+            y, _, _ = run_rs(_plan(N, 2, direction, 1, kernel, 2, epilogue), x, w, "nk", torch.float32)
             assert np.array_equal(_np(y), ref)
 
 
-def test_in_place_dropped_signal_times_out():
+@pytest.mark.parametrize("epilogue", [1, 2])
+def test_in_place_dropped_signal_times_out(epilogue):
     """A contributor that never signals: its successor's addition and the
     owner's read wait for it, time out, and the next call is correct."""
     N, M, k, n = 4, 1024, 128, 256
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=5, w_layout="nk")
-    p = _plan(N, 1, "uni", 1)
+    p = _plan(N, 1, "uni", 1, PAIR, 0, epilogue)
     p.set_option(cm.CM_OPT_TIMEOUT_NS, 50_000_000)
     p.set_option(cm.CM_OPT_SKIP_SIGNAL, (cm.CM_OP_GEMM_RS << 16) | (1 << 8) | 1)
     _, st, info = run_rs(p, x, w, "nk", torch.float32, check=False)
@@ -119,3 +146,25 @@ def test_in_place_back_to_back_on_one_workspace():
     assert st == 0, (st, info)
     for y, ref in zip(outs, refs):
         assert oracle.normwise_max_rel_err(_np(y), ref) <= TOL_F32
+
+
+@pytest.mark.parametrize("N,chunks", [(4, 1), (8, 2)])
+def test_task_orders_agree_bitwise(N, chunks):
+    """Rank-blocked and step-major task orders only reorder the tiles: every
+    output element is the same dot product (AllGather->GEMM) or the same
+    ring-ordered fp32 sum (GEMM->ReduceScatter), so the bits agree."""
+    m, K, n = 256, 384, 768
+    x, w = gen.ag_inputs(N, m, K, n, gen.NORMAL1, gen.NORMAL002, seed=61, w_layout="nk")
+    xr, wr = gen.rs_inputs(N, N * m, K, n, gen.NORMAL1, gen.NORMAL002, seed=62, w_layout="nk")
+    from test_gpu_parity import run_ag
+    outs = []
+    for order in (1, 2):
+        p = cm.Plan(N, chunks, "uni")
+        p.set_option(cm.CM_OPT_TASK_ORDER, order)
+        y, _, _ = run_ag(p, x, w, "nk", torch.float32)
+        yr, _, _ = run_rs(p, xr, wr, "nk", torch.float32)
+        outs.append((y, yr))
+    assert torch.equal(outs[0][0], outs[1][0])
+    assert torch.equal(outs[0][1], outs[1][1])
+    ref = oracle.gemm_rs(gen.bf16_bits(xr), gen.bf16_bits(wr), "nk")
+    assert oracle.normwise_max_rel_err(_np(outs[1][1]), ref) <= TOL_F32

@@ -3,7 +3,9 @@ tile's tensor-memory accumulator (CM_OPT_RS_PRELOAD = 1: all of it; 3: half,
 the rest added in the epilogue): the same result as the epilogue-add path
 (0), against the oracle, exactly on integer inputs, and at the full MLP
 sweep size on sampled rows.  The automatic choice (2, the default) picks one
-of the first two by the tile's K-slice count; it is checked against both."""
+of the first two by the tile's K-slice count; it is checked against both.
+The preload applies to buckets in per-step buffers (CM_OPT_RS_IN_PLACE = 0),
+which every test here uses."""
 
 import numpy as np
 import pytest
@@ -21,6 +23,7 @@ def _plan(N, chunks, direction, preload, kernel=0):
     p = cm.Plan(N, chunks, direction)
     p.set_option(cm.CM_OPT_KERNEL, kernel)
     p.set_option(cm.CM_OPT_RS_PRELOAD, preload)
+    p.set_option(cm.CM_OPT_RS_IN_PLACE, 0)   # the preload reads per-step bucket buffers
     return p
 
 
@@ -84,7 +87,9 @@ def test_automatic_choice_matches_the_path_it_picks(k, picked):
     all preloaded for at most 8 K slices, none beyond."""
     N, M, n = 4, 2048, 512
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=k, w_layout="nk")
-    auto, _, _ = run_rs(cm.Plan(N, 1, "uni"), x, w, "nk")
+    p = cm.Plan(N, 1, "uni")
+    p.set_option(cm.CM_OPT_RS_IN_PLACE, 0)   # default preload option, per-step buffers
+    auto, _, _ = run_rs(p, x, w, "nk")
     y, _, _ = run_rs(_plan(N, 1, "uni", picked), x, w, "nk")
     assert torch.equal(auto, y)
 

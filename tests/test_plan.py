@@ -68,15 +68,18 @@ def test_each_rank_uses_each_shard_once(N, direction):
 @pytest.mark.parametrize("N", [1, 2, 3, 4, 5, 8, 16])
 @pytest.mark.parametrize("direction", ["uni", "bidi", "none"])
 @pytest.mark.parametrize("serial", [False, True])
-def test_waits_point_to_earlier_tasks(N, direction, serial):
+@pytest.mark.parametrize("order", [0, 2])
+def test_waits_point_to_earlier_tasks(N, direction, serial, order):
     """Every flag has exactly one signalling task, earlier in the table than
-    every task waiting on it, and of an earlier ring step."""
+    every task waiting on it, and of an earlier ring step -- in the ring's
+    own order and in step-major order."""
     p = cm.Plan(N, 2, direction)
     if serial:
         p.set_option(cm.CM_OPT_SERIAL_STEPS, 1)
+    p.set_option(cm.CM_OPT_TASK_ORDER, order)
     for op in (AG, RS):
         tasks = p.tasks(op)
-        if serial or direction != "uni":
+        if serial or direction != "uni" or order == 2:
             assert [t.step for t in tasks] == sorted(t.step for t in tasks)
         signallers = {}
         for idx, t in enumerate(tasks):
@@ -91,6 +94,22 @@ def test_waits_point_to_earlier_tasks(N, direction, serial):
                     assert f in signallers, (op, f)
                     assert signallers[f][0] < idx
                     assert signallers[f][1] < t.step
+
+
+def test_step_major_order_is_a_permutation_of_the_ring_order():
+    """CM_OPT_TASK_ORDER = 2 lists the same tasks, sorted by step then rank."""
+    for d in ("uni", "bidi"):
+        p = cm.Plan(8, 2, d)
+        for op in (AG, RS):
+            ring_order = p.tasks(op)
+            p.set_option(cm.CM_OPT_TASK_ORDER, 2)
+            sm = p.tasks(op)
+            p.set_option(cm.CM_OPT_TASK_ORDER, 0)
+            key = lambda t: (t.rank, t.step, t.stream, t.out_idx)
+            assert sorted(map(key, ring_order)) == sorted(map(key, sm))
+            assert [(t.step, t.rank) for t in sm] == sorted((t.step, t.rank) for t in sm)
+    with pytest.raises(cm.CMError):
+        cm.Plan(4, 1, "uni").set_option(cm.CM_OPT_TASK_ORDER, 3)
 
 
 @pytest.mark.parametrize("N", [2, 3, 5, 8, 16])
@@ -210,15 +229,19 @@ def _simulate(p, op, mtiles, ntiles, grid, seed, band=0):
     N, c = p.N, p.chunks
     tasks = p.tasks(op)
     tiles = kernel_tile_order(tasks, c, mtiles, ntiles, band)
+    # readiness counters as the kernels keep them: AG one per (flag, chunk,
+    # row tile) -- the row tile's forward (column tile 0 here, as the
+    # single-CTA kernel does) bumps it once; RS one per (flag, chunk, row
+    # tile, column tile), bumped once when that bucket tile is written
     flags = {}
-    tgt_ag_in, tgt_ag_free = mtiles, mtiles * ntiles
-    tgt_rs = mtiles * ntiles
+    tgt_ag_in, tgt_ag_free = 1, ntiles
+    tgt_rs = 1
 
-    def f(i, q):
-        return flags.get((i, q), 0)
+    def f(*key):
+        return flags.get(key, 0)
 
-    def bump(i, q):
-        flags[(i, q)] = f(i, q) + 1
+    def bump(*key):
+        flags[key] = f(*key) + 1
 
     slots = {}     # AG: (slot, q, mt) -> shard id
     bufs = {}      # RS: (buf, q, mt, nt) -> (bucket, frozenset(contributors))
@@ -235,32 +258,32 @@ def _simulate(p, op, mtiles, ntiles, grid, seed, band=0):
         t = tasks[ti]
         if op == AG:
             if phase[b] == 0:       # load A (needs the slot chunk forwarded)
-                if t.wait_in[0] >= 0 and f(t.wait_in[0], q) < tgt_ag_in:
+                if t.wait_in[0] >= 0 and f(t.wait_in[0], q, mt) < tgt_ag_in:
                     return False
                 shard = t.a_slab if t.a_src == 0 else slots.get((t.a_slab, q, mt))
                 if p.direction != "none":
                     assert shard == t.out_idx, f"task {ti} read shard {shard}, wants {t.out_idx}"
                 outputs[(t.rank, t.out_idx, q, mt, nt)] = True
                 if t.sig_done >= 0:
-                    bump(t.sig_done, q)
+                    bump(t.sig_done, q, mt)
                 phase[b] = 1
                 return True
             fwd = nt == 0 and (t.fwd_slot[0] >= 0 or t.fwd_slot[1] >= 0)
             if fwd:
                 for j in range(2):
-                    if t.fwd_slot[j] >= 0 and t.wait_free[j] >= 0 and f(t.wait_free[j], q) < tgt_ag_free:
+                    if t.fwd_slot[j] >= 0 and t.wait_free[j] >= 0 and f(t.wait_free[j], q, mt) < tgt_ag_free:
                         return False
                 for j in range(2):
                     if t.fwd_slot[j] >= 0:
                         slots[(t.fwd_slot[j], q, mt)] = t.out_idx
                         if t.sig_fwd[j] >= 0:
-                            bump(t.sig_fwd[j], q)
+                            bump(t.sig_fwd[j], q, mt)
         else:
             if phase[b] == 0:       # main loop: no cross-CTA dependency
                 phase[b] = 1
                 return True
             for fl in list(t.wait_in) + [t.wait_free[0]]:
-                if fl >= 0 and f(fl, q) < tgt_rs:
+                if fl >= 0 and f(fl, q, mt, nt) < tgt_rs:
                     return False
             if t.a_src == 2:
                 contrib = frozenset(range(N))
@@ -281,7 +304,7 @@ def _simulate(p, op, mtiles, ntiles, grid, seed, band=0):
                 assert (t.out_idx, q, mt, nt) not in outputs
                 outputs[(t.out_idx, q, mt, nt)] = contrib
             if t.sig_done >= 0:
-                bump(t.sig_done, q)
+                bump(t.sig_done, q, mt, nt)
         phase[b] = 0
         cur[b] += 1
         return True
@@ -307,12 +330,14 @@ def _simulate(p, op, mtiles, ntiles, grid, seed, band=0):
 @pytest.mark.parametrize("grid", [1, 3, 16])
 @pytest.mark.parametrize("group", [1, 4])
 @pytest.mark.parametrize("in_place", [1, 0])
-def test_protocol_simulation(N, direction, chunks, grid, group, in_place):
-    if not in_place and (grid == 3 or group == 1):
-        pytest.skip("per-step RS buffers: a subset of the grid")
+@pytest.mark.parametrize("order", [0, 2])
+def test_protocol_simulation(N, direction, chunks, grid, group, in_place, order):
+    if (not in_place or order == 2) and (grid == 3 or group == 1):
+        pytest.skip("per-step RS buffers and step-major order: a subset of the grid")
     p = cm.Plan(N, chunks, direction)
     p.set_option(cm.CM_OPT_TILE_GROUP, group)
     p.set_option(cm.CM_OPT_RS_IN_PLACE, in_place)
+    p.set_option(cm.CM_OPT_TASK_ORDER, order)
     c = p.chunks
     mtiles, ntiles = 2, 2
     for seed in range(3):
