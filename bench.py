@@ -464,19 +464,22 @@ def run_reference(args):
 
 
 def choose_peak(peaks, timed_s, clocks):
-    """The measured dense bf16 peak that matches how the kernel ran: the burst
-    figure (a GEMM timed alone, clocks at their maximum) for a short timed
-    region or one whose median SM clock under load stayed at the maximum; the
-    sustained figure (seconds under the power cap) only for a region of a
-    second or more whose clocks came down."""
+    """The measured dense bf16 peak that matches the clocks the kernel ran at.
+    The burst figure (a GEMM timed alone, at full clocks) when the median SM
+    clock sampled under load during the timed region stayed at its maximum;
+    the sustained figure (seconds of back-to-back GEMMs under the power cap,
+    whose clocks came down the same way) when it did not.  Without clock
+    samples, the length of the timed region decides (under 1 s: burst)."""
     burst, sust = float(peaks["bf16_tflops"]), float(peaks["bf16_tflops_sustained"])
     sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
-    at_max = sm is not None and mx and sm >= 0.97 * mx
+    if sm is not None and mx:
+        if sm >= 0.97 * mx:
+            return burst, "burst", f"median SM clock {sm:.0f} MHz, at its maximum {mx:.0f}"
+        return sust, "sustained", (f"median SM clock {sm:.0f} MHz under load, below its maximum {mx:.0f} "
+                                   f"(reasons {','.join(clocks.get('reasons') or []) or 'none'})")
     if timed_s < 1.0:
-        return burst, "burst", f"timed region {timed_s:.3f} s < 1 s"
-    if at_max or sm is None:
-        return burst, "burst", f"median SM clock {sm} MHz of max {mx}"
-    return sust, "sustained", f"timed region {timed_s:.2f} s, median SM clock {sm} of max {mx} MHz"
+        return burst, "burst", f"no clock samples; timed region {timed_s:.3f} s < 1 s"
+    return sust, "sustained", f"no clock samples; timed region {timed_s:.2f} s"
 
 
 def step_config(N, chunks, direction, shapes):
@@ -732,16 +735,16 @@ def run_configs(args):
     """Every configuration's ops: ms per call (median of interleaved rounds
     with the undecomposed op in this kernel and torch.matmul on the
     concatenated operands), TFLOP/s, and the roofline fractions (tensor
-    against the measured burst bf16 peak -- each call is short and timed
-    between others -- and HBM against the measured copy bandwidth for the
-    algorithmic bytes), one JSON line each."""
+    against the measured dense bf16 peak that matches the clocks sampled
+    during the rounds, see choose_peak, and HBM against the measured copy
+    bandwidth for the algorithmic bytes), one JSON line each."""
     import torch
     import __graft_entry__
     from collective_matmul_decomposition_gb300 import inputs as gen
     __graft_entry__.build()
     device = torch.device("cuda", 0)
     peaks, kind = load_peaks()
-    burst, hbm = float(peaks["bf16_tflops"]), float(peaks["hbm_gbs"])
+    hbm = float(peaks["hbm_gbs"])
     cache = {}
     for name, op, ring, chunks in CONFIG_RUNS:
         if name not in cache:
@@ -769,24 +772,27 @@ def run_configs(args):
         mono.check((op,))
         if alt is not None:
             alt.check(("rs",))
+        clocks = clk.summary()
+        timed_s = max(20, args.steps) * sum(t.values()) / 1e3
+        peak, peak_which, peak_why = choose_peak(peaks, timed_s, clocks)
         f_ag, f_rs = flops(data["shapes"], N)
         fl = f_ag if op == "ag" else f_rs
         tf = fl / (t["dec"] / 1e3) / 1e12
         ring_b, alg_b = algorithmic_bytes(op, N, data["shapes"][op], 4 if yd == torch.float32 else 2)
         gbs = alg_b / (t["dec"] / 1e3) / 1e9
         ai = fl / alg_b
-        bound = "tensor" if ai >= burst * 1e12 / (hbm * 1e9) else "hbm"
+        bound = "tensor" if ai >= peak * 1e12 / (hbm * 1e9) else "hbm"
         print(json.dumps({
             "config": name, "op": op, "N": N, "chunks": chunks, "ring": ring,
             "ms": t["dec"], "tflops": tf, "bound": bound,
-            "frac_tensor": tf / burst, "algorithmic_bytes": alg_b, "ring_bytes": ring_b,
+            "frac_tensor": tf / peak, "algorithmic_bytes": alg_b, "ring_bytes": ring_b,
             "achieved_gbs": gbs, "frac_hbm": gbs / hbm, "flop_per_byte": ai,
-            "frac": tf / burst if bound == "tensor" else gbs / hbm,
+            "frac": tf / peak if bound == "tensor" else gbs / hbm,
             "ms_undecomposed": t["none"], "ms_torch": t["torch"],
             "vs_undecomposed_time": t["dec"] / t["none"], "vs_torch_time": t["dec"] / t["torch"],
             "ms_rs_per_step_buffers": t.get("per_step"),
-            "rounds": max(20, args.steps), "clocks": clk.summary(),
-            "peak_source": f"bf16_tflops (burst) {burst} and hbm_gbs {hbm} of {kind}"}), flush=True)
+            "rounds": max(20, args.steps), "clocks": clocks,
+            "peak_source": f"{peak_which} dense bf16 {peak} ({peak_why}) and hbm_gbs {hbm} of {kind}"}), flush=True)
         del st, alt
     return 0
 
@@ -798,29 +804,45 @@ NVLINK_GBS, NVLINK_HOP_US = 900.0, 2.0
 
 
 def run_gate(args):
-    """The cost model against measurement.  For each workload: the decomposed
-    and the undecomposed op timed on this GPU, the model's prediction of both
-    with rates derived for one GPU (all N ranks share its GEMM rate and HBM,
-    and the native collective is free because every partial already sits in
-    one memory), its choice, and its choice for the same shapes under
-    NVLink-class rates (a projection)."""
+    """The cost model against measurement, with rates calibrated on this GPU.
+
+    For each workload and op: the decomposed and the undecomposed op timed
+    interleaved, and the model's prediction of both.  The model's one-GPU
+    rates are measured separately from the decomposed op they predict:
+    - compute: each rank's share of this GPU's rate on the undecomposed op of
+      the same shape (so the undecomposed prediction equals its measurement
+      by construction; the decomposed prediction is the test);
+    - ring: each rank's share of the ring's own throughput, from the same
+      ring run with almost no compute (AllGather->GEMM with 256 output
+      columns, GEMM->ReduceScatter with a contraction of 64): the bytes one
+      hop carries, summed over ranks and steps, over that call's time;
+    - the native collective moves nothing on one GPU (every partial already
+      sits in one memory), a message costs one flag round trip (1 us), and
+      the realigning addition runs at each rank's share of the HBM copy rate.
+    Each line gives the predictions, the relative error of the decomposed
+    one, the model's choice and whether measurement agrees (within 5 %), the
+    choice under NVLink-class rates as a labelled projection, and the
+    Einsum-level choice (which collective to decompose) for the same shapes
+    under those rates."""
     import torch
     import __graft_entry__
     from collective_matmul_decomposition_gb300 import cm
+    from collective_matmul_decomposition_gb300 import inputs as gen
     __graft_entry__.build()
     device = torch.device("cuda", 0)
     peaks, kind = load_peaks()
     hbm = float(peaks["hbm_gbs"])
-    cases = [("sp_mlp_fc1_ag_n8", ("ag",)), ("sp_mlp_fc2_rs_n8", ("rs",)), ("gpt3_h12288_s2048_n8", ("ag", "rs"))]
-    cases += [(f"{WORKLOAD}:N={N}", ("ag", "rs")) for N in (4, 8, 16)]
-    for name, ops in cases:
+    cases = [("sp_mlp_fc1_ag_n8", ("ag",), None), ("sp_mlp_fc2_rs_n8", ("rs",), None),
+             ("gpt3_h12288_s2048_n8", ("ag", "rs"), None), ("gpt3_h12288_s2048_n8", ("ag", "rs"), "uni")]
+    cases += [(f"{WORKLOAD}:N={N}", ("ag", "rs"), None) for N in (4, 8, 16)]
+    for name, ops, ring_override in cases:
         if name.startswith(WORKLOAD):
             N = int(name.split("=")[1])
             data, direction, chunks = make_step_inputs(N, device), "uni", 1
         else:
-            from collective_matmul_decomposition_gb300 import inputs as gen
             N, data = named_workload_inputs(name)
             direction, chunks = gen.WORKLOADS[name]["direction"], gen.WORKLOADS[name]["chunks"]
+        direction = ring_override or direction
         f_ag, f_rs = flops(data["shapes"], N)
         dec, mono = Step(N, chunks, direction, data, device), Step(N, 1, "none", data, device)
         for op in ops:
@@ -834,32 +856,73 @@ def run_gate(args):
             sh = data["shapes"][op]
             rows, K, n = (sh["m"], sh["K"], sh["n"]) if op == "ag" else (sh["M"], sh["k"], sh["n"])
             code = cm.CM_OP_AG_GEMM if op == "ag" else cm.CM_OP_GEMM_RS
+            ring_bytes, ms_ring = ring_calibration(cm, torch, device, op, N, direction, chunks, rows, K, n)
             rate = fl / (ms_none / 1e3) / 1e12   # this GPU's rate on the undecomposed op
-            # one GPU: the ranks share its GEMM rate and HBM (a rotation byte is
-            # read and written), the native collective moves nothing (every
-            # partial is already in one memory), and a message costs at least
-            # one release/acquire flag round trip (~1 us)
-            one_gpu = dict(gemm_tflops=rate / N, ring_gbs=hbm / (2 * N), coll_gbs=1e12, hop_us=1.0, mem_gbs=hbm / N)
-            pred_dec = cm.cost_estimate(N, chunks, direction, code, rows, K, n, one_gpu)
-            pred_none = cm.cost_estimate(N, 1, "none", code, rows, K, n, one_gpu)
+            ring_gbs = ring_bytes / (ms_ring / 1e3) / 1e9
+            one_gpu = dict(gemm_tflops=rate / N, ring_gbs=ring_gbs / N, coll_gbs=1e12, hop_us=1.0,
+                           mem_gbs=hbm / 2 / N)
+            pred_dec = cm.cost_estimate(N, chunks, direction, code, rows, K, n, one_gpu) / 1e3
+            pred_none = cm.cost_estimate(N, 1, "none", code, rows, K, n, one_gpu) / 1e3
             pick = cm.plan_choose(N, code, rows, K, n, one_gpu)
             nvl = dict(gemm_tflops=rate, ring_gbs=NVLINK_GBS, coll_gbs=NVLINK_GBS, hop_us=NVLINK_HOP_US, mem_gbs=hbm)
             pick_nvl = cm.plan_choose(N, code, rows, K, n, nvl)
+            m_e = rows if op == "ag" else rows // N
+            k_e = K
+            ein = cm.plan_choose_einsum(N, m_e, k_e, n, nvl)
             faster = "decomposed" if ms_dec < ms_none else "undecomposed"
             # within 5 % either way is a tie, and a tie agrees with either choice
             agrees = (ms_none <= ms_dec * 1.05) if pick[1] == "none" else (ms_dec <= ms_none * 1.05)
             print(json.dumps({"gate": name, "op": op, "N": N, "chunks": chunks, "ring": direction,
                               "measured_ms": {"decomposed": ms_dec, "undecomposed": ms_none, "faster": faster},
-                              "one_gpu_model": {"rates": one_gpu, "decomposed_ms": pred_dec / 1e3,
-                                                "undecomposed_ms": pred_none / 1e3,
+                              "calibration": {"ring_bytes": ring_bytes, "ring_ms": ms_ring, "ring_gbs": ring_gbs,
+                                              "gemm_tflops": rate},
+                              "one_gpu_model": {"rates": one_gpu, "decomposed_ms": pred_dec,
+                                                "undecomposed_ms": pred_none,
+                                                "decomposed_rel_err": (pred_dec - ms_dec) / ms_dec,
+                                                "undecomposed_rel_err": (pred_none - ms_none) / ms_none,
                                                 "choice": {"chunks": pick[0], "ring": pick[1]},
                                                 "agrees_with_measurement": agrees},
                               "nvlink_projection": {"rates": nvl, "choice": {"chunks": pick_nvl[0], "ring": pick_nvl[1]},
-                                                    "predicted_ms": pick_nvl[2] / 1e3},
+                                                    "predicted_ms": pick_nvl[2] / 1e3,
+                                                    "einsum_offering_both": {"decompose": ein[0], "chunks": ein[1],
+                                                                             "ring": ein[2],
+                                                                             "predicted_ms": ein[3] / 1e3,
+                                                                             "m": m_e, "K": k_e, "n": n}},
                               "peak_source": kind}), flush=True)
         del dec, mono, data
         torch.cuda.empty_cache()
     return 0
+
+
+def ring_calibration(cm, torch, device, op, N, direction, chunks, rows, K, n):
+    """The ring's own throughput with almost no compute: (bytes one hop
+    carries, summed over ranks and steps; median ms of one call).  AG: the
+    same shards (m x K) rotated, 256 output columns; RS: the same buckets
+    ((rows/N) x n fp32) circulated, a contraction of 64."""
+    from collective_matmul_decomposition_gb300 import inputs as gen
+    plan = cm.Plan(N, chunks, direction)
+    hops = N - 1
+    if op == "ag":
+        n_cal = 256
+        x, w = gen.ag_inputs(N, rows, K, n_cal, gen.NORMAL1, gen.NORMAL002, seed=77, w_layout="nk")
+        x, w = x.to(device), w.to(device)
+        y = torch.empty(N, N * rows, n_cal, dtype=torch.bfloat16, device=device)
+        ws = torch.empty(plan.ag_workspace_size(rows, K), dtype=torch.uint8, device=device)
+        fn = lambda: cm.cm_ag_gemm(plan, x, w, y, ws, "nk")
+        ring_bytes = N * hops * rows * K * 2
+    else:
+        k_cal = 64
+        x, w = gen.rs_inputs(N, rows, k_cal, n, gen.NORMAL1, gen.NORMAL002, seed=78, w_layout="nk")
+        x, w = x.to(device), w.to(device)
+        y = torch.empty(N, rows // N, n, dtype=torch.bfloat16, device=device)
+        ws = torch.empty(plan.rs_workspace_size(rows, n), dtype=torch.uint8, device=device)
+        fn = lambda: cm.cm_gemm_rs(plan, x, w, y, ws, "nk")
+        ring_bytes = N * hops * (rows // N) * n * 4
+    ms = time_interleaved({"ring": fn}, 20, torch, warmup=3)["ring"]
+    st, info = cm.cm_check_status(ws)
+    if st != 0:
+        raise RuntimeError(f"ring calibration: device status {st} {info}")
+    return ring_bytes, ms
 
 
 def run_backward(args):

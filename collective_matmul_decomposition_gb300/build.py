@@ -12,6 +12,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libcm.so")
+# the same library with every computed index bounds-checked in the kernels
+# (CM_DEBUG_BOUNDS): an index outside its buffer is reported as CM_ERR_BOUNDS
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(BUILD_DEBUG, "libcm_debug.so")
 INCLUDE = os.path.join(ROOT, "include")
 
 SOURCES = ["cm_kernel.cu", "cm_kernel_pair.cu", "cm_api.cu", "cm_plan.cpp", "cm_noalloc.cu", "cm_cost.cpp", "cm_reduce.cu"]
@@ -34,20 +38,23 @@ def _stale(target, deps):
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every translation unit in parallel, then link the shared library."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile every translation unit in parallel, then link the shared library
+    (debug=True: the bounds-checked build, in its own folder)."""
+    build_dir, lib = (BUILD_DEBUG, LIB_DEBUG) if debug else (BUILD, LIB)
+    os.makedirs(build_dir, exist_ok=True)
     hdrs = [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "cm.h")]
     nvcc = _nvcc()
+    flags = NVCC_FLAGS + (["-DCM_DEBUG_BOUNDS=1"] if debug else [])
     objs = []
     jobs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src + ".o")
+        o = os.path.join(build_dir, src + ".o")
         objs.append(o)
         if force or _stale(o, [s] + hdrs):
             extra = ["-x", "cu"] if src.endswith(".cu") else []
-            jobs.append([nvcc] + ARCH + NVCC_FLAGS + extra + ["-c", s, "-o", o])
+            jobs.append([nvcc] + ARCH + flags + extra + ["-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -58,12 +65,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
 
     with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
         list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

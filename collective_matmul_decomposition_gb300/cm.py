@@ -13,9 +13,12 @@ import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "_build", "libcm.so")
+# the bounds-checked build of the same library (CM_DEBUG_BOUNDS)
+DEBUG_LIB_PATH = os.path.join(PKG, "_build_debug", "libcm_debug.so")
 
 CM_OK, CM_ERR_INVALID_ARG, CM_ERR_SHAPE, CM_ERR_ALIGNMENT = 0, 1, 2, 3
 CM_ERR_UNSUPPORTED, CM_ERR_CUDA, CM_ERR_TIMEOUT, CM_ERR_WORKSPACE = 4, 5, 6, 7
+CM_ERR_BOUNDS = 8
 CM_RING_UNI, CM_RING_BIDI, CM_RING_NONE = 0, 1, 2
 CM_BF16, CM_F32 = 0, 1
 CM_W_KN, CM_W_NK = 0, 1
@@ -27,6 +30,7 @@ CM_OPT_RS_PRELOAD = 11
 CM_OPT_RS_IN_PLACE = 12
 CM_OPT_TASK_ORDER = 13
 CM_OPT_RS_EPILOGUE = 14
+CM_OPT_DEBUG_FLAG_OFFSET = 15
 CM_MAX_RANKS, CM_MAX_CHUNKS = 16, 8
 
 DIRECTIONS = {"uni": CM_RING_UNI, "bidi": CM_RING_BIDI, "none": CM_RING_NONE}
@@ -39,7 +43,7 @@ EXPORTS = ["cm_plan", "cm_plan_destroy", "cm_plan_steps", "cm_plan_step", "cm_pl
            "cm_ag_gemm_noalloc", "cm_ag_gemm_noalloc_check_status", "cm_cost_estimate", "cm_plan_choose",
            "cm_gemm_rs_pipelined_workspace_size", "cm_gemm_rs_pipelined",
            "cm_backward_pair_workspace_size", "cm_backward_pair",
-           "cm_cannon_workspace_size", "cm_cannon_gemm"]
+           "cm_cannon_workspace_size", "cm_cannon_gemm", "cm_einsum_cost", "cm_plan_choose_einsum"]
 CM_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -126,8 +130,26 @@ def load():
     lib.cm_plan_choose.argtypes = [i32, i32, i64, i64, i64, rp, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
                                    ctypes.POINTER(ctypes.c_double)]
     lib.cm_plan_choose.restype = i32
+    lib.cm_einsum_cost.argtypes = [i32, i32, i32, i32, i64, i64, i64, rp, ctypes.POINTER(ctypes.c_double)]
+    lib.cm_einsum_cost.restype = i32
+    lib.cm_plan_choose_einsum.argtypes = [i32, i64, i64, i64, rp, i32, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                          ctypes.POINTER(i32), ctypes.POINTER(ctypes.c_double)]
+    lib.cm_plan_choose_einsum.restype = i32
     _lib = lib
     return lib
+
+
+def bounds_checked():
+    """A second binding of this module, to the bounds-checked build of the
+    library (every computed flag, slot, row and buffer index checked in the
+    kernels; an index outside its buffer is reported as CM_ERR_BOUNDS)."""
+    import importlib.util
+    spec = importlib.util.spec_from_file_location(__name__ + "_bounds_checked", os.path.abspath(__file__))
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod.LIB_PATH = DEBUG_LIB_PATH
+    mod.load()
+    return mod
 
 
 def status_string(status: int) -> str:
@@ -304,6 +326,27 @@ def plan_choose(n_ranks, op, rows, K, n, rates, max_chunks=CM_MAX_CHUNKS):
                                  ctypes.byref(d), ctypes.byref(us)), "cm_plan_choose")
     name = {v: k for k, v in DIRECTIONS.items()}[d.value]
     return c.value, name, us.value
+
+
+def einsum_cost(n_ranks, chunks, direction, decompose, m, K, n, rates) -> float:
+    """Predicted time (us) of one way to run an Einsum that offers both
+    collectives: decompose = "ag", "rs" or "none" (both native)."""
+    which = {"ag": CM_OP_AG_GEMM, "rs": CM_OP_GEMM_RS, "none": -1}[decompose]
+    us = ctypes.c_double()
+    r = _rates(rates)
+    _check(load().cm_einsum_cost(n_ranks, chunks, DIRECTIONS[direction], which, m, K, n, ctypes.byref(r),
+                                 ctypes.byref(us)), "cm_einsum_cost")
+    return us.value
+
+
+def plan_choose_einsum(n_ranks, m, K, n, rates, max_chunks=CM_MAX_CHUNKS):
+    """Which collective of such an Einsum to decompose: ("ag" | "rs" | "none", chunks, direction, us)."""
+    w, c, d, us = ctypes.c_int(), ctypes.c_int(), ctypes.c_int(), ctypes.c_double()
+    r = _rates(rates)
+    _check(load().cm_plan_choose_einsum(n_ranks, m, K, n, ctypes.byref(r), max_chunks, ctypes.byref(w),
+                                        ctypes.byref(c), ctypes.byref(d), ctypes.byref(us)), "cm_plan_choose_einsum")
+    name = {CM_OP_AG_GEMM: "ag", CM_OP_GEMM_RS: "rs", -1: "none"}[w.value]
+    return name, c.value, {v: k for k, v in DIRECTIONS.items()}[d.value], us.value
 
 
 def version() -> str:

@@ -208,6 +208,7 @@ cm_status setup_launch(const PlanImpl &pl, const KernelChoice &kc, KParams &kp, 
     uint8_t *w8 = static_cast<uint8_t *>(ws);
     kp.status = reinterpret_cast<uint32_t *>(w8);
     kp.flags = reinterpret_cast<uint32_t *>(w8 + l.flags_off);
+    kp.flag_words = int64_t(l.flags_bytes / sizeof(uint32_t));
     kp.timeout_ns = uint64_t(pl.timeout_ns);
     kp.static_tiles = pl.static_tiles;
     kp.l2_hint_a = pl.l2_hints & 0xf;
@@ -359,6 +360,12 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.acc = nullptr;
     kp.x_bytes = static_cast<const uint8_t *>(x);
     kp.slot_bytes = bufs;
+    kp.x_total = int64_t(N) * m * K * 2;
+    kp.slot_total = int64_t(l.buf_bytes);
+    kp.y_elems = int64_t(N) * N * m * n;
+    kp.a0_slabs = int(slabs);
+    kp.a1_slabs = l.buf_bytes > 0 ? int(int64_t(N) * streams_of(pl) * pl.sched[CM_OP_AG_GEMM].steps * c) : int(slabs);
+    kp.b_slabs = N;
     kp.row_bytes = K * 2;
     kp.y_rank_stride = int64_t(N) * m * n;
     kp.out_rows_per_idx = none ? int64_t(N) * m : m;
@@ -412,6 +419,10 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     }
     kp.y = y;
     kp.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
+    kp.y_elems = M * n;
+    kp.acc_bufs = int(rs_bufs(pl));
+    kp.a0_slabs = kp.a1_slabs = N * N * c;
+    kp.b_slabs = N;
     if (l.buf_bytes > 0) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
         const int64_t nbufs = rs_bufs(pl);
         if (!make_acc_maps(kp, promo, kp.acc, n, rows_c, nbufs * c)) return CM_ERR_CUDA;
@@ -493,6 +504,10 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     if (!make_acc_maps(kp, promo, P, n, rows_c, int64_t(N) * N * c)) return CM_ERR_CUDA;
     kp.y = y;
     kp.acc = P;
+    kp.y_elems = M * n;
+    kp.acc_bufs = N * N;
+    kp.a0_slabs = kp.a1_slabs = N * N * c;
+    kp.b_slabs = N;
     kp.y_rank_stride = 0;
     kp.out_rows_per_idx = Mb;
     kp.acc_buf_stride = Mb * n;
@@ -505,8 +520,11 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
     kp.rs_groups = rs_groups(pl, k);
-    set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n);
-    kp.tiles_per_task = kp.mtiles_c * kp.ntiles;   // one chunk per launch
+    // chunks of at most 128 rows go two to a launch, one per CTA of each pair
+    // tile (the ring path's chunk pairing), instead of half-empty pair tiles
+    set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
+    kp.tiles_per_task = kp.mtiles_c * kp.ntiles;   // one chunk (or chunk pair) per launch
+    const int per_launch = kp.chunk_pair ? 2 : 1;
     kp.tgt_in = kp.tgt_free = 0;
     int sms = 0, max_clusters = 0;
     st = setup_launch(pl, kc, kp, l, ws, &sms, &max_clusters);
@@ -533,17 +551,18 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     kp.task_begin = 0;
     kp.task_end = ntasks;
     if (cudaMemsetAsync(ws, 0, l.buf_off, s) != cudaSuccess) return CM_ERR_CUDA;
-    for (int j = 0; j < c; ++j) {
-        // GEMM of chunk j on the caller's stream; its reduction on the side
-        // stream, under the GEMM of chunk j + 1
-        kp.q_only = j;
-        kp.tile_counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + kCounterOff) + j;
+    for (int g = 0; g < c / per_launch; ++g) {
+        // GEMM of chunk g (or chunks 2g and 2g + 1) on the caller's stream;
+        // their reduction on the side stream, under the next launch's GEMM
+        kp.q_only = g;
+        kp.tile_counter = reinterpret_cast<uint32_t *>(static_cast<uint8_t *>(ws) + kCounterOff) + g;
         const int64_t tiles = int64_t(ntasks) * kp.tiles_per_task;
         if (launch_tiles(pl, kc, kp, b_mn ? 1 : 0, tiles, max_clusters, sms, s) != cudaSuccess) return CM_ERR_CUDA;
-        if (cudaEventRecord(ss->ev[j], s) != cudaSuccess) return CM_ERR_CUDA;
-        if (cudaStreamWaitEvent(ss->stream, ss->ev[j], 0) != cudaSuccess) return CM_ERR_CUDA;
-        if (launch_reduce_chunk(P, y, N, Mb, rows_c, n, j, y_dtype == CM_F32, sms, ss->stream) != cudaSuccess)
-            return CM_ERR_CUDA;
+        if (cudaEventRecord(ss->ev[g], s) != cudaSuccess) return CM_ERR_CUDA;
+        if (cudaStreamWaitEvent(ss->stream, ss->ev[g], 0) != cudaSuccess) return CM_ERR_CUDA;
+        for (int j = g * per_launch; j < (g + 1) * per_launch; ++j)
+            if (launch_reduce_chunk(P, y, N, Mb, rows_c, n, j, y_dtype == CM_F32, sms, ss->stream) != cudaSuccess)
+                return CM_ERR_CUDA;
     }
     if (cudaEventRecord(ss->ev[CM_MAX_CHUNKS], ss->stream) != cudaSuccess) return CM_ERR_CUDA;
     if (cudaStreamWaitEvent(s, ss->ev[CM_MAX_CHUNKS], 0) != cudaSuccess) return CM_ERR_CUDA;
@@ -630,6 +649,8 @@ cm_status cm_backward_pair(cm_plan_t plan, const void *x, const void *w, const v
     kp.tmA1 = kp.tmA0;
     if (!make_map(&kp.tmB, promo, xg, uint64_t(K), uint64_t(T), uint64_t(N), 64, kBK)) return CM_ERR_CUDA;
     kp.y = dw;
+    kp.y_elems = int64_t(N) * n * K;
+    kp.a0_slabs = kp.a1_slabs = kp.b_slabs = N;
     kp.y_rank_stride = n * K;
     kp.out_rows_per_idx = n;
     kp.op = 0;
@@ -734,6 +755,9 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
     if (!make_acc_maps(kp, promo, acc, bn, bm, int64_t(P) * 2)) return CM_ERR_CUDA;
     kp.y = c;
     kp.acc = acc;
+    kp.y_elems = int64_t(P) * bm * bn;
+    kp.acc_bufs = P * 2;
+    kp.a0_slabs = kp.a1_slabs = kp.b_slabs = P;
     kp.out_rows_per_idx = bm;
     kp.acc_buf_stride = bm * bn;
     kp.op = 1;
@@ -827,7 +851,8 @@ cm_status cm_check_status(const void *ws, cm_stream_t stream, int32_t info[4]) {
     if (info)
         for (int i = 0; i < 4; ++i) info[i] = int32_t(h[i]);
     if (h[0] == 0) return CM_OK;
-    return h[0] == uint32_t(CM_ERR_TIMEOUT) ? CM_ERR_TIMEOUT : CM_ERR_CUDA;
+    if (h[0] == uint32_t(CM_ERR_TIMEOUT) || h[0] == uint32_t(CM_ERR_BOUNDS)) return cm_status(h[0]);
+    return CM_ERR_CUDA;
 }
 
 const char *cm_status_string(cm_status s) {
@@ -840,10 +865,15 @@ const char *cm_status_string(cm_status s) {
         case CM_ERR_CUDA: return "CUDA error";
         case CM_ERR_TIMEOUT: return "device-side wait timed out";
         case CM_ERR_WORKSPACE: return "workspace missing or too small";
+        case CM_ERR_BOUNDS: return "computed index outside its buffer (bounds-checked build)";
     }
     return "unknown status";
 }
 
-const char *cm_version(void) { return "cm 0.1 (sm_103a tcgen05/TMA persistent kernel)"; }
+#ifdef CM_DEBUG_BOUNDS
+const char *cm_version(void) { return "cm 0.2 (sm_103a tcgen05/TMA persistent kernel; bounds-checked)"; }
+#else
+const char *cm_version(void) { return "cm 0.2 (sm_103a tcgen05/TMA persistent kernel)"; }
+#endif
 
 }  // extern "C"

@@ -206,3 +206,74 @@ extern "C" cm_status cm_plan_choose(int n_ranks, cm_op op, int64_t rows, int64_t
     if (us) *us = best;
     return CM_OK;
 }
+
+// One Einsum that offers both collectives ("Overlap Communication with
+// Dependent Computation via Decomposition in Large Deep Learning Models",
+// section "The idea", knowing when to decline: the cost model "picks which of
+// two candidate collectives to overlap when an Einsum offers both").  Per
+// rank: its A operand is the AllGather of N row shards [m, K], it multiplies
+// that [N*m, K] by its [K, n] weight, and the [N*m, n] result is summed over
+// the ranks and scattered, bucket o being rows o*m.. of the sum.  Only one
+// collective can become the ring (the loop runs over input shards or over
+// output buckets); the other stays native:
+//   gather decomposed:  the AG ring, then the native ReduceScatter of the
+//                       fp32 result;
+//   scatter decomposed: the native AllGather, then the RS ring;
+//   neither:            native AllGather, GEMM, native ReduceScatter.
+extern "C" cm_status cm_einsum_cost(int n_ranks, int chunks, cm_direction dir, int decompose, int64_t m, int64_t K,
+                                    int64_t n, const cm_rates *rates, double *us) {
+    if (!us || !rates_ok(rates) || n_ranks < 1 || n_ranks > CM_MAX_RANKS || chunks < 1 || chunks > CM_MAX_CHUNKS ||
+        m < 1 || K < 1 || n < 1 || (dir != CM_RING_UNI && dir != CM_RING_BIDI && dir != CM_RING_NONE) ||
+        (decompose != -1 && decompose != CM_OP_AG_GEMM && decompose != CM_OP_GEMM_RS))
+        return CM_ERR_INVALID_ARG;
+    const Rates R = to_rates(rates);
+    const int N = n_ranks;
+    const double dm = double(m), dK = double(K), dn = double(n);
+    const double ag_native = (N - 1) * dm * dK * 2.0 / R.coll_b_per_us;   // gather of N-1 shards
+    const double rs_native = (N - 1) * dm * dn * 4.0 / R.coll_b_per_us;   // scatter of N-1 fp32 buckets
+    const double gemm = 2.0 * N * dm * dK * dn / R.flop_per_us;
+    const bool ring = dir != CM_RING_NONE && N > 1;
+    if (decompose == CM_OP_AG_GEMM && ring) {
+        *us = ag_time(R, N, chunks, dir, dm, dK, dn) + rs_native;
+    } else if (decompose == CM_OP_GEMM_RS && ring) {
+        *us = ag_native + rs_time(R, N, chunks, dir, double(N) * dm, dK, dn);
+    } else {
+        *us = ag_native + gemm + rs_native;
+    }
+    return CM_OK;
+}
+
+extern "C" cm_status cm_plan_choose_einsum(int n_ranks, int64_t m, int64_t K, int64_t n, const cm_rates *rates,
+                                           int max_chunks, int *decompose, int *chunks, cm_direction *dir,
+                                           double *us) {
+    if (!decompose || !chunks || !dir || max_chunks < 1 || max_chunks > CM_MAX_CHUNKS) return CM_ERR_INVALID_ARG;
+    double best = 0.0;
+    cm_status st = cm_einsum_cost(n_ranks, 1, CM_RING_NONE, -1, m, K, n, rates, &best);
+    if (st != CM_OK) return st;
+    int bw = -1, bc = 1;
+    cm_direction bd = CM_RING_NONE;
+    // candidates in order of simplicity: the gather, then the scatter; one-way
+    // before two-way rings; fewer chunks first (a chunk must split the shard,
+    // or the bucket -- also m rows -- evenly).  Ties keep the simpler choice.
+    for (int which : {int(CM_OP_AG_GEMM), int(CM_OP_GEMM_RS)})
+        for (int d = 0; d < 2 && n_ranks > 1; ++d) {
+            const cm_direction cand = d == 0 ? CM_RING_UNI : CM_RING_BIDI;
+            for (int c = 1; c <= max_chunks; c *= 2) {
+                if (m % c != 0) continue;
+                double t = 0.0;
+                st = cm_einsum_cost(n_ranks, c, cand, which, m, K, n, rates, &t);
+                if (st != CM_OK) return st;
+                if (t < best * (1.0 - 1e-9)) {
+                    best = t;
+                    bw = which;
+                    bc = c;
+                    bd = cand;
+                }
+            }
+        }
+    *decompose = bw;
+    *chunks = bc;
+    *dir = bd;
+    if (us) *us = best;
+    return CM_OK;
+}

@@ -57,6 +57,9 @@ __device__ void producer(const KParams &p, const Smem &s, int total) {
     for (int t = blockIdx.x; t < total; t += gridDim.x) {
         if (*s.abort) break;
         const TileCoord c = decode(p, t);
+        if (!in_bounds(p, c.task >= p.task_begin && c.task < p.task_end && c.q >= 0 && c.q < p.chunks,
+                       kSiteBoundsTask, c.task, c.q))
+            break;
         const cm_task &tk = p.tasks[c.task];
         if (p.op == 0 && tk.wait_in[0] >= 0) {
             if (!wait_flag(p, s.abort, flag_ptr(p, tk.wait_in[0], c.q, c.mt, 0), p.tgt_in, kSiteProducerFlag, c.task, c.q)) break;
@@ -227,8 +230,17 @@ __device__ void epilogue(const KParams &p, const Smem &s, int total, uint32_t tm
         tc_fence_after();
 
         const int row = c.mt * kBM + et;          // row inside the chunk
-        const bool row_ok = row < p.rows_c;
         const int64_t crow = int64_t(c.q) * p.rows_c + row;   // row inside the shard / bucket
+        bool row_ok = row < p.rows_c;
+        if (kCheckBounds && row_ok) {   // debug builds: every global row this thread touches
+            const int64_t yrow = (p.op == 0 ? int64_t(tk.rank) * (p.y_rank_stride / p.n) : 0) +
+                                 int64_t(tk.out_idx) * p.out_rows_per_idx + crow;
+            const bool y_ok = (yrow + 1) * p.n <= p.y_elems;
+            const bool okb = p.op == 0 ? y_ok
+                                       : tk.out_buf < p.acc_bufs && tk.in_buf[0] < p.acc_bufs &&
+                                             tk.in_buf[1] < p.acc_bufs && (tk.out_buf >= 0 || y_ok);
+            row_ok = in_bounds(p, okb, p.op == 0 ? kSiteBoundsOutput : kSiteBoundsBucket, c.task, c.q);
+        }
         for (int cb = 0; cb < kBN / 32; ++cb) {
             uint32_t v[32];
             tmem_ld32(tmem_base + (uint32_t(ew * 32) << 16) + uint32_t(accb * kBN + cb * 32), v);

@@ -36,6 +36,13 @@ enum Site : uint32_t {
     kSiteTmemEmpty = 6,
     kSiteTmemFull = 7,
     kSiteForwardFull = 8,
+    // debug builds (CM_DEBUG_BOUNDS): which computed index fell outside its buffer
+    kSiteBoundsFlag = 16,
+    kSiteBoundsForward = 17,
+    kSiteBoundsOutput = 18,
+    kSiteBoundsBucket = 19,
+    kSiteBoundsSlab = 20,
+    kSiteBoundsTask = 21,
 };
 
 struct KParams {
@@ -79,6 +86,13 @@ struct KParams {
                                // of at most 128 rows), and the tile decode's chunk index is g
     int tiles_per_task, task_begin, task_end;
     uint32_t tgt_in, tgt_free;
+    // extents the bounds checks of debug builds compare computed indices with
+    int64_t flag_words;        // readiness counters after p.flags
+    int64_t x_total;           // bytes of x (AG, the forwarder's source for step 0)
+    int64_t slot_total;        // bytes of the receive slots (AG)
+    int64_t y_elems;           // elements of the output
+    int acc_bufs;              // RS accumulator buffers of acc_buf_stride elements
+    int a0_slabs, a1_slabs, b_slabs;   // third extent of tmA0, tmA1, tmB
     cm_task tasks[kMaxTasks];
 };
 

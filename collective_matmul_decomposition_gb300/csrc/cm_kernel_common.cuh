@@ -62,9 +62,40 @@ __device__ __forceinline__ TileCoord decode(const KParams &p, int t) {
 // together (every column tile of the forwarding task sends a slice of them);
 // RS, one per (id, chunk, row tile, column tile) -- the bucket tile a task
 // adds to depends only on its predecessor's same tile.
+#ifdef CM_DEBUG_BOUNDS
+constexpr bool kCheckBounds = true;
+#else
+constexpr bool kCheckBounds = false;
+#endif
+// Word of the status block that a rejected flag access is sent to (debug
+// builds); no wait on it ever completes, so its waiters see the failure.
+constexpr int kSinkWord = 48;
+
+// Debug builds: record that a computed index fell outside its buffer
+// (CM_ERR_BOUNDS, with task, chunk and which index), unless an earlier
+// failure was recorded.  The caller then skips the access.
+__device__ __noinline__ void report_bounds(const KParams &p, uint32_t site, int task, int q) {
+    if (atomicCAS(p.status, 0u, uint32_t(CM_ERR_BOUNDS)) == 0u) {
+        p.status[1] = uint32_t(task);
+        p.status[2] = uint32_t(q);
+        p.status[3] = site;
+        __threadfence();
+    }
+}
+
+// true if `ok`; in debug builds a false `ok` is reported first.  Release
+// builds compile the check away (always true).
+__device__ __forceinline__ bool in_bounds(const KParams &p, bool ok, uint32_t site, int task, int q) {
+    if (!kCheckBounds || ok) return true;
+    report_bounds(p, site, task, q);
+    return false;
+}
+
 __device__ __forceinline__ uint32_t *flag_ptr(const KParams &p, int id, int q, int mt, int nt) {
     size_t w = (size_t(id) * size_t(p.chunks) + size_t(q)) * size_t(p.mtiles_c) + size_t(mt);
     if (p.op == 1) w = w * size_t(p.ntiles) + size_t(nt);
+    if (!in_bounds(p, id >= 0 && q >= 0 && q < p.chunks && int64_t(w) < p.flag_words, kSiteBoundsFlag, id, q))
+        return p.status + kSinkWord;
     return p.flags + w;
 }
 

@@ -178,6 +178,12 @@ __device__ void producer(const KParams &p, const PSmem &s, int total, const Cl &
         int rr = c.rr, slab = c.slab;
         const uint64_t tm_a = c.a_src == 1 ? tm_a1 : tm_a0;
         const int a_row = c.a_row, n0 = c.n0, nk = c.nk;
+        if (kCheckBounds) {
+            const int runs = (nk + p.kblocks - 1) / p.kblocks;   // ranks a summed tile walks through
+            const int a_lim = c.a_src == 1 ? p.a1_slabs : p.a0_slabs;
+            in_bounds(p, slab >= 0 && slab + (runs - 1) * slab_step < a_lim && rr >= 0 && rr + runs - 1 < p.b_slabs,
+                      kSiteBoundsSlab, c.task, c.q);
+        }
         int kb = 0;
         bool ok = true;
         bool free_ready = mbar_test_wait(s.empty + stage, phase ^ 1u);
@@ -283,6 +289,11 @@ __device__ void scheduler(const KParams &p, const PSmem &s, int total) {
         if (t >= total) t = -1;
         TileCoord c = {0, 0, 0, 0};
         if (t >= 0) c = decode(p, t);
+        if (t >= 0 && !in_bounds(p, c.task >= p.task_begin && c.task < p.task_end && c.q >= 0 && c.q < p.chunks,
+                                 kSiteBoundsTask, c.task, c.q)) {
+            t = -1;   // publish the end: nothing of this tile is loaded, computed or stored
+            c = {p.task_begin, 0, 0, 0};
+        }
         const cm_task &tk = p.tasks[c.task];
         // AG: the tile's A rows arrive by the ring; the producers that read
         // this entry see them (acquire here, release to them by the queue)
@@ -471,6 +482,14 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
                 if (tk.fwd_slot[j] >= 0)
                     dst[j] = p.slot_bytes + (int64_t(tk.fwd_slot[j] * p.chunks + c.q) * p.rows_c + row0) * rb;
             const int64_t bytes = int64_t(nrows) * rb;
+            if (kCheckBounds) {
+                const uint8_t *sb = tk.a_src == 1 ? p.slot_bytes : p.x_bytes;
+                const int64_t st = tk.a_src == 1 ? p.slot_total : p.x_total;
+                bool okb = src >= sb && src - sb + bytes <= st;
+                for (int j = 0; j < 2; ++j)
+                    if (dst[j]) okb = okb && dst[j] >= p.slot_bytes && dst[j] - p.slot_bytes + bytes <= p.slot_total;
+                if (!in_bounds(p, okb, kSiteBoundsForward, c.task, c.q)) break;
+            }
             const int np = int((bytes + kFwdPiece - 1) / kFwdPiece);
             auto piece = [&](int i) { return uint32_t(min(int64_t(kFwdPiece), bytes - int64_t(i) * kFwdPiece)); };
             mbar_expect_tx(&s.fbar[0], piece(0));
@@ -511,6 +530,9 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
 __device__ __forceinline__ void ag_store_slice(const KParams &p, const cm_task &tk, int64_t crow, int col0,
                                                const uint32_t (&v)[32]) {
     const int64_t orow = int64_t(tk.rank) * p.y_rank_stride + (int64_t(tk.out_idx) * p.out_rows_per_idx + crow) * p.n;
+    if (!in_bounds(p, orow >= 0 && orow + col0 + min(32, p.n - col0) <= p.y_elems, kSiteBoundsOutput, tk.rank,
+                   tk.out_idx))
+        return;
     if (p.y_f32) {
         float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(p.y) + orow + col0);
 #pragma unroll
@@ -655,6 +677,12 @@ __device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_
         // the bucket is accumulated where it lies: its partial sum is not read here
         const bool in_place = tk.out_buf >= 0 && tk.in_buf[0] == tk.out_buf;
         bool skip = false;   // a bucket load failed (the kernel is aborting): no further copies this tile
+        if (kCheckBounds) {
+            bool okb = tk.out_buf < p.acc_bufs && tk.in_buf[0] < p.acc_bufs && tk.in_buf[1] < p.acc_bufs;
+            if (tk.out_buf < 0)
+                okb = okb && (int64_t(tk.out_idx) * p.out_rows_per_idx + int64_t(c.q + 1) * p.rows_c) * p.n <= p.y_elems;
+            skip = !in_bounds(p, okb, kSiteBoundsBucket, c.task, c.q);
+        }
 #pragma unroll 1
         for (int cb = 0; cb < 4; ++cb) {
             const int col_local = half * 128 + cb * 32;
@@ -834,6 +862,13 @@ __device__ void epilogue_rs_grp(const KParams &p, const PSmem &s, uint32_t tmem_
         // the bucket is accumulated where it lies: its partial sum is not read here
         const bool in_place = tk.out_buf >= 0 && tk.in_buf[0] == tk.out_buf;
         const int64_t brow0 = int64_t(c.q) * p.rows_c + row_w;   // warp's first row in the bucket
+        bool skip = false;   // debug builds: a buffer index outside its buffer; no global access this tile
+        if (kCheckBounds) {
+            bool okb = tk.out_buf < p.acc_bufs && tk.in_buf[0] < p.acc_bufs && tk.in_buf[1] < p.acc_bufs;
+            if (tk.out_buf < 0)
+                okb = okb && (int64_t(tk.out_idx) * p.out_rows_per_idx + int64_t(c.q + 1) * p.rows_c) * p.n <= p.y_elems;
+            skip = !in_bounds(p, okb, kSiteBoundsBucket, c.task, c.q);
+        }
         const uint32_t tcol = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN);
         uint32_t v[2][32];
         tmem_ld32(tcol, v[0]);
@@ -843,7 +878,7 @@ __device__ void epilogue_rs_grp(const KParams &p, const PSmem &s, uint32_t tmem_
             uint32_t(&cur)[32] = v[cb & 1];
             if (cb + 1 < kBN / 32) tmem_ld32(tcol + uint32_t((cb + 1) * 32), v[(cb + 1) & 1]);   // in flight
             const int col0 = c.nt * kBN + cb * 32;
-            if (col0 < p.n) {
+            if (col0 < p.n && !skip) {
                 float4 *wr = reinterpret_cast<float4 *>(buf + lane * 128);
 #pragma unroll
                 for (int k = 0; k < 8; ++k)

@@ -32,9 +32,11 @@
 //   (0,0) | (1,0..1) | (2,0..2) | ... | (N-1,0..N-1) | (0,1..N-1) | (1,2..N-1) | ...
 // -- each rank's steps run in order right after its predecessor's, and a
 // rank's weight shard W_r is streamed in two runs instead of once per step.
-// Bidirectional rings (two predecessors, one each way), the undecomposed op
-// and the step-serial mode: step-major, and inside a step by rank, so that a
-// rank's clockwise and counter-clockwise tasks share one pass over W_r.
+// Bidirectional rings (two predecessors, one each way): stream-blocked --
+// the clockwise stream rank-blocked, then the counter-clockwise stream
+// rank-blocked over the mirrored ranks -- so W_r is streamed in about four
+// runs.  The undecomposed op and the step-serial mode: step-major, and
+// inside a step by rank.  CM_OPT_TASK_ORDER may run any ring step-major.
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -140,21 +142,77 @@ struct Ids {
     int fid(int kind, int r, int i, int d) const { return ((kind * N + r) * S + i) * 2 + d; }
 };
 
-// Position of task (r, i) in the rank-blocked order of a one-way ring.
-int rank_blocked_key(int N, int r, int i) {
-    if (i <= r) return r * (r + 1) / 2 + i;                          // block (r, 0..r)
-    const int first = N * (N + 1) / 2;                               // after all (r, 0..r) blocks
-    return first + r * (N - 1) - r * (r - 1) / 2 + (i - r - 1);      // block (r, r+1..N-1)
+// Position of task (r, i), 0 <= i < S, in the rank-blocked order of a chain
+// of S steps over N ranks in which (r, i) waits for (r - 1, i - 1): the
+// blocks (r, 0..min(r, S-1)) for r = 0..N-1, then the tails (r, r+1..S-1).
+// Whatever a task waits for comes earlier -- in the block before its own, or
+// (for a tail, and for rank 0's wrap to rank N-1) in an earlier tail or
+// block -- and each rank's tasks form at most two runs.
+long rank_blocked_key(int N, int S, int r, int i) {
+    long before = 0, first = 0, tails = 0;
+    for (int q = 0; q < N; ++q) {
+        const int blk = std::min(q, S - 1) + 1;   // tasks of block q
+        if (q < r) before += blk;
+        first += blk;
+        if (q < r) tails += std::max(0, S - 1 - q);
+    }
+    if (i <= r) return before + i;
+    return first + tails + (i - r - 1);
 }
 
-// Sort `tasks` into execution order -- rank-blocked (rank_blocked true) or
-// step-major -- and fill in the tile groups and the step index `sb`.
-void order_and_index(PlanImpl &p, int op, std::vector<cm_task> &tasks, bool rank_blocked, std::vector<int> &sb) {
-    if (rank_blocked) {
+// Keys of the stream-blocked order of a bidirectional ring: the clockwise
+// stream's tasks in rank-blocked order (their chain runs r-1 -> r), then the
+// counter-clockwise stream's in rank-blocked order of the mirrored ranks
+// N-1-r (their chain runs r+1 -> r).  Each rank's weight shard is then read
+// in at most four runs instead of once per step.  GEMM -> ReduceScatter
+// owners (which add both partial buckets) follow the later of their own last
+// counter-clockwise task and the counter-clockwise task they wait for, so
+// that they usually join their rank's last run.
+std::vector<double> stream_blocked_keys(const PlanImpl &p, int op, const std::vector<cm_task> &tasks) {
+    const int N = p.N;
+    int S[2] = {0, 0};   // steps of each stream's chain (one past the largest step)
+    for (const cm_task &t : tasks)
+        if (!(op == CM_OP_GEMM_RS && t.out_buf < 0)) S[t.stream] = std::max(S[t.stream], t.step + 1);
+    const double off = 1e7;   // the counter-clockwise pass after every clockwise task
+    auto key_of = [&](int stream, int r, int i) {
+        return stream == 0 ? double(rank_blocked_key(N, S[0], r, i))
+                           : off + double(rank_blocked_key(N, S[1], N - 1 - r, i));
+    };
+    std::vector<double> keys(tasks.size());
+    for (size_t j = 0; j < tasks.size(); ++j) {
+        const cm_task &t = tasks[j];
+        if (op == CM_OP_GEMM_RS && t.out_buf < 0) {   // owner
+            if (S[1] == 0) {
+                keys[j] = off + t.rank;   // no counter-clockwise stream: after the clockwise pass
+            } else {
+                const int last = S[1] - 1;
+                keys[j] = std::max(key_of(1, t.rank, last), key_of(1, (t.rank + 1) % N, last)) + 0.5;
+            }
+        } else {
+            keys[j] = key_of(t.stream, t.rank, t.step);
+        }
+    }
+    return keys;
+}
+
+// Sort `tasks` into execution order -- kind 1: the ring's blocked order
+// (rank-blocked for a one-way ring, stream-blocked for a bidirectional one);
+// kind 0: step-major -- and fill in the tile groups and the step index `sb`.
+void order_and_index(PlanImpl &p, int op, std::vector<cm_task> &tasks, bool blocked, std::vector<int> &sb) {
+    if (blocked && p.dir == CM_RING_UNI) {
         const int N = p.N;
         std::stable_sort(tasks.begin(), tasks.end(), [N](const cm_task &x, const cm_task &y) {
-            return rank_blocked_key(N, x.rank, x.step) < rank_blocked_key(N, y.rank, y.step);
+            return rank_blocked_key(N, N, x.rank, x.step) < rank_blocked_key(N, N, y.rank, y.step);
         });
+    } else if (blocked && p.dir == CM_RING_BIDI) {
+        const std::vector<double> keys = stream_blocked_keys(p, op, tasks);
+        std::vector<size_t> idx(tasks.size());
+        for (size_t j = 0; j < idx.size(); ++j) idx[j] = j;
+        std::stable_sort(idx.begin(), idx.end(), [&keys](size_t a, size_t b) { return keys[a] < keys[b]; });
+        std::vector<cm_task> sorted;
+        sorted.reserve(tasks.size());
+        for (size_t j : idx) sorted.push_back(tasks[j]);
+        tasks.swap(sorted);
     } else {
         // inside a step, a rank's tasks (its clockwise and counter-clockwise
         // shard or bucket) sit together: they share W_r and form one tile
@@ -182,11 +240,11 @@ void order_and_index(PlanImpl &p, int op, std::vector<cm_task> &tasks, bool rank
 }
 
 // Both execution orders of one op's tasks: the ring's own (rank-blocked for a
-// one-way ring, step-major otherwise and in the step-serial mode) and the
-// step-major one.
+// one-way ring, stream-blocked for a bidirectional one, step-major for the
+// undecomposed op and in the step-serial mode) and the step-major one.
 void set_orders(PlanImpl &p, int op, const std::vector<cm_task> &tasks) {
     p.tasks[op] = tasks;
-    order_and_index(p, op, p.tasks[op], p.dir == CM_RING_UNI && !p.serial_steps, p.step_begin[op]);
+    order_and_index(p, op, p.tasks[op], p.dir != CM_RING_NONE && !p.serial_steps, p.step_begin[op]);
     p.tasks_sm[op] = tasks;
     order_and_index(p, op, p.tasks_sm[op], false, p.step_begin_sm[op]);
 }
@@ -300,6 +358,15 @@ void build_rs_tasks(PlanImpl &p) {
     set_orders(p, CM_OP_GEMM_RS, tasks);
 }
 
+// Bounds-checked builds: the planted out-of-range done-signal ids of
+// CM_OPT_DEBUG_FLAG_OFFSET.
+void apply_debug_offset(PlanImpl &p) {
+    if (p.debug_flag_offset <= 0) return;
+    for (auto *v : {&p.tasks[CM_OP_GEMM_RS], &p.tasks_sm[CM_OP_GEMM_RS]})
+        for (cm_task &t : *v)
+            if (t.sig_done >= 0) t.sig_done = int16_t(t.sig_done + p.debug_flag_offset);
+}
+
 void apply_skip(PlanImpl &p) {
     if (p.skip_signal < 0) return;
     const int op = int((p.skip_signal >> 16) & 0xff);
@@ -322,6 +389,7 @@ void rebuild(PlanImpl &p) {
     build_ag_tasks(p);
     build_rs_tasks(p);
     apply_skip(p);
+    apply_debug_offset(p);
 }
 
 }  // namespace cm
@@ -437,6 +505,19 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
         case CM_OPT_STATIC_TILES:
             p.static_tiles = value != 0;
             return CM_OK;
+        case CM_OPT_DEBUG_FLAG_OFFSET:
+#ifdef CM_DEBUG_BOUNDS
+            if (value < 0 || value > 4096) return CM_ERR_INVALID_ARG;
+            p.debug_flag_offset = int(value);
+            try {
+                cm::rebuild(p);
+            } catch (...) {
+                return CM_ERR_INVALID_ARG;
+            }
+            return CM_OK;
+#else
+            return CM_ERR_INVALID_ARG;   // a testing aid of the bounds-checked build only
+#endif
         case CM_OPT_RS_EPILOGUE:
             if (value < 0 || value > 2) return CM_ERR_INVALID_ARG;
             p.rs_epilogue = int(value);

@@ -65,7 +65,8 @@ typedef enum cm_status {
     CM_ERR_UNSUPPORTED = 4,   /* legal request this build does not run */
     CM_ERR_CUDA = 5,          /* a CUDA runtime/driver call failed */
     CM_ERR_TIMEOUT = 6,       /* a device-side bounded wait expired */
-    CM_ERR_WORKSPACE = 7      /* workspace null or smaller than required */
+    CM_ERR_WORKSPACE = 7,     /* workspace null or smaller than required */
+    CM_ERR_BOUNDS = 8         /* debug build: a computed index fell outside its buffer (access not made) */
 } cm_status;
 
 typedef enum cm_direction {
@@ -294,9 +295,11 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
 /*
  * cm_check_status -- synchronise `stream` and read the device status word of
  * the last call that used `ws`.  Returns CM_OK, CM_ERR_TIMEOUT (a bounded
- * wait expired; the outputs of that call are undefined) or CM_ERR_CUDA.
- * If info is non-NULL it receives {code, task, chunk, site} of the first
- * failure.
+ * wait expired; the outputs of that call are undefined), CM_ERR_BOUNDS (a
+ * library built with bounds checks -- CM_DEBUG_BOUNDS -- found a computed
+ * flag, slot, row or buffer index outside its buffer and skipped that
+ * access; the outputs are undefined) or CM_ERR_CUDA.  If info is non-NULL it
+ * receives {code, task, chunk, site} of the first failure.
  */
 cm_status cm_check_status(const void *ws, cm_stream_t stream, int32_t info[4]);
 
@@ -387,6 +390,13 @@ const char *cm_status_string(cm_status status);
  *                        otherwise (the faster of the two in measurement).
  *                        The same fp32 additions in the same order: the same
  *                        bits.
+ *  CM_OPT_DEBUG_FLAG_OFFSET  only in a library built with bounds checks
+ *                        (CM_DEBUG_BOUNDS; other builds return
+ *                        CM_ERR_INVALID_ARG): adds `value` (>= 0) to the flag
+ *                        id of every GEMM -> ReduceScatter task's done signal,
+ *                        a planted mistake that puts those signals beyond the
+ *                        flag words, so that tests can see the checks turn it
+ *                        into CM_ERR_BOUNDS.  0 clears it.
  */
 typedef enum cm_option {
     CM_OPT_TIMEOUT_NS = 0,
@@ -403,7 +413,8 @@ typedef enum cm_option {
     CM_OPT_RS_PRELOAD = 11,
     CM_OPT_RS_IN_PLACE = 12,
     CM_OPT_TASK_ORDER = 13,
-    CM_OPT_RS_EPILOGUE = 14
+    CM_OPT_RS_EPILOGUE = 14,
+    CM_OPT_DEBUG_FLAG_OFFSET = 15
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);
@@ -451,6 +462,35 @@ cm_status cm_cost_estimate(int n_ranks, int chunks, cm_direction dir, cm_op op, 
                            int64_t n, const cm_rates *rates, double *us);
 cm_status cm_plan_choose(int n_ranks, cm_op op, int64_t rows, int64_t K, int64_t n, const cm_rates *rates,
                          int max_chunks, int *chunks, cm_direction *dir, double *us);
+
+/*
+ * One Einsum that offers both collectives (same page, section "The idea":
+ * the cost model "picks which of two candidate collectives to overlap when
+ * an Einsum offers both").  Per rank: the A operand is the AllGather of N row
+ * shards [m, K]; the rank multiplies the gathered [N*m, K] by its [K, n]
+ * weight; the [N*m, n] fp32 result is summed over the ranks and scattered
+ * (bucket o = rows o*m .. o*m + m - 1).  Only one collective can become the
+ * ring; the other stays native.
+ *
+ * cm_einsum_cost -- predicted time in us of one candidate:
+ *   decompose = CM_OP_AG_GEMM: the AllGather ring (chunks, dir), then the
+ *     native ReduceScatter;
+ *   decompose = CM_OP_GEMM_RS: the native AllGather, then the ReduceScatter
+ *     ring;
+ *   decompose = -1 (or dir CM_RING_NONE, or n_ranks 1): both native around
+ *     the GEMM.
+ *   Errors: CM_ERR_INVALID_ARG for a bad argument or rate.
+ * cm_plan_choose_einsum -- the fastest of: both native, and each collective
+ *   decomposed with one-way and bidirectional rings of 1, 2, 4 ...
+ *   max_chunks chunks that split m evenly.  *decompose receives
+ *   CM_OP_AG_GEMM, CM_OP_GEMM_RS or -1 (decline: both native); *chunks and
+ *   *dir the ring; *us (optional) the predicted time.  Ties keep the simpler
+ *   choice (native, then the gather, one-way, fewer chunks).
+ */
+cm_status cm_einsum_cost(int n_ranks, int chunks, cm_direction dir, int decompose, int64_t m, int64_t K, int64_t n,
+                         const cm_rates *rates, double *us);
+cm_status cm_plan_choose_einsum(int n_ranks, int64_t m, int64_t K, int64_t n, const cm_rates *rates, int max_chunks,
+                                int *decompose, int *chunks, cm_direction *dir, double *us);
 
 /* Library version string. */
 const char *cm_version(void);

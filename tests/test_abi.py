@@ -154,3 +154,21 @@ def test_no_multicast_load_in_the_kernels():
         for line in open(os.path.join(csrc, f)):
             if "multicast::cluster" in line:
                 assert "cp.async" not in line and "tcgen05.commit" in line, (f, line)
+
+
+def test_bounds_checked_build_loads_and_only_it_takes_the_planted_offset(lib):
+    """The bounds-checked build exports the same symbols; only it accepts
+    CM_OPT_DEBUG_FLAG_OFFSET (a testing aid for its checks)."""
+    dbg = cm.bounds_checked()
+    for name in _declared():
+        assert hasattr(dbg.load(), name), name
+    assert "bounds-checked" in dbg.version()
+    p = cm.Plan(4, 1, "uni")
+    with pytest.raises(cm.CMError):
+        p.set_option(cm.CM_OPT_DEBUG_FLAG_OFFSET, 8)
+    q = dbg.Plan(4, 1, "uni")
+    q.set_option(dbg.CM_OPT_DEBUG_FLAG_OFFSET, 8)
+    base = {t.sig_done for t in cm.Plan(4, 1, "uni").tasks(cm.CM_OP_GEMM_RS)}
+    moved = {t.sig_done for t in q.tasks(dbg.CM_OP_GEMM_RS)}
+    assert moved == {s + 8 for s in base}
+    assert cm.status_string(cm.CM_ERR_BOUNDS)

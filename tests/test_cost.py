@@ -219,3 +219,93 @@ def test_argument_errors(lib):
         assert lib.cm_cost_estimate(4, 1, 0, AG, 64, 64, 64, ref(rb), ref(us)) == cm.CM_ERR_INVALID_ARG
     with pytest.raises(cm.CMError):
         cm.plan_choose(4, AG, 64, 64, 64, rates(), max_chunks=0)
+
+
+# ---- one Einsum that offers both collectives ----------------------------------
+# Per rank: gathered A [N*m, K] (N row shards [m, K]), weight [K, n], the
+# [N*m, n] fp32 result summed over ranks and scattered in buckets of m rows.
+
+def einsum_native(r, N, m, K, n):
+    """Both collectives native around the GEMM (closed form)."""
+    coll = r["coll_gbs"] * 1e3
+    return ((N - 1) * m * K * 2 / coll + 2.0 * N * m * K * n / (r["gemm_tflops"] * 1e6)
+            + (N - 1) * m * n * 4 / coll)
+
+
+def test_einsum_native_closed_form():
+    r = rates()
+    for N, m, K, n in ((2, 64, 256, 512), (8, 512, 4096, 2048), (16, 128, 1024, 8192)):
+        assert cm.einsum_cost(N, 1, "none", "none", m, K, n, r) == pytest.approx(einsum_native(r, N, m, K, n),
+                                                                                  rel=1e-12)
+        # a ring direction with nothing decomposed, or one rank, is the same thing
+        assert cm.einsum_cost(N, 2, "uni", "none", m, K, n, r) == pytest.approx(einsum_native(r, N, m, K, n))
+    assert cm.einsum_cost(1, 1, "uni", "ag", 64, 256, 512, r) == pytest.approx(einsum_native(r, 1, 64, 256, 512))
+
+
+def test_einsum_each_decomposition_is_its_ring_plus_the_other_native():
+    """Decomposing the gather = the AG ring (cm_cost_estimate) + native
+    scatter; decomposing the scatter = native gather + the RS ring over the
+    N*m gathered rows."""
+    r = rates(tflops=700.0, ring=300.0, coll=500.0, hop=3.0)
+    N, m, K, n = 8, 512, 4096, 2048
+    coll = r["coll_gbs"] * 1e3
+    for c, d in itertools.product((1, 2, 4), ("uni", "bidi")):
+        want_ag = cm.cost_estimate(N, c, d, AG, m, K, n, r) + (N - 1) * m * n * 4 / coll
+        want_rs = (N - 1) * m * K * 2 / coll + cm.cost_estimate(N, c, d, RS, N * m, K, n, r)
+        assert cm.einsum_cost(N, c, d, "ag", m, K, n, r) == pytest.approx(want_ag, rel=1e-12)
+        assert cm.einsum_cost(N, c, d, "rs", m, K, n, r) == pytest.approx(want_rs, rel=1e-12)
+
+
+def test_einsum_free_communication_keeps_everything_native():
+    """With free links nothing is gained by a ring: ties keep the native form."""
+    r = rates(ring=1e12, coll=1e12, hop=0.0)
+    w, c, d, us = cm.plan_choose_einsum(8, 512, 4096, 2048, r)
+    assert (w, c, d) == ("none", 1, "none")
+    assert us == pytest.approx(2.0 * 8 * 512 * 4096 * 2048 / (r["gemm_tflops"] * 1e6), rel=1e-9)
+
+
+def test_einsum_decomposes_the_heavier_collective():
+    """A wide contraction (K >> n) makes the gather the big transfer; a wide
+    output (n >> K) makes the fp32 scatter the big one.  The choice follows."""
+    r = rates(tflops=1000.0, ring=400.0, coll=500.0)
+    w, _, _, _ = cm.plan_choose_einsum(8, 1024, 16384, 512, r)
+    assert w == "ag"
+    w, _, _, _ = cm.plan_choose_einsum(8, 1024, 512, 16384, r)
+    assert w == "rs"
+
+
+def test_einsum_declines_thin_compute():
+    """Little compute and a slow ring: neither ring can hide its transfer."""
+    r = rates(tflops=2000.0, ring=20.0, coll=600.0)
+    w, c, d, us = cm.plan_choose_einsum(8, 256, 256, 256, r)
+    assert (w, c, d) == ("none", 1, "none")
+    assert us == pytest.approx(einsum_native(r, 8, 256, 256, 256), rel=1e-9)
+
+
+def test_einsum_choice_is_the_minimum_over_candidates():
+    rnd = random.Random(23)
+    for _ in range(40):
+        r = rates(tflops=rnd.uniform(50, 2000), ring=rnd.uniform(5, 900), coll=rnd.uniform(5, 900),
+                  hop=rnd.uniform(0, 50), mem=rnd.uniform(500, 8000))
+        N = rnd.choice([2, 3, 4, 8, 16])
+        m, K, n = rnd.choice([64, 256, 1024]), rnd.choice([256, 4096]), rnd.choice([512, 8192])
+        w, c, d, us = cm.plan_choose_einsum(N, m, K, n, r)
+        cands = [cm.einsum_cost(N, 1, "none", "none", m, K, n, r)]
+        cands += [cm.einsum_cost(N, cc, dd, ww, m, K, n, r)
+                  for ww in ("ag", "rs") for dd in ("uni", "bidi") for cc in (1, 2, 4, 8) if m % cc == 0]
+        assert us == pytest.approx(min(cands), rel=1e-8)
+        assert us == pytest.approx(cm.einsum_cost(N, c, d, w, m, K, n, r), rel=1e-12)
+
+
+def test_einsum_argument_errors(lib):
+    ctypes = __import__("ctypes")
+    r = cm._rates(rates())
+    us = ctypes.c_double()
+    assert lib.cm_einsum_cost(4, 1, 0, 5, 64, 64, 64, ctypes.byref(r), ctypes.byref(us)) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_einsum_cost(4, 1, 0, AG, 0, 64, 64, ctypes.byref(r), ctypes.byref(us)) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_einsum_cost(4, 1, 0, AG, 64, 64, 64, None, ctypes.byref(us)) == cm.CM_ERR_INVALID_ARG
+    w, c, d = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+    assert lib.cm_plan_choose_einsum(4, 64, 64, 64, ctypes.byref(r), 0, ctypes.byref(w), ctypes.byref(c),
+                                     ctypes.byref(d), None) == cm.CM_ERR_INVALID_ARG
+    assert lib.cm_plan_choose_einsum(4, 64, 64, 64, ctypes.byref(r), 4, None, ctypes.byref(c),
+                                     ctypes.byref(d), None) == cm.CM_ERR_INVALID_ARG

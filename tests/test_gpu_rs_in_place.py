@@ -148,9 +148,11 @@ def test_in_place_back_to_back_on_one_workspace():
         assert oracle.normwise_max_rel_err(_np(y), ref) <= TOL_F32
 
 
-@pytest.mark.parametrize("N,chunks", [(4, 1), (8, 2)])
-def test_task_orders_agree_bitwise(N, chunks):
-    """Rank-blocked and step-major task orders only reorder the tiles: every
+@pytest.mark.parametrize("direction", ["uni", "bidi"])
+@pytest.mark.parametrize("N,chunks", [(4, 1), (8, 2), (5, 1)])
+def test_task_orders_agree_bitwise(N, chunks, direction):
+    """The ring's own task order (rank-blocked one-way, stream-blocked
+    two-way) and the step-major one only reorder the tiles: every
     output element is the same dot product (AllGather->GEMM) or the same
     ring-ordered fp32 sum (GEMM->ReduceScatter), so the bits agree."""
     m, K, n = 256, 384, 768
@@ -159,7 +161,7 @@ def test_task_orders_agree_bitwise(N, chunks):
     from test_gpu_parity import run_ag
     outs = []
     for order in (1, 2):
-        p = cm.Plan(N, chunks, "uni")
+        p = cm.Plan(N, chunks, direction)
         p.set_option(cm.CM_OPT_TASK_ORDER, order)
         y, _, _ = run_ag(p, x, w, "nk", torch.float32)
         yr, _, _ = run_rs(p, xr, wr, "nk", torch.float32)

@@ -72,14 +72,15 @@ def test_each_rank_uses_each_shard_once(N, direction):
 def test_waits_point_to_earlier_tasks(N, direction, serial, order):
     """Every flag has exactly one signalling task, earlier in the table than
     every task waiting on it, and of an earlier ring step -- in the ring's
-    own order and in step-major order."""
+    own order (rank-blocked one-way, stream-blocked two-way) and in
+    step-major order."""
     p = cm.Plan(N, 2, direction)
     if serial:
         p.set_option(cm.CM_OPT_SERIAL_STEPS, 1)
     p.set_option(cm.CM_OPT_TASK_ORDER, order)
     for op in (AG, RS):
         tasks = p.tasks(op)
-        if serial or direction != "uni" or order == 2:
+        if serial or direction == "none" or order == 2:
             assert [t.step for t in tasks] == sorted(t.step for t in tasks)
         signallers = {}
         for idx, t in enumerate(tasks):
@@ -94,6 +95,27 @@ def test_waits_point_to_earlier_tasks(N, direction, serial, order):
                     assert f in signallers, (op, f)
                     assert signallers[f][0] < idx
                     assert signallers[f][1] < t.step
+
+
+@pytest.mark.parametrize("N", [3, 4, 8, 16])
+def test_bidi_stream_blocked_runs(N):
+    """A two-way ring's own order: clockwise tasks before counter-clockwise
+    ones (owners aside), and each rank's tasks in at most five runs -- its
+    weight shard is read that many times instead of once per step."""
+    p = cm.Plan(N, 1, "bidi")
+    for op in (AG, RS):
+        tasks = p.tasks(op)
+        streams = [t.stream for t in tasks if not (op == RS and t.out_buf < 0)]
+        assert streams == sorted(streams)
+        runs = {}
+        prev = None
+        for t in tasks:
+            if t.rank != prev:
+                runs[t.rank] = runs.get(t.rank, 0) + 1
+            prev = t.rank
+        assert max(runs.values()) <= 5, runs
+        if N >= 8:
+            assert max(runs.values()) < p.steps(op)
 
 
 def test_step_major_order_is_a_permutation_of_the_ring_order():
