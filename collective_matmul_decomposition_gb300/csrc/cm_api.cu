@@ -29,9 +29,14 @@ constexpr int64_t kPreloadAllKSlices = 8;
 // groups were 2-6 % faster on one-way rings of 8 and 16 ranks with at least
 // 28 K slices per tile and on two-way rings of 16 ranks; the TMA epilogue
 // was as fast or faster everywhere else (6-11 % on the GPT-3 layer, 24 K
-// slices; 1-3 % at 4 ranks and on two-way rings of 8).
-int rs_groups(const PlanImpl &pl, int64_t k) {
+// slices; 1-3 % at 4 ranks and on two-way rings of 8).  Those tiles read
+// nothing back (buckets in place, pipelined partials); where every tile
+// loads its input -- buckets in per-step buffers, Cannon's chained
+// accumulator (q = 4: 1.17 against 1.37 ms) -- the TMA epilogue is used.
+// reads_inputs: the tiles of the call load a received bucket in the epilogue.
+int rs_groups(const PlanImpl &pl, int64_t k, bool reads_inputs) {
     if (pl.rs_epilogue != 0) return pl.rs_epilogue == 2 ? 1 : 0;
+    if (reads_inputs) return 0;
     const int64_t kslices = (k + kBK - 1) / kBK;
     const bool many_ranks = pl.N >= 16 || (pl.N >= 8 && pl.dir == CM_RING_UNI);
     return many_ranks && kslices >= 28 ? 1 : 0;
@@ -450,7 +455,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    kp.rs_groups = rs_groups(pl, k);
+    kp.rs_groups = rs_groups(pl, k, !pl.rs_in_place);
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
     const bool sm = use_step_major(pl, int64_t(N) * k * n * 2);
     return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, sm, reinterpret_cast<cudaStream_t>(stream));
@@ -519,7 +524,7 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    kp.rs_groups = rs_groups(pl, k);
+    kp.rs_groups = rs_groups(pl, k, false);
     // chunks of at most 128 rows go two to a launch, one per CTA of each pair
     // tile (the ring path's chunk pairing), instead of half-empty pair tiles
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
@@ -768,7 +773,7 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
     kp.n = int(bn);
     kp.y_f32 = c_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    kp.rs_groups = rs_groups(pl, bk);
+    kp.rs_groups = rs_groups(pl, bk, true);
     set_tiling(kc, CM_OP_GEMM_RS, kp, bm, bn);
     kp.tgt_in = kp.tgt_free = 0;
     WsLayout l;

@@ -386,8 +386,11 @@ const char *cm_status_string(cm_status status);
  *                        coalesced vector adds (red.global.add.v4.f32),
  *                        stores and loads; 0 (default) two groups for rings
  *                        of 8 ranks (one-way) or 16 (either) whose tiles
- *                        have at least 28 K slices of 64, the TMA path
- *                        otherwise (the faster of the two in measurement).
+ *                        have at least 28 K slices of 64 and read nothing
+ *                        back (buckets in place, pipelined partials), the
+ *                        TMA path otherwise -- per-step buffers and Cannon's
+ *                        chained accumulator included (the faster of the two
+ *                        in measurement).
  *                        The same fp32 additions in the same order: the same
  *                        bits.
  *  CM_OPT_DEBUG_FLAG_OFFSET  only in a library built with bounds checks
