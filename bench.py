@@ -1038,6 +1038,10 @@ def run_profile_case(args):
         st.plan.set_option(st.cm.CM_OPT_RS_PRELOAD, args.rs_preload)
     if args.rs_in_place >= 0:
         st.set_rs_in_place(args.rs_in_place)
+    if args.rs_epilogue >= 0:
+        st.plan.set_option(st.cm.CM_OPT_RS_EPILOGUE, args.rs_epilogue)
+    if args.task_order >= 0:
+        st.plan.set_option(st.cm.CM_OPT_TASK_ORDER, args.task_order)
     fn = {"ag": st.ag, "rs": st.rs, "rs_pipe": st.rs_pipe}[args.profile]
     f_ag, f_rs = flops(data["shapes"], N)
     ms = time_loop(fn, args.steps, torch, warmup=args.warmup)
@@ -1045,6 +1049,7 @@ def run_profile_case(args):
     fl = f_ag if args.profile == "ag" else f_rs
     print(json.dumps({"profile_case": args.workload, "op": args.profile, "N": N, "chunks": args.chunks,
                       "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group, "l2_hints": args.l2_hints, "l2_promotion": args.l2_promotion, "row_band": args.row_band, "rs_preload": args.rs_preload, "rs_in_place": args.rs_in_place,
+                      "rs_epilogue": args.rs_epilogue, "task_order": args.task_order,
                       "ms": ms, "tflops": fl / (ms / 1e3) / 1e12}), flush=True)
     return 0
 
@@ -1075,6 +1080,8 @@ def main(argv=None):
     ap.add_argument("--row-band", type=int, default=-1, help="CM_OPT_ROW_BAND for --profile (-1 = default)")
     ap.add_argument("--rs-preload", type=int, default=-1, help="CM_OPT_RS_PRELOAD for --profile (-1 = default)")
     ap.add_argument("--rs-in-place", type=int, default=-1, help="CM_OPT_RS_IN_PLACE for --profile (-1 = default)")
+    ap.add_argument("--rs-epilogue", type=int, default=-1, help="CM_OPT_RS_EPILOGUE for --profile (-1 = default)")
+    ap.add_argument("--task-order", type=int, default=-1, help="CM_OPT_TASK_ORDER for --profile (-1 = default)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="oracle seconds for the cpu_baseline of the default arm")
     ap.add_argument("--ref-seconds", type=float, default=120.0,

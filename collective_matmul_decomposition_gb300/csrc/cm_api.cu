@@ -23,7 +23,9 @@ constexpr int64_t kPreloadAllKSlices = 8;
 
 // CM_OPT_RS_EPILOGUE: 1 = every epilogue warp on every tile, TMA copies
 // through shared memory; 2 = two warp groups, one per accumulator, with
-// vector reductions; 0 = automatic.
+// vector reductions; 3 = every epilogue warp on every tile, vector
+// reductions; 0 = automatic.  Returns the kernel's mode (KParams::rs_epi):
+// the option value less one.
 // The automatic choice, measured over the MLP sweep (h=8192, ffn=28672,
 // s=8192) and the GPT-3 attention-out GEMM-RS with both interleaved: two
 // groups were 2-6 % faster on one-way rings of 8 and 16 ranks with at least
@@ -33,9 +35,13 @@ constexpr int64_t kPreloadAllKSlices = 8;
 // nothing back (buckets in place, pipelined partials); where every tile
 // loads its input -- buckets in per-step buffers, Cannon's chained
 // accumulator (q = 4: 1.17 against 1.37 ms) -- the TMA epilogue is used.
+// Every warp with vector reductions (3) measured in between: GPT-3
+// attention-out 0.462 ms against 0.440 (TMA) and 0.475 (groups), within
+// 1.5 % of the better of the other two on the MLP sweep; it is never chosen
+// automatically.
 // reads_inputs: the tiles of the call load a received bucket in the epilogue.
-int rs_groups(const PlanImpl &pl, int64_t k, bool reads_inputs) {
-    if (pl.rs_epilogue != 0) return pl.rs_epilogue == 2 ? 1 : 0;
+int rs_epi_mode(const PlanImpl &pl, int64_t k, bool reads_inputs) {
+    if (pl.rs_epilogue != 0) return pl.rs_epilogue - 1;
     if (reads_inputs) return 0;
     const int64_t kslices = (k + kBK - 1) / kBK;
     const bool many_ranks = pl.N >= 16 || (pl.N >= 8 && pl.dir == CM_RING_UNI);
@@ -177,10 +183,12 @@ void set_tiling(const KernelChoice &kc, int op, KParams &kp, int64_t rows_c, int
         kp.tgt_in = uint32_t(kc.pair ? per_tile * kp.ntiles : 1);
         kp.tgt_free = 0;   // receive slots are written once: nothing waits for a slot to be free
     } else {
-        // signals of the same bucket tile: CTA pairs, one per warp of the
-        // epilogue group that drains it (two groups) or one per CTA (TMA
-        // epilogue), in each CTA holding the chunk; single CTAs, one per tile
-        kp.tgt_in = uint32_t(kc.pair ? (kp.rs_groups ? per_tile * (kPairEpiWarps / 2) : per_tile) : 1);
+        // signals of the same bucket tile: CTA pairs, one per warp that
+        // drains it (vector epilogues: the four of a group, or all eight) or
+        // one per CTA (TMA epilogue), in each CTA holding the chunk; single
+        // CTAs, one per tile
+        const uint32_t warps = kp.rs_epi == 1 ? kPairEpiWarps / 2 : kp.rs_epi == 2 ? kPairEpiWarps : 1;
+        kp.tgt_in = uint32_t(kc.pair ? per_tile * warps : 1);
         kp.tgt_free = kp.tgt_in;
     }
 }
@@ -455,7 +463,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    kp.rs_groups = rs_groups(pl, k, !pl.rs_in_place);
+    kp.rs_epi = rs_epi_mode(pl, k, !pl.rs_in_place);
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
     const bool sm = use_step_major(pl, int64_t(N) * k * n * 2);
     return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, sm, reinterpret_cast<cudaStream_t>(stream));
@@ -524,7 +532,7 @@ cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    kp.rs_groups = rs_groups(pl, k, false);
+    kp.rs_epi = rs_epi_mode(pl, k, false);
     // chunks of at most 128 rows go two to a launch, one per CTA of each pair
     // tile (the ring path's chunk pairing), instead of half-empty pair tiles
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
@@ -631,11 +639,14 @@ cm_status cm_backward_pair(cm_plan_t plan, const void *x, const void *w, const v
         if (cudaEventRecord(ss->ev[0], s) != cudaSuccess) return CM_ERR_CUDA;
         if (cudaStreamWaitEvent(ag, ss->ev[0], 0) != cudaSuccess) return CM_ERR_CUDA;
     }
+    // rank r receives shards 0..N-1 in order, into one contiguous [T][K]
+    // buffer: shard j of x lands at row block j, so the N shards of one rank
+    // go as one copy (fewer, larger copies keep the copy engine's per-copy
+    // cost off the critical path)
     for (int r = 0; r < N; ++r)
-        for (int j = 0; j < N; ++j)
-            if (cudaMemcpyAsync(xg + (size_t(r) * N + j) * shard, static_cast<const uint8_t *>(x) + size_t(j) * shard,
-                                shard, cudaMemcpyDeviceToDevice, ag) != cudaSuccess)
-                return CM_ERR_CUDA;
+        if (cudaMemcpyAsync(xg + size_t(r) * N * shard, x, size_t(N) * shard, cudaMemcpyDeviceToDevice, ag) !=
+            cudaSuccess)
+            return CM_ERR_CUDA;
     if (pl.bulk_overlap && cudaEventRecord(ss->ev[1], ag) != cudaSuccess) return CM_ERR_CUDA;
 
     // 2. the data gradient: GEMM -> ReduceScatter of dY_r @ W_r on the ring
@@ -696,6 +707,32 @@ cm_status cm_backward_pair(cm_plan_t plan, const void *x, const void *w, const v
         return CM_ERR_CUDA;
     return CM_OK;
 }
+
+// Device-to-device copies issued in order, with each copy that continues the
+// previous one in both source and destination merged into it: a rotation
+// by whole blocks becomes a few large copies instead of one per block.
+struct CopyList {
+    struct C {
+        uint8_t *dst;
+        const uint8_t *src;
+        size_t bytes;
+    };
+    C c[2 * CM_MAX_RANKS];
+    int n = 0;
+    void add(uint8_t *dst, const uint8_t *src, size_t bytes) {
+        if (n > 0 && c[n - 1].dst + c[n - 1].bytes == dst && c[n - 1].src + c[n - 1].bytes == src) {
+            c[n - 1].bytes += bytes;
+            return;
+        }
+        c[n++] = C{dst, src, bytes};
+    }
+    bool issue(cudaStream_t st) const {
+        for (int k = 0; k < n; ++k)
+            if (cudaMemcpyAsync(c[k].dst, c[k].src, c[k].bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+                return false;
+        return true;
+    }
+};
 
 // Cannon workspace: the status block, two fp32 accumulators per rank
 // (ping-pong across steps), then two sets of rotated A blocks and two of B.
@@ -773,7 +810,7 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
     kp.n = int(bn);
     kp.y_f32 = c_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    kp.rs_groups = rs_groups(pl, bk, true);
+    kp.rs_epi = rs_epi_mode(pl, bk, true);
     set_tiling(kc, CM_OP_GEMM_RS, kp, bm, bn);
     kp.tgt_in = kp.tgt_free = 0;
     WsLayout l;
@@ -828,19 +865,24 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
             if (step == 0 && cudaStreamWaitEvent(ss->stream, ev[0], 0) != cudaSuccess) return CM_ERR_CUDA;
             if (step >= 1 && cudaStreamWaitEvent(ss->stream, ev[1 + q + step - 1], 0) != cudaSuccess)
                 return CM_ERR_CUDA;
+            CopyList cl;
             for (int rho = 0; rho < P; ++rho) {
                 const int i = rho / q, j = rho % q;
-                const int ra = i * q + (j + 1) % q, rb = ((i + 1) % q) * q + j;   // right and lower neighbours
-                const uint8_t *sa = step == 0 ? a_in + size_t(i * q + held_k(i, (j + 1) % q, 0)) * a_blk
-                                              : aset[step % 2] + size_t(ra) * a_blk;
-                const uint8_t *sb = step == 0 ? b_in + size_t(held_k((i + 1) % q, j, 0) * q + j) * b_blk
-                                              : bset[step % 2] + size_t(rb) * b_blk;
-                if (cudaMemcpyAsync(aset[nx % 2] + size_t(rho) * a_blk, sa, a_blk, cudaMemcpyDeviceToDevice,
-                                    ss->stream) != cudaSuccess ||
-                    cudaMemcpyAsync(bset[nx % 2] + size_t(rho) * b_blk, sb, b_blk, cudaMemcpyDeviceToDevice,
-                                    ss->stream) != cudaSuccess)
-                    return CM_ERR_CUDA;
+                const int ra = i * q + (j + 1) % q;   // right neighbour
+                cl.add(aset[nx % 2] + size_t(rho) * a_blk,
+                       step == 0 ? a_in + size_t(i * q + held_k(i, (j + 1) % q, 0)) * a_blk
+                                 : aset[step % 2] + size_t(ra) * a_blk,
+                       a_blk);
             }
+            for (int rho = 0; rho < P; ++rho) {
+                const int i = rho / q, j = rho % q;
+                const int rb = ((i + 1) % q) * q + j;   // lower neighbour
+                cl.add(bset[nx % 2] + size_t(rho) * b_blk,
+                       step == 0 ? b_in + size_t(held_k((i + 1) % q, j, 0) * q + j) * b_blk
+                                 : bset[step % 2] + size_t(rb) * b_blk,
+                       b_blk);
+            }
+            if (!cl.issue(ss->stream)) return CM_ERR_CUDA;
             if (cudaEventRecord(ev[1 + nx], ss->stream) != cudaSuccess) return CM_ERR_CUDA;
         }
     }

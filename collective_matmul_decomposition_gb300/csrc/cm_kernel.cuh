@@ -80,8 +80,9 @@ struct KParams {
     int pre_stages;            // ... as this many ring stages per tile (4: every slice, 2: the first two
                                //     32-column slices of each epilogue warp)
     int pre_box_rows;          // rows of a tmAccIn box (128, or rows_c if smaller)
-    int rs_groups;             // CTA pairs, RS: 1 = two epilogue warp groups (one per accumulator) with
-                               // vector reductions; 0 = every epilogue warp on every tile, TMA copies
+    int rs_epi;                // CTA pairs, RS epilogue: 0 = every epilogue warp on every tile, TMA
+                               // copies; 1 = two epilogue warp groups (one per accumulator) with vector
+                               // reductions; 2 = every epilogue warp on every tile, vector reductions
     int chunk_pair;            // CTA pairs: a pair tile covers chunks 2g and 2g+1 (one per CTA; chunks
                                // of at most 128 rows), and the tile decode's chunk index is g
     int tiles_per_task, task_begin, task_end;

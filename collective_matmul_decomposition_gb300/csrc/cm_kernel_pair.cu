@@ -789,18 +789,23 @@ __device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_
     if (lane == 0) bulk_wait<0>();
 }
 
-// GEMM -> ReduceScatter epilogue in two warp groups (CM_OPT_RS_EPILOGUE =
-// 2).  The eight epilogue warps form two groups of four, one per TMEM
-// accumulator: group g takes every other tile (the ones
-// the MMA thread put in accumulator g), so two tiles' epilogues -- and their
-// latencies (input flags, the wait for a tile's adds to be performed) --
-// overlap.  In a group, warp w reads TMEM lanes 32*(w % 4).. and handles those
-// 32 rows x 256 columns of the tile in eight 32-column slices.  A slice read
-// from TMEM (one row per lane) is turned round through the warp's 4 KB
-// buffer, so that each lane then holds four consecutive columns of 8 rows and
-// 8 lanes cover a row's 128 bytes: every global access below is a coalesced
-// 16-byte vector, and none goes through the TMA unit, which stays free for
-// the operand loads.
+// GEMM -> ReduceScatter epilogue with vector accesses, in one of two warp
+// arrangements:
+//  - GROUPS (CM_OPT_RS_EPILOGUE = 2): the eight epilogue warps form two
+//    groups of four, one per TMEM accumulator: group g takes every other
+//    tile (the ones the MMA thread put in accumulator g), so two tiles'
+//    epilogues -- and their latencies (input flags, the wait for a tile's
+//    adds to be performed) -- overlap.  Warp w reads TMEM lanes 32*(w % 4)..
+//    and handles those 32 rows x 256 columns of the tile in eight 32-column
+//    slices;
+//  - all warps (CM_OPT_RS_EPILOGUE = 3): every warp on every tile, as the
+//    TMA epilogue: warp w takes rows 32*(w % 4).. and columns 128*(w / 4)..
+//    in four slices, so a tile drains in half the time of a group's.
+// A slice read from TMEM (one row per lane) is turned round through the
+// warp's 4 KB buffer, so that each lane then holds four consecutive columns
+// of 8 rows and 8 lanes cover a row's 128 bytes: every global access below is
+// a coalesced 16-byte vector, and none goes through the TMA unit, which stays
+// free for the operand loads.
 //  - a bucket kept in place (in_buf[0] == out_buf): the slice is added into
 //    the bucket where it lies (red.global.add.v4.f32, performed at L2);
 //  - the first contributor (no input): the slice is stored as the bucket;
@@ -811,26 +816,31 @@ __device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_
 // TMEM slices are loaded one ahead.  Each warp signals its share of a tile
 // on its own, once its lanes' accesses are ordered before the signal (a
 // fence in every lane, a warp barrier, a release by lane 0): a consumer waits
-// for all four warps of the group in each CTA, and no warp waits for another.
+// for every warp that drains the tile (four or eight) in each CTA, and no
+// warp waits for another.
 
-__device__ void epilogue_rs_grp(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
+template <bool GROUPS>
+__device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
+    constexpr int kSlices = GROUPS ? kBN / 32 : kBN / 64;   // 32-column slices per warp and tile
     const int e = int(threadIdx.x) / 32 - 4;   // 0..7
     const int lane = int(threadIdx.x) & 31;
     const int quad = e & 3;                    // TMEM lanes 32*quad.. (warp % 4)
-    const int grp = e >> 2;                    // accumulator (and tile parity) of this warp's group
+    const int grp = e >> 2;                    // GROUPS: accumulator (and tile parity) of this warp's group;
+                                               // else the warp's half of the tile's columns
+    const int col_w = GROUPS ? 0 : grp * (kBN / 2);   // warp's first column in the tile
     const uint32_t tempty_leader0 = mapa_shared(smem_u32(&s.tempty[0]), cl.leader);   // buffer b: +8*b
     uint8_t *buf = s.fbuf[0] + e * 4096;   // 32 rows x 128 bytes; 16-byte chunk j of row r at j ^ (r & 7)
     const int tr = lane >> 3, tc = lane & 7;   // turned round: rows 4i + tr, columns 4tc..4tc+3 of the slice
     QueueReader qr;
     if (lane == 0) qr.init(s);
-    const int accb = grp;
+    int accb = GROUPS ? grp : 0;
     uint32_t acc_phase = 0;
     for (int j = 0;; ++j) {
         QTile e;
         if (lane == 0) e = qr.next(p, s, true);   // every warp reads (and releases) every entry
         const int t = __shfl_sync(0xffffffffu, e.t, 0);
         if (t < 0) break;
-        if ((j & 1) != grp) continue;   // the other group's tile
+        if (GROUPS && (j & 1) != grp) continue;   // the other group's tile
         TileCoord c;
         c.task = __shfl_sync(0xffffffffu, e.task, 0);
         c.q = __shfl_sync(0xffffffffu, e.q, 0);
@@ -869,15 +879,15 @@ __device__ void epilogue_rs_grp(const KParams &p, const PSmem &s, uint32_t tmem_
                 okb = okb && (int64_t(tk.out_idx) * p.out_rows_per_idx + int64_t(c.q + 1) * p.rows_c) * p.n <= p.y_elems;
             skip = !in_bounds(p, okb, kSiteBoundsBucket, c.task, c.q);
         }
-        const uint32_t tcol = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN);
+        const uint32_t tcol = tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN + col_w);
         uint32_t v[2][32];
         tmem_ld32(tcol, v[0]);
         tmem_wait_ld_regs(v[0]);
 #pragma unroll
-        for (int cb = 0; cb < kBN / 32; ++cb) {
+        for (int cb = 0; cb < kSlices; ++cb) {
             uint32_t(&cur)[32] = v[cb & 1];
-            if (cb + 1 < kBN / 32) tmem_ld32(tcol + uint32_t((cb + 1) * 32), v[(cb + 1) & 1]);   // in flight
-            const int col0 = c.nt * kBN + cb * 32;
+            if (cb + 1 < kSlices) tmem_ld32(tcol + uint32_t((cb + 1) * 32), v[(cb + 1) & 1]);   // in flight
+            const int col0 = c.nt * kBN + col_w + cb * 32;
             if (col0 < p.n && !skip) {
                 float4 *wr = reinterpret_cast<float4 *>(buf + lane * 128);
 #pragma unroll
@@ -941,12 +951,12 @@ __device__ void epilogue_rs_grp(const KParams &p, const PSmem &s, uint32_t tmem_
                     }
                 }
             }
-            if (cb + 1 < kBN / 32) tmem_wait_ld_regs(v[(cb + 1) & 1]);
+            if (cb + 1 < kSlices) tmem_wait_ld_regs(v[(cb + 1) & 1]);
         }
         // half preload: the next tile in this accumulator adds onto every
         // column, so the columns it will not preload must read zero
         if (p.pre_stages > 0 && p.pre_stages < 4) {
-            for (int h = 0; h < 2; ++h)
+            for (int h = GROUPS ? 0 : grp; h < (GROUPS ? 2 : grp + 1); ++h)
                 for (int cb = p.pre_stages; cb < 4; ++cb)
                     tmem_zero32(tmem_base + (uint32_t(quad * 32) << 16) + uint32_t(accb * kBN + h * 128 + cb * 32));
             tmem_wait_st();
@@ -959,7 +969,12 @@ __device__ void epilogue_rs_grp(const KParams &p, const PSmem &s, uint32_t tmem_
             __syncwarp();
             if (lane == 0 && !*s.abort) red_release_add(flag_ptr(p, tk.sig_done, c.q, c.mt, c.nt), 1u);
         }
-        acc_phase ^= 1u;
+        if (GROUPS) {
+            acc_phase ^= 1u;
+        } else if (++accb == 2) {
+            accb = 0;
+            acc_phase ^= 1u;
+        }
     }
 }
 
@@ -1001,7 +1016,7 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
             mbar_init(&s.tfull[i], 1);
             // epilogue warps of both CTAs that drain accumulator i: all eight,
             // or the four of the group that owns it (RS in two groups)
-            mbar_init(&s.tempty[i], 2 * (p.op == 1 && p.rs_groups ? kPEpiWarps / 2 : kPEpiWarps));
+            mbar_init(&s.tempty[i], 2 * (p.op == 1 && p.rs_epi == 1 ? kPEpiWarps / 2 : kPEpiWarps));
             mbar_init(&s.fbar[i], 1);
         }
         mbar_init(s.drain, 1);
@@ -1063,8 +1078,10 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     } else if (warp >= 4) {
         if (p.op == 0)
             epilogue_ag(p, s, tmem_base, cl);
-        else if (p.rs_groups)
-            epilogue_rs_grp(p, s, tmem_base, cl);
+        else if (p.rs_epi == 1)
+            epilogue_rs_vec<true>(p, s, tmem_base, cl);
+        else if (p.rs_epi == 2)
+            epilogue_rs_vec<false>(p, s, tmem_base, cl);
         else
             epilogue_rs_tma(p, s, tmem_base, cl);
     }

@@ -519,7 +519,7 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
             return CM_ERR_INVALID_ARG;   // a testing aid of the bounds-checked build only
 #endif
         case CM_OPT_RS_EPILOGUE:
-            if (value < 0 || value > 2) return CM_ERR_INVALID_ARG;
+            if (value < 0 || value > 3) return CM_ERR_INVALID_ARG;
             p.rs_epilogue = int(value);
             return CM_OK;
         case CM_OPT_TASK_ORDER:

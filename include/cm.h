@@ -131,9 +131,11 @@ cm_status cm_plan_step(cm_plan_t plan, cm_op op, int rank, int step, int stream,
  * one-way ring, rank-blocked -- rank 0's step 0, rank 1's steps 0..1, ...,
  * rank N-1's steps 0..N-1, then rank 0's steps 1..N-1, rank 1's steps
  * 2..N-1, ... -- so each rank's weight shard is streamed in two runs; for a
- * bidirectional ring, CM_RING_NONE and the step-serial mode, step-major and
- * by rank inside a step (CM_OPT_TASK_ORDER runs a one-way ring step-major
- * too).  Every flag a task waits on is raised by an earlier
+ * bidirectional ring, stream-blocked (each stream's tasks in that order, the
+ * counter-clockwise one over mirrored ranks; see CM_OPT_TASK_ORDER); for
+ * CM_RING_NONE and the step-serial mode, step-major and by rank inside a
+ * step (CM_OPT_TASK_ORDER runs a ring step-major too).  Every flag a task
+ * waits on is raised by an earlier
  * task.  Exposed so tests can check the table's dependency structure on the
  * host.
  */
@@ -375,8 +377,11 @@ const char *cm_status_string(cm_status status);
  *                        48 MB -- they stay in L2 either way -- and
  *                        rank-blocked otherwise.  cm_plan_tasks lists the
  *                        step-major table under 2 and the ring's own order
- *                        under 0 and 1.  Bidirectional rings always run
- *                        step-major.  The same results.
+ *                        under 0 and 1.  A bidirectional ring's own order
+ *                        is stream-blocked: the clockwise stream's tasks
+ *                        rank-blocked, then the counter-clockwise stream's
+ *                        rank-blocked over the mirrored ranks, each owner
+ *                        after the tasks it waits for.  The same results.
  *  CM_OPT_RS_EPILOGUE    how the CTA-pair kernel moves GEMM -> ReduceScatter
  *                        tiles out of tensor memory: 1 every epilogue warp
  *                        on every tile, the bucket slices copied by TMA
@@ -384,7 +389,10 @@ const char *cm_status_string(cm_status status);
  *                        2 two groups of epilogue warps, one per tensor-memory
  *                        accumulator, so that two tiles drain at once, with
  *                        coalesced vector adds (red.global.add.v4.f32),
- *                        stores and loads; 0 (default) two groups for rings
+ *                        stores and loads; 3 every epilogue warp on every
+ *                        tile (as 1) with the vector accesses of 2, so that a
+ *                        tile drains in half the time of a group's and the
+ *                        TMA unit carries only operand loads; 0 (default) two groups for rings
  *                        of 8 ranks (one-way) or 16 (either) whose tiles
  *                        have at least 28 K slices of 64 and read nothing
  *                        back (buckets in place, pipelined partials), the

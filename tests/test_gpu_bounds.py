@@ -87,6 +87,8 @@ def test_ag_same_bits_no_report(dbg, N, chunks, direction, opts):
     (4, 1, "uni", {"CM_OPT_RS_EPILOGUE": 1}),
     (4, 2, "uni", {"CM_OPT_RS_EPILOGUE": 2}),
     (8, 4, "uni", {"CM_OPT_RS_EPILOGUE": 2}),           # chunk pairs, two warp groups
+    (8, 4, "uni", {"CM_OPT_RS_EPILOGUE": 3}),           # chunk pairs, every warp with vector adds
+    (4, 2, "bidi", {"CM_OPT_RS_EPILOGUE": 3, "CM_OPT_RS_IN_PLACE": 0}),
     (5, 1, "bidi", {"CM_OPT_RS_EPILOGUE": 1, "CM_OPT_RS_PRELOAD": 1}),
     (4, 2, "bidi", {"CM_OPT_RS_IN_PLACE": 0, "CM_OPT_RS_PRELOAD": 3}),
     (4, 1, "uni", {"CM_OPT_KERNEL": 1}),
@@ -137,7 +139,7 @@ def test_other_entry_points_no_report(dbg):
     assert st == 0, (st, info)
 
 
-@pytest.mark.parametrize("epilogue", [1, 2])
+@pytest.mark.parametrize("epilogue", [1, 2, 3])
 def test_planted_flag_index_is_reported(dbg, epilogue):
     N, M, k, n = 4, 1024, 128, 512
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=46, w_layout="nk")

@@ -40,8 +40,8 @@ def _plan(N, chunks, direction, in_place, kernel=PAIR, preload=0, epilogue=0):
 
 
 # the CTA-pair kernel with each RS epilogue (TMA copies / two warp groups
-# with vector adds), and the single-CTA kernel
-KERNEL_EPILOGUES = [(PAIR, 1), (PAIR, 2), (SINGLE, 0)]
+# with vector adds / every warp with vector adds), and the single-CTA kernel
+KERNEL_EPILOGUES = [(PAIR, 1), (PAIR, 2), (PAIR, 3), (SINGLE, 0)]
 
 
 @pytest.mark.parametrize("kernel,epilogue", KERNEL_EPILOGUES)
@@ -68,18 +68,19 @@ def test_in_place_matches_per_step_buffers_bitwise(kernel, epilogue, N, M, k, n,
 @pytest.mark.parametrize("preload", [0, 1, 3])
 @pytest.mark.parametrize("direction", ["uni", "bidi"])
 def test_rs_epilogues_agree_bitwise(in_place, preload, direction):
-    """The two CTA-pair RS epilogues make the same fp32 additions in the same
+    """The CTA-pair RS epilogues make the same fp32 additions in the same
     order: the same bits, in both bucket modes and every preload mode."""
     N, M, k, n = 8, 2048, 256, 1288
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=71, w_layout="nk")
     ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
-    ys = []
-    for epilogue in (1, 2):
+    ys = {}
+    for epilogue in (1, 2, 3):
         for ydtype in (torch.float32, torch.bfloat16):
             y, _, _ = run_rs(_plan(N, 2, direction, in_place, PAIR, preload, epilogue), x, w, "nk", ydtype)
             assert oracle.normwise_max_rel_err(_np(y), ref) <= (TOL_F32 if ydtype == torch.float32 else TOL)
-            ys.append(y)
-    assert torch.equal(ys[0], ys[2]) and torch.equal(ys[1], ys[3])
+            ys[epilogue, ydtype] = y
+    for ydtype in (torch.float32, torch.bfloat16):
+        assert torch.equal(ys[1, ydtype], ys[2, ydtype]) and torch.equal(ys[1, ydtype], ys[3, ydtype])
 
 
 @pytest.mark.parametrize("preload", [0, 1, 2, 3])
@@ -110,7 +111,7 @@ def test_in_place_exact_on_integers():
             assert np.array_equal(_np(y), ref)
 
 
-@pytest.mark.parametrize("epilogue", [1, 2])
+@pytest.mark.parametrize("epilogue", [1, 2, 3])
 def test_in_place_dropped_signal_times_out(epilogue):
     """A contributor that never signals: its successor's addition and the
     owner's read wait for it, time out, and the next call is correct."""
