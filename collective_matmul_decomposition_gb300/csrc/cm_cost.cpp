@@ -4,9 +4,9 @@
 // "Overlap Communication with Dependent Computation via Decomposition in
 // Large Deep Learning Models", section "The idea" (knowing when to decline)
 // and section "What it costs": the decomposed ring drives one link per
-// direction instead of the full collective topology, so when the compute is
-// too small to hide the longer transfer, overlap loses; a simple peak-rate
-// model gates the rewrite per operation.  A bidirectional ring's pre-shift
+// direction instead of the full collective topology, so the rewrite loses
+// whenever a step's compute is shorter than its (slower) transfer; a model
+// built from peak rates decides per operation whether to rewrite.  A bidirectional ring's pre-shift
 // and realigning addition are charged as unoverlappable.  "Hiding
 // Tensor-Parallel Collectives: AG/RS Overlap in Megatron", section 6: more
 // chunks shorten the exposed first transfer but add a per-chunk cost.
@@ -209,8 +209,9 @@ extern "C" cm_status cm_plan_choose(int n_ranks, cm_op op, int64_t rows, int64_t
 
 // One Einsum that offers both collectives ("Overlap Communication with
 // Dependent Computation via Decomposition in Large Deep Learning Models",
-// section "The idea", knowing when to decline: the cost model "picks which of
-// two candidate collectives to overlap when an Einsum offers both").  Per
+// section "The idea", knowing when to decline: where one Einsum has both a
+// gathered input and a scattered output, the same cost model also decides
+// which of the two collectives to turn into the ring).  Per
 // rank: its A operand is the AllGather of N row shards [m, K], it multiplies
 // that [N*m, K] by its [K, n] weight, and the [N*m, n] result is summed over
 // the ranks and scattered, bucket o being rows o*m.. of the sum.  Only one

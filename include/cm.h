@@ -476,8 +476,9 @@ cm_status cm_plan_choose(int n_ranks, cm_op op, int64_t rows, int64_t K, int64_t
 
 /*
  * One Einsum that offers both collectives (same page, section "The idea":
- * the cost model "picks which of two candidate collectives to overlap when
- * an Einsum offers both").  Per rank: the A operand is the AllGather of N row
+ * where an Einsum has both a gathered input and a scattered output, the
+ * cost model also decides which of the two to overlap).  Per rank: the A
+ * operand is the AllGather of N row
  * shards [m, K]; the rank multiplies the gathered [N*m, K] by its [K, n]
  * weight; the [N*m, n] fp32 result is summed over the ranks and scattered
  * (bucket o = rows o*m .. o*m + m - 1).  Only one collective can become the

@@ -7,8 +7,9 @@
  *
  * It computes the plain definitions that the decomposition reaches exactly
  * ("Overlap Communication with Dependent Computation via Decomposition in
- * Large Deep Learning Models", section "Why it works": concatenation and
- * summation are linear, so the decomposed loop equals the monolithic op):
+ * Large Deep Learning Models", section "Why it works": gathering and summing
+ * are linear maps, so the decomposed loop reaches the monolithic result
+ * exactly):
  *
  *   AllGather -> GEMM:   Y_r = concat_j(X_j) @ W_r            for every rank r
  *                        (section "The idea", AllGather -> Einsum paragraph;
@@ -16,8 +17,8 @@
  *   GEMM -> ReduceScatter: Y_o = (sum_r X_r @ W_r)[rows of bucket o]
  *                        (section "The idea", Einsum -> ReduceScatter
  *                         paragraph; "Hiding Tensor-Parallel Collectives",
- *                         section 4: output shard i is the sum of all ranks'
- *                         contributions to it)
+ *                         section 4: rank i's output shard adds up what
+ *                         every rank contributed to those rows)
  *
  * Arithmetic: bf16 inputs are decoded bit-exactly to double; every output
  * element is a sequential sum over the contraction index k = 0..K-1 in
