@@ -1042,6 +1042,8 @@ def run_profile_case(args):
         st.plan.set_option(st.cm.CM_OPT_RS_EPILOGUE, args.rs_epilogue)
     if args.task_order >= 0:
         st.plan.set_option(st.cm.CM_OPT_TASK_ORDER, args.task_order)
+    if args.rs_col_slabs >= 0:
+        st.plan.set_option(st.cm.CM_OPT_RS_COL_SLABS, args.rs_col_slabs)
     fn = {"ag": st.ag, "rs": st.rs, "rs_pipe": st.rs_pipe}[args.profile]
     f_ag, f_rs = flops(data["shapes"], N)
     ms = time_loop(fn, args.steps, torch, warmup=args.warmup)
@@ -1050,6 +1052,7 @@ def run_profile_case(args):
     print(json.dumps({"profile_case": args.workload, "op": args.profile, "N": N, "chunks": args.chunks,
                       "ring": args.ring, "kernel": args.kernel, "static_tiles": args.static_tiles, "tile_group": args.tile_group, "l2_hints": args.l2_hints, "l2_promotion": args.l2_promotion, "row_band": args.row_band, "rs_preload": args.rs_preload, "rs_in_place": args.rs_in_place,
                       "rs_epilogue": args.rs_epilogue, "task_order": args.task_order,
+                      "rs_col_slabs": args.rs_col_slabs,
                       "ms": ms, "tflops": fl / (ms / 1e3) / 1e12}), flush=True)
     return 0
 
@@ -1082,6 +1085,7 @@ def main(argv=None):
     ap.add_argument("--rs-in-place", type=int, default=-1, help="CM_OPT_RS_IN_PLACE for --profile (-1 = default)")
     ap.add_argument("--rs-epilogue", type=int, default=-1, help="CM_OPT_RS_EPILOGUE for --profile (-1 = default)")
     ap.add_argument("--task-order", type=int, default=-1, help="CM_OPT_TASK_ORDER for --profile (-1 = default)")
+    ap.add_argument("--rs-col-slabs", type=int, default=-1, help="CM_OPT_RS_COL_SLABS for --profile (-1 = default)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0,
                     help="oracle seconds for the cpu_baseline of the default arm")
     ap.add_argument("--ref-seconds", type=float, default=120.0,

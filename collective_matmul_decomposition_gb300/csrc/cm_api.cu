@@ -48,6 +48,20 @@ int rs_epi_mode(const PlanImpl &pl, int64_t k, bool reads_inputs) {
     return many_ranks && kslices >= 28 ? 1 : 0;
 }
 
+// CM_OPT_RS_COL_SLABS: the GEMM -> ReduceScatter tile order in that many
+// passes over the tasks, one slab of column tiles each (0: one pass); the
+// largest count not above it that divides the column tiles.  A pass touches
+// 1/slabs of every bucket but reads all of X again.  Measured (interleaved):
+// two slabs made the GPT-3 attention-out one-way ring 4-5 % faster (0.420
+// against 0.440 ms) and changed the two-way ring by under 2 %; on the MLP
+// sweep and the Megatron-SP fc2 one pass was as fast or faster (four and
+// eight slabs up to 20 % slower), so one pass stays the default.
+int rs_col_slabs(const PlanImpl &pl, int ntiles) {
+    int c = std::max(1, pl.rs_col_slabs);
+    while (c > 1 && ntiles % c != 0) --c;
+    return c;
+}
+
 // Ring stages of received bucket per tile for CM_OPT_RS_PRELOAD = mode.
 int preload_stages(int mode, int64_t kslices) {
     switch (mode) {
@@ -465,6 +479,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.a_box_rows = int(box_rows);
     kp.rs_epi = rs_epi_mode(pl, k, !pl.rs_in_place);
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
+    kp.col_slabs = rs_col_slabs(pl, kp.ntiles);
     const bool sm = use_step_major(pl, int64_t(N) * k * n * 2);
     return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, sm, reinterpret_cast<cudaStream_t>(stream));
 }

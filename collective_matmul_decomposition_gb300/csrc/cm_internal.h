@@ -47,6 +47,7 @@ struct PlanImpl {
     int rs_in_place = 1;    // see CM_OPT_RS_IN_PLACE
     int task_order = 0;     // see CM_OPT_TASK_ORDER
     int rs_epilogue = 0;    // see CM_OPT_RS_EPILOGUE
+    int rs_col_slabs = 0;   // see CM_OPT_RS_COL_SLABS
     int debug_flag_offset = 0;   // see CM_OPT_DEBUG_FLAG_OFFSET (bounds-checked builds)
     int64_t skip_signal = -1;
     Schedule sched[2];                    // per cm_op

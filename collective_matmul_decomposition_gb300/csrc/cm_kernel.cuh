@@ -61,6 +61,8 @@ struct KParams {
                                // instead of the next index of the global counter
     int l2_hint_a, l2_hint_b;  // CTA-pair kernel: L2 priority of A / B loads (0 normal, 1 evict_last, 2 evict_first)
     int row_band;              // row tiles per band of the tile order (0 = a whole task group)
+    int col_slabs;             // > 1: the tile order makes this many passes over the tasks, each over
+                               // one slab of ntiles / col_slabs column tiles (ntiles a multiple of it)
     int q_only;                // >= 0: this launch covers only chunk q_only of every task
     const uint8_t *x_bytes;    // AG: x and the receive slots as bytes (pair forwarder)
     uint8_t *slot_bytes;

@@ -22,27 +22,35 @@ struct TileCoord {
 // `row_band` row tiles (0: one band); each band runs through every column
 // tile before the next band starts, so the tiles running together share one
 // block of weight columns (W_r of the group's rank) and one band of A rows.
+// With column slabs (col_slabs > 1) all of that runs once per slab of
+// ntiles / col_slabs column tiles, slab after slab: the tasks' buckets are
+// then touched one slab at a time.
 __device__ __forceinline__ TileCoord decode(const KParams &p, int t) {
     TileCoord c;
-    const int task = p.task_begin + t / p.tiles_per_task;
+    const int slabs = p.col_slabs > 1 ? p.col_slabs : 1;
+    const int nts = p.ntiles / slabs;                  // column tiles of one slab
+    const int tpt = p.tiles_per_task / slabs;          // tiles of one task in one slab
+    const int slab = t / ((p.task_end - p.task_begin) * tpt);
+    t -= slab * (p.task_end - p.task_begin) * tpt;
+    const int task = p.task_begin + t / tpt;
     const int16_t grp = p.tasks[task].tile_group;
     const int gsize = grp >> 8, gpos = grp & 0xff;
     const int gfirst = task - gpos;
-    int u = t - (gfirst - p.task_begin) * p.tiles_per_task;   // tile index inside the group
-    const int rows = gsize * p.mtiles_c;                       // row tiles of the group
-    const int per_q = rows * p.ntiles;
+    int u = t - (gfirst - p.task_begin) * tpt;   // tile index inside the group
+    const int rows = gsize * p.mtiles_c;          // row tiles of the group
+    const int per_q = rows * nts;
     c.q = u / per_q;
     u -= c.q * per_q;
     if (p.q_only >= 0) c.q = p.q_only;   // one chunk per launch: u never reaches a second one
     const int band = p.row_band > 0 && p.row_band < rows ? p.row_band : rows;
     const int full = rows / band;
-    const int in_full = full * band * p.ntiles;
+    const int in_full = full * band * nts;
     int b0, bs;   // first row tile and row tiles of this tile's band
     if (u < in_full) {
-        const int b = u / (band * p.ntiles);
+        const int b = u / (band * nts);
         b0 = b * band;
         bs = band;
-        u -= b * band * p.ntiles;
+        u -= b * band * nts;
     } else {
         b0 = full * band;
         bs = rows - b0;
@@ -53,7 +61,7 @@ __device__ __forceinline__ TileCoord decode(const KParams &p, int t) {
     const int off = rho / p.mtiles_c;
     c.mt = rho - off * p.mtiles_c;
     c.task = gfirst + off;
-    c.nt = g;
+    c.nt = slab * nts + g;
     return c;
 }
 

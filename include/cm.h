@@ -401,6 +401,13 @@ const char *cm_status_string(cm_status status);
  *                        in measurement).
  *                        The same fp32 additions in the same order: the same
  *                        bits.
+ *  CM_OPT_RS_COL_SLABS   cm_gemm_rs: the tile order in `value` passes over
+ *                        the tasks, each over one slab of the column tiles
+ *                        (the largest count not above `value` that divides
+ *                        them), so that a pass touches 1/value of every
+ *                        bucket; 0 (default) or 1: one pass.  Values 0..64.
+ *                        The same fp32 additions in the same order: the same
+ *                        bits.
  *  CM_OPT_DEBUG_FLAG_OFFSET  only in a library built with bounds checks
  *                        (CM_DEBUG_BOUNDS; other builds return
  *                        CM_ERR_INVALID_ARG): adds `value` (>= 0) to the flag
@@ -425,7 +432,8 @@ typedef enum cm_option {
     CM_OPT_RS_IN_PLACE = 12,
     CM_OPT_TASK_ORDER = 13,
     CM_OPT_RS_EPILOGUE = 14,
-    CM_OPT_DEBUG_FLAG_OFFSET = 15
+    CM_OPT_DEBUG_FLAG_OFFSET = 15,
+    CM_OPT_RS_COL_SLABS = 16
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);
