@@ -55,7 +55,7 @@ int rs_epi_mode(const PlanImpl &pl, int64_t k, bool reads_inputs) {
 // two slabs made the GPT-3 attention-out one-way ring 4-5 % faster (0.420
 // against 0.440 ms) and changed the two-way ring by under 2 %; on the MLP
 // sweep and the Megatron-SP fc2 one pass was as fast or faster (four and
-// eight slabs up to 20 % slower), so one pass stays the default.
+// eight slabs slower, by up to 50 %), so one pass stays the default.
 int rs_col_slabs(const PlanImpl &pl, int ntiles) {
     int c = std::max(1, pl.rs_col_slabs);
     while (c > 1 && ntiles % c != 0) --c;
