@@ -25,6 +25,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -95,11 +96,19 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_of(text: str) -> str:
+    """C/C++/CUDA source without its comments and blank lines: what the
+    compiler sees, so that a comment edit does not retire a measurement."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_hash() -> str:
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "collective_matmul_decomposition_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "collective_matmul_decomposition_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(code_of(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -33,10 +33,15 @@
 //             receive slot with 1-D TMA bulk copies through two 16 KB buffers,
 //             then bumps the slot's ready flag -- the rotation copy in flight
 //             while the partial GEMMs read the shard.
-//   warps 4-11  epilogue (both CTAs): 8 warps, TMEM lane quarter = warp % 4,
-//             column half = (warp - 4) / 4.  AG writes shard rows of Y_r; RS
-//             moves the fp32 bucket through a 4 KB swizzled buffer per warp
-//             with TMA loads and stores.
+//   warps 4-11  epilogue (both CTAs): 8 warps, TMEM lane quarter = warp % 4.
+//             AG writes shard rows of Y_r (column half = (warp - 4) / 4).  RS
+//             adds the tile into its bucket where the bucket lies (or, with
+//             per-step buffers, adds the received bucket and stores the sum
+//             to the next buffer); the owner rounds the complete bucket into
+//             y.  Three arrangements (p.rs_epi): every warp on every tile
+//             with TMA copies through a 4 KB swizzled buffer per warp; two
+//             groups of four warps, one per TMEM accumulator, with coalesced
+//             vector accesses; every warp on every tile with vector accesses.
 //
 // RS preload (p.pre_stages > 0): for a tile that receives a bucket, the
 // scheduler acquires the bucket's flag before publishing the tile, the

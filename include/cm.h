@@ -204,8 +204,12 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
  *  w  N weight shards, bf16: W_r at w + r*k*n, laid out per `wlayout`.
  *  y  [N][M/N][n] (y_dtype): bucket o = rows o*M/N.. of sum_r X_r @ W_r.
  *  ws, ws_bytes: workspace of at least cm_gemm_rs_workspace_size(plan, M, n)
- *  bytes.  Accumulation across ranks is fp32; the home rank rounds once to
- *  y_dtype.  Outputs must not alias inputs or the workspace.
+ *  bytes.  Accumulation across ranks is fp32, in ring order; the home rank
+ *  rounds once to y_dtype.  On one GPU a bucket is not copied from rank to
+ *  rank: by default (CM_OPT_RS_IN_PLACE) it stays in one workspace buffer
+ *  per ring stream, and passing it on is releasing its readiness flag to
+ *  the next contributor, which adds its product into it there.  Outputs
+ *  must not alias inputs or the workspace.
  *  Errors: as cm_ag_gemm, with CM_ERR_SHAPE also for M % N != 0 or
  *  (M/N) % chunks != 0, and k in the role of K.
  */

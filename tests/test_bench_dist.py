@@ -55,3 +55,13 @@ def test_single_process_defaults(monkeypatch):
     assert bench.dist_env() == (0, 1, 0)
     assert bench.dist_max(3.5) == 3.5
     assert bench.aggregate(2e12, 5, 1, 2.0) == pytest.approx(5.0)
+
+
+def test_kernel_hash_ignores_comments_only():
+    """The traffic figures stay tied to the kernel code: a comment edit keeps
+    the hash, a code edit changes it."""
+    import bench
+    src = "int a = 1; // one\n/* block\n comment */\nint b = 2;\n"
+    assert bench.code_of(src) == bench.code_of("int a = 1;   // other words\n\nint b = 2;\n")
+    assert bench.code_of(src) != bench.code_of("int a = 1;\nint b = 3;\n")
+    assert len(bench.kernel_hash()) == 16
