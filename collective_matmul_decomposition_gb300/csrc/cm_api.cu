@@ -112,7 +112,8 @@ WsLayout rs_layout(const PlanImpl &p, int64_t M, int64_t n) {
     l.flags_bytes = size_t(p.flag_ids[CM_OP_GEMM_RS]) * size_t(p.chunks) * row_tiles(rows_c) *
                     size_t((n + kBN - 1) / kBN) * sizeof(uint32_t);
     l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
-    l.buf_bytes = size_t(rs_bufs(p)) * size_t(M / p.N) * size_t(n) * sizeof(float);
+    const size_t elem = p.rs_bucket_bf16 ? 2 : sizeof(float);   // CM_OPT_RS_BUCKET_BF16
+    l.buf_bytes = size_t(rs_bufs(p)) * size_t(M / p.N) * size_t(n) * elem;
     l.total = l.buf_off + l.buf_bytes;
     return l;
 }
@@ -433,6 +434,9 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.q_only = -1;
     const int promo = pl.l2_promotion;
     const KernelChoice kc = choose_kernel(pl);
+    // bf16 buckets: CTA pairs, buckets in place, a vector epilogue, no preload
+    const bool bf16_buckets = pl.rs_bucket_bf16 && rs_bufs(pl) > 0;
+    if (bf16_buckets && (!kc.pair || !pl.rs_in_place || pl.rs_epilogue == 1)) return CM_ERR_UNSUPPORTED;
     const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
     // x [N][M][k] viewed as [N*N*c][rows_c][k]: slab (r*N + bucket)*c + chunk
     if (!make_map(&kp.tmA0, promo, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
@@ -450,7 +454,8 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.acc_bufs = int(rs_bufs(pl));
     kp.a0_slabs = kp.a1_slabs = N * N * c;
     kp.b_slabs = N;
-    if (l.buf_bytes > 0) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
+    kp.acc_bf16 = bf16_buckets ? 1 : 0;
+    if (l.buf_bytes > 0 && !bf16_buckets) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
         const int64_t nbufs = rs_bufs(pl);
         if (!make_acc_maps(kp, promo, kp.acc, n, rows_c, nbufs * c)) return CM_ERR_CUDA;
         // received buckets through the operand ring: each CTA of a pair loads
@@ -478,6 +483,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
     kp.rs_epi = rs_epi_mode(pl, k, !pl.rs_in_place);
+    if (bf16_buckets && kp.rs_epi == 0) kp.rs_epi = 2;   // the TMA epilogue moves fp32 boxes only
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
     kp.col_slabs = rs_col_slabs(pl, kp.ntiles);
     const bool sm = use_step_major(pl, int64_t(N) * k * n * 2);

@@ -226,6 +226,11 @@ __device__ __forceinline__ void red_add_v4(float *p, const float4 &v) {
                  "f"(v.w)
                  : "memory");
 }
+// Four bf16 values (two bf16x2 words) added where they lie, at L2; each sum
+// is rounded to bf16 there.
+__device__ __forceinline__ void red_add_v2_bf16x2(void *p, uint32_t lo, uint32_t hi) {
+    asm volatile("red.relaxed.gpu.global.add.noftz.v2.bf16x2 [%0], {%1, %2};" ::"l"(p), "r"(lo), "r"(hi) : "memory");
+}
 __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

@@ -824,6 +824,37 @@ __device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_
 // for every warp that drains the tile (four or eight) in each CTA, and no
 // warp waits for another.
 
+// Four consecutive bucket elements at element offset e of the accumulator
+// buffers, as fp32 (bf16 buckets are widened exactly).
+__device__ __forceinline__ float4 load_bucket4(const KParams &p, int64_t e) {
+    if (!p.acc_bf16) return __ldcg(reinterpret_cast<const float4 *>(p.acc + e));
+    const uint2 w = __ldcg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.acc) + e));
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
+    return make_float4(lo.x, lo.y, hi.x, hi.y);
+}
+
+// Four consecutive bucket elements at element offset e: added where they
+// lie (add) or stored (the bucket's first contribution).  bf16 buckets take
+// the values rounded to bf16 (RNE); the addition rounds again, at L2.
+__device__ __forceinline__ void put_bucket4(const KParams &p, int64_t e, const float4 &v, bool add) {
+    if (!p.acc_bf16) {
+        float *d = p.acc + e;
+        if (add)
+            red_add_v4(d, v);
+        else
+            __stcg(reinterpret_cast<float4 *>(d), v);
+        return;
+    }
+    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+    const uint32_t wl = *reinterpret_cast<uint32_t *>(&lo), wh = *reinterpret_cast<uint32_t *>(&hi);
+    __nv_bfloat16 *d = reinterpret_cast<__nv_bfloat16 *>(p.acc) + e;
+    if (add)
+        red_add_v2_bf16x2(d, wl, wh);
+    else
+        __stcg(reinterpret_cast<uint2 *>(d), make_uint2(wl, wh));
+}
+
 template <bool GROUPS>
 __device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     constexpr int kSlices = GROUPS ? kBN / 32 : kBN / 64;   // 32-column slices per warp and tile
@@ -912,12 +943,12 @@ __device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_
                 for (int jj = 0; jj < 2; ++jj) {
                     if (tk.in_buf[jj] < 0 || (jj == 0 && (in_place || (pre >= 0 && (cb & 3) < p.pre_stages))))
                         continue;
-                    const float *src = p.acc + int64_t(tk.in_buf[jj]) * p.acc_buf_stride + brow0 * p.n + col;
+                    const int64_t src = int64_t(tk.in_buf[jj]) * p.acc_buf_stride + brow0 * p.n + col;
                     float4 a[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         if (col_ok && row_w + 4 * i + tr < p.rows_c)
-                            a[i] = __ldcg(reinterpret_cast<const float4 *>(src + int64_t(4 * i + tr) * p.n));
+                            a[i] = load_bucket4(p, src + int64_t(4 * i + tr) * p.n);
                         else
                             a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -929,15 +960,11 @@ __device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_
                     }
                 }
                 if (tk.out_buf >= 0) {
-                    float *dst = p.acc + int64_t(tk.out_buf) * p.acc_buf_stride + brow0 * p.n + col;
+                    const int64_t dst = int64_t(tk.out_buf) * p.acc_buf_stride + brow0 * p.n + col;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         if (!col_ok || row_w + 4 * i + tr >= p.rows_c) continue;
-                        float *d = dst + int64_t(4 * i + tr) * p.n;
-                        if (in_place)
-                            red_add_v4(d, x[i]);
-                        else
-                            __stcg(reinterpret_cast<float4 *>(d), x[i]);
+                        put_bucket4(p, dst + int64_t(4 * i + tr) * p.n, x[i], in_place);
                     }
                 } else {   // owner: the bucket is home
                     const int64_t orow0 = (int64_t(tk.out_idx) * p.out_rows_per_idx + brow0) * p.n + col;

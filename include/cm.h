@@ -412,6 +412,16 @@ const char *cm_status_string(cm_status status);
  *                        bucket; 0 (default) or 1: one pass.  Values 0..64.
  *                        The same fp32 additions in the same order: the same
  *                        bits.
+ *  CM_OPT_RS_BUCKET_BF16 cm_gemm_rs on a ring: 1 holds the buckets in bf16
+ *                        instead of fp32 (half the bucket bytes; every hop
+ *                        rounds the contribution and the sum to bf16, so the
+ *                        error grows with N -- a measured variant, not the
+ *                        default); 0 (default) fp32.  Needs the CTA-pair
+ *                        kernel, buckets in place and a vector epilogue
+ *                        (CM_OPT_RS_EPILOGUE 0, 2 or 3; 0 then picks 3 where
+ *                        it would pick the TMA one); no preload.  Otherwise
+ *                        cm_gemm_rs returns CM_ERR_UNSUPPORTED.  The
+ *                        workspace size follows the setting.
  *  CM_OPT_DEBUG_FLAG_OFFSET  only in a library built with bounds checks
  *                        (CM_DEBUG_BOUNDS; other builds return
  *                        CM_ERR_INVALID_ARG): adds `value` (>= 0) to the flag
@@ -437,7 +447,8 @@ typedef enum cm_option {
     CM_OPT_TASK_ORDER = 13,
     CM_OPT_RS_EPILOGUE = 14,
     CM_OPT_DEBUG_FLAG_OFFSET = 15,
-    CM_OPT_RS_COL_SLABS = 16
+    CM_OPT_RS_COL_SLABS = 16,
+    CM_OPT_RS_BUCKET_BF16 = 17
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);
