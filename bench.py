@@ -784,6 +784,18 @@ def run_configs(args):
         clocks = clk.summary()
         timed_s = max(20, args.steps) * sum(t.values()) / 1e3
         peak, peak_which, peak_why = choose_peak(peaks, timed_s, clocks)
+        # the decomposed output against torch.matmul of the same operands
+        # (normwise max relative error; the parity tests hold the oracle's)
+        with torch.no_grad():
+            ref = torch_fn().float()
+            if op == "ag":
+                sh = data["shapes"]["ag"]
+                ref = ref.reshape(N * sh["m"], N, sh["n"]).permute(1, 0, 2)
+                got = st.y1.float()
+            else:
+                ref = ref.reshape(N, -1, ref.shape[-1])
+                got = st.y2.float()
+            err_vs_torch = float((got - ref).abs().max() / ref.abs().max())
         f_ag, f_rs = flops(data["shapes"], N)
         fl = f_ag if op == "ag" else f_rs
         tf = fl / (t["dec"] / 1e3) / 1e12
@@ -800,6 +812,7 @@ def run_configs(args):
             "ms_undecomposed": t["none"], "ms_torch": t["torch"],
             "vs_undecomposed_time": t["dec"] / t["none"], "vs_torch_time": t["dec"] / t["torch"],
             "ms_rs_per_step_buffers": t.get("per_step"),
+            "max_rel_err_vs_torch": err_vs_torch,
             "rounds": max(20, args.steps), "clocks": clocks,
             "peak_source": f"{peak_which} dense bf16 {peak} ({peak_why}) and hbm_gbs {hbm} of {kind}"}), flush=True)
         del st, alt

@@ -1,6 +1,7 @@
 // cm_api.cu -- the C ABI: argument checks, workspace layout, TMA tensor maps
 // and the launch of the persistent kernel.
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <algorithm>
 #include <cstring>
@@ -332,6 +333,17 @@ cm_status check_common(cm_plan_t plan, const void *x, const void *w, cm_wlayout 
 
 using namespace cm;
 
+// An NVTX range for the host side of one call (and of each step a call
+// enqueues): profilers show which call a launch belongs to, and ncu can be
+// limited to one call with --nvtx --nvtx-include.  With no tool attached a
+// range costs a branch.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+
 extern "C" {
 
 size_t cm_ag_gemm_workspace_size(cm_plan_t plan, int64_t m, int64_t K) {
@@ -346,6 +358,7 @@ size_t cm_gemm_rs_workspace_size(cm_plan_t plan, int64_t M, int64_t n) {
 
 cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y, cm_dtype y_dtype,
                      int64_t m, int64_t K, int64_t n, void *ws, size_t ws_bytes, cm_stream_t stream) {
+    const NvtxRange range("cm_ag_gemm");
     cm_status st = check_common(plan, x, w, wlayout, y, y_dtype, m, K, n);
     if (st != CM_OK) return st;
     const PlanImpl &pl = plan->impl;
@@ -413,6 +426,7 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
 
 cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y, cm_dtype y_dtype,
                      int64_t M, int64_t k, int64_t n, void *ws, size_t ws_bytes, cm_stream_t stream) {
+    const NvtxRange range("cm_gemm_rs");
     cm_status st = check_common(plan, x, w, wlayout, y, y_dtype, M, k, n);
     if (st != CM_OK) return st;
     const PlanImpl &pl = plan->impl;
@@ -498,6 +512,7 @@ size_t cm_gemm_rs_pipelined_workspace_size(cm_plan_t plan, int64_t M, int64_t n)
 cm_status cm_gemm_rs_pipelined(cm_plan_t plan, const void *x, const void *w, cm_wlayout wlayout, void *y,
                                cm_dtype y_dtype, int64_t M, int64_t k, int64_t n, void *ws, size_t ws_bytes,
                                cm_stream_t stream) {
+    const NvtxRange range("cm_gemm_rs_pipelined");
     cm_status st = check_common(plan, x, w, wlayout, y, y_dtype, M, k, n);
     if (st != CM_OK) return st;
     const PlanImpl &pl = plan->impl;
@@ -627,6 +642,7 @@ size_t cm_backward_pair_workspace_size(cm_plan_t plan, int64_t m, int64_t K, int
 cm_status cm_backward_pair(cm_plan_t plan, const void *x, const void *w, const void *dy, void *dx, cm_dtype dx_dtype,
                            void *dw, cm_dtype dw_dtype, int64_t m, int64_t K, int64_t n, void *ws, size_t ws_bytes,
                            cm_stream_t stream) {
+    const NvtxRange range("cm_backward_pair");
     if (!plan || !x || !w || !dy || !dx || !dw) return CM_ERR_INVALID_ARG;
     if ((dx_dtype != CM_BF16 && dx_dtype != CM_F32) || (dw_dtype != CM_BF16 && dw_dtype != CM_F32))
         return CM_ERR_INVALID_ARG;
@@ -783,6 +799,7 @@ size_t cm_cannon_workspace_size(cm_plan_t plan, int64_t bm, int64_t bk, int64_t 
 
 cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayout blayout, void *c, cm_dtype c_dtype,
                          int64_t bm, int64_t bk, int64_t bn, void *ws, size_t ws_bytes, cm_stream_t stream) {
+    const NvtxRange range("cm_cannon_gemm");
     cm_status st = check_common(plan, a, b, blayout, c, c_dtype, bm, bk, bn);
     if (st != CM_OK) return st;
     const PlanImpl &pl = plan->impl;
@@ -844,6 +861,7 @@ cm_status cm_cannon_gemm(cm_plan_t plan, const void *a, const void *b, cm_wlayou
     if (cudaEventRecord(ev[0], s) != cudaSuccess) return CM_ERR_CUDA;
     auto held_k = [q](int i, int j, int step) { return (i + j + step) % q; };
     for (int step = 0; step < q; ++step) {
+        const NvtxRange step_range("cm_cannon_gemm step");
         // GEMM of this step: rank (i, j) multiplies A_{i,k} B_{k,j}, k = (i+j+step) mod q,
         // adding the accumulator of the previous step; the last step writes C
         if (step > 0 && cudaStreamWaitEvent(s, ev[1 + step], 0) != cudaSuccess) return CM_ERR_CUDA;
