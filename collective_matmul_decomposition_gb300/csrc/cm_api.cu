@@ -49,19 +49,43 @@ int rs_epi_mode(const PlanImpl &pl, int64_t k, bool reads_inputs) {
     return many_ranks && kslices >= 28 ? 1 : 0;
 }
 
+// CM_OPT_RS_BUCKET_HINT: the L2 policy of fp32 bucket writes and adds
+// (kernel: 0 none, 1 evict_first, 2 evict_last).  Automatic (option 0): one
+// ring stream's buckets take M*n*4 bytes; up to kBucketsInL2Bytes they can
+// stay in L2 from one contribution to the next, and evict_last keeps them
+// there; beyond that, no policy.  Measured (interleaved, two runs on two
+// boxes, against no policy): GPT-3 attention-out (100 MB of buckets) 1.8-2.0 %
+// faster one-way and 3.0-3.5 % two-way with evict_last, Megatron-SP fc2
+// (67 MB) 0.6-1.5 %; on the MLP (268 MB) evict_first gained 1.8 % at N=8 in
+// one run and lost 1.0-2.2 % at N=4 and 8 in the other, evict_last within
+// 1 %.  Option 3: no policy.
+constexpr int64_t kBucketsInL2Bytes = int64_t(128) << 20;
+
+int rs_bucket_hint(const PlanImpl &pl, int64_t M, int64_t n) {
+    if (pl.rs_bucket_hint == 3) return 0;
+    if (pl.rs_bucket_hint != 0) return pl.rs_bucket_hint;
+    return M * n * 4 <= kBucketsInL2Bytes ? 2 : 0;
+}
+
 // CM_OPT_RS_COL_SLABS: the GEMM -> ReduceScatter tile order in that many
-// passes over the tasks, one slab of column tiles each (0: one pass); the
-// largest count not above it that divides the column tiles.  A pass touches
-// 1/slabs of every bucket but reads all of X again.  Measured (interleaved):
-// two slabs made the GPT-3 attention-out one-way ring 4-5 % faster (0.420
-// against 0.440 ms) and changed the two-way ring by under 2 %; on the MLP
-// sweep and the Megatron-SP fc2 one pass was as fast or faster (four and
-// eight slabs slower, by up to 50 %), so one pass stays the default.
-int rs_col_slabs(const PlanImpl &pl, int ntiles) {
-    int c = std::max(1, pl.rs_col_slabs);
+// passes over the tasks, one slab of column tiles each; the largest count
+// not above it that divides the column tiles.  A pass touches 1/slabs of
+// every bucket but reads all of X again.  Automatic (0): two slabs for a
+// one-way ring whose buckets fit L2 (kBucketsInL2Bytes) and whose tiles have
+// at least 16 K slices, else one pass.  Measured (interleaved, three runs):
+// two slabs made the GPT-3 attention-out one-way ring 3-5 % faster (0.441
+// against 0.456 ms with the bucket policy), left its two-way ring within
+// 2 % (slower), and slowed the Megatron-SP fc2 (4 K slices) by 5-7 % and
+// the MLP sweep (268 MB of buckets) by up to 1 %; three or more slabs were
+// slower everywhere, by up to 50 %.
+int rs_col_slabs(const PlanImpl &pl, int ntiles, int64_t M, int64_t n, int64_t k) {
+    int c = pl.rs_col_slabs;
+    if (c == 0)
+        c = pl.dir == CM_RING_UNI && M * n * 4 <= kBucketsInL2Bytes && (k + kBK - 1) / kBK >= 16 ? 2 : 1;
     while (c > 1 && ntiles % c != 0) --c;
     return c;
 }
+
 
 // Ring stages of received bucket per tile for CM_OPT_RS_PRELOAD = mode.
 int preload_stages(int mode, int64_t kslices) {
@@ -469,6 +493,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.a0_slabs = kp.a1_slabs = N * N * c;
     kp.b_slabs = N;
     kp.acc_bf16 = bf16_buckets ? 1 : 0;
+    kp.bucket_hint = rs_bucket_hint(pl, M, n);
     if (l.buf_bytes > 0 && !bf16_buckets) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
         const int64_t nbufs = rs_bufs(pl);
         if (!make_acc_maps(kp, promo, kp.acc, n, rows_c, nbufs * c)) return CM_ERR_CUDA;
@@ -499,7 +524,7 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.rs_epi = rs_epi_mode(pl, k, !pl.rs_in_place);
     if (bf16_buckets && kp.rs_epi == 0) kp.rs_epi = 2;   // the TMA epilogue moves fp32 boxes only
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
-    kp.col_slabs = rs_col_slabs(pl, kp.ntiles);
+    kp.col_slabs = rs_col_slabs(pl, kp.ntiles, M, n, k);
     const bool sm = use_step_major(pl, int64_t(N) * k * n * 2);
     return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, sm, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -91,6 +91,23 @@ __device__ __forceinline__ void tma_reduce_add_3d(const void *tmap, const void *
         "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src))
         : "memory");
 }
+// The same two with an L2 eviction-priority policy (createpolicy) for the
+// written lines.
+__device__ __forceinline__ void tma_store_3d_hint(const void *tmap, const void *src, int c0, int c1, int c2,
+                                                  uint64_t policy) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src)), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void tma_reduce_add_3d_hint(const void *tmap, const void *src, int c0, int c1, int c2,
+                                                       uint64_t policy) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group.L2::cache_hint [%0, {%1, %2, %3}], [%4], %5;" ::"l"(
+            reinterpret_cast<uint64_t>(tmap)),
+        "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(src)), "l"(policy)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {
@@ -224,6 +241,17 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 __device__ __forceinline__ void red_add_v4(float *p, const float4 &v) {
     asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
                  "f"(v.w)
+                 : "memory");
+}
+// red_add_v4 and a 16-byte store with an L2 eviction-priority policy.
+__device__ __forceinline__ void red_add_v4_hint(float *p, const float4 &v, uint64_t policy) {
+    asm volatile("red.relaxed.gpu.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
+                 "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
+                 : "memory");
+}
+__device__ __forceinline__ void st_v4_hint(float *p, const float4 &v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
+                 "f"(v.w), "l"(policy)
                  : "memory");
 }
 // Four bf16 values (two bf16x2 words) added where they lie, at L2; each sum

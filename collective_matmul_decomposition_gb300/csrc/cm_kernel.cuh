@@ -56,6 +56,8 @@ struct KParams {
     float *acc;                // RS circulating accumulators (bf16 elements when acc_bf16)
     int acc_bf16;              // CTA pairs, RS buckets in place with a vector epilogue: buckets held
                                // in bf16 (CM_OPT_RS_BUCKET_BF16)
+    int bucket_hint;           // CTA pairs, RS fp32 bucket writes and adds: L2 policy (0 none,
+                               // 1 evict_first, 2 evict_last; CM_OPT_RS_BUCKET_HINT)
     uint32_t *flags;
     uint32_t *status;
     uint32_t *tile_counter;    // dynamic tile scheduler (CTA-pair kernel), zero at launch

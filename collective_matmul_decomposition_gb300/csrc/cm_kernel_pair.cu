@@ -614,6 +614,11 @@ __device__ void epilogue_ag(const KParams &p, const PSmem &s, uint32_t tmem_base
 }
 
 
+// L2 policy of bucket writes and adds (CM_OPT_RS_BUCKET_HINT; unused at 0).
+__device__ __forceinline__ uint64_t bucket_policy(const KParams &p) {
+    return p.bucket_hint == 2 ? policy_evict_last() : policy_evict_first();
+}
+
 // Row `row` of a 32 x 32 fp32 box staged by TMA with the 128-byte swizzle:
 // 16-byte chunk j of row r sits at chunk position j ^ (r & 7).
 __device__ __forceinline__ float4 *swz_row(uint8_t *buf, int row) { return reinterpret_cast<float4 *>(buf + row * 128); }
@@ -736,10 +741,17 @@ __device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_
                 __syncwarp();
                 if (lane == 0) {
                     const int slab = tk.out_buf * p.chunks + c.q;
-                    if (in_place)
+                    if (p.bucket_hint) {
+                        const uint64_t pol = bucket_policy(p);
+                        if (in_place)
+                            tma_reduce_add_3d_hint(&p.tmAcc, buf, col0, row_w, slab, pol);
+                        else
+                            tma_store_3d_hint(&p.tmAcc, buf, col0, row_w, slab, pol);
+                    } else if (in_place) {
                         tma_reduce_add_3d(&p.tmAcc, buf, col0, row_w, slab);
-                    else
+                    } else {
                         tma_store_3d(&p.tmAcc, buf, col0, row_w, slab);
+                    }
                     bulk_commit();
                     store_pending = true;
                 }
@@ -837,13 +849,19 @@ __device__ __forceinline__ float4 load_bucket4(const KParams &p, int64_t e) {
 // Four consecutive bucket elements at element offset e: added where they
 // lie (add) or stored (the bucket's first contribution).  bf16 buckets take
 // the values rounded to bf16 (RNE); the addition rounds again, at L2.
-__device__ __forceinline__ void put_bucket4(const KParams &p, int64_t e, const float4 &v, bool add) {
+__device__ __forceinline__ void put_bucket4(const KParams &p, int64_t e, const float4 &v, bool add, uint64_t pol) {
     if (!p.acc_bf16) {
         float *d = p.acc + e;
-        if (add)
+        if (p.bucket_hint) {
+            if (add)
+                red_add_v4_hint(d, v, pol);
+            else
+                st_v4_hint(d, v, pol);
+        } else if (add) {
             red_add_v4(d, v);
-        else
+        } else {
             __stcg(reinterpret_cast<float4 *>(d), v);
+        }
         return;
     }
     __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
@@ -869,6 +887,7 @@ __device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_
     const int tr = lane >> 3, tc = lane & 7;   // turned round: rows 4i + tr, columns 4tc..4tc+3 of the slice
     QueueReader qr;
     if (lane == 0) qr.init(s);
+    const uint64_t pol = bucket_policy(p);
     int accb = GROUPS ? grp : 0;
     uint32_t acc_phase = 0;
     for (int j = 0;; ++j) {
@@ -964,7 +983,7 @@ __device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         if (!col_ok || row_w + 4 * i + tr >= p.rows_c) continue;
-                        put_bucket4(p, dst + int64_t(4 * i + tr) * p.n, x[i], in_place);
+                        put_bucket4(p, dst + int64_t(4 * i + tr) * p.n, x[i], in_place, pol);
                     }
                 } else {   // owner: the bucket is home
                     const int64_t orow0 = (int64_t(tk.out_idx) * p.out_rows_per_idx + brow0) * p.n + col;

@@ -409,7 +409,10 @@ const char *cm_status_string(cm_status status);
  *                        the tasks, each over one slab of the column tiles
  *                        (the largest count not above `value` that divides
  *                        them), so that a pass touches 1/value of every
- *                        bucket; 0 (default) or 1: one pass.  Values 0..64.
+ *                        bucket; 1: one pass; 0 (default): two for a one-way
+ *                        ring whose buckets take at most 128 MB and whose
+ *                        tiles have at least 16 K slices, else one.  Values
+ *                        0..64.
  *                        The same fp32 additions in the same order: the same
  *                        bits.
  *  CM_OPT_RS_BUCKET_BF16 cm_gemm_rs on a ring: 1 holds the buckets in bf16
@@ -422,6 +425,13 @@ const char *cm_status_string(cm_status status);
  *                        it would pick the TMA one); no preload.  Otherwise
  *                        cm_gemm_rs returns CM_ERR_UNSUPPORTED.  The
  *                        workspace size follows the setting.
+ *  CM_OPT_RS_BUCKET_HINT cm_gemm_rs on the CTA-pair kernel: L2 eviction
+ *                        priority of the fp32 bucket writes and adds -- 1
+ *                        evict_first, 2 evict_last, 3 none; 0 (default)
+ *                        evict_last when one ring stream's buckets (M*n*4
+ *                        bytes) take at most 128 MB and can stay in L2,
+ *                        none otherwise.  Only cache behaviour changes: the
+ *                        same bits.
  *  CM_OPT_DEBUG_FLAG_OFFSET  only in a library built with bounds checks
  *                        (CM_DEBUG_BOUNDS; other builds return
  *                        CM_ERR_INVALID_ARG): adds `value` (>= 0) to the flag
@@ -448,7 +458,8 @@ typedef enum cm_option {
     CM_OPT_RS_EPILOGUE = 14,
     CM_OPT_DEBUG_FLAG_OFFSET = 15,
     CM_OPT_RS_COL_SLABS = 16,
-    CM_OPT_RS_BUCKET_BF16 = 17
+    CM_OPT_RS_BUCKET_BF16 = 17,
+    CM_OPT_RS_BUCKET_HINT = 18
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);

@@ -60,6 +60,7 @@ def test_plan_arguments(lib):
                      (cm.CM_OPT_KERNEL, -1), (cm.CM_OPT_KERNEL, 3),
                      (cm.CM_OPT_RS_EPILOGUE, -1), (cm.CM_OPT_RS_EPILOGUE, 4),
                      (cm.CM_OPT_RS_COL_SLABS, -1), (cm.CM_OPT_RS_COL_SLABS, 65),
+                     (cm.CM_OPT_RS_BUCKET_HINT, -1), (cm.CM_OPT_RS_BUCKET_HINT, 4),
                      (cm.CM_OPT_TASK_ORDER, -1), (cm.CM_OPT_TASK_ORDER, 3)):
         with pytest.raises(cm.CMError):
             p.set_option(opt, bad)

@@ -187,6 +187,7 @@ def test_column_slabs_agree_bitwise(kernel, epilogue, N, M, k, n, chunks, direct
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=N * 7 + slabs, w_layout="nk")
     ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
     p1 = _plan(N, chunks, direction, 1, kernel, 0, epilogue)
+    p1.set_option(cm.CM_OPT_RS_COL_SLABS, 1)
     y1, _, _ = run_rs(p1, x, w, "nk", torch.float32)
     ps = _plan(N, chunks, direction, 1, kernel, 0, epilogue)
     ps.set_option(cm.CM_OPT_RS_COL_SLABS, slabs)
@@ -238,3 +239,19 @@ def test_bf16_buckets_unsupported_combinations():
         with pytest.raises(cm.CMError) as e:
             cm.cm_gemm_rs(p, xd, wd, y, ws, "nk")
         assert e.value.status == cm.CM_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("epilogue", [1, 2, 3])
+@pytest.mark.parametrize("hint", [0, 1, 2])
+def test_bucket_l2_hints_keep_the_bits(epilogue, hint):
+    """CM_OPT_RS_BUCKET_HINT changes only the L2 policy of the bucket writes
+    and adds: the same bits as with no policy (3)."""
+    N, M, k, n = 8, 2048, 192, 1032
+    x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=hint * 10 + epilogue, w_layout="nk")
+    p0 = _plan(N, 2, "uni", 1, PAIR, 0, epilogue)
+    p0.set_option(cm.CM_OPT_RS_BUCKET_HINT, 3)
+    y0, _, _ = run_rs(p0, x, w, "nk", torch.float32)
+    p = _plan(N, 2, "uni", 1, PAIR, 0, epilogue)
+    p.set_option(cm.CM_OPT_RS_BUCKET_HINT, hint)
+    y1, _, _ = run_rs(p, x, w, "nk", torch.float32)
+    assert torch.equal(y0, y1)
