@@ -32,8 +32,7 @@ CM_OPT_TASK_ORDER = 13
 CM_OPT_RS_EPILOGUE = 14
 CM_OPT_DEBUG_FLAG_OFFSET = 15
 CM_OPT_RS_COL_SLABS = 16
-CM_OPT_RS_BUCKET_BF16 = 17
-CM_OPT_RS_BUCKET_HINT = 18
+CM_OPT_RS_BUCKET_HINT = 17
 CM_MAX_RANKS, CM_MAX_CHUNKS = 16, 8
 
 DIRECTIONS = {"uni": CM_RING_UNI, "bidi": CM_RING_BIDI, "none": CM_RING_NONE}

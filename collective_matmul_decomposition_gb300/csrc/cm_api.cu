@@ -49,8 +49,10 @@ int rs_epi_mode(const PlanImpl &pl, int64_t k, bool reads_inputs) {
     return many_ranks && kslices >= 28 ? 1 : 0;
 }
 
-// CM_OPT_RS_BUCKET_HINT: the L2 policy of fp32 bucket writes and adds
-// (kernel: 0 none, 1 evict_first, 2 evict_last).  Automatic (option 0): one
+// CM_OPT_RS_BUCKET_HINT: the L2 policy of the TMA epilogue's bucket writes
+// and adds (kernel: 0 none, 1 evict_first, 2 evict_last; the vector
+// epilogues take none: a build whose vector epilogues also carried the
+// policy variants ran the default MLP GEMM-RS 1-2 % slower).  Automatic (option 0): one
 // ring stream's buckets take M*n*4 bytes; up to kBucketsInL2Bytes they can
 // stay in L2 from one contribution to the next, and evict_last keeps them
 // there; beyond that, no policy.  Measured (interleaved, two runs on two
@@ -137,8 +139,7 @@ WsLayout rs_layout(const PlanImpl &p, int64_t M, int64_t n) {
     l.flags_bytes = size_t(p.flag_ids[CM_OP_GEMM_RS]) * size_t(p.chunks) * row_tiles(rows_c) *
                     size_t((n + kBN - 1) / kBN) * sizeof(uint32_t);
     l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
-    const size_t elem = p.rs_bucket_bf16 ? 2 : sizeof(float);   // CM_OPT_RS_BUCKET_BF16
-    l.buf_bytes = size_t(rs_bufs(p)) * size_t(M / p.N) * size_t(n) * elem;
+    l.buf_bytes = size_t(rs_bufs(p)) * size_t(M / p.N) * size_t(n) * sizeof(float);
     l.total = l.buf_off + l.buf_bytes;
     return l;
 }
@@ -472,9 +473,6 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.q_only = -1;
     const int promo = pl.l2_promotion;
     const KernelChoice kc = choose_kernel(pl);
-    // bf16 buckets: CTA pairs, buckets in place, a vector epilogue, no preload
-    const bool bf16_buckets = pl.rs_bucket_bf16 && rs_bufs(pl) > 0;
-    if (bf16_buckets && (!kc.pair || !pl.rs_in_place || pl.rs_epilogue == 1)) return CM_ERR_UNSUPPORTED;
     const uint32_t box_rows = uint32_t(std::min<int64_t>(kBM, rows_c));
     // x [N][M][k] viewed as [N*N*c][rows_c][k]: slab (r*N + bucket)*c + chunk
     if (!make_map(&kp.tmA0, promo, x, uint64_t(k), uint64_t(rows_c), uint64_t(N) * N * c, kBK, box_rows)) return CM_ERR_CUDA;
@@ -492,9 +490,8 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.acc_bufs = int(rs_bufs(pl));
     kp.a0_slabs = kp.a1_slabs = N * N * c;
     kp.b_slabs = N;
-    kp.acc_bf16 = bf16_buckets ? 1 : 0;
     kp.bucket_hint = rs_bucket_hint(pl, M, n);
-    if (l.buf_bytes > 0 && !bf16_buckets) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
+    if (l.buf_bytes > 0) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
         const int64_t nbufs = rs_bufs(pl);
         if (!make_acc_maps(kp, promo, kp.acc, n, rows_c, nbufs * c)) return CM_ERR_CUDA;
         // received buckets through the operand ring: each CTA of a pair loads
@@ -522,7 +519,6 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
     kp.rs_epi = rs_epi_mode(pl, k, !pl.rs_in_place);
-    if (bf16_buckets && kp.rs_epi == 0) kp.rs_epi = 2;   // the TMA epilogue moves fp32 boxes only
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
     kp.col_slabs = rs_col_slabs(pl, kp.ntiles, M, n, k);
     const bool sm = use_step_major(pl, int64_t(N) * k * n * 2);

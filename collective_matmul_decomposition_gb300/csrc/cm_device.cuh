@@ -243,22 +243,6 @@ __device__ __forceinline__ void red_add_v4(float *p, const float4 &v) {
                  "f"(v.w)
                  : "memory");
 }
-// red_add_v4 and a 16-byte store with an L2 eviction-priority policy.
-__device__ __forceinline__ void red_add_v4_hint(float *p, const float4 &v, uint64_t policy) {
-    asm volatile("red.relaxed.gpu.global.add.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x),
-                 "f"(v.y), "f"(v.z), "f"(v.w), "l"(policy)
-                 : "memory");
-}
-__device__ __forceinline__ void st_v4_hint(float *p, const float4 &v, uint64_t policy) {
-    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z),
-                 "f"(v.w), "l"(policy)
-                 : "memory");
-}
-// Four bf16 values (two bf16x2 words) added where they lie, at L2; each sum
-// is rounded to bf16 there.
-__device__ __forceinline__ void red_add_v2_bf16x2(void *p, uint32_t lo, uint32_t hi) {
-    asm volatile("red.relaxed.gpu.global.add.noftz.v2.bf16x2 [%0], {%1, %2};" ::"l"(p), "r"(lo), "r"(hi) : "memory");
-}
 __device__ __forceinline__ void red_release_add(uint32_t *p, uint32_t v) {
     asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }

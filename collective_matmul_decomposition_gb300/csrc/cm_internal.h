@@ -48,7 +48,6 @@ struct PlanImpl {
     int task_order = 0;     // see CM_OPT_TASK_ORDER
     int rs_epilogue = 0;    // see CM_OPT_RS_EPILOGUE
     int rs_col_slabs = 0;   // see CM_OPT_RS_COL_SLABS
-    int rs_bucket_bf16 = 0; // see CM_OPT_RS_BUCKET_BF16
     int rs_bucket_hint = 0; // see CM_OPT_RS_BUCKET_HINT
     int debug_flag_offset = 0;   // see CM_OPT_DEBUG_FLAG_OFFSET (bounds-checked builds)
     int64_t skip_signal = -1;

@@ -53,11 +53,9 @@ struct KParams {
     CUtensorMap tmAccIn;  // the same view, 32-column x pre_box_rows boxes: received buckets
                           // loaded through the operand ring (rs_preload)
     void *y;
-    float *acc;                // RS circulating accumulators (bf16 elements when acc_bf16)
-    int acc_bf16;              // CTA pairs, RS buckets in place with a vector epilogue: buckets held
-                               // in bf16 (CM_OPT_RS_BUCKET_BF16)
-    int bucket_hint;           // CTA pairs, RS fp32 bucket writes and adds: L2 policy (0 none,
-                               // 1 evict_first, 2 evict_last; CM_OPT_RS_BUCKET_HINT)
+    float *acc;                // RS circulating accumulators
+    int bucket_hint;           // CTA pairs, TMA RS epilogue: L2 policy of bucket writes and adds
+                               // (0 none, 1 evict_first, 2 evict_last; CM_OPT_RS_BUCKET_HINT)
     uint32_t *flags;
     uint32_t *status;
     uint32_t *tile_counter;    // dynamic tile scheduler (CTA-pair kernel), zero at launch

@@ -635,6 +635,7 @@ __device__ __forceinline__ float4 *swz_row(uint8_t *buf, int row) { return reint
 //    the slice added, and the sum TMA-stored to the next rank's buffer;
 //  - the owner: the received partial bucket(s) are TMA-loaded, the slice
 //    added, and the sum rounded into the output.
+template <bool HINT>
 __device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     const int e = int(threadIdx.x) / 32 - 4;   // 0..7
     const int lane = int(threadIdx.x) & 31;
@@ -741,7 +742,7 @@ __device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_
                 __syncwarp();
                 if (lane == 0) {
                     const int slab = tk.out_buf * p.chunks + c.q;
-                    if (p.bucket_hint) {
+                    if (HINT) {
                         const uint64_t pol = bucket_policy(p);
                         if (in_place)
                             tma_reduce_add_3d_hint(&p.tmAcc, buf, col0, row_w, slab, pol);
@@ -836,43 +837,6 @@ __device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_
 // for every warp that drains the tile (four or eight) in each CTA, and no
 // warp waits for another.
 
-// Four consecutive bucket elements at element offset e of the accumulator
-// buffers, as fp32 (bf16 buckets are widened exactly).
-__device__ __forceinline__ float4 load_bucket4(const KParams &p, int64_t e) {
-    if (!p.acc_bf16) return __ldcg(reinterpret_cast<const float4 *>(p.acc + e));
-    const uint2 w = __ldcg(reinterpret_cast<const uint2 *>(reinterpret_cast<const __nv_bfloat16 *>(p.acc) + e));
-    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.x));
-    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w.y));
-    return make_float4(lo.x, lo.y, hi.x, hi.y);
-}
-
-// Four consecutive bucket elements at element offset e: added where they
-// lie (add) or stored (the bucket's first contribution).  bf16 buckets take
-// the values rounded to bf16 (RNE); the addition rounds again, at L2.
-__device__ __forceinline__ void put_bucket4(const KParams &p, int64_t e, const float4 &v, bool add, uint64_t pol) {
-    if (!p.acc_bf16) {
-        float *d = p.acc + e;
-        if (p.bucket_hint) {
-            if (add)
-                red_add_v4_hint(d, v, pol);
-            else
-                st_v4_hint(d, v, pol);
-        } else if (add) {
-            red_add_v4(d, v);
-        } else {
-            __stcg(reinterpret_cast<float4 *>(d), v);
-        }
-        return;
-    }
-    __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-    const uint32_t wl = *reinterpret_cast<uint32_t *>(&lo), wh = *reinterpret_cast<uint32_t *>(&hi);
-    __nv_bfloat16 *d = reinterpret_cast<__nv_bfloat16 *>(p.acc) + e;
-    if (add)
-        red_add_v2_bf16x2(d, wl, wh);
-    else
-        __stcg(reinterpret_cast<uint2 *>(d), make_uint2(wl, wh));
-}
-
 template <bool GROUPS>
 __device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_base, const Cl &cl) {
     constexpr int kSlices = GROUPS ? kBN / 32 : kBN / 64;   // 32-column slices per warp and tile
@@ -887,7 +851,6 @@ __device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_
     const int tr = lane >> 3, tc = lane & 7;   // turned round: rows 4i + tr, columns 4tc..4tc+3 of the slice
     QueueReader qr;
     if (lane == 0) qr.init(s);
-    const uint64_t pol = bucket_policy(p);
     int accb = GROUPS ? grp : 0;
     uint32_t acc_phase = 0;
     for (int j = 0;; ++j) {
@@ -962,12 +925,12 @@ __device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_
                 for (int jj = 0; jj < 2; ++jj) {
                     if (tk.in_buf[jj] < 0 || (jj == 0 && (in_place || (pre >= 0 && (cb & 3) < p.pre_stages))))
                         continue;
-                    const int64_t src = int64_t(tk.in_buf[jj]) * p.acc_buf_stride + brow0 * p.n + col;
+                    const float *src = p.acc + int64_t(tk.in_buf[jj]) * p.acc_buf_stride + brow0 * p.n + col;
                     float4 a[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i)
                         if (col_ok && row_w + 4 * i + tr < p.rows_c)
-                            a[i] = load_bucket4(p, src + int64_t(4 * i + tr) * p.n);
+                            a[i] = __ldcg(reinterpret_cast<const float4 *>(src + int64_t(4 * i + tr) * p.n));
                         else
                             a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
@@ -979,11 +942,15 @@ __device__ void epilogue_rs_vec(const KParams &p, const PSmem &s, uint32_t tmem_
                     }
                 }
                 if (tk.out_buf >= 0) {
-                    const int64_t dst = int64_t(tk.out_buf) * p.acc_buf_stride + brow0 * p.n + col;
+                    float *dst = p.acc + int64_t(tk.out_buf) * p.acc_buf_stride + brow0 * p.n + col;
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         if (!col_ok || row_w + 4 * i + tr >= p.rows_c) continue;
-                        put_bucket4(p, dst + int64_t(4 * i + tr) * p.n, x[i], in_place, pol);
+                        float *d = dst + int64_t(4 * i + tr) * p.n;
+                        if (in_place)
+                            red_add_v4(d, x[i]);
+                        else
+                            __stcg(reinterpret_cast<float4 *>(d), x[i]);
                     }
                 } else {   // owner: the bucket is home
                     const int64_t orow0 = (int64_t(tk.out_idx) * p.out_rows_per_idx + brow0) * p.n + col;
@@ -1133,8 +1100,10 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
             epilogue_rs_vec<true>(p, s, tmem_base, cl);
         else if (p.rs_epi == 2)
             epilogue_rs_vec<false>(p, s, tmem_base, cl);
+        else if (p.bucket_hint)
+            epilogue_rs_tma<true>(p, s, tmem_base, cl);
         else
-            epilogue_rs_tma(p, s, tmem_base, cl);
+            epilogue_rs_tma<false>(p, s, tmem_base, cl);
     }
     tc_fence_before();
     __syncthreads();

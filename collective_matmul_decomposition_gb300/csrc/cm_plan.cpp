@@ -522,10 +522,6 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
             if (value < 0 || value > 3) return CM_ERR_INVALID_ARG;
             p.rs_bucket_hint = int(value);
             return CM_OK;
-        case CM_OPT_RS_BUCKET_BF16:
-            if (value != 0 && value != 1) return CM_ERR_INVALID_ARG;
-            p.rs_bucket_bf16 = int(value);
-            return CM_OK;
         case CM_OPT_RS_COL_SLABS:
             if (value < 0 || value > 64) return CM_ERR_INVALID_ARG;
             p.rs_col_slabs = int(value);

@@ -415,18 +415,9 @@ const char *cm_status_string(cm_status status);
  *                        0..64.
  *                        The same fp32 additions in the same order: the same
  *                        bits.
- *  CM_OPT_RS_BUCKET_BF16 cm_gemm_rs on a ring: 1 holds the buckets in bf16
- *                        instead of fp32 (half the bucket bytes; every hop
- *                        rounds the contribution and the sum to bf16, so the
- *                        error grows with N -- a measured variant, not the
- *                        default); 0 (default) fp32.  Needs the CTA-pair
- *                        kernel, buckets in place and a vector epilogue
- *                        (CM_OPT_RS_EPILOGUE 0, 2 or 3; 0 then picks 3 where
- *                        it would pick the TMA one); no preload.  Otherwise
- *                        cm_gemm_rs returns CM_ERR_UNSUPPORTED.  The
- *                        workspace size follows the setting.
- *  CM_OPT_RS_BUCKET_HINT cm_gemm_rs on the CTA-pair kernel: L2 eviction
- *                        priority of the fp32 bucket writes and adds -- 1
+ *  CM_OPT_RS_BUCKET_HINT cm_gemm_rs on the CTA-pair kernel with the TMA
+ *                        epilogue: L2 eviction priority of the bucket writes
+ *                        and adds -- 1
  *                        evict_first, 2 evict_last, 3 none; 0 (default)
  *                        evict_last when one ring stream's buckets (M*n*4
  *                        bytes) take at most 128 MB and can stay in L2,
@@ -458,8 +449,7 @@ typedef enum cm_option {
     CM_OPT_RS_EPILOGUE = 14,
     CM_OPT_DEBUG_FLAG_OFFSET = 15,
     CM_OPT_RS_COL_SLABS = 16,
-    CM_OPT_RS_BUCKET_BF16 = 17,
-    CM_OPT_RS_BUCKET_HINT = 18
+    CM_OPT_RS_BUCKET_HINT = 17
 } cm_option;
 
 cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value);

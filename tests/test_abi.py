@@ -88,11 +88,6 @@ def test_workspace_sizes(lib):
     assert p.rs_workspace_size(8192, 8192) >= 8 * 8 * 1024 * 8192 * 4
     with pytest.raises(cm.CMError):
         p.set_option(cm.CM_OPT_RS_IN_PLACE, 2)
-    p.set_option(cm.CM_OPT_RS_IN_PLACE, 1)
-    p.set_option(cm.CM_OPT_RS_BUCKET_BF16, 1)  # bf16 buckets: half the bytes
-    assert 8 * 1024 * 8192 * 2 <= p.rs_workspace_size(8192, 8192) < 9 * 1024 * 8192 * 2
-    with pytest.raises(cm.CMError):
-        p.set_option(cm.CM_OPT_RS_BUCKET_BF16, 2)
     b = cm.Plan(8, 1, "bidi")
     assert b.ag_workspace_size(m, K) >= 4 * 8 * m * K * 2
     assert cm.Plan(8, 1, "none").ag_workspace_size(m, K) < 1 << 20

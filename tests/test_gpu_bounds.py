@@ -88,7 +88,7 @@ def test_ag_same_bits_no_report(dbg, N, chunks, direction, opts):
     (4, 2, "uni", {"CM_OPT_RS_EPILOGUE": 2}),
     (8, 4, "uni", {"CM_OPT_RS_EPILOGUE": 2}),           # chunk pairs, two warp groups
     (8, 4, "uni", {"CM_OPT_RS_EPILOGUE": 3}),           # chunk pairs, every warp with vector adds
-    (5, 1, "bidi", {"CM_OPT_RS_BUCKET_BF16": 1}),       # bf16 buckets
+    (5, 1, "bidi", {"CM_OPT_RS_BUCKET_HINT": 2}),       # TMA epilogue with an L2 policy
     (4, 2, "bidi", {"CM_OPT_RS_EPILOGUE": 3, "CM_OPT_RS_IN_PLACE": 0}),
     (5, 1, "bidi", {"CM_OPT_RS_EPILOGUE": 1, "CM_OPT_RS_PRELOAD": 1}),
     (4, 2, "bidi", {"CM_OPT_RS_IN_PLACE": 0, "CM_OPT_RS_PRELOAD": 3}),

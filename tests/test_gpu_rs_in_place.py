@@ -197,55 +197,12 @@ def test_column_slabs_agree_bitwise(kernel, epilogue, N, M, k, n, chunks, direct
     assert torch.equal(y1, ys)
 
 
-@pytest.mark.parametrize("epilogue", [0, 2, 3])
-@pytest.mark.parametrize("N,M,k,n,chunks,direction", [
-    (4, 1024, 128, 1024, 1, "uni"),
-    (8, 4096, 256, 2048, 4, "uni"),       # chunk pairs
-    (5, 1280, 136, 520, 1, "bidi"),       # odd N, ragged k and n: the owner loads two bf16 buckets
-    (16, 4096, 192, 768, 2, "uni"),       # sixteen hops of bf16 rounding
-])
-def test_bf16_buckets(epilogue, N, M, k, n, chunks, direction):
-    """CM_OPT_RS_BUCKET_BF16: the buckets circulate in bf16.  Every hop
-    rounds the contribution and the sum to bf16, so the result meets the
-    stated bf16 bar (not the fp32 one); the additions keep the ring order,
-    so the bits repeat from call to call and agree between the vector
-    epilogues."""
-    x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=N * 13 + k, w_layout="nk")
-    ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
-    p = _plan(N, chunks, direction, 1, PAIR, 0, epilogue)
-    p.set_option(cm.CM_OPT_RS_BUCKET_BF16, 1)
-    y1, _, _ = run_rs(p, x, w, "nk", torch.float32)
-    y2, _, _ = run_rs(p, x, w, "nk", torch.float32)
-    assert torch.isfinite(y1).all()
-    assert oracle.normwise_max_rel_err(_np(y1), ref) <= TOL
-    assert torch.equal(y1, y2)
-    q = _plan(N, chunks, direction, 1, PAIR, 0, 3 if epilogue == 2 else 2)
-    q.set_option(cm.CM_OPT_RS_BUCKET_BF16, 1)
-    y3, _, _ = run_rs(q, x, w, "nk", torch.float32)
-    assert torch.equal(y1, y3)
-
-
-def test_bf16_buckets_unsupported_combinations():
-    """bf16 buckets need the CTA-pair kernel, buckets in place and a vector
-    epilogue; other combinations are refused before any device work."""
-    N, M, k, n = 4, 1024, 128, 512
-    x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=3, w_layout="nk")
-    xd, wd = x.to("cuda:0"), w.to("cuda:0")
-    for in_place, kernel, epilogue in ((0, PAIR, 0), (1, SINGLE, 0), (1, PAIR, 1)):
-        p = _plan(N, 1, "uni", in_place, kernel, 0, epilogue)
-        p.set_option(cm.CM_OPT_RS_BUCKET_BF16, 1)
-        ws = torch.empty(p.rs_workspace_size(M, n), dtype=torch.uint8, device="cuda:0")
-        y = torch.empty(N, M // N, n, dtype=torch.float32, device="cuda:0")
-        with pytest.raises(cm.CMError) as e:
-            cm.cm_gemm_rs(p, xd, wd, y, ws, "nk")
-        assert e.value.status == cm.CM_ERR_UNSUPPORTED
-
-
 @pytest.mark.parametrize("epilogue", [1, 2, 3])
 @pytest.mark.parametrize("hint", [0, 1, 2])
 def test_bucket_l2_hints_keep_the_bits(epilogue, hint):
-    """CM_OPT_RS_BUCKET_HINT changes only the L2 policy of the bucket writes
-    and adds: the same bits as with no policy (3)."""
+    """CM_OPT_RS_BUCKET_HINT changes only the L2 policy of the TMA
+    epilogue's bucket writes and adds (the vector epilogues take none): the
+    same bits as with no policy (3)."""
     N, M, k, n = 8, 2048, 192, 1032
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=hint * 10 + epilogue, w_layout="nk")
     p0 = _plan(N, 2, "uni", 1, PAIR, 0, epilogue)
