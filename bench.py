@@ -885,6 +885,8 @@ def run_gate(args):
                            mem_gbs=hbm / 2 / N)
             pred_dec = cm.cost_estimate(N, chunks, direction, code, rows, K, n, one_gpu) / 1e3
             pred_none = cm.cost_estimate(N, 1, "none", code, rows, K, n, one_gpu) / 1e3
+            # the same rates for both ring directions: which one the model prefers
+            pred_ring = {d: cm.cost_estimate(N, chunks, d, code, rows, K, n, one_gpu) / 1e3 for d in ("uni", "bidi")}
             pick = cm.plan_choose(N, code, rows, K, n, one_gpu)
             nvl = dict(gemm_tflops=rate, ring_gbs=NVLINK_GBS, coll_gbs=NVLINK_GBS, hop_us=NVLINK_HOP_US, mem_gbs=hbm)
             pick_nvl = cm.plan_choose(N, code, rows, K, n, nvl)
@@ -903,7 +905,8 @@ def run_gate(args):
                                                 "decomposed_rel_err": (pred_dec - ms_dec) / ms_dec,
                                                 "undecomposed_rel_err": (pred_none - ms_none) / ms_none,
                                                 "choice": {"chunks": pick[0], "ring": pick[1]},
-                                                "agrees_with_measurement": agrees},
+                                                "agrees_with_measurement": agrees,
+                                                "decomposed_ms_by_ring": pred_ring},
                               "nvlink_projection": {"rates": nvl, "choice": {"chunks": pick_nvl[0], "ring": pick_nvl[1]},
                                                     "predicted_ms": pick_nvl[2] / 1e3,
                                                     "einsum_offering_both": {"decompose": ein[0], "chunks": ein[1],
