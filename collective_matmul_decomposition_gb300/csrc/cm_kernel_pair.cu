@@ -30,7 +30,7 @@
 //             per tile, the accumulator to the barriers of both CTAs.
 //   warp 2    AG forwarder (both CTAs): every tile copies a slice of its CTA's
 //             128 shard rows (1/column-tiles of them) to the ring neighbour's
-//             receive slot with 1-D TMA bulk copies through two 16 KB buffers,
+//             receive slot with 1-D TMA bulk copies through four 8 KB buffers,
 //             then bumps the slot's ready flag -- the rotation copy in flight
 //             while the partial GEMMs read the shard.
 //   warps 4-11  epilogue (both CTAs): 8 warps, TMEM lane quarter = warp % 4.
@@ -67,13 +67,14 @@ constexpr int kPThreads = 384;
 constexpr int kPEpiWarps = kPairEpiWarps;
 constexpr int kHalfA = kCtaRows * kBK * 2;   // 16 KB
 constexpr int kHalfB = (kBN / 2) * kBK * 2;  // 16 KB
-constexpr int kFwdPiece = 16384;             // forwarder copy granule
+constexpr int kFwdPiece = 8192;              // forwarder copy granule
+constexpr int kFwdBufs = 4;                  // forwarder buffers (the same 32 KB as the RS epilogue's)
 constexpr int kQueue = 6;                    // tile-index queue depth
 constexpr int CL = 2;                        // CTAs per cluster: one pair
 // RS preload: ring stage ps carries the 32-column fp32 boxes at columns
 // 32*ps and 128 + 32*ps of the tile (slice ps of both epilogue column
 // halves); p.pre_stages of them (2 or 4) precede the K slices.
-constexpr int kPSmemBytes = kPStages * (kHalfA + kHalfB) + 2 * kFwdPiece + 1024 + 1024;
+constexpr int kPSmemBytes = kPStages * (kHalfA + kHalfB) + kFwdBufs * kFwdPiece + 1024 + 1024;
 
 // Position of this CTA in its cluster.
 struct Cl {
@@ -84,7 +85,8 @@ struct Cl {
 
 struct PSmem {
     uint8_t *a0, *b0;   // ring stage 0 of A and B; stage i is kHalfA (kHalfB) bytes further
-    uint8_t *fbuf[2];   // AG: forwarder copy buffers; RS: the same 32 KB as 8 epilogue-warp buffers
+    uint8_t *fbuf[1];   // AG: kFwdBufs forwarder copy buffers of kFwdPiece bytes from fbuf[0]; RS: the
+                        // same 32 KB as 8 epilogue-warp buffers
     uint64_t *full, *empty, *tfull, *tempty, *drain, *fbar, *qfull, *qempty, *ebar, *started;
     int32_t *qent;      // tile queue: kQueue entries of kQWords words, each CTA its own (see QTile)
     uint32_t *tmem_slot;
@@ -459,7 +461,7 @@ __device__ void mma_issuer(const KParams &p, const PSmem &s, uint32_t tmem_base,
 __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
     QueueReader qr;
     qr.init(s);
-    uint32_t fph[2] = {0u, 0u};
+    uint32_t fph = 0;   // bit b: the phase of buffer b's barrier
     // every tile of a row tile forwards a slice of the rows: column tile nt
     // copies rows [nt*per, (nt+1)*per) of this CTA's 128, so the shard chunk
     // moves while all its tiles run instead of one tile doing all of it
@@ -495,29 +497,39 @@ __device__ void forwarder(const KParams &p, const PSmem &s, const Cl &cl) {
                     if (dst[j]) okb = okb && dst[j] >= p.slot_bytes && dst[j] - p.slot_bytes + bytes <= p.slot_total;
                 if (!in_bounds(p, okb, kSiteBoundsForward, c.task, c.q)) break;
             }
+            // pieces go through kFwdBufs buffers: up to kFwdBufs loads in
+            // flight, each buffer refilled once the store of its previous
+            // piece has read it
             const int np = int((bytes + kFwdPiece - 1) / kFwdPiece);
             auto piece = [&](int i) { return uint32_t(min(int64_t(kFwdPiece), bytes - int64_t(i) * kFwdPiece)); };
-            mbar_expect_tx(&s.fbar[0], piece(0));
-            bulk_load(s.fbuf[0], src, piece(0), &s.fbar[0]);
+            auto fbuf = [&](int b) { return s.fbuf[0] + b * kFwdPiece; };
+            auto load = [&](int i) {
+                const int b = i % kFwdBufs;
+                mbar_expect_tx(&s.fbar[b], piece(i));
+                bulk_load(fbuf(b), src + int64_t(i) * kFwdPiece, piece(i), &s.fbar[b]);
+            };
+            int issued = min(np, kFwdBufs);
+            for (int i = 0; i < issued; ++i) load(i);
             for (int i = 0; i < np && ok; ++i) {
-                const int b = i & 1;
-                if (i + 1 < np) {
-                    if (i >= 1) bulk_wait_read<0>();   // the store of piece i-1 has left buffer b^1
-                    mbar_expect_tx(&s.fbar[b ^ 1], piece(i + 1));
-                    bulk_load(s.fbuf[b ^ 1], src + int64_t(i + 1) * kFwdPiece, piece(i + 1), &s.fbar[b ^ 1]);
-                }
-                ok = wait_mbar<false>(p, s.abort, &s.fbar[b], fph[b], kSiteForwardFull, c.task, c.q);
+                const int b = i % kFwdBufs;
+                ok = wait_mbar<false>(p, s.abort, &s.fbar[b], (fph >> b) & 1u, kSiteForwardFull, c.task, c.q);
                 if (!ok) {
-                    // leaving early: piece i, and piece i + 1 if it was
-                    // requested, may still be landing in this CTA's buffers
-                    drain_mbar<false>(p, &s.fbar[b], fph[b]);
-                    if (i + 1 < np) drain_mbar<false>(p, &s.fbar[b ^ 1], fph[b ^ 1]);
+                    // leaving early: pieces i .. issued - 1 (one per buffer)
+                    // may still be landing in this CTA's buffers
+                    for (int j = i; j < issued; ++j) {
+                        const int bj = j % kFwdBufs;
+                        drain_mbar<false>(p, &s.fbar[bj], (fph >> bj) & 1u);
+                    }
                     break;
                 }
-                fph[b] ^= 1u;
+                fph ^= 1u << b;
                 for (int j = 0; j < 2; ++j)
-                    if (dst[j]) bulk_store(dst[j] + int64_t(i) * kFwdPiece, s.fbuf[b], piece(i));
+                    if (dst[j]) bulk_store(dst[j] + int64_t(i) * kFwdPiece, fbuf(b), piece(i));
                 bulk_commit();
+                if (i >= 1 && issued < np) {
+                    bulk_wait_read<1>();   // every store but piece i's has read its buffer: piece i-1's is free
+                    load(issued++);
+                }
             }
             bulk_wait<0>();   // the copies are complete in global memory
             if (!ok) break;
@@ -1004,19 +1016,18 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
     s.a0 = base;
     s.b0 = base + kPStages * kHalfA;
     s.fbuf[0] = base + kPStages * (kHalfA + kHalfB);
-    s.fbuf[1] = s.fbuf[0] + kFwdPiece;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(s.fbuf[1] + kFwdPiece);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(s.fbuf[0] + kFwdBufs * kFwdPiece);
     s.full = bars;
     s.empty = s.full + kPStages;
     s.tfull = s.empty + kPStages;
     s.tempty = s.tfull + 2;
     s.drain = s.tempty + 2;
     s.fbar = s.drain + 1;
-    s.qfull = s.fbar + 2;
+    s.qfull = s.fbar + kFwdBufs;
     s.qempty = s.qfull + kQueue;
     s.ebar = s.qempty + kQueue;
     s.started = s.ebar + kPEpiWarps;
-    s.qent = reinterpret_cast<int32_t *>(s.started + 1);   // 16-byte aligned: 40 barriers precede it
+    s.qent = reinterpret_cast<int32_t *>(s.started + 1);   // 16-byte aligned: 42 barriers precede it
     s.tmem_slot = reinterpret_cast<uint32_t *>(s.qent + kQWords * kQueue);
     s.abort = reinterpret_cast<volatile int *>(s.tmem_slot + 1);
 
@@ -1035,8 +1046,8 @@ __global__ void __launch_bounds__(kPThreads, 1) cm_pair_kernel(const __grid_cons
             // epilogue warps of both CTAs that drain accumulator i: all eight,
             // or the four of the group that owns it (RS in two groups)
             mbar_init(&s.tempty[i], 2 * (p.op == 1 && p.rs_epi == 1 ? kPEpiWarps / 2 : kPEpiWarps));
-            mbar_init(&s.fbar[i], 1);
         }
+        for (int i = 0; i < kFwdBufs; ++i) mbar_init(&s.fbar[i], 1);
         mbar_init(s.drain, 1);
         mbar_init(s.started, 1);
         // queue slot releases: 8 epilogue warps per CTA and (AG) both forwarders
