@@ -807,7 +807,10 @@ __device__ void epilogue_rs_tma(const KParams &p, const PSmem &s, uint32_t tmem_
                 store_pending = false;
                 fence_proxy_async_global();
             }
-            __threadfence();
+            // every warp's copies are complete before the barrier; the
+            // leader's release after it covers them (release is cumulative
+            // over what the barrier orders before it), so no per-thread fence
+            // is needed here (one measured 2 % slower on tiles of 4-24 K slices)
             bar_sync(1, kPEpiWarps * 32);
             if (leader_thread && !*s.abort) red_release_add(flag_ptr(p, tk.sig_done, c.q, c.mt, c.nt), 1u);
         }
