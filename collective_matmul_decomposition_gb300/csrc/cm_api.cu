@@ -49,6 +49,11 @@ int rs_epi_mode(const PlanImpl &pl, int64_t k, bool reads_inputs) {
     return many_ranks && kslices >= 28 ? 1 : 0;
 }
 
+// One ring stream's buckets, M*n*4 bytes, fit in L2 with room to spare up to
+// this size: the automatic choices of CM_OPT_RS_IN_PLACE, CM_OPT_RS_COL_SLABS
+// and CM_OPT_RS_BUCKET_HINT follow it.
+constexpr int64_t kBucketsInL2Bytes = int64_t(128) << 20;
+
 // CM_OPT_RS_BUCKET_HINT: the L2 policy of the TMA epilogue's bucket writes
 // and adds (kernel: 0 none, 1 evict_first, 2 evict_last; the vector
 // epilogues take none: a build whose vector epilogues also carried the
@@ -61,7 +66,6 @@ int rs_epi_mode(const PlanImpl &pl, int64_t k, bool reads_inputs) {
 // (67 MB) 0.6-1.5 %; on the MLP (268 MB) evict_first gained 1.8 % at N=8 in
 // one run and lost 1.0-2.2 % at N=4 and 8 in the other, evict_last within
 // 1 %.  Option 3: no policy.
-constexpr int64_t kBucketsInL2Bytes = int64_t(128) << 20;
 
 int rs_bucket_hint(const PlanImpl &pl, int64_t M, int64_t n) {
     if (pl.rs_bucket_hint == 3) return 0;
@@ -125,11 +129,26 @@ WsLayout ag_layout(const PlanImpl &p, int64_t m, int64_t K) {
     return l;
 }
 
+// CM_OPT_RS_IN_PLACE for a call of M x n: 1 in place, 0 per-step buffers, 2
+// (automatic) in place where one stream's buckets fit L2, per-step buffers
+// otherwise.  Measured (interleaved, each with its automatic epilogue): in
+// place was 6-10 % faster on the GPT-3 attention-out (100 MB of buckets) and
+// 2-3 % on the Megatron-SP fc2 (67 MB); per-step buffers were 2-4 % faster
+// on the MLP at N = 4 and 8 and on the two-way N = 16 ring (268 MB), and
+// even on the one-way N = 16 ring.  Where the buckets stay in L2, an add
+// where the bucket lies costs one L2 read-modify-write; where they do not,
+// the TMA epilogue's streaming load-add-store of per-step buffers keeps the
+// tensor pipe fed better than reduce-adds that each go to DRAM.
+bool rs_in_place_for(const PlanImpl &p, int64_t M, int64_t n) {
+    if (p.rs_in_place != 2) return p.rs_in_place != 0;
+    return M * n * 4 <= kBucketsInL2Bytes;
+}
+
 // RS accumulator buffers of [M/N][n] fp32: one per (bucket, ring stream) when
 // buckets are accumulated in place, else one per (rank, ring stream, step).
-int64_t rs_bufs(const PlanImpl &p) {
+int64_t rs_bufs(const PlanImpl &p, bool in_place) {
     if (p.dir == CM_RING_NONE || p.N <= 1) return 0;
-    const int64_t per = p.rs_in_place ? 1 : p.sched[CM_OP_GEMM_RS].steps;
+    const int64_t per = in_place ? 1 : p.sched[CM_OP_GEMM_RS].steps;
     return int64_t(p.N) * streams_of(p) * per;
 }
 
@@ -139,7 +158,7 @@ WsLayout rs_layout(const PlanImpl &p, int64_t M, int64_t n) {
     l.flags_bytes = size_t(p.flag_ids[CM_OP_GEMM_RS]) * size_t(p.chunks) * row_tiles(rows_c) *
                     size_t((n + kBN - 1) / kBN) * sizeof(uint32_t);
     l.buf_off = align_up(l.flags_off + l.flags_bytes, 1024);
-    l.buf_bytes = size_t(rs_bufs(p)) * size_t(M / p.N) * size_t(n) * sizeof(float);
+    l.buf_bytes = size_t(rs_bufs(p, rs_in_place_for(p, M, n))) * size_t(M / p.N) * size_t(n) * sizeof(float);
     l.total = l.buf_off + l.buf_bytes;
     return l;
 }
@@ -291,19 +310,23 @@ bool use_step_major(const PlanImpl &pl, int64_t weight_bytes) {
     return weight_bytes <= kStepMajorWeightBytes;
 }
 
+// rs_per_step: a GEMM -> ReduceScatter call with per-step buffers (the plan's
+// second RS task table).
 cm_status run(const PlanImpl &pl, const KernelChoice &kc, int op, KParams &kp, const WsLayout &l, void *ws,
-              bool b_mn, bool step_major, cudaStream_t stream) {
+              bool b_mn, bool step_major, cudaStream_t stream, bool rs_per_step = false) {
     int sms = 0, max_clusters = 0;
     cm_status st = setup_launch(pl, kc, kp, l, ws, &sms, &max_clusters);
     if (st != CM_OK) return st;
-    const auto &tasks = step_major ? pl.tasks_sm[op] : pl.tasks[op];
+    const bool ps = op == CM_OP_GEMM_RS && rs_per_step;
+    const auto &tasks = step_major ? (ps ? pl.rs_ps_sm : pl.tasks_sm[op]) : (ps ? pl.rs_ps : pl.tasks[op]);
     const int ntasks = int(tasks.size());
     if (ntasks > kMaxTasks) return CM_ERR_UNSUPPORTED;
     std::memcpy(kp.tasks, tasks.data(), sizeof(cm_task) * size_t(ntasks));
     // status word and flags start at zero for every call
     if (cudaMemsetAsync(ws, 0, l.buf_off, stream) != cudaSuccess) return CM_ERR_CUDA;
     uint8_t *w8 = static_cast<uint8_t *>(ws);
-    const auto &sb = step_major ? pl.step_begin_sm[op] : pl.step_begin[op];
+    const auto &sb = step_major ? (ps ? pl.rs_ps_step_begin_sm : pl.step_begin_sm[op])
+                                : (ps ? pl.rs_ps_step_begin : pl.step_begin[op]);
     const int nsteps = int(sb.size()) - 1;
     const int launches = pl.serial_steps ? nsteps : 1;
     for (int i = 0; i < launches; ++i) {
@@ -487,12 +510,13 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.y = y;
     kp.acc = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + l.buf_off);
     kp.y_elems = M * n;
-    kp.acc_bufs = int(rs_bufs(pl));
+    const bool in_place = rs_in_place_for(pl, M, n);
+    kp.acc_bufs = int(rs_bufs(pl, in_place));
     kp.a0_slabs = kp.a1_slabs = N * N * c;
     kp.b_slabs = N;
     kp.bucket_hint = rs_bucket_hint(pl, M, n);
     if (l.buf_bytes > 0) {   // accumulators as [bufs*chunks][rows_c][n] fp32, 32 x 32 boxes
-        const int64_t nbufs = rs_bufs(pl);
+        const int64_t nbufs = rs_bufs(pl, in_place);
         if (!make_acc_maps(kp, promo, kp.acc, n, rows_c, nbufs * c)) return CM_ERR_CUDA;
         // received buckets through the operand ring: each CTA of a pair loads
         // its 128 rows of the tile as 32-column boxes (one per 16 KB stage
@@ -518,11 +542,11 @@ cm_status cm_gemm_rs(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
     kp.n = int(n);
     kp.y_f32 = y_dtype == CM_F32;
     kp.a_box_rows = int(box_rows);
-    kp.rs_epi = rs_epi_mode(pl, k, !pl.rs_in_place);
+    kp.rs_epi = rs_epi_mode(pl, k, !in_place);
     set_tiling(kc, CM_OP_GEMM_RS, kp, rows_c, n, true);
     kp.col_slabs = rs_col_slabs(pl, kp.ntiles, M, n, k);
     const bool sm = use_step_major(pl, int64_t(N) * k * n * 2);
-    return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, sm, reinterpret_cast<cudaStream_t>(stream));
+    return run(pl, kc, CM_OP_GEMM_RS, kp, l, ws, b_mn, sm, reinterpret_cast<cudaStream_t>(stream), !in_place);
 }
 
 size_t cm_gemm_rs_pipelined_workspace_size(cm_plan_t plan, int64_t M, int64_t n) {

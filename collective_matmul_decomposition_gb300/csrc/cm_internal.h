@@ -44,7 +44,7 @@ struct PlanImpl {
     int row_band = 0;       // see CM_OPT_ROW_BAND
     int bulk_overlap = 1;   // see CM_OPT_BULK_OVERLAP
     int rs_preload = 2;     // see CM_OPT_RS_PRELOAD
-    int rs_in_place = 1;    // see CM_OPT_RS_IN_PLACE
+    int rs_in_place = 2;    // see CM_OPT_RS_IN_PLACE (2: chosen per call)
     int task_order = 0;     // see CM_OPT_TASK_ORDER
     int rs_epilogue = 0;    // see CM_OPT_RS_EPILOGUE
     int rs_col_slabs = 0;   // see CM_OPT_RS_COL_SLABS
@@ -57,6 +57,11 @@ struct PlanImpl {
     int flag_ids[2] = {0, 0};             // ids used per op (before * chunks)
     std::vector<int> step_begin[2];       // first task index of each step (+ end sentinel)
     std::vector<int> step_begin_sm[2];    // the same for tasks_sm
+    // GEMM -> ReduceScatter with one buffer per (rank, stream, step): the same
+    // tasks as tasks[CM_OP_GEMM_RS] / tasks_sm[...] (buckets in place) with
+    // other buffer indices, in both orders
+    std::vector<cm_task> rs_ps, rs_ps_sm;
+    std::vector<int> rs_ps_step_begin, rs_ps_step_begin_sm;
 };
 
 }  // namespace cm

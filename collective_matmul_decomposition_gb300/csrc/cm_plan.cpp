@@ -293,7 +293,7 @@ void build_ag_tasks(PlanImpl &p) {
     set_orders(p, CM_OP_AG_GEMM, tasks);
 }
 
-void build_rs_tasks(PlanImpl &p) {
+void build_rs_tasks(PlanImpl &p, bool in_place) {
     const int N = p.N;
     const Schedule &s = p.sched[CM_OP_GEMM_RS];
     const int S = s.steps, D = s.streams;
@@ -303,7 +303,6 @@ void build_rs_tasks(PlanImpl &p) {
     // accumulator buffer that (rank r, stream d, step) reads and a step-i
     // contributor to bucket o writes: one per bucket and stream (in place),
     // or one per (rank, stream, step) (written once)
-    const bool in_place = p.rs_in_place != 0;
     auto acc = [&](int r, int d, int step, int bucket) {
         return in_place ? bucket * D + d : (r * D + d) * S + step;
     };
@@ -355,14 +354,21 @@ void build_rs_tasks(PlanImpl &p) {
                     tasks.push_back(t);
                 }
     }
-    set_orders(p, CM_OP_GEMM_RS, tasks);
+    if (in_place) {
+        set_orders(p, CM_OP_GEMM_RS, tasks);
+    } else {
+        p.rs_ps = tasks;
+        order_and_index(p, CM_OP_GEMM_RS, p.rs_ps, p.dir != CM_RING_NONE && !p.serial_steps, p.rs_ps_step_begin);
+        p.rs_ps_sm = tasks;
+        order_and_index(p, CM_OP_GEMM_RS, p.rs_ps_sm, false, p.rs_ps_step_begin_sm);
+    }
 }
 
 // Bounds-checked builds: the planted out-of-range done-signal ids of
 // CM_OPT_DEBUG_FLAG_OFFSET.
 void apply_debug_offset(PlanImpl &p) {
     if (p.debug_flag_offset <= 0) return;
-    for (auto *v : {&p.tasks[CM_OP_GEMM_RS], &p.tasks_sm[CM_OP_GEMM_RS]})
+    for (auto *v : {&p.tasks[CM_OP_GEMM_RS], &p.tasks_sm[CM_OP_GEMM_RS], &p.rs_ps, &p.rs_ps_sm})
         for (cm_task &t : *v)
             if (t.sig_done >= 0) t.sig_done = int16_t(t.sig_done + p.debug_flag_offset);
 }
@@ -373,7 +379,12 @@ void apply_skip(PlanImpl &p) {
     const int rank = int((p.skip_signal >> 8) & 0xff);
     const int step = int(p.skip_signal & 0xff);
     if (op > 1) return;
-    for (auto *v : {&p.tasks[op], &p.tasks_sm[op]})
+    std::vector<std::vector<cm_task> *> tables = {&p.tasks[op], &p.tasks_sm[op]};
+    if (op == CM_OP_GEMM_RS) {
+        tables.push_back(&p.rs_ps);
+        tables.push_back(&p.rs_ps_sm);
+    }
+    for (auto *v : tables)
         for (cm_task &t : *v)
             if (t.rank == rank && t.step == step) {
                 t.sig_fwd[0] = t.sig_fwd[1] = -1;
@@ -387,7 +398,8 @@ void rebuild(PlanImpl &p) {
     build_ag_schedule(p);
     build_rs_schedule(p);
     build_ag_tasks(p);
-    build_rs_tasks(p);
+    build_rs_tasks(p, true);
+    build_rs_tasks(p, false);
     apply_skip(p);
     apply_debug_offset(p);
 }
@@ -444,7 +456,9 @@ cm_status cm_plan_step(cm_plan_t plan, cm_op op, int rank, int step, int stream,
 
 int cm_plan_tasks(cm_plan_t plan, cm_op op, cm_task *out, int capacity) {
     if (!plan || (op != CM_OP_AG_GEMM && op != CM_OP_GEMM_RS)) return -1;
-    const auto &t = plan->impl.task_order == 2 ? plan->impl.tasks_sm[op] : plan->impl.tasks[op];
+    const cm::PlanImpl &pl = plan->impl;
+    const bool ps = op == CM_OP_GEMM_RS && pl.rs_in_place == 0;   // per-step table; 1 and 2 list the in-place one
+    const auto &t = pl.task_order == 2 ? (ps ? pl.rs_ps_sm : pl.tasks_sm[op]) : (ps ? pl.rs_ps : pl.tasks[op]);
     for (int i = 0; i < capacity && i < int(t.size()); ++i) out[i] = t[size_t(i)];
     return int(t.size());
 }
@@ -534,14 +548,9 @@ cm_status cm_plan_set_option(cm_plan_t plan, cm_option option, int64_t value) {
             if (value < 0 || value > 2) return CM_ERR_INVALID_ARG;
             p.task_order = int(value);
             return CM_OK;
-        case CM_OPT_RS_IN_PLACE:
-            if (value != 0 && value != 1) return CM_ERR_INVALID_ARG;
+        case CM_OPT_RS_IN_PLACE:   // both task tables are built; each call picks one
+            if (value < 0 || value > 2) return CM_ERR_INVALID_ARG;
             p.rs_in_place = int(value);
-            try {
-                cm::rebuild(p);
-            } catch (...) {
-                return CM_ERR_INVALID_ARG;
-            }
             return CM_OK;
         case CM_OPT_SKIP_SIGNAL:
             p.skip_signal = value < 0 ? -1 : value;

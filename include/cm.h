@@ -160,7 +160,10 @@ typedef struct cm_task {
 } cm_task;
 
 /* Copy the task table of `op` into out[0..capacity); returns the number of
- * tasks (which may exceed capacity), or -1 for a bad plan/op.  Host only. */
+ * tasks (which may exceed capacity), or -1 for a bad plan/op.  Host only.
+ * For CM_OP_GEMM_RS it lists the per-step-buffer table when
+ * CM_OPT_RS_IN_PLACE is 0 and the in-place one otherwise (a call chooses
+ * between the two by its shape when the option is 2). */
 int cm_plan_tasks(cm_plan_t plan, cm_op op, cm_task *out, int capacity);
 
 /*
@@ -169,8 +172,8 @@ int cm_plan_tasks(cm_plan_t plan, cm_op op, cm_task *out, int capacity);
  * flags and, for a ring with N > 1: for AG, one receive slot per (rank, ring
  * stream, step), each [m][K] bf16, written once per call, so no task waits
  * for one to be freed; for RS, one fp32 accumulator [M/N][n] per (bucket,
- * ring stream) -- or per (rank, ring stream, step) with CM_OPT_RS_IN_PLACE =
- * 0.  The caller allocates it (256-byte
+ * ring stream) when the buckets are kept in place, or per (rank, ring
+ * stream, step) otherwise (CM_OPT_RS_IN_PLACE).  The caller allocates it (256-byte
  * aligned) and owns it; its contents need no initialisation (each call clears
  * the status block and flags with one memset on its stream).  Calls that
  * share a workspace must be ordered on the GPU (one stream).
@@ -206,9 +209,11 @@ cm_status cm_ag_gemm(cm_plan_t plan, const void *x, const void *w, cm_wlayout wl
  *  ws, ws_bytes: workspace of at least cm_gemm_rs_workspace_size(plan, M, n)
  *  bytes.  Accumulation across ranks is fp32, in ring order; the home rank
  *  rounds once to y_dtype.  On one GPU a bucket is not copied from rank to
- *  rank: by default (CM_OPT_RS_IN_PLACE) it stays in one workspace buffer
- *  per ring stream, and passing it on is releasing its readiness flag to
- *  the next contributor, which adds its product into it there.  Outputs
+ *  rank: it stays in one workspace buffer per ring stream, and passing it
+ *  on is releasing its readiness flag to the next contributor, which adds
+ *  its product into it there -- or, with per-step buffers, the next
+ *  contributor reads it and writes the sum to a buffer of its own
+ *  (CM_OPT_RS_IN_PLACE chooses).  Outputs
  *  must not alias inputs or the workspace.
  *  Errors: as cm_ag_gemm, with CM_ERR_SHAPE also for M % N != 0 or
  *  (M/N) % chunks != 0, and k in the role of K.
@@ -361,17 +366,20 @@ const char *cm_status_string(cm_status status);
  *                        the owner's tiles read a bucket, so only they are
  *                        preloaded.
  *  CM_OPT_RS_IN_PLACE    cm_gemm_rs (and the backward pair's data gradient)
- *                        on a ring: 1 (default) keeps each bucket in one fp32
- *                        buffer per ring stream that the first contributor
- *                        writes and every later one adds its partial product
- *                        into where it lies (a TMA reduce-add at L2 on the
- *                        CTA-pair kernel), in ring order, each after its
- *                        predecessor's flag; 0 gives every (rank, stream,
- *                        step) its own buffer, written once by the previous
- *                        rank and read by the next.  The same fp32 sums in
- *                        the same order.  Changes the workspace size (N
- *                        buffers per stream instead of N per stream and
- *                        step), so size the workspace after setting it.
+ *                        on a ring: 1 keeps each bucket in one fp32 buffer
+ *                        per ring stream that the first contributor writes
+ *                        and every later one adds its partial product into
+ *                        where it lies (a reduce-add at L2), in ring order,
+ *                        each after its predecessor's flag; 0 gives every
+ *                        (rank, stream, step) its own buffer, written once by
+ *                        the previous rank and read by the next; 2 (default)
+ *                        chooses per call: in place when one stream's buckets
+ *                        (M*n*4 bytes) take at most 128 MB and stay in L2,
+ *                        per-step buffers otherwise.  The same fp32 sums in
+ *                        the same order.  The workspace size follows the
+ *                        choice (N buffers per stream in place, N per stream
+ *                        and step otherwise), so size the workspace after
+ *                        setting it, for the call's M and n.
  *  CM_OPT_TASK_ORDER     order of a one-way ring's tasks: 1 rank-blocked
  *                        (see cm_task: each weight shard streamed in two
  *                        runs), 2 step-major (every rank's step 0, then every

@@ -82,12 +82,16 @@ def test_workspace_sizes(lib):
     p = cm.Plan(8, 1, "uni")
     m, K = 1024, 8192
     assert p.ag_workspace_size(m, K) >= 2 * 8 * m * K * 2
-    # RS buckets in place: one [M/N][n] fp32 buffer per bucket
+    # RS, automatic: 268 MB of buckets do not fit L2, so per-step buffers
+    # (one per rank and step); 64 MB do, so in place (one per bucket)
+    assert p.rs_workspace_size(8192, 8192) >= 8 * 8 * 1024 * 8192 * 4
+    assert 8 * 512 * 4096 * 4 <= p.rs_workspace_size(4096, 4096) < 9 * 512 * 4096 * 4
+    p.set_option(cm.CM_OPT_RS_IN_PLACE, 1)     # in place: one [M/N][n] fp32 buffer per bucket
     assert 8 * 1024 * 8192 * 4 <= p.rs_workspace_size(8192, 8192) < 9 * 1024 * 8192 * 4
     p.set_option(cm.CM_OPT_RS_IN_PLACE, 0)     # one per (rank, step)
-    assert p.rs_workspace_size(8192, 8192) >= 8 * 8 * 1024 * 8192 * 4
+    assert p.rs_workspace_size(4096, 4096) >= 8 * 8 * 512 * 4096 * 4
     with pytest.raises(cm.CMError):
-        p.set_option(cm.CM_OPT_RS_IN_PLACE, 2)
+        p.set_option(cm.CM_OPT_RS_IN_PLACE, 3)
     b = cm.Plan(8, 1, "bidi")
     assert b.ag_workspace_size(m, K) >= 4 * 8 * m * K * 2
     assert cm.Plan(8, 1, "none").ag_workspace_size(m, K) < 1 << 20
