@@ -834,10 +834,12 @@ def run_gate(args):
     - compute: each rank's share of this GPU's rate on the undecomposed op of
       the same shape (so the undecomposed prediction equals its measurement
       by construction; the decomposed prediction is the test);
-    - ring: each rank's share of the ring's own throughput, from the same
-      ring run with almost no compute (AllGather->GEMM with 256 output
-      columns, GEMM->ReduceScatter with a contraction of 64): the bytes one
-      hop carries, summed over ranks and steps, over that call's time;
+    - ring: GEMM->ReduceScatter, each rank's share of the ring's own
+      throughput, from the same ring run with almost no compute (a
+      contraction of 64): the bytes one hop carries, summed over ranks and
+      steps, over that call's time; AllGather->GEMM, each rank's share of
+      the HBM copy rate (the same kind of run, with 256 output columns, is
+      latency-bound and is printed for reference);
     - the native collective moves nothing on one GPU (every partial already
       sits in one memory), a message costs one flag round trip (1 us), and
       the realigning addition runs at each rank's share of the HBM copy rate.
@@ -881,7 +883,14 @@ def run_gate(args):
             ring_bytes, ms_ring = ring_calibration(cm, torch, device, op, N, direction, chunks, rows, K, n)
             rate = fl / (ms_none / 1e3) / 1e12   # this GPU's rate on the undecomposed op
             ring_gbs = ring_bytes / (ms_ring / 1e3) / 1e9
-            one_gpu = dict(gemm_tflops=rate / N, ring_gbs=ring_gbs / N, coll_gbs=1e12, hop_us=1.0,
+            # AG: a forward reads and writes each byte once, so a rank's link is
+            # its share of the HBM copy rate (the peak-rate reading); the
+            # calibration run, with one column tile per row tile, forwards from
+            # a few tiles at a time and measures their latency instead (kept in
+            # the line for reference).  RS: the calibration runs the real bucket
+            # epilogue on every tile, so its rate is the ring's.
+            ring_model = hbm / 2 if op == "ag" else ring_gbs
+            one_gpu = dict(gemm_tflops=rate / N, ring_gbs=ring_model / N, coll_gbs=1e12, hop_us=1.0,
                            mem_gbs=hbm / 2 / N)
             pred_dec = cm.cost_estimate(N, chunks, direction, code, rows, K, n, one_gpu) / 1e3
             pred_none = cm.cost_estimate(N, 1, "none", code, rows, K, n, one_gpu) / 1e3
