@@ -65,3 +65,19 @@ def test_kernel_hash_ignores_comments_only():
     assert bench.code_of(src) == bench.code_of("int a = 1;   // other words\n\nint b = 2;\n")
     assert bench.code_of(src) != bench.code_of("int a = 1;\nint b = 3;\n")
     assert len(bench.kernel_hash()) == 16
+
+
+def test_sweep_best_names_the_fastest_point_per_op():
+    import bench
+    pts = [
+        {"op": "ag", "N": 4, "chunks": 1, "ring": "uni", "ms": 2.2, "frac_of_peak": 0.90},
+        {"op": "rs", "N": 4, "chunks": 1, "ring": "uni", "ms": 2.3, "frac_of_peak": 0.88},
+        {"op": "ag", "N": 8, "chunks": 2, "ring": "bidi", "ms": 2.1, "frac_of_peak": 0.95},
+        {"op": "rs", "N": 16, "chunks": 4, "ring": "pipelined", "ms": 3.0, "frac_of_peak": 0.6},
+        {"op": "ag", "N": 16, "chunks": 4, "ring": "uni", "ms": 2.15, "frac_of_peak": 0.93},
+    ]
+    best = {b["sweep_best"]: b for b in bench.sweep_best(pts)}
+    assert list(best) == ["ag", "rs"]
+    assert (best["ag"]["N"], best["ag"]["chunks"], best["ag"]["ring"], best["ag"]["ms"]) == (8, 2, "bidi", 2.1)
+    assert (best["rs"]["N"], best["rs"]["ring"], best["rs"]["ms"]) == (4, "uni", 2.3)
+    assert bench.sweep_best([]) == []
