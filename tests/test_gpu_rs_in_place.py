@@ -180,16 +180,18 @@ def test_task_orders_agree_bitwise(N, chunks, direction):
     (5, 1280, 136, 1536, 1, "bidi", 3),     # odd N, three slabs of two column tiles
     (4, 2048, 320, 1032, 2, "bidi", 2),     # ragged last column tile: the count falls back to a divisor
 ])
-def test_column_slabs_agree_bitwise(kernel, epilogue, N, M, k, n, chunks, direction, slabs):
+@pytest.mark.parametrize("in_place", [1, 0])
+def test_column_slabs_agree_bitwise(kernel, epilogue, N, M, k, n, chunks, direction, slabs, in_place):
     """CM_OPT_RS_COL_SLABS only reorders the tiles: every bucket tile gets
     the same additions in the same ring order, so the bits agree with one
-    pass, and with the oracle within the fp32 bar."""
+    pass, and with the oracle within the fp32 bar, for buckets in place and
+    for per-step buffers."""
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=N * 7 + slabs, w_layout="nk")
     ref = oracle.gemm_rs(gen.bf16_bits(x), gen.bf16_bits(w), "nk")
-    p1 = _plan(N, chunks, direction, 1, kernel, 0, epilogue)
+    p1 = _plan(N, chunks, direction, in_place, kernel, 0, epilogue)
     p1.set_option(cm.CM_OPT_RS_COL_SLABS, 1)
     y1, _, _ = run_rs(p1, x, w, "nk", torch.float32)
-    ps = _plan(N, chunks, direction, 1, kernel, 0, epilogue)
+    ps = _plan(N, chunks, direction, in_place, kernel, 0, epilogue)
     ps.set_option(cm.CM_OPT_RS_COL_SLABS, slabs)
     ys, _, _ = run_rs(ps, x, w, "nk", torch.float32)
     assert torch.isfinite(ys).all()
