@@ -19,9 +19,10 @@
 // (rank, stream, step) has its own receive slot (AG), written once.  RS
 // buckets live either in one fp32 buffer per (bucket, stream) that every
 // contributor after the first accumulates into in place (in_buf[0] ==
-// out_buf: the kernels add their partial product to it where it lies), or --
-// CM_OPT_RS_IN_PLACE = 0 -- in one buffer per (rank, stream, step), written
-// once and read by the next rank.  Either way the only dependency is
+// out_buf: the kernels add their partial product to it where it lies), or in
+// one buffer per (rank, stream, step), written once and read by the next
+// rank.  Both tables are built; each call takes one (CM_OPT_RS_IN_PLACE, by
+// default from the size of the buckets).  Either way the only dependency is
 // readiness: task (r, i) needs what its ring predecessor produced at step
 // i-1, and that predecessor is the buffer's only other user at the time.
 // Every flag a task waits on is signalled by a task earlier in the table,
