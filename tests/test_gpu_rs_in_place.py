@@ -112,12 +112,14 @@ def test_in_place_exact_on_integers():
 
 
 @pytest.mark.parametrize("epilogue", [1, 2, 3])
-def test_in_place_dropped_signal_times_out(epilogue):
-    """A contributor that never signals: its successor's addition and the
-    owner's read wait for it, time out, and the next call is correct."""
+@pytest.mark.parametrize("in_place", [1, 0])
+def test_in_place_dropped_signal_times_out(epilogue, in_place):
+    """A contributor that never signals: its successor's addition (or load)
+    and the owner's read wait for it, time out, and the next call is
+    correct, with buckets in place and with per-step buffers."""
     N, M, k, n = 4, 1024, 128, 256
     x, w = gen.rs_inputs(N, M, k, n, gen.NORMAL1, gen.NORMAL002, seed=5, w_layout="nk")
-    p = _plan(N, 1, "uni", 1, PAIR, 0, epilogue)
+    p = _plan(N, 1, "uni", in_place, PAIR, 0, epilogue)
     p.set_option(cm.CM_OPT_TIMEOUT_NS, 50_000_000)
     p.set_option(cm.CM_OPT_SKIP_SIGNAL, (cm.CM_OP_GEMM_RS << 16) | (1 << 8) | 1)
     _, st, info = run_rs(p, x, w, "nk", torch.float32, check=False)
