@@ -99,6 +99,28 @@ def test_workspace_sizes(lib):
     assert lib.cm_ag_gemm_workspace_size(None, 1, 1) == 0
 
 
+def test_rs_bucket_mode_boundary(lib):
+    """The automatic bucket mode keeps buckets in place up to 128 MiB of
+    buckets per ring stream (M*n*4 bytes) and gives every hop its own buffer
+    above that; the workspace size follows the mode the call will take."""
+    N, n = 8, 8192
+    p = cm.Plan(N, 1, "uni")
+    at = 4096                      # 4096 * 8192 * 4 B = 128 MiB exactly: in place
+    above = at + N                 # one more row per bucket: per-step buffers
+    assert at * n * 4 == 128 << 20
+    one_set = at * n * 4
+    assert one_set <= p.rs_workspace_size(at, n) < one_set + (8 << 20)
+    steps = p.steps(cm.CM_OP_GEMM_RS)
+    assert p.rs_workspace_size(above, n) >= steps * above * n * 4
+    p.set_option(cm.CM_OPT_RS_IN_PLACE, 1)
+    assert p.rs_workspace_size(above, n) < above * n * 4 + (8 << 20)
+    p.set_option(cm.CM_OPT_RS_IN_PLACE, 0)
+    assert p.rs_workspace_size(at, n) >= steps * one_set
+    # two-way rings: one bucket set per ring stream, the rule per stream
+    b = cm.Plan(N, 1, "bidi")
+    assert 2 * one_set <= b.rs_workspace_size(at, n) < 2 * one_set + (8 << 20)
+
+
 def test_compute_calls_reject_bad_arguments_without_device_work(lib):
     p = cm.Plan(2, 2, "uni")
     fake = ctypes.c_void_p(1 << 20)   # never dereferenced: every check fails first
