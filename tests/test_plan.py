@@ -69,12 +69,15 @@ def test_each_rank_uses_each_shard_once(N, direction):
 @pytest.mark.parametrize("direction", ["uni", "bidi", "none"])
 @pytest.mark.parametrize("serial", [False, True])
 @pytest.mark.parametrize("order", [0, 2])
-def test_waits_point_to_earlier_tasks(N, direction, serial, order):
+@pytest.mark.parametrize("in_place", [2, 0])
+def test_waits_point_to_earlier_tasks(N, direction, serial, order, in_place):
     """Every flag has exactly one signalling task, earlier in the table than
     every task waiting on it, and of an earlier ring step -- in the ring's
     own order (rank-blocked one-way, stream-blocked two-way) and in
-    step-major order."""
+    step-major order, for the GEMM-RS table of buckets in place and that of
+    per-step buffers."""
     p = cm.Plan(N, 2, direction)
+    p.set_option(cm.CM_OPT_RS_IN_PLACE, in_place)
     if serial:
         p.set_option(cm.CM_OPT_SERIAL_STEPS, 1)
     p.set_option(cm.CM_OPT_TASK_ORDER, order)
@@ -224,33 +227,38 @@ def test_in_place_buckets_form_one_chain_each(N, direction):
         assert chain[-1].out_buf < 0 and chain[-1].rank == b // streams   # the owner reads it last
 
 
-def kernel_tile_order(tasks, c, mtiles, ntiles, band=0):
-    """The kernels' tile order: task groups (cm_task.tile_group) in table
-    order; inside a group chunk, row band (`band` row tiles of the group's
-    task-by-task row tiles; 0 = one band), column tile, row tile of the band."""
+def kernel_tile_order(tasks, c, mtiles, ntiles, band=0, slabs=1):
+    """The kernels' tile order: with column slabs (GEMM-RS), one pass over
+    the whole order per slab of ntiles / slabs column tiles; in a pass, task
+    groups (cm_task.tile_group) in table order; inside a group chunk, row
+    band (`band` row tiles of the group's task-by-task row tiles; 0 = one
+    band), column tile, row tile of the band."""
+    assert ntiles % slabs == 0
+    nts = ntiles // slabs
     out = []
-    t = 0
-    while t < len(tasks):
-        size = tasks[t].tile_group >> 8
-        assert size >= 1 and all((tasks[t + j].tile_group & 0xff) == j for j in range(size))
-        assert len({tasks[t + j].rank for j in range(size)}) == 1, "a group is one rank's tasks"
-        rows = size * mtiles
-        b = band if 0 < band < rows else rows
-        for q in range(c):
-            for b0 in range(0, rows, b):
-                for nt in range(ntiles):
-                    for rho in range(b0, min(rows, b0 + b)):
-                        out.append((t + rho // mtiles, q, rho % mtiles, nt))
-        t += size
+    for slab in range(slabs):
+        t = 0
+        while t < len(tasks):
+            size = tasks[t].tile_group >> 8
+            assert size >= 1 and all((tasks[t + j].tile_group & 0xff) == j for j in range(size))
+            assert len({tasks[t + j].rank for j in range(size)}) == 1, "a group is one rank's tasks"
+            rows = size * mtiles
+            b = band if 0 < band < rows else rows
+            for q in range(c):
+                for b0 in range(0, rows, b):
+                    for g in range(nts):
+                        for rho in range(b0, min(rows, b0 + b)):
+                            out.append((t + rho // mtiles, q, rho % mtiles, slab * nts + g))
+            t += size
     return out
 
 
-def _simulate(p, op, mtiles, ntiles, grid, seed, band=0):
+def _simulate(p, op, mtiles, ntiles, grid, seed, band=0, slabs=1):
     """Run the task table like the kernel: returns final outputs (see module doc)."""
     rnd = random.Random(seed)
     N, c = p.N, p.chunks
     tasks = p.tasks(op)
-    tiles = kernel_tile_order(tasks, c, mtiles, ntiles, band)
+    tiles = kernel_tile_order(tasks, c, mtiles, ntiles, band, slabs)
     # readiness counters as the kernels keep them: AG one per (flag, chunk,
     # row tile) -- the row tile's forward (column tile 0 here, as the
     # single-CTA kernel does) bumps it once; RS one per (flag, chunk, row
@@ -386,6 +394,37 @@ def test_protocol_simulation_row_bands(N, direction, chunks, grid, band):
         assert len(out) == N * N * c * mtiles * ntiles
         out = _simulate(p, RS, mtiles, ntiles, grid, seed, band)
         assert all(v == frozenset(range(N)) for v in out.values())
+
+
+@pytest.mark.parametrize("N", [3, 4, 8])
+@pytest.mark.parametrize("direction", ["uni", "bidi"])
+@pytest.mark.parametrize("grid", [3, 16])
+@pytest.mark.parametrize("slabs", [2, 3])
+@pytest.mark.parametrize("in_place", [1, 0])
+def test_protocol_simulation_column_slabs(N, direction, grid, slabs, in_place):
+    """Column slabs (GEMM-RS) run the tile order once per slab of column
+    tiles: a bucket tile's predecessor is in the same slab and earlier, so no
+    wait cycle, and every bucket still collects every rank once."""
+    p = cm.Plan(N, 1, direction)
+    p.set_option(cm.CM_OPT_RS_IN_PLACE, in_place)
+    mtiles, ntiles = 2, 6
+    for seed in range(2):
+        out = _simulate(p, RS, mtiles, ntiles, grid, seed, 0, slabs)
+        assert len(out) == N * mtiles * ntiles
+        assert all(v == frozenset(range(N)) for v in out.values())
+
+
+@pytest.mark.parametrize("slabs", [1, 2, 3, 6])
+def test_column_slab_order_is_a_permutation(slabs):
+    p = cm.Plan(8, 2, "uni")
+    tasks = p.tasks(RS)
+    base = kernel_tile_order(tasks, 2, 3, 6)
+    order = kernel_tile_order(tasks, 2, 3, 6, 0, slabs)
+    assert sorted(order) == sorted(base)
+    # every pass covers only its own slab's columns
+    per = len(order) // slabs
+    for s_ in range(slabs):
+        assert {nt for (_, _, _, nt) in order[s_ * per:(s_ + 1) * per]} == set(range(s_ * 6 // slabs, (s_ + 1) * 6 // slabs))
 
 
 @pytest.mark.parametrize("band", [0, 1, 2, 3, 5, 100])
