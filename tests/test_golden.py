@@ -61,6 +61,35 @@ def test_ag_worked_example_ring_and_messages():
     check_messages(trace, g["messages"])
 
 
+def test_ag_worked_example_bidi_messages():
+    """The bidirectional ring on the same three ranks: the own shard leaves
+    both ways at step 0 and nothing is forwarded after it."""
+    g = load("ag_gemm_n3_worked.json")
+    trace = []
+    y = ring.ag_gemm_ring(bits(g["x"]), bits(g["w"]), g["w_layout"], direction="bidi", trace=trace)
+    assert np.array_equal(y, np.asarray(g["y"], dtype=np.float64))
+    check_messages(trace, g["messages_bidi"])
+
+
+def test_ag_worked_example_four_ranks_bidi():
+    """Four ranks over the bidirectional ring: two clockwise hops (one
+    forward at step 1) and one counter-clockwise hop, worked by hand; the
+    oracle's definition and the ring give the same outputs."""
+    g = load("ag_gemm_n4_bidi_worked.json")
+    x, w = bits(g["x"]), bits(g["w"])
+    want = np.asarray(g["y"], dtype=np.float64)
+    assert np.array_equal(oracle.ag_gemm(x, w, g["w_layout"]), want)
+    trace = []
+    y = ring.ag_gemm_ring(x, w, g["w_layout"], direction="bidi", trace=trace)
+    assert np.array_equal(y, want)
+    check_messages(trace, g["messages_bidi"])
+    # the one-way ring sends a different set of messages for the same result
+    trace_uni = []
+    ring.ag_gemm_ring(x, w, g["w_layout"], direction="uni", trace=trace_uni)
+    with pytest.raises(AssertionError):
+        check_messages(trace_uni, g["messages_bidi"])
+
+
 def test_rs_worked_example_oracle():
     g = load("gemm_rs_n3_worked.json")
     y = oracle.gemm_rs(bits(g["x"]), bits(g["w"]), g["w_layout"])
