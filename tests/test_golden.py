@@ -105,6 +105,21 @@ def test_rs_worked_example_ring_and_partial_buckets(direction):
     check_messages(trace, g["messages_" + direction])
 
 
+@pytest.mark.parametrize("direction", ["uni", "bidi"])
+def test_rs_worked_example_four_ranks(direction):
+    """Four ranks: three forwards per bucket one-way; two clockwise hops and
+    one counter-clockwise hop on the bidirectional ring, whose owner adds
+    partials of unequal length (the realigning addition)."""
+    g = load("gemm_rs_n4_worked.json")
+    x, w = bits(g["x"]), bits(g["w"])
+    want = np.asarray(g["y"], dtype=np.float64)
+    assert np.array_equal(oracle.gemm_rs(x, w, g["w_layout"]), want)
+    trace = []
+    y = ring.gemm_rs_ring(x, w, g["w_layout"], direction=direction, trace=trace)
+    assert np.array_equal(y, want)
+    check_messages(trace, g["messages_" + direction])
+
+
 def test_plant_wrong_bucket_start_fails_worked_example():
     """A ring that started bucket o at rank o (instead of o+1) would still sum
     every contribution, but its messages would not be the hand-worked ones."""
