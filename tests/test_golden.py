@@ -133,6 +133,25 @@ def test_plant_wrong_bucket_start_fails_worked_example():
         check_messages(trace, shifted)
 
 
+def test_cannon_worked_example():
+    """Cannon's rotation on a 3 x 3 grid with 1 x 1 blocks: the product and
+    the block every message carries (the skew, A moving left, B moving up),
+    worked by hand; the oracle's definition agrees on the product."""
+    g = load("cannon_q3_worked.json")
+    q = g["q"]
+    A = np.asarray(g["A"], dtype=np.float32)
+    B = np.asarray(g["B"], dtype=np.float32)
+    a_blocks = bits(A.reshape(q * q, 1, 1))                     # A_{i,k} at i*q + k
+    b_blocks = bits(B.reshape(q * q, 1, 1))                     # B_{k,j} at k*q + j ("kn": [bk][bn])
+    want = np.asarray(g["C"], dtype=np.float64).reshape(q * q, 1, 1)
+    c, log = ring.cannon_gemm(a_blocks, b_blocks, q, g["b_layout"], return_log=True)
+    assert np.array_equal(c, want)
+    got = sorted((e[0], e[1], e[2], e[3], tuple(e[4])) for e in log)
+    exp = sorted((m["step"], m["stream"], m["src"], m["dst"], tuple(m["block"])) for m in g["messages"])
+    assert got == exp
+    assert np.array_equal(oracle.gemm(bits(A), bits(B), "kn"), np.asarray(g["C"], dtype=np.float64))
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("direction", ["uni", "bidi"])
 def test_worked_examples_on_gpu(direction):
