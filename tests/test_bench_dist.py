@@ -81,3 +81,25 @@ def test_sweep_best_names_the_fastest_point_per_op():
     assert (best["ag"]["N"], best["ag"]["chunks"], best["ag"]["ring"], best["ag"]["ms"]) == (8, 2, "bidi", 2.1)
     assert (best["rs"]["N"], best["rs"]["ring"], best["rs"]["ms"]) == (4, "uni", 2.3)
     assert bench.sweep_best([]) == []
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    """Under torchrun the reference arm's other ranks join the process group
+    and leave at once, without work and without a line of output."""
+    import argparse
+    import bench
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    joined = []
+    monkeypatch.setattr(bench, "dist_init", lambda backend: joined.append(backend) or (1, 2))
+
+    def no_work(*a, **k):
+        raise AssertionError("rank 1 must not build inputs or time the oracle")
+
+    monkeypatch.setattr(bench, "make_step_inputs", no_work)
+    monkeypatch.setattr(bench, "oracle_sample", no_work)
+    args = argparse.Namespace(gpus=2, steps=2, warmup=3, ref_seconds=1.0)
+    assert bench.run_reference(args) == 0
+    assert joined == ["gloo"]
+    assert capsys.readouterr().out == ""
